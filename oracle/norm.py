@@ -1,0 +1,229 @@
+"""LayerNorm / RMSNorm forward and backward with fused output quantization.
+
+Oracle side, fp64, plain numpy.  Source: the page "Implementation:NVIDIA
+TransformerEngine PyTorch Ext Normalization":
+
+* Description: forward functions normalize and optionally quantize the
+  output (paths UNFUSED, FULLY_FUSED for delayed scaling and MXFP8,
+  FUSED_NORM_AMAX_FP8 for current scaling); backward functions return dx,
+  dgamma and dbeta; gamma may be zero-centered; sm_margin only tunes
+  occupancy (so it has no effect on any value computed here).
+* Signature / I/O Contract: layernorm_fwd(input, weight, bias, eps, quantizer,
+  sm_margin, zero_centered_gamma) -> (output, mu, rsigma); rmsnorm_fwd has no
+  bias and no mu ("Mean (LayerNorm only)"); layernorm_bwd(dz, x, mu, rsigma,
+  gamma, ...) -> (dx, dgamma, dbeta); rmsnorm_bwd(dz, x, rsigma, gamma, ...)
+  -> (dx, dgamma).
+
+The pages print no formula.  Readings taken (the plainest standard ones):
+* variance is the biased one (divide by H); eps is added inside the square
+  root for both norms; rsigma = 1 / sqrt(var + eps) (LayerNorm) and
+  rsigma = 1 / sqrt(mean(x**2) + eps) (RMSNorm);
+* zero-centered gamma means the effective weight is 1 + gamma, and dgamma is
+  taken with respect to the stored gamma (same value, since d(1+g)/dg = 1);
+* eps reaches the kernels as an fp32 argument, so its fp32 value is used;
+* mu and rsigma are returned as fp32 (rounded once from fp64);
+* the unquantized output is y rounded once to the output dtype;
+* the quantization stage starts from y32 = fp32(y) and then follows exact
+  IEEE fp32 steps, so that it can be compared bit for bit:
+    delayed  p = fp32(y32 * s), code = E4M3(p), amax = max |y32| over the
+             whole tensor, scale_inv = fp32(1 / s);
+    current  amax as above, s = fp32(448 / amax) (s = 1 when amax = 0),
+             then as delayed;
+    MXFP8    per block of 32 (1x32 along a row, and 32x1 down a column):
+             A = max |y32|, code_e8m0(A), element code = E4M3(y32 * 2**-e)
+             (a power-of-two scaling, exact); the columnwise data is stored
+             transposed, [H, N], with scales [H, N/32].
+* the backward takes mu and rsigma as given (the saved fp32 values), forms
+  xhat = (x - mu) * rsigma (RMSNorm: x * rsigma), dy = dz * g_eff and
+    LayerNorm  dx = rsigma * (dy - mean(dy) - xhat * mean(dy * xhat))
+    RMSNorm    dx = rsigma * (dy - xhat * mean(dy * xhat))
+  dgamma = sum over rows of dz * xhat, dbeta = sum over rows of dz; dx is
+  rounded once to the dtype of x, dgamma / dbeta to fp32.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+from .formats import E4M3_MAX, bf16_bits, e4m3_encode, e8m0_from_amax
+
+QUANT_MODES = ("none", "fp8_delayed", "fp8_current", "mxfp8")
+MX_BLOCK = 32
+
+
+def _f64(a) -> np.ndarray:
+    return np.asarray(a, dtype=np.float64)
+
+
+def _eps32(eps: float) -> float:
+    return float(np.float32(eps))
+
+
+def _g_eff(gamma, zero_centered_gamma: bool) -> np.ndarray:
+    g = _f64(gamma)
+    return 1.0 + g if zero_centered_gamma else g
+
+
+# --------------------------------------------------------------- statistics
+def layernorm_stats(x, eps):
+    """Per-row mean m and r = 1/sqrt(var + eps), two-pass, fp64 -> (m, r)."""
+    x = _f64(x)
+    H = x.shape[-1]
+    m = np.sum(x, axis=-1) / H
+    d = x - m[..., None]
+    v = np.sum(d * d, axis=-1) / H
+    r = 1.0 / np.sqrt(v + _eps32(eps))
+    return m, r
+
+
+def rmsnorm_stats(x, eps):
+    """Per-row r = 1/sqrt(mean(x**2) + eps), fp64."""
+    x = _f64(x)
+    H = x.shape[-1]
+    ms = np.sum(x * x, axis=-1) / H
+    return 1.0 / np.sqrt(ms + _eps32(eps))
+
+
+def norm_apply(x, m, r, gamma, beta, zero_centered_gamma):
+    """y = (x - m) * r * g_eff + beta; m None -> RMSNorm (no centering)."""
+    x = _f64(x)
+    g = _g_eff(gamma, zero_centered_gamma)
+    c = x if m is None else x - _f64(m)[..., None]
+    y = c * _f64(r)[..., None] * g
+    if beta is not None:
+        y = y + _f64(beta)
+    return y
+
+
+# ------------------------------------------------------------- quantization
+def fp8_codes(y32, s) -> np.ndarray:
+    """E4M3 codes of fp32(y32 * s) (one fp32 multiply, then E4M3 rounding)."""
+    p = np.asarray(y32, dtype=np.float32) * np.float32(s)
+    return e4m3_encode(p.astype(np.float64))
+
+
+def tensor_amax(y32) -> np.float32:
+    """max |y32| over the whole tensor (NaN if any element is NaN)."""
+    a = np.abs(np.asarray(y32, dtype=np.float32))
+    if a.size == 0:
+        return np.float32(0.0)
+    return np.float32(np.max(a))
+
+
+def current_scale(amax) -> np.float32:
+    """s = fp32(448 / amax) by one IEEE fp32 division; amax = 0 -> 1."""
+    a = np.float32(amax)
+    if a == 0:
+        return np.float32(1.0)
+    return np.float32(np.float32(E4M3_MAX) / a)
+
+
+def scale_inverse(s) -> np.float32:
+    return np.float32(np.float32(1.0) / np.float32(s))
+
+
+def mx_blocks_1d(y32_rows) -> tuple[np.ndarray, np.ndarray]:
+    """MX-quantize along the last axis in blocks of 32 -> (codes, e8m0)."""
+    y = np.asarray(y32_rows, dtype=np.float32)
+    n, h = y.shape
+    assert h % MX_BLOCK == 0
+    yb = y.reshape(n, h // MX_BLOCK, MX_BLOCK)
+    a = np.abs(yb)
+    nanblk = np.isnan(a).any(axis=-1)
+    amax = np.where(nanblk, np.float32(np.nan), np.nanmax(np.where(np.isnan(a), 0, a), axis=-1))
+    code = e8m0_from_amax(amax)
+    e = code.astype(np.int64) - 127
+    scaled = yb.astype(np.float64) * np.ldexp(1.0, (-e).astype(np.int32))[..., None]
+    q = e4m3_encode(scaled)
+    q = np.where(nanblk[..., None], np.uint8(0x7F), q).astype(np.uint8)
+    return q.reshape(n, h), code
+
+
+def quantize(y32, mode: str, scale=None, amax=None) -> dict:
+    """Quantization stage for a block of fp32 pre-quantization rows.
+
+    ``y32`` [n, H] fp32.  For fp8_current the tensor-wide ``amax`` may be
+    given (when y32 is only a sample of the rows); otherwise it is taken from
+    y32.  Returns the fields the entry points return for that mode.
+    """
+    y32 = np.asarray(y32, dtype=np.float32)
+    if mode == "fp8_delayed":
+        s = np.float32(scale)
+        return {"data": fp8_codes(y32, s), "amax": tensor_amax(y32),
+                "scale_inv": scale_inverse(s)}
+    if mode == "fp8_current":
+        am = tensor_amax(y32) if amax is None else np.float32(amax)
+        s = current_scale(am)
+        return {"data": fp8_codes(y32, s), "amax": am, "scale": s,
+                "scale_inv": scale_inverse(s)}
+    if mode == "mxfp8":
+        rq, rs = mx_blocks_1d(y32)
+        cq, cs = mx_blocks_1d(np.ascontiguousarray(y32.T))
+        return {"data": rq, "row_scales": rs, "col_data": cq, "col_scales": cs}
+    raise ValueError(mode)
+
+
+def _out_none(y, out_dtype: str):
+    if out_dtype == "bf16":
+        return bf16_bits(y)
+    if out_dtype == "f32":
+        return y.astype(np.float32)
+    raise ValueError(out_dtype)
+
+
+# ------------------------------------------------------------------ forward
+def _fwd(x, m, r, gamma, beta, zcg, mode, out_dtype, scale, amax):
+    y = norm_apply(x, m, r, gamma, beta, zcg)
+    res = {"y": y, "rsigma": np.asarray(r, dtype=np.float64).astype(np.float32)}
+    if m is not None:
+        res["mu"] = np.asarray(m, dtype=np.float64).astype(np.float32)
+    if mode == "none":
+        res["data"] = _out_none(y, out_dtype)
+    else:
+        res.update(quantize(y.astype(np.float32), mode, scale=scale, amax=amax))
+    return res
+
+
+def layernorm_fwd(x, gamma, beta, eps, zero_centered_gamma=False, mode="none",
+                  out_dtype="bf16", scale=None, amax=None) -> dict:
+    """LayerNorm forward -> dict(data, mu, rsigma, y, [amax, scale_inv, ...])."""
+    m, r = layernorm_stats(x, eps)
+    return _fwd(x, m, r, gamma, beta, zero_centered_gamma, mode, out_dtype, scale, amax)
+
+
+def rmsnorm_fwd(x, gamma, eps, zero_centered_gamma=False, mode="none",
+                out_dtype="bf16", scale=None, amax=None) -> dict:
+    """RMSNorm forward -> dict(data, rsigma, y, ...); no mu."""
+    r = rmsnorm_stats(x, eps)
+    return _fwd(x, None, r, gamma, None, zero_centered_gamma, mode, out_dtype, scale, amax)
+
+
+# ----------------------------------------------------------------- backward
+def _bwd(dz, x, mu, rsigma, gamma, zcg, dtype):
+    dz = _f64(dz)
+    x = _f64(x)
+    r = _f64(rsigma)[:, None]
+    xhat = (x if mu is None else x - _f64(mu)[:, None]) * r
+    dy = dz * _g_eff(gamma, zcg)
+    c2 = np.mean(dy * xhat, axis=1, keepdims=True)
+    if mu is None:
+        dx = r * (dy - xhat * c2)
+    else:
+        c1 = np.mean(dy, axis=1, keepdims=True)
+        dx = r * (dy - c1 - xhat * c2)
+    res = {"dx64": dx, "dgamma64": np.sum(dz * xhat, axis=0)}
+    res["dx"] = bf16_bits(dx) if dtype == "bf16" else dx.astype(np.float32)
+    res["dgamma"] = res["dgamma64"].astype(np.float32)
+    if mu is not None:
+        res["dbeta64"] = np.sum(dz, axis=0)
+        res["dbeta"] = res["dbeta64"].astype(np.float32)
+    return res
+
+
+def layernorm_bwd(dz, x, mu, rsigma, gamma, zero_centered_gamma=False, dtype="bf16") -> dict:
+    """LayerNorm backward -> dict(dx, dgamma, dbeta, and their fp64 forms)."""
+    return _bwd(dz, x, mu, rsigma, gamma, zero_centered_gamma, dtype)
+
+
+def rmsnorm_bwd(dz, x, rsigma, gamma, zero_centered_gamma=False, dtype="bf16") -> dict:
+    """RMSNorm backward -> dict(dx, dgamma, and fp64 forms); no dbeta."""
+    return _bwd(dz, x, None, rsigma, gamma, zero_centered_gamma, dtype)

@@ -1,0 +1,273 @@
+"""CPU pins of the oracle's normalization arithmetic.
+
+Pins (none of them re-runs the oracle's own formula):
+* closed forms worked by hand (tests/golden/norm_closed_forms.txt);
+* exact rational statistics (fractions + 50-digit decimal square roots);
+* invariants: mean(xhat) = 0, mean(xhat**2) = var/(var+eps), LayerNorm equal
+  to RMSNorm on rows with zero mean, scale invariance;
+* central finite differences of L = sum(dz * y) for dx, dgamma, dbeta,
+  plus sum_j dx_ij = 0 (LayerNorm) and sum_j dx_ij x_ij = 0 (RMSNorm, eps=0);
+* pure-Python loop re-derivations of the MXFP8 blocks (rowwise and the
+  transposed columnwise layout) on tiny inputs, with a brute-force E4M3.
+"""
+import math
+import os
+from decimal import Decimal, getcontext
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+import oracle
+import rn_inputs
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _floats(s):
+    return [float(t) for t in s.split()]
+
+
+def _closed_forms():
+    out = []
+    with open(os.path.join(GOLDEN, "norm_closed_forms.txt")) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            out.append([t.strip() for t in line.split("|")])
+    return out
+
+
+@pytest.mark.parametrize("row", _closed_forms(), ids=lambda r: r[0] + "-" + r[3].replace(" ", "_"))
+def test_closed_forms(row):
+    op, zc, eps, x, g, b, mu, rs, y = row
+    x = np.array([_floats(x)])
+    g = np.array(_floats(g), np.float32)
+    zc = bool(int(zc))
+    eps = float(eps)
+    if op == "ln":
+        r = oracle.layernorm_fwd(x, g, np.array(_floats(b), np.float32), eps, zc, "none", "f32")
+        assert r["mu"][0] == np.float32(float(mu))
+    else:
+        r = oracle.rmsnorm_fwd(x, g, eps, zc, "none", "f32")
+        assert "mu" not in r
+    assert r["rsigma"][0] == np.float32(float(rs))
+    np.testing.assert_allclose(r["y"][0], _floats(y), rtol=1e-15, atol=1e-15)
+
+
+def test_stats_exact_rational():
+    """mu and rsigma against exact rational mean/variance and a 50-digit sqrt."""
+    getcontext().prec = 50
+    rng = np.random.default_rng(5)
+    for H in (1, 2, 7, 64, 333):
+        x = rn_inputs.bf16_bits_to_f32(rn_inputs.to_bf16_bits(rng.normal(0.5, 2.0, (3, H)))).astype(np.float64)
+        eps = 1e-5
+        m, r = oracle.layernorm_stats(x, eps)
+        rr = oracle.rmsnorm_stats(x, eps)
+        e = Fraction(float(np.float32(eps)))
+        for i in range(3):
+            xs = [Fraction(float(v)) for v in x[i]]
+            mean = sum(xs) / H
+            var = sum((v - mean) ** 2 for v in xs) / H
+            ms = sum(v * v for v in xs) / H
+            want_r = 1 / (Decimal(var.numerator) / Decimal(var.denominator) + Decimal(e.numerator) / Decimal(e.denominator)).sqrt()
+            want_rr = 1 / (Decimal(ms.numerator) / Decimal(ms.denominator) + Decimal(e.numerator) / Decimal(e.denominator)).sqrt()
+            assert abs(m[i] - float(mean)) <= 4 * np.spacing(abs(float(mean)) + 1e-300) + 1e-15 * float(sum(abs(v) for v in xs) / H)
+            assert abs(r[i] - float(want_r)) <= 8 * np.spacing(float(want_r))
+            assert abs(rr[i] - float(want_rr)) <= 8 * np.spacing(float(want_rr))
+
+
+def test_invariants_mean_zero_var_ratio():
+    rng = np.random.default_rng(6)
+    x = rng.normal(0.3, 1.7, (16, 96))
+    eps = 1e-3
+    m, r = oracle.layernorm_stats(x, eps)
+    xhat = oracle.norm_apply(x, m, r, np.ones(96), None, False)
+    var = np.var(x, axis=1)                       # numpy's biased variance
+    np.testing.assert_allclose(np.mean(xhat, axis=1), 0, atol=1e-14)
+    np.testing.assert_allclose(np.mean(xhat ** 2, axis=1), var / (var + np.float32(eps)), rtol=1e-13)
+
+
+def test_layernorm_equals_rmsnorm_on_zero_mean_rows():
+    rng = np.random.default_rng(7)
+    a = rng.normal(size=(8, 32))
+    x = np.concatenate([a, -a], axis=1)           # every row has mean exactly 0
+    g = (1 + 0.1 * rng.normal(size=64)).astype(np.float32)
+    ln = oracle.layernorm_fwd(x, g, np.zeros(64, np.float32), 1e-6, False, "none", "f32")
+    rms = oracle.rmsnorm_fwd(x, g, 1e-6, False, "none", "f32")
+    np.testing.assert_allclose(ln["y"], rms["y"], rtol=1e-14, atol=1e-14)
+    assert np.all(np.abs(ln["mu"]) < 1e-15)    # zero up to fp64 summation rounding
+
+
+def test_scale_invariance_and_zero_centered():
+    rng = np.random.default_rng(8)
+    x = rng.normal(size=(4, 64))
+    g = rng.normal(0, 0.1, 64).astype(np.float32)
+    b = rng.normal(0, 0.1, 64).astype(np.float32)
+    y1 = oracle.layernorm_fwd(x, g, b, 0.0, True, "none", "f32")["y"]
+    y2 = oracle.layernorm_fwd(1000.0 * x + 5.0, g, b, 0.0, True, "none", "f32")["y"]
+    np.testing.assert_allclose(y1, y2, rtol=1e-9, atol=1e-12)
+    # zero-centered gamma g is the same as plain gamma 1 + g
+    y3 = oracle.layernorm_fwd(x, (1.0 + g.astype(np.float64)), b, 0.0, False, "none", "f32")["y"]
+    np.testing.assert_allclose(y1, y3, rtol=1e-14, atol=1e-14)
+
+
+def test_h1_layernorm_is_beta():
+    x = np.array([[3.5], [-2.0]])
+    r = oracle.layernorm_fwd(x, np.array([2.0], np.float32), np.array([0.25], np.float32), 1e-5, False, "none", "f32")
+    np.testing.assert_array_equal(r["y"], [[0.25], [0.25]])
+
+
+# ----------------------------------------------------------- backward pins
+def _loss(x, g, b, dz, eps, zc, ln):
+    if ln:
+        y = oracle.layernorm_fwd(x, g, b, eps, zc, "none", "f32")["y"]
+    else:
+        y = oracle.rmsnorm_fwd(x, g, eps, zc, "none", "f32")["y"]
+    return float(np.sum(dz * y))
+
+
+@pytest.mark.parametrize("ln", [True, False])
+@pytest.mark.parametrize("zc", [False, True])
+@pytest.mark.parametrize("H", [8, 40])
+def test_backward_finite_differences(ln, zc, H):
+    rng = np.random.default_rng(9 + H)
+    N = 3
+    x = rng.normal(0.2, 1.3, (N, H))
+    g = rng.normal(0.1 if zc else 1.0, 0.3, H)
+    b = rng.normal(0, 0.3, H)
+    dz = rng.normal(size=(N, H))
+    eps = 1e-2
+    if ln:
+        m, r = oracle.layernorm_stats(x, eps)
+        res = oracle.layernorm_bwd(dz, x, m, r, g, zc, "f32")
+    else:
+        r = oracle.rmsnorm_stats(x, eps)
+        res = oracle.rmsnorm_bwd(dz, x, r, g, zc, "f32")
+    h = 1e-6
+    fd_x = np.zeros_like(x)
+    for i in range(N):
+        for j in range(H):
+            xp = x.copy(); xp[i, j] += h
+            xm = x.copy(); xm[i, j] -= h
+            fd_x[i, j] = (_loss(xp, g, b, dz, eps, zc, ln) - _loss(xm, g, b, dz, eps, zc, ln)) / (2 * h)
+    fd_g = np.zeros(H)
+    fd_b = np.zeros(H)
+    for j in range(H):
+        gp = g.copy(); gp[j] += h
+        gm = g.copy(); gm[j] -= h
+        fd_g[j] = (_loss(x, gp, b, dz, eps, zc, ln) - _loss(x, gm, b, dz, eps, zc, ln)) / (2 * h)
+        bp = b.copy(); bp[j] += h
+        bm = b.copy(); bm[j] -= h
+        fd_b[j] = (_loss(x, g, bp, dz, eps, zc, ln) - _loss(x, g, bm, dz, eps, zc, ln)) / (2 * h)
+    np.testing.assert_allclose(res["dx64"], fd_x, rtol=1e-6, atol=1e-7)
+    np.testing.assert_allclose(res["dgamma64"], fd_g, rtol=1e-6, atol=1e-7)
+    if ln:
+        np.testing.assert_allclose(res["dbeta64"], fd_b, rtol=1e-6, atol=1e-7)
+    else:
+        assert "dbeta" not in res
+
+
+def test_backward_row_identities():
+    rng = np.random.default_rng(10)
+    x = rng.normal(size=(5, 48))
+    dz = rng.normal(size=(5, 48))
+    g = rng.normal(1, 0.2, 48)
+    m, r = oracle.layernorm_stats(x, 1e-5)
+    dx = oracle.layernorm_bwd(dz, x, m, r, g, False, "f32")["dx64"]
+    np.testing.assert_allclose(dx.sum(axis=1), 0, atol=1e-12)      # shift invariance
+    rr = oracle.rmsnorm_stats(x, 0.0)
+    dxr = oracle.rmsnorm_bwd(dz, x, rr, g, False, "f32")["dx64"]
+    np.testing.assert_allclose((dxr * x).sum(axis=1), 0, atol=1e-11)  # scale invariance
+
+
+def test_backward_dbeta_is_column_sum_of_dz():
+    rng = np.random.default_rng(11)
+    x = rng.normal(size=(6, 16))
+    dz = rng.normal(size=(6, 16))
+    m, r = oracle.layernorm_stats(x, 1e-5)
+    res = oracle.layernorm_bwd(dz, x, m, r, np.ones(16), False, "f32")
+    for j in range(16):
+        assert res["dbeta64"][j] == pytest.approx(math.fsum(dz[:, j]), abs=1e-13)
+
+
+# -------------------------------------------------------------- MXFP8 pins
+def _bf_e4m3(v):
+    """Brute-force nearest E4M3 code of one value (ties to even code)."""
+    dec = oracle.e4m3_decode(np.arange(0x7F, dtype=np.uint8))
+    a = min(abs(v), 448.0)
+    best = min(range(0x7F), key=lambda c: (abs(a - dec[c]), c % 2))
+    return best | (0x80 if math.copysign(1.0, v) < 0 else 0)
+
+
+def _loop_mx_scale(block):
+    A = max(abs(float(t)) for t in block)
+    if A == 0:
+        return 0
+    _, k = math.frexp(A)
+    return max(-127, min(127, k - 1 - 8)) + 127
+
+
+def test_mxfp8_blocks_by_loops():
+    rng = np.random.default_rng(12)
+    N, H = 64, 96
+    # rows and columns with very different magnitudes so that row and column
+    # blocks get different scales (a transposition mistake would show)
+    y = (rng.normal(size=(N, H)) * np.exp2(rng.integers(-6, 7, N))[:, None]
+         * np.exp2(rng.integers(-5, 6, H))[None, :]).astype(np.float32)
+    r = oracle.quantize(y, "mxfp8")
+    assert r["data"].shape == (N, H) and r["row_scales"].shape == (N, H // 32)
+    assert r["col_data"].shape == (H, N) and r["col_scales"].shape == (H, N // 32)
+    for i in range(N):
+        for jb in range(H // 32):
+            blk = [float(t) for t in y[i, jb * 32:(jb + 1) * 32]]
+            code = _loop_mx_scale(blk)
+            assert r["row_scales"][i, jb] == code
+            for t in range(0, 32, 7):
+                assert r["data"][i, jb * 32 + t] == _bf_e4m3(blk[t] * 2.0 ** (127 - code))
+    for j in range(H):
+        for ib in range(N // 32):
+            blk = [float(t) for t in y[ib * 32:(ib + 1) * 32, j]]
+            code = _loop_mx_scale(blk)
+            assert r["col_scales"][j, ib] == code
+            for t in range(0, 32, 5):
+                assert r["col_data"][j, ib * 32 + t] == _bf_e4m3(blk[t] * 2.0 ** (127 - code))
+
+
+def test_mxfp8_dequant_error_bound():
+    """decode(q) * 2**e is within half an E4M3 step of y (no block saturates
+    beyond 448 * 2**e by more than the top step)."""
+    rng = np.random.default_rng(13)
+    y = (rng.normal(size=(64, 64)) * 3.0).astype(np.float32)
+    r = oracle.quantize(y, "mxfp8")
+    e = r["row_scales"].astype(np.int64) - 127
+    deq = oracle.e4m3_decode(r["data"]).reshape(64, 2, 32) * np.exp2(e)[..., None]
+    yy = y.astype(np.float64).reshape(64, 2, 32)
+    scaled = np.abs(yy) * np.exp2(-e)[..., None]
+    step = np.where(scaled < 2.0 ** -6, 2.0 ** -9, np.exp2(np.floor(np.log2(np.maximum(scaled, 1e-30))) - 3))
+    err = np.abs(deq - yy) * np.exp2(-e)[..., None]
+    ok = (err <= step / 2 + 1e-12) | (scaled >= 448)
+    assert ok.all()
+
+
+def test_fp8_pipeline_by_loops():
+    """Whole fwd (LayerNorm + delayed FP8) on a tiny case by plain loops."""
+    w = rn_inputs.make("ln_delayed", N=3, H=64)
+    x = w.x_f64()
+    res = oracle.layernorm_fwd(x, w.gamma, w.beta, w.eps, True, "fp8_delayed", scale=w.scale)
+    eps = float(np.float32(w.eps))
+    amax = 0.0
+    for i in range(3):
+        row = [float(t) for t in x[i]]
+        m = math.fsum(row) / 64
+        v = math.fsum((t - m) ** 2 for t in row) / 64
+        rs = 1 / math.sqrt(v + eps)
+        assert res["mu"][i] == np.float32(m) and res["rsigma"][i] == np.float32(rs)
+        for j in range(64):
+            y = (row[j] - m) * rs * (1.0 + float(w.gamma[j])) + float(w.beta[j])
+            y32 = np.float32(y)
+            amax = max(amax, abs(float(y32)))
+            p = float(np.float32(y32 * np.float32(w.scale)))
+            assert res["data"][i, j] == _bf_e4m3(p)
+    assert res["amax"] == np.float32(amax)
