@@ -1,0 +1,567 @@
+#!/usr/bin/env python3
+"""Benchmark of the fused LayerNorm / RMSNorm library on one GB300.
+
+Headline step (one pass of the hot path over one batch): LayerNorm forward
+with fused FP8 delayed-scaling output, then LayerNorm backward (dx, dgamma,
+dbeta), zero-centered gamma, x and dz bf16 [8192 x 4096] (synthetic, seeded,
+rn_inputs workload "ln_delayed").  Metric: effective HBM GB/s, i.e.
+algorithmic bytes (every input read once, every output written once) per
+second of kernel time, with L2 flushed before each forward and each backward.
+
+Also reported (key "workloads"): the other workloads at full size, each as
+GB/s, rows/s and the fraction of the HBM peak.
+
+Usage:  python bench.py [--steps K] [--warmup W] [--impl rn|reference]
+Multi-GPU (torchrun): every rank runs the same workload independently
+(replicas; the path has no exchange step on one node's data here).
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+FALLBACK_HBM_GBS = 6800.0
+PROFILE_DIR = os.path.join(ROOT, "profiles")
+METRIC = "norm fwd/bwd effective HBM GB/s (+rows/s) and % of GB300 8 TB/s peak, 1 GPU"
+
+
+# ------------------------------------------------------------------ helpers
+def hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        try:
+            d = json.load(open(path))
+            flat = {}
+
+            def walk(o, pre=""):
+                if isinstance(o, dict):
+                    for k, v in o.items():
+                        walk(v, f"{pre}{k}.")
+                else:
+                    flat[pre[:-1]] = o
+            walk(d)
+            for k, v in flat.items():
+                if "hbm" in k.lower() and isinstance(v, (int, float)) and v > 100:
+                    return float(v), "measured", k
+        except Exception:
+            pass
+    return FALLBACK_HBM_GBS, "fallback", None
+
+
+def algorithmic_bytes(kind, N, H, esz, ln, extra=None):
+    """Bytes every kernel must move at least once (inputs read, outputs written)."""
+    E = N * H
+    vec = H * 4 * (2 if ln else 1)          # gamma (+ beta) fp32
+    stats = N * 4 * (2 if ln else 1)        # mu (+) rsigma fp32
+    if kind == "fwd_none":
+        return E * esz + E * esz + vec + stats
+    if kind == "fwd_fp8":                    # x in, codes out
+        return E * esz + E * 1 + vec + stats
+    if kind == "fwd_fp8_current":            # x read twice (amax pass, quantize pass)
+        return 2 * E * esz + E * 1 + vec + 2 * stats
+    if kind == "fwd_mxfp8":                  # x in, row + col codes and scales out
+        return E * esz + 2 * E + 2 * (E // 32) + vec + stats
+    if kind == "bwd":                        # dz, x in, dx out, dgamma (+dbeta) out
+        return 3 * E * esz + stats + H * 4 + vec
+    raise ValueError(kind)
+
+
+def kernel_source_hash(files):
+    h = hashlib.sha256()
+    for f in files:
+        h.update(open(os.path.join(ROOT, "mxfp8_quantization_gb300", "csrc", f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def profile_traffic(name, files):
+    """dram bytes per launch from a committed ncu summary, if the kernel
+    source still matches the hash recorded with it; else None."""
+    path = os.path.join(PROFILE_DIR, name)
+    if not os.path.exists(path):
+        return None
+    txt = open(path).read()
+    m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", txt)
+    hsh = re.search(r"source_hash:\s*([0-9a-f]+)", txt)
+    if not m or not hsh or hsh.group(1) != kernel_source_hash(files):
+        return None
+    return float(m.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling in the background."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.t0 = self.t1 = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-i", str(self.gpu), "-lms", "20"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+
+    def mark(self, which):
+        setattr(self, which, time.time())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.1)
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=5)
+        rows = [r.split(", ") for r in out.strip().splitlines() if r.count(",") >= 8]
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            for n, v in zip(names, r[5:9]):
+                if v.strip().lower() in ("active", "1"):
+                    reasons.add(n)
+        # samples are taken every 20 ms across warm-up and the timed loop;
+        # the loop itself is short, so all samples under load are reported
+        loaded = [s for s in sm if s > 0]
+        return {"sm_mhz": statistics.median(loaded) if loaded else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": sorted(reasons),
+                "samples": len(rows)}
+
+
+# ---------------------------------------------------------------- our arm
+class Prepared:
+    """Device buffers and ctypes argument lists for repeated C-ABI calls."""
+
+    def __init__(self, rn, torch, w, ln=True):
+        self.rn, self.torch, self.w, self.ln = rn, torch, w, ln
+        dev = "cuda"
+        bf16 = w.dtype == "bf16"
+        tdt = torch.bfloat16 if bf16 else torch.float32
+        to = (lambda a: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(dev)) if bf16 \
+            else (lambda a: torch.from_numpy(a).to(dev))
+        self.x = to(w.x)
+        self.dz = to(w.dz) if w.dz is not None else None
+        self.gamma = torch.from_numpy(w.gamma).to(dev)
+        self.beta = torch.from_numpy(w.beta).to(dev) if (ln and w.beta is not None) else None
+        N, H = w.N, w.H
+        self.N, self.H, self.esz = N, H, (2 if bf16 else 4)
+        self.mu = torch.empty(N, dtype=torch.float32, device=dev)
+        self.rs = torch.empty(N, dtype=torch.float32, device=dev)
+        self.dtype_code = 0 if bf16 else 1
+        self.tdt = tdt
+
+    def stream(self):
+        return ctypes.c_void_p(self.torch.cuda.current_stream().cuda_stream)
+
+    def fwd_args(self, mode, scale=None):
+        rn, torch = self.rn, self.torch
+        o = rn._Output()
+        N, H = self.N, self.H
+        keep = []
+        if mode == "fp8_delayed":
+            data = torch.empty((N, H), dtype=torch.uint8, device="cuda")
+            self.scale_t = torch.tensor([scale], dtype=torch.float32, device="cuda")
+            sinv = torch.empty(1, dtype=torch.float32, device="cuda")
+            amax = torch.empty(1, dtype=torch.float32, device="cuda")
+            o.data, o.scale, o.scale_inv, o.amax = (data.data_ptr(), self.scale_t.data_ptr(),
+                                                    sinv.data_ptr(), amax.data_ptr())
+            keep = [data, sinv, amax]
+        elif mode == "fp8_current":
+            data = torch.empty((N, H), dtype=torch.uint8, device="cuda")
+            sc, sinv, amax = (torch.empty(1, dtype=torch.float32, device="cuda") for _ in range(3))
+            o.data, o.scale_out, o.scale_inv, o.amax = (data.data_ptr(), sc.data_ptr(),
+                                                        sinv.data_ptr(), amax.data_ptr())
+            keep = [data, sc, sinv, amax]
+        elif mode == "mxfp8":
+            d = torch.empty((N, H), dtype=torch.uint8, device="cuda")
+            rsc = torch.empty((N, H // 32), dtype=torch.uint8, device="cuda")
+            cd = torch.empty((H, N), dtype=torch.uint8, device="cuda")
+            csc = torch.empty((H, N // 32), dtype=torch.uint8, device="cuda")
+            o.data, o.row_scales, o.col_data, o.col_scales = (d.data_ptr(), rsc.data_ptr(),
+                                                              cd.data_ptr(), csc.data_ptr())
+            keep = [d, rsc, cd, csc]
+        else:
+            data = torch.empty((N, H), dtype=self.tdt, device="cuda")
+            o.data, o.out_dtype = data.data_ptr(), self.dtype_code
+            keep = [data]
+        self.fwd_keep = keep
+        self.fwd_out = o
+        mcode = rn.QUANT_MODES[mode]
+        w = self.w
+        vp = ctypes.c_void_p
+        if self.ln:
+            return ("rn_layernorm_fwd",
+                    [vp(self.x.data_ptr()), self.dtype_code, vp(self.gamma.data_ptr()),
+                     vp(self.beta.data_ptr()) if self.beta is not None else None, N, H,
+                     ctypes.c_float(w.eps), int(w.zero_centered_gamma), 0, mcode,
+                     ctypes.byref(o), vp(self.mu.data_ptr()), vp(self.rs.data_ptr())])
+        return ("rn_rmsnorm_fwd",
+                [vp(self.x.data_ptr()), self.dtype_code, vp(self.gamma.data_ptr()), N, H,
+                 ctypes.c_float(w.eps), int(w.zero_centered_gamma), 0, mcode, ctypes.byref(o),
+                 vp(self.rs.data_ptr())])
+
+    def bwd_args(self, sm_margin=0):
+        rn, torch = self.rn, self.torch
+        N, H = self.N, self.H
+        need = rn.bwd_workspace_bytes(N, H, self.tdt, self.ln)
+        self.ws = torch.empty(max(need, 16), dtype=torch.uint8, device="cuda")
+        self.wsn = ctypes.c_size_t(self.ws.numel())
+        self.dx = torch.empty((N, H), dtype=self.tdt, device="cuda")
+        self.dg = torch.empty(H, dtype=torch.float32, device="cuda")
+        self.db = torch.empty(H, dtype=torch.float32, device="cuda")
+        vp = ctypes.c_void_p
+        w = self.w
+        if self.ln:
+            return ("rn_layernorm_bwd",
+                    [vp(self.dz.data_ptr()), vp(self.x.data_ptr()), self.dtype_code,
+                     vp(self.mu.data_ptr()), vp(self.rs.data_ptr()), vp(self.gamma.data_ptr()), N, H,
+                     int(w.zero_centered_gamma), sm_margin, vp(self.dx.data_ptr()),
+                     vp(self.dg.data_ptr()), vp(self.db.data_ptr()), vp(self.ws.data_ptr()),
+                     ctypes.byref(self.wsn)])
+        return ("rn_rmsnorm_bwd",
+                [vp(self.dz.data_ptr()), vp(self.x.data_ptr()), self.dtype_code,
+                 vp(self.rs.data_ptr()), vp(self.gamma.data_ptr()), N, H,
+                 int(w.zero_centered_gamma), sm_margin, vp(self.dx.data_ptr()),
+                 vp(self.dg.data_ptr()), vp(self.ws.data_ptr()), ctypes.byref(self.wsn)])
+
+
+def call(lib, fa, stream):
+    fn, args = fa
+    st = getattr(lib, fn)(*args, stream)
+    if st != 0:
+        raise RuntimeError(f"{fn} failed with status {st}")
+
+
+def time_calls(torch, lib, calls, steps, warmup, flush):
+    """Time each call in `calls` (list of (name, fa)) per step with CUDA events
+    on the launching stream; L2 is flushed before every call (untimed)."""
+    s = torch.cuda.current_stream()
+    stream = ctypes.c_void_p(s.cuda_stream)
+    for _ in range(warmup):
+        for _, fa in calls:
+            flush()
+            call(lib, fa, stream)
+    torch.cuda.synchronize()
+    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in calls] for _ in range(steps)]
+    for k in range(steps):
+        for (name, fa), (a, b) in zip(calls, ev[k]):
+            flush()
+            a.record(s)
+            call(lib, fa, stream)
+            b.record(s)
+    torch.cuda.synchronize()
+    return {name: [ev[k][i][0].elapsed_time(ev[k][i][1]) for k in range(steps)]
+            for i, (name, _) in enumerate(calls)}
+
+
+def run_rn(args):
+    import torch
+    import torch.distributed as dist
+
+    import mxfp8_quantization_gb300 as rn
+    import rn_inputs
+    from mxfp8_quantization_gb300 import _build
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl")
+    if rank == 0 or world == 1:
+        _build.build()
+    if world > 1:
+        dist.barrier()
+    lib = rn._load()
+
+    l2 = torch.cuda.get_device_properties(local).L2_cache_size
+    flush_buf = torch.empty(2 * l2, dtype=torch.uint8, device="cuda")
+
+    def flush():
+        flush_buf.fill_(1)
+
+    peak, peak_kind, peak_key = hbm_peak()
+
+    # ---------------------------------------------------- headline workload
+    w = rn_inputs.make("ln_delayed")
+    N, H = w.N, w.H
+    P = Prepared(rn, torch, w, ln=True)
+    fwd = P.fwd_args("fp8_delayed", scale=w.scale)
+    bwd = P.bwd_args()
+    sampler = ClockSampler(local)
+    sampler.start()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t_wall0 = time.time()
+    times = time_calls(torch, lib, [("fwd", fwd), ("bwd", bwd)], args.steps, args.warmup, flush)
+    t_wall = time.time() - t_wall0
+    clocks = sampler.stop()
+    fwd_ms = statistics.mean(times["fwd"])
+    bwd_ms = statistics.mean(times["bwd"])
+    ms_step = fwd_ms + bwd_ms
+    if world > 1:
+        t = torch.tensor([ms_step, fwd_ms, bwd_ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_step, fwd_ms, bwd_ms = (float(v) for v in t.tolist())
+    b_fwd = algorithmic_bytes("fwd_fp8", N, H, 2, True)
+    b_bwd = algorithmic_bytes("bwd", N, H, 2, True)
+    step_bytes = b_fwd + b_bwd
+    value = world * step_bytes / (ms_step * 1e-3) / 1e9
+
+    # ------------------------------------------------ end to end, host data
+    e2e = None
+    if rank == 0:
+        e2e = run_e2e(torch, lib, P, fwd, bwd, w, max(3, min(args.steps, 20)), step_bytes)
+
+    # ------------------------------------------------------ other workloads
+    extra = {}
+    if not args.quick and rank == 0:
+        extra = run_other_workloads(torch, rn, lib, rn_inputs, flush, peak,
+                                    max(3, min(args.steps, 20)), args.warmup)
+
+    if rank != 0:
+        if world > 1:
+            dist.barrier()
+            dist.destroy_process_group()
+        return
+    cpu = cpu_baseline(w, step_bytes) if not args.no_cpu else None
+    bwd_gbs = b_bwd / (bwd_ms * 1e-3) / 1e9
+    fwd_gbs = b_fwd / (fwd_ms * 1e-3) / 1e9
+    traffic = profile_traffic("rn_bwd_ln_bf16_8192x4096.md", ["rn_bwd.cu", "rn_device.cuh"])
+    line = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_step, 6),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded rn_inputs workload ln_delayed)",
+        "config": {"workload": "LayerNorm fwd (fused FP8 E4M3 delayed scaling, zero-centered gamma) "
+                               "+ bwd, x/dz bf16 [8192 x 4096]",
+                   "rows": N, "hidden": H, "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
+                   "l2": "flushed (2x L2 write) before every fwd and bwd call, outside the timed events",
+                   "rows_per_s": round(world * N / (ms_step * 1e-3), 1),
+                   "fwd_ms": round(fwd_ms, 6), "bwd_ms": round(bwd_ms, 6),
+                   "fwd_GBps": round(fwd_gbs, 1), "bwd_GBps": round(bwd_gbs, 1),
+                   "algorithmic_bytes_per_step": step_bytes,
+                   "pct_of_8TBps": round(100 * value / world / 8000.0, 2),
+                   "wall_s_timed_loop": round(t_wall, 3)},
+        "roofline": {"kernel": "rn_layernorm_bwd call (rn_bwd_kernel + rn_colreduce_kernel)",
+                     "bound": "hbm", "achieved": round(bwd_gbs, 1), "peak": peak,
+                     "peak_kind": f"{peak_kind}" + (f" ({peak_key})" if peak_key else ""),
+                     "unit": "GB/s", "frac": round(bwd_gbs / peak, 4),
+                     "traffic": traffic, "algorithmic_bytes": b_bwd},
+        "roofline_fwd": {"kernel": "rn_layernorm_fwd call (rn_fwd_kernel, FP8 delayed)",
+                         "bound": "hbm", "achieved": round(fwd_gbs, 1), "peak": peak,
+                         "unit": "GB/s", "frac": round(fwd_gbs / peak, 4),
+                         "traffic": profile_traffic("rn_fwd_ln_fp8_delayed_bf16_8192x4096.md",
+                                                    ["rn_fwd.cu", "rn_device.cuh"]),
+                         "algorithmic_bytes": b_fwd},
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": 3 * args.steps,
+        "clocks": clocks,
+        "workloads": extra,
+    }
+    print(json.dumps(line))
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def run_e2e(torch, lib, P, fwd, bwd, w, steps, step_bytes):
+    """Same step through the C ABI with host data: pinned-host inputs copied
+    in and the step's results copied out inside the timed region."""
+    hx = torch.empty(P.x.shape, dtype=P.x.dtype, pin_memory=True)
+    hx.copy_(P.x.cpu())
+    hdz = torch.empty(P.dz.shape, dtype=P.dz.dtype, pin_memory=True)
+    hdz.copy_(P.dz.cpu())
+    hg = P.gamma.cpu().pin_memory()
+    hb = P.beta.cpu().pin_memory()
+    outs = [P.fwd_keep[0], P.mu, P.rs, P.fwd_keep[2], P.dx, P.dg, P.db]
+    houts = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs]
+    s = torch.cuda.current_stream()
+    stream = ctypes.c_void_p(s.cuda_stream)
+    h2d = sum(t.numel() * t.element_size() for t in (hx, hdz, hg, hb))
+    d2h = sum(t.numel() * t.element_size() for t in outs)
+
+    def step():
+        P.x.copy_(hx, non_blocking=True)
+        P.dz.copy_(hdz, non_blocking=True)
+        P.gamma.copy_(hg, non_blocking=True)
+        P.beta.copy_(hb, non_blocking=True)
+        call(lib, fwd, stream)
+        call(lib, bwd, stream)
+        for d, h in zip(outs, houts):
+            h.copy_(d, non_blocking=True)
+
+    for _ in range(2):
+        step()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(s)
+    for _ in range(steps):
+        step()
+    b.record(s)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / steps
+    return {"value": round(step_bytes / (ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+            "ms_per_step": round(ms, 4), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+
+def run_other_workloads(torch, rn, lib, rn_inputs, flush, peak, steps, warmup):
+    res = {}
+
+    def report(name, kind, N, H, esz, ln, ms, launches):
+        b = algorithmic_bytes(kind, N, H, esz, ln)
+        gbs = b / (ms * 1e-3) / 1e9
+        res[name] = {"ms": round(ms, 5), "GBps": round(gbs, 1), "rows_per_s": round(N / (ms * 1e-3), 1),
+                     "frac_of_peak": round(gbs / peak, 4), "pct_of_8TBps": round(gbs / 80.0, 2),
+                     "algorithmic_bytes": b, "kernels_per_call": launches}
+
+    w = rn_inputs.make("rms_small")
+    P = Prepared(rn, torch, w, ln=False)
+    calls = [("none", P.fwd_args("none"))]
+    t = time_calls(torch, lib, calls, steps, warmup, flush)
+    report("rms_256x1024_fwd_none", "fwd_none", w.N, w.H, 2, False, statistics.mean(t["none"]), 1)
+    calls = [("dl", P.fwd_args("fp8_delayed", scale=w.scale)), ("bwd", P.bwd_args())]
+    t = time_calls(torch, lib, calls, steps, warmup, flush)
+    report("rms_256x1024_fwd_fp8_delayed", "fwd_fp8", w.N, w.H, 2, False, statistics.mean(t["dl"]), 1)
+    report("rms_256x1024_bwd", "bwd", w.N, w.H, 2, False, statistics.mean(t["bwd"]), 2)
+    del P
+
+    w = rn_inputs.make("rms_current")
+    P = Prepared(rn, torch, w, ln=False)
+    t = time_calls(torch, lib, [("cur", P.fwd_args("fp8_current"))], steps, warmup, flush)
+    report("rms_16384x8192_fwd_fp8_current", "fwd_fp8_current", w.N, w.H, 2, False,
+           statistics.mean(t["cur"]), 2)
+    del P, w
+
+    w = rn_inputs.make("mxfp8")
+    for ln in (True, False):
+        P = Prepared(rn, torch, w, ln=ln)
+        t = time_calls(torch, lib, [("mx", P.fwd_args("mxfp8"))], steps, warmup, flush)
+        report(f"{'ln' if ln else 'rms'}_65536x2048_fwd_mxfp8", "fwd_mxfp8", w.N, w.H, 2, ln,
+               statistics.mean(t["mx"]), 1)
+        del P
+    del w
+
+    for name in ("bwd_f32", "bwd_bf16"):
+        w = rn_inputs.make(name)
+        esz = 4 if w.dtype == "f32" else 2
+        for ln in (True, False):
+            P = Prepared(rn, torch, w, ln=ln)
+            P.fwd_args("none")
+            call(lib, P.fwd_args("none"), P.stream())      # mu / rsigma for the backward
+            for margin in (0, 16):
+                t = time_calls(torch, lib, [("b", P.bwd_args(margin))], steps, warmup, flush)
+                report(f"{'ln' if ln else 'rms'}_{w.N}x{w.H}_{w.dtype}_bwd_margin{margin}", "bwd",
+                       w.N, w.H, esz, ln, statistics.mean(t["b"]), 2)
+            del P
+        del w
+    torch.cuda.synchronize()
+    return res
+
+
+def cpu_baseline(w, step_bytes):
+    """The oracle as it stands, on this host, over the whole headline
+    workload once (fwd + FP8 delayed quantization + bwd)."""
+    import oracle
+    x = w.x_f64()
+    dz = w.dz_f64()
+    t0 = time.time()
+    f = oracle.layernorm_fwd(x, w.gamma, w.beta, w.eps, True, "fp8_delayed", scale=w.scale)
+    oracle.layernorm_bwd(dz, x, f["mu"], f["rsigma"], w.gamma, True, "bf16")
+    dt = time.time() - t0
+    return {"value": round(step_bytes / dt / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"the full workload, {w.N} rows x {w.H}, one fwd+bwd pass ({dt:.1f} s, "
+                      "numpy fp64, one thread)"}
+
+
+# ---------------------------------------------------------- reference arm
+def run_reference(args):
+    """The oracle (the only reference this method has here) on host cores;
+    each step is a bounded 32-row sample of the headline workload."""
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import oracle
+    import rn_inputs
+    w = rn_inputs.make("ln_delayed")
+    rows = 32
+    per_sample = algorithmic_bytes("fwd_fp8", rows, w.H, 2, True) + algorithmic_bytes("bwd", rows, w.H, 2, True)
+
+    def step(k):
+        r0 = (k * rows) % w.N
+        sl = slice(r0, r0 + rows)
+        x = w.x_f64(sl)
+        dz = w.dz_f64(sl)
+        f = oracle.layernorm_fwd(x, w.gamma, w.beta, w.eps, True, "fp8_delayed", scale=w.scale)
+        oracle.layernorm_bwd(dz, x, f["mu"], f["rsigma"], w.gamma, True, "bf16")
+
+    for k in range(args.warmup):
+        step(k)
+    t0 = time.time()
+    for k in range(args.steps):
+        step(k)
+    dt = (time.time() - t0) / args.steps
+    v = per_sample / dt / 1e9
+    line = {"impl": "reference", "metric": METRIC, "value": round(v, 4), "unit": "GB/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(dt * 1e3, 4), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded rn_inputs workload ln_delayed)",
+            "config": {"workload": "LayerNorm fwd (FP8 delayed) + bwd, bf16 [8192 x 4096], "
+                                   f"each step a {rows}-row sample"},
+            "cpu_baseline": {"value": round(v, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                             "sample": f"{rows} rows of 8192 per step"},
+            "e2e": {"value": round(v, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="rn", choices=["rn", "reference"])
+    ap.add_argument("--quick", action="store_true", help="headline workload only")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_rn(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,193 @@
+/*
+ * rn.h — C ABI of a GB300 (sm_103a) library of fused LayerNorm / RMSNorm
+ * kernels with FP8 (E4M3) and MXFP8 output quantization.
+ *
+ * What is computed follows the page "Implementation:NVIDIA TransformerEngine
+ * PyTorch Ext Normalization": forward functions normalize each row of x and
+ * optionally quantize the output, choosing between an unfused path, a fully
+ * fused kernel (delayed-scaling FP8, MXFP8) and a norm+amax-then-quantize
+ * path (current-scaling FP8) (section "Description"); they return the output,
+ * mu (LayerNorm only) and rsigma (section "I/O Contract"); backward functions
+ * return dx, dgamma and dbeta; gamma may be zero-centered; sm_margin leaves
+ * SMs free; calls that need scratch memory follow a two-step protocol (query
+ * the workspace size, allocate, execute).
+ *
+ * Arithmetic (the page gives no formula; standard readings):
+ *   LayerNorm  mu = mean(x), var = mean((x-mu)^2), rsigma = 1/sqrt(var+eps),
+ *              y = (x-mu)*rsigma*g + beta
+ *   RMSNorm    rsigma = 1/sqrt(mean(x^2)+eps), y = x*rsigma*g
+ *   g = 1 + gamma when zero_centered_gamma, else gamma.
+ *   Statistics are accumulated in fp32; y is formed in fp32 ("y32").
+ *   FP8_DELAYED  code = E4M3(fp32(y32*scale)), amax = max|y32| (whole tensor)
+ *   FP8_CURRENT  amax = max|y32|, scale = 448/amax (1 if amax == 0), then as
+ *                FP8_DELAYED; x is read twice (norm+amax pass, quantize pass)
+ *   MXFP8        per block of 32 (1x32 along rows and 32x1 down columns):
+ *                e = floor(log2(max|y32|)) - 8 clamped to [-127,127], stored
+ *                as the E8M0 byte e+127; code = E4M3(y32 * 2^-e)
+ *   E4M3 conversion: round to nearest even, saturate to +-448, NaN -> 0x7F.
+ *
+ * Conventions for every entry point:
+ *   - All tensor arguments are DEVICE pointers, row-major, owned by the
+ *     caller; the library allocates no memory and keeps no state apart from
+ *     per-device attribute caches and a device-side error word.
+ *   - Every call is asynchronous on `stream` (a cudaStream_t; NULL = the
+ *     legacy default stream) and never synchronizes.
+ *   - x is [N, H]; gamma, beta are fp32 [H]; mu, rsigma are fp32 [N].
+ *   - Pointers must be 16-byte aligned; H must be a multiple of 8 for bf16
+ *     and of 4 for fp32.  MXFP8 additionally needs H % 32 == 0 and
+ *     N % 32 == 0.  Violations return RN_ERR_UNSUPPORTED (shape/alignment)
+ *     or RN_ERR_INVALID (missing pointer, bad enum, negative size) before
+ *     anything is launched.
+ *   - 0 <= sm_margin < number of SMs; the persistent grid uses
+ *     (SMs - sm_margin) CTAs.  No result depends on sm_margin.
+ *   - N == 0 is valid and launches nothing (the backward then writes zeros
+ *     to dgamma/dbeta).
+ *   - RN_ERR_CUDA reports a failed launch (cudaGetLastError) or a failed
+ *     device query.
+ */
+#ifndef RN_H_
+#define RN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  RN_QUANT_NONE = 0,        /* unquantized output in out_dtype */
+  RN_QUANT_FP8_DELAYED = 1, /* E4M3 with a caller-given scale */
+  RN_QUANT_FP8_CURRENT = 2, /* E4M3 with scale = 448 / amax of this tensor */
+  RN_QUANT_MXFP8 = 3        /* E4M3 with E8M0 scales per 1x32 and 32x1 block */
+} rn_quant_mode;
+
+typedef enum { RN_BF16 = 0, RN_F32 = 1 } rn_dtype;
+
+typedef enum {
+  RN_OK = 0,
+  RN_ERR_INVALID = 1,     /* bad argument (NULL where required, bad enum) */
+  RN_ERR_UNSUPPORTED = 2, /* valid request this library does not run */
+  RN_ERR_WORKSPACE = 3,   /* workspace missing or smaller than required */
+  RN_ERR_CUDA = 4         /* CUDA runtime error */
+} rn_status;
+
+/*
+ * Output descriptor of the forward calls and rn_quantize_only.  Fields a
+ * mode does not use must be NULL.
+ *   data        NONE: [N, H] in out_dtype.  FP8_*: uint8 E4M3 codes [N, H].
+ *               MXFP8: rowwise uint8 E4M3 codes [N, H].
+ *   row_scales  MXFP8: E8M0 bytes [N, H/32] (scale of data[i, 32b:32b+32]).
+ *   col_data    MXFP8: columnwise codes stored TRANSPOSED, uint8 [H, N]:
+ *               col_data[j, i] is the code of y[i, j] in its 32x1 block.
+ *   col_scales  MXFP8: E8M0 bytes [H, N/32] (scale of col_data[j, 32b:32b+32]).
+ *   scale       FP8_DELAYED: input, device fp32 scalar.
+ *   scale_out   FP8_CURRENT: output, device fp32 scalar (448 / amax).
+ *   scale_inv   FP8_*: output, device fp32 scalar 1/scale (IEEE division).
+ *   amax        FP8_*: output, device fp32 scalar max|y32|; the library
+ *               zeroes it on `stream` before reducing into it.
+ *   out_dtype   NONE only: RN_BF16 or RN_F32 (fp32 returns y32 itself).
+ * MXFP8 may skip either direction: data == NULL skips the rowwise output
+ * (row_scales must then be NULL too), col_data == NULL the columnwise one.
+ */
+typedef struct {
+  void* data;
+  uint8_t* row_scales;
+  uint8_t* col_data;
+  uint8_t* col_scales;
+  const float* scale;
+  float* scale_out;
+  float* scale_inv;
+  float* amax;
+  rn_dtype out_dtype;
+} rn_output;
+
+/*
+ * LayerNorm forward (page section "Signature": layernorm_fwd(input, weight,
+ * bias, eps, quantizer, sm_margin, zero_centered_gamma) -> (output, mu,
+ * rsigma)).  x: [N, H] in x_dtype; gamma, beta: fp32 [H]; writes *out per
+ * `mode`, mu and rsigma (fp32 [N]).  No scratch memory is used in any mode,
+ * so the forward takes no workspace.
+ */
+rn_status rn_layernorm_fwd(const void* x, rn_dtype x_dtype, const float* gamma,
+                           const float* beta, int64_t N, int64_t H, float eps,
+                           int zero_centered_gamma, int sm_margin,
+                           rn_quant_mode mode, const rn_output* out, float* mu,
+                           float* rsigma, void* stream);
+
+/*
+ * RMSNorm forward (page: rmsnorm_fwd(input, weight, eps, quantizer,
+ * sm_margin, zero_centered_gamma); mu is "LayerNorm only").  As
+ * rn_layernorm_fwd without beta and mu.
+ */
+rn_status rn_rmsnorm_fwd(const void* x, rn_dtype x_dtype, const float* gamma,
+                         int64_t N, int64_t H, float eps,
+                         int zero_centered_gamma, int sm_margin,
+                         rn_quant_mode mode, const rn_output* out,
+                         float* rsigma, void* stream);
+
+/*
+ * LayerNorm backward (page: layernorm_bwd(dz, x, mu, rsigma, gamma,
+ * sm_margin, zero_centered_gamma) -> (dx, dgamma, dbeta)).
+ *   dz, x, dx: [N, H] in `dtype`; mu, rsigma: the forward's fp32 [N];
+ *   gamma: fp32 [H] (stored value; zero_centered_gamma as in the forward);
+ *   dgamma, dbeta: fp32 [H], overwritten.
+ * dgamma/dbeta are reduced in two deterministic stages: fixed row chunks
+ * (their size depends on N and H only) write fp32 partial sums into the
+ * workspace, then a second kernel adds the chunks in index order.  Results
+ * are bitwise reproducible and independent of sm_margin.
+ * Workspace protocol: with workspace == NULL the call only stores the
+ * required byte count in *workspace_bytes and returns RN_OK; otherwise
+ * *workspace_bytes must hold the size of `workspace` (16-byte aligned,
+ * caller-owned, contents need not be initialized); too small ->
+ * RN_ERR_WORKSPACE.  The workspace must not be shared by calls that may run
+ * concurrently.
+ */
+rn_status rn_layernorm_bwd(const void* dz, const void* x, rn_dtype dtype,
+                           const float* mu, const float* rsigma,
+                           const float* gamma, int64_t N, int64_t H,
+                           int zero_centered_gamma, int sm_margin, void* dx,
+                           float* dgamma, float* dbeta, void* workspace,
+                           size_t* workspace_bytes, void* stream);
+
+/*
+ * RMSNorm backward (page: rmsnorm_bwd(dz, x, rsigma, gamma, sm_margin,
+ * zero_centered_gamma) -> (dx, dgamma)).  As rn_layernorm_bwd without mu
+ * and dbeta.
+ */
+rn_status rn_rmsnorm_bwd(const void* dz, const void* x, rn_dtype dtype,
+                         const float* rsigma, const float* gamma, int64_t N,
+                         int64_t H, int zero_centered_gamma, int sm_margin,
+                         void* dx, float* dgamma, void* workspace,
+                         size_t* workspace_bytes, void* stream);
+
+/*
+ * Quantization stage alone on caller-given fp32 values y [N, H] (the
+ * page's UNFUSED path: norm, then a separate quantize).  Same output
+ * descriptor and arithmetic as the fused forward for `mode`
+ * (FP8_DELAYED, FP8_CURRENT or MXFP8); lets the quantizer be checked bit
+ * for bit on arbitrary fp32 inputs.
+ */
+rn_status rn_quantize_only(const float* y, int64_t N, int64_t H,
+                           rn_quant_mode mode, const rn_output* out,
+                           void* stream);
+
+/* Static message for a status code. */
+const char* rn_status_str(rn_status s);
+
+/*
+ * Reads and clears the device-side error word of the current device
+ * (synchronizes the device).  Kernels never trap: a pipeline wait that
+ * exceeds its time limit records a nonzero code here and the kernel runs
+ * to completion.  *code = 0 means no error was recorded.
+ */
+rn_status rn_device_error(unsigned int* code);
+
+/* ABI version of this header (increments on incompatible change). */
+int rn_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* RN_H_ */

@@ -1,0 +1,435 @@
+// C ABI of the library (declared in include/rn.h): argument validation,
+// launch planning and dispatch.  Everything here runs on the host and
+// checks every argument before anything is enqueued.
+#include <atomic>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "rn_internal.h"
+
+namespace rn {
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::atomic<int> g_sms[kMaxDevices];
+std::atomic<int> g_smem[kMaxDevices];
+
+constexpr int kMaxConsumers = 512;
+constexpr int kBwdTileRows = 8;
+constexpr int kBwdTargetChunks = 1024;  // chunks per call, roughly
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int round_up(int v, int m) { return (v + m - 1) / m * m; }
+
+int elem_size(rn_dtype d) { return d == RN_BF16 ? 2 : 4; }
+
+bool dtype_ok(rn_dtype d) { return d == RN_BF16 || d == RN_F32; }
+
+// x rows must be whole 16-byte chunks (bulk copies and vector loads)
+bool row_ok(int64_t H, rn_dtype d) { return (H * elem_size(d)) % 16 == 0; }
+
+// smallest group count in {1, 2, 4} that keeps the consumer threads <= cap
+int pick_ng(int nchunks, int cap, int max_ng) {
+  for (int ng = 1; ng <= max_ng; ng *= 2)
+    if ((nchunks + ng - 1) / ng <= cap) return ng;
+  return 0;
+}
+
+}  // namespace
+
+rn_status device_info(DeviceInfo* out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return RN_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return RN_ERR_UNSUPPORTED;
+  int sms = g_sms[dev].load(std::memory_order_relaxed);
+  int smem = g_smem[dev].load(std::memory_order_relaxed);
+  if (sms <= 0 || smem <= 0) {
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return RN_ERR_CUDA;
+    if (cudaDeviceGetAttribute(&smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+      return RN_ERR_CUDA;
+    g_sms[dev].store(sms, std::memory_order_relaxed);
+    g_smem[dev].store(smem, std::memory_order_relaxed);
+  }
+  out->sms = sms;
+  out->smem_optin = smem;
+  return RN_OK;
+}
+
+namespace {
+
+// ---------------------------------------------------------------- planning
+struct RowPlan {
+  int ng, T, wpr, Q;
+  Launch l;
+};
+
+// rows per tile: start from one row per consumer warp (at least 8) and
+// halve while the tile would take more than a third of the ring, so that
+// rows keep streaming in while a tile is being worked on
+int pick_tile(int w, int q) {
+  int T = w > 8 ? w : 8;
+  while (T > 1 && 3 * T > q) T /= 2;
+  return T;
+}
+
+// row-wise forward: ring of Q row slots, tiles of T rows
+rn_status plan_fwd(int H, int esz, int N, int sm_margin, const DeviceInfo& di, RowPlan* pl) {
+  const int vec = 16 / esz;
+  const int nchunks = H / vec;
+  const int ng = pick_ng(nchunks, kMaxConsumers, 4);
+  if (ng == 0) return RN_ERR_UNSUPPORTED;
+  const int th = round_up((nchunks + ng - 1) / ng, 32);
+  const int w = th / 32;
+  const size_t row_bytes = (size_t)H * esz;
+  // worst-case fixed part: stats [2][32] float2, slice partials [32] float4,
+  // amax scratch, alignment slack
+  const size_t fixed = 2 * 32 * sizeof(float2) + 32 * 16 + 32 * sizeof(uint32_t) + 64;
+  const size_t avail = (size_t)di.smem_optin > fixed ? di.smem_optin - fixed : 0;
+  int Q = (int)(avail / (row_bytes + 16));
+  if (Q > 128) Q = 128;
+  if (Q < 2) return RN_ERR_UNSUPPORTED;
+  const int T = pick_tile(w, Q);
+  pl->ng = ng;
+  pl->T = T;
+  pl->wpr = w > T ? w / T : 1;
+  pl->Q = Q;
+  pl->l.threads = th + 32;
+  pl->l.smem = (size_t)Q * row_bytes + fixed + (size_t)Q * 16;
+  const int n_tiles = (N + T - 1) / T;
+  const int g = di.sms - sm_margin;
+  pl->l.grid = n_tiles < g ? (n_tiles > 0 ? n_tiles : 1) : g;
+  return RN_OK;
+}
+
+rn_status plan_mx(int H, int esz, int N, int sm_margin, const DeviceInfo& di, RowPlan* pl) {
+  const int nchunks = H / 4;
+  const int ng = pick_ng(nchunks, kMaxConsumers, 2);
+  if (ng == 0) return RN_ERR_UNSUPPORTED;
+  const int th = round_up((nchunks + ng - 1) / ng, 32);
+  const size_t row_bytes = (size_t)H * esz;
+  const size_t fixed = 2 * 32 * sizeof(float2) + 64;
+  const size_t avail = (size_t)di.smem_optin > fixed ? di.smem_optin - fixed : 0;
+  int Q = (int)(avail / (row_bytes + 16));
+  if (Q > 128) Q = 128;
+  if (Q < 33) return RN_ERR_UNSUPPORTED;
+  pl->ng = ng;
+  pl->T = 32;
+  pl->Q = Q;
+  pl->l.threads = th + 32;
+  pl->l.smem = (size_t)Q * row_bytes + fixed + (size_t)Q * 16;
+  const int n_tiles = N / 32;
+  const int g = di.sms - sm_margin;
+  pl->l.grid = n_tiles < g ? (n_tiles > 0 ? n_tiles : 1) : g;
+  return RN_OK;
+}
+
+// backward chunking: a chunk is R = 8 * max(1, N / 8192) rows, a function
+// of N only (never of the grid or the device), so the dgamma/dbeta partials
+// and their sum are independent of sm_margin; a tile (T rows, T | 8) never
+// straddles two chunks
+struct BwdShape {
+  int ng, th, chunk_rows, n_chunks;
+};
+
+rn_status bwd_shape(int64_t N, int64_t H, int esz, BwdShape* s) {
+  const int vec = 16 / esz;
+  const int nchunks = (int)(H / vec);
+  const int ng = pick_ng(nchunks, 256, 4);
+  if (ng == 0) return RN_ERR_UNSUPPORTED;
+  s->ng = ng;
+  s->th = round_up((nchunks + ng - 1) / ng, 32);
+  const int64_t m = N / (int64_t)(kBwdTileRows * kBwdTargetChunks);
+  s->chunk_rows = kBwdTileRows * (int)(m < 1 ? 1 : m);
+  s->n_chunks = (int)((N + s->chunk_rows - 1) / s->chunk_rows);
+  return RN_OK;
+}
+
+size_t bwd_workspace(const BwdShape& s, int64_t H, bool ln) {
+  return (size_t)s.n_chunks * (ln ? 2 : 1) * (size_t)H * sizeof(float);
+}
+
+// ---------------------------------------------------------------- checks
+bool out_fields_only(const rn_output* o, bool data, bool rs, bool cd, bool cs, bool sc, bool so,
+                     bool si, bool am) {
+  return (o->data != nullptr) == data && (o->row_scales != nullptr) == rs &&
+         (o->col_data != nullptr) == cd && (o->col_scales != nullptr) == cs &&
+         (o->scale != nullptr) == sc && (o->scale_out != nullptr) == so &&
+         (o->scale_inv != nullptr) == si && (o->amax != nullptr) == am;
+}
+
+rn_status check_out(rn_quant_mode mode, const rn_output* o, int64_t N, int64_t H) {
+  if (o == nullptr) return RN_ERR_INVALID;
+  switch (mode) {
+    case RN_QUANT_NONE:
+      if (!out_fields_only(o, true, false, false, false, false, false, false, false))
+        return RN_ERR_INVALID;
+      if (o->out_dtype != RN_BF16 && o->out_dtype != RN_F32) return RN_ERR_INVALID;
+      break;
+    case RN_QUANT_FP8_DELAYED:
+      if (!out_fields_only(o, true, false, false, false, true, false, true, true))
+        return RN_ERR_INVALID;
+      break;
+    case RN_QUANT_FP8_CURRENT:
+      if (!out_fields_only(o, true, false, false, false, false, true, true, true))
+        return RN_ERR_INVALID;
+      break;
+    case RN_QUANT_MXFP8: {
+      const bool rowwise = o->data != nullptr, colwise = o->col_data != nullptr;
+      if (!rowwise && !colwise) return RN_ERR_INVALID;
+      if (!out_fields_only(o, rowwise, rowwise, colwise, colwise, false, false, false, false))
+        return RN_ERR_INVALID;
+      if (H % 32 != 0 || N % 32 != 0) return RN_ERR_UNSUPPORTED;
+      if (colwise && !aligned(o->col_data, 16)) return RN_ERR_UNSUPPORTED;
+      break;
+    }
+    default:
+      return RN_ERR_INVALID;
+  }
+  if (o->data != nullptr && !aligned(o->data, 16)) return RN_ERR_UNSUPPORTED;
+  if (o->amax && !aligned(o->amax, 4)) return RN_ERR_UNSUPPORTED;
+  return RN_OK;
+}
+
+rn_status check_margin(int sm_margin, const DeviceInfo& di) {
+  return (sm_margin < 0 || sm_margin >= di.sms) ? RN_ERR_INVALID : RN_OK;
+}
+
+// ---------------------------------------------------------------- forward
+rn_status fwd_common(int nk, const void* x, rn_dtype dt, const float* gamma, const float* beta,
+                     int64_t N, int64_t H, float eps, int zcg, int sm_margin, rn_quant_mode mode,
+                     const rn_output* out, float* mu, float* rsigma, cudaStream_t stream) {
+  if (x == nullptr || !dtype_ok(dt) || N < 0 || H < 1 || N > INT32_MAX || H > INT32_MAX)
+    return RN_ERR_INVALID;
+  if (nk != kIdentity && (gamma == nullptr || rsigma == nullptr)) return RN_ERR_INVALID;
+  if (nk == kLn && mu == nullptr) return RN_ERR_INVALID;
+  if (nk == kIdentity && mode == RN_QUANT_NONE) return RN_ERR_INVALID;
+  rn_status st = check_out(mode, out, N, H);
+  if (st != RN_OK) return st;
+  if (!row_ok(H, dt) || !aligned(x, 16)) return RN_ERR_UNSUPPORTED;
+  if ((gamma && !aligned(gamma, 4)) || (beta && !aligned(beta, 4)) ||
+      (mu && !aligned(mu, 4)) || (rsigma && !aligned(rsigma, 4)))
+    return RN_ERR_UNSUPPORTED;
+  DeviceInfo di;
+  if ((st = device_info(&di)) != RN_OK) return st;
+  if ((st = check_margin(sm_margin, di)) != RN_OK) return st;
+  if (N == 0 && mode == RN_QUANT_NONE) return RN_OK;
+  if (N == 0 && mode == RN_QUANT_MXFP8) return RN_OK;
+  const bool bf16 = dt == RN_BF16;
+  const int esz = elem_size(dt);
+
+  if (mode == RN_QUANT_MXFP8) {
+    RowPlan pl;
+    if ((st = plan_mx((int)H, esz, (int)N, sm_margin, di, &pl)) != RN_OK) return st;
+    MxParams p{};
+    p.x = x;
+    p.gamma = gamma;
+    p.beta = beta;
+    p.data = static_cast<uint8_t*>(out->data);
+    p.row_scales = out->row_scales;
+    p.col_data = out->col_data;
+    p.col_scales = out->col_scales;
+    p.mu = mu;
+    p.rsigma = rsigma;
+    p.N = (int)N;
+    p.H = (int)H;
+    p.eps = eps;
+    p.zcg = zcg ? 1 : 0;
+    p.Q = pl.Q;
+    p.n_tiles = (int)(N / 32);
+    return launch_mx(nk, bf16, pl.ng, p, pl.l, stream);
+  }
+
+  RowPlan pl;
+  if ((st = plan_fwd((int)H, esz, (int)N, sm_margin, di, &pl)) != RN_OK) return st;
+  FwdParams p{};
+  p.x = x;
+  p.gamma = gamma;
+  p.beta = beta;
+  p.out = out->data;
+  p.mu = mu;
+  p.rsigma = rsigma;
+  p.scale = out->scale;
+  p.amax = out->amax;
+  p.scale_inv = out->scale_inv;
+  p.scale_out = out->scale_out;
+  p.N = (int)N;
+  p.H = (int)H;
+  p.eps = eps;
+  p.zcg = zcg ? 1 : 0;
+  p.out_f32 = (mode == RN_QUANT_NONE && out->out_dtype == RN_F32) ? 1 : 0;
+  p.T = pl.T;
+  p.wpr = pl.wpr;
+  p.Q = pl.Q;
+  p.n_tiles = (int)((N + pl.T - 1) / pl.T);
+  p.reverse = 0;
+
+  switch (mode) {
+    case RN_QUANT_NONE:
+      return launch_fwd(nk, bf16, pl.ng, kQNone, p, pl.l, stream);
+    case RN_QUANT_FP8_DELAYED:
+      if (cudaMemsetAsync(out->amax, 0, sizeof(float), stream) != cudaSuccess) return RN_ERR_CUDA;
+      return launch_fwd(nk, bf16, pl.ng, kQDelayed, p, pl.l, stream);
+    case RN_QUANT_FP8_CURRENT:
+      if (cudaMemsetAsync(out->amax, 0, sizeof(float), stream) != cudaSuccess) return RN_ERR_CUDA;
+      if ((st = launch_fwd(nk, bf16, pl.ng, kQCurAmax, p, pl.l, stream)) != RN_OK) return st;
+      p.reverse = 1;
+      return launch_fwd(nk, bf16, pl.ng, kQCurQuant, p, pl.l, stream);
+    default:
+      return RN_ERR_INVALID;
+  }
+}
+
+// ---------------------------------------------------------------- backward
+rn_status bwd_common(bool ln, const void* dz, const void* x, rn_dtype dt, const float* mu,
+                     const float* rsigma, const float* gamma, int64_t N, int64_t H, int zcg,
+                     int sm_margin, void* dx, float* dgamma, float* dbeta, void* ws,
+                     size_t* ws_bytes, cudaStream_t stream) {
+  if (!dtype_ok(dt) || N < 0 || H < 1 || N > INT32_MAX || H > INT32_MAX) return RN_ERR_INVALID;
+  BwdShape sh;
+  rn_status st;
+  if (!row_ok(H, dt)) return RN_ERR_UNSUPPORTED;
+  if ((st = bwd_shape(N, H, elem_size(dt), &sh)) != RN_OK) return st;
+  const size_t need = bwd_workspace(sh, H, ln);
+  if (ws == nullptr) {
+    if (ws_bytes == nullptr) return RN_ERR_INVALID;
+    *ws_bytes = need;
+    return RN_OK;
+  }
+  if (dz == nullptr || x == nullptr || rsigma == nullptr || gamma == nullptr || dx == nullptr ||
+      dgamma == nullptr)
+    return RN_ERR_INVALID;
+  if (ln && (mu == nullptr || dbeta == nullptr)) return RN_ERR_INVALID;
+  if (ws_bytes == nullptr || *ws_bytes < need) return RN_ERR_WORKSPACE;
+  if (!aligned(dz, 16) || !aligned(x, 16) || !aligned(dx, 16) || !aligned(ws, 16) ||
+      !aligned(gamma, 4) || !aligned(rsigma, 4) || (mu && !aligned(mu, 4)) ||
+      !aligned(dgamma, 4) || (dbeta && !aligned(dbeta, 4)))
+    return RN_ERR_UNSUPPORTED;
+  DeviceInfo di;
+  if ((st = device_info(&di)) != RN_OK) return st;
+  if ((st = check_margin(sm_margin, di)) != RN_OK) return st;
+  if (N == 0) {
+    if (cudaMemsetAsync(dgamma, 0, H * sizeof(float), stream) != cudaSuccess) return RN_ERR_CUDA;
+    if (ln && cudaMemsetAsync(dbeta, 0, H * sizeof(float), stream) != cudaSuccess)
+      return RN_ERR_CUDA;
+    return RN_OK;
+  }
+  const int esz = elem_size(dt);
+  const size_t row_bytes = (size_t)H * esz;
+  const size_t fixed = (size_t)H * sizeof(float) + 2 * kBwdTileRows * sizeof(float4) +
+                       32 * sizeof(float2) + 64;
+  const size_t avail = (size_t)di.smem_optin > fixed ? di.smem_optin - fixed : 0;
+  int Q = (int)(avail / (2 * row_bytes + 16));
+  if (Q > 64) Q = 64;
+  if (Q < 2) return RN_ERR_UNSUPPORTED;
+  const int w = sh.th / 32;
+  int T = kBwdTileRows;                   // divides every chunk
+  while (T > 1 && 3 * T > Q) T /= 2;
+  Launch l;
+  l.threads = sh.th + 32;
+  l.smem = (size_t)Q * 2 * row_bytes + fixed + (size_t)Q * 16;
+  const int g = di.sms - sm_margin;
+  l.grid = sh.n_chunks < g ? sh.n_chunks : g;
+
+  BwdParams p{};
+  p.dz = dz;
+  p.x = x;
+  p.mu = mu;
+  p.rsigma = rsigma;
+  p.gamma = gamma;
+  p.dx = dx;
+  p.part = static_cast<float*>(ws);
+  p.N = (int)N;
+  p.H = (int)H;
+  p.zcg = zcg ? 1 : 0;
+  p.T = T;
+  p.wpr = w > T ? w / T : 1;
+  p.tiles_per_chunk = sh.chunk_rows / T;
+  p.Q = Q;
+  p.n_tiles = (int)((N + T - 1) / T);
+  p.n_chunks = sh.n_chunks;
+  if ((st = launch_bwd(ln, dt == RN_BF16, sh.ng, p, l, stream)) != RN_OK) return st;
+  ColReduceParams c{};
+  c.part = p.part;
+  c.dgamma = dgamma;
+  c.dbeta = dbeta;
+  c.H = (int)H;
+  c.n_chunks = sh.n_chunks;
+  c.nacc = ln ? 2 : 1;
+  return launch_colreduce(c, stream);
+}
+
+}  // namespace
+}  // namespace rn
+
+using namespace rn;
+
+extern "C" {
+
+rn_status rn_layernorm_fwd(const void* x, rn_dtype x_dtype, const float* gamma, const float* beta,
+                           int64_t N, int64_t H, float eps, int zero_centered_gamma, int sm_margin,
+                           rn_quant_mode mode, const rn_output* out, float* mu, float* rsigma,
+                           void* stream) {
+  return fwd_common(kLn, x, x_dtype, gamma, beta, N, H, eps, zero_centered_gamma, sm_margin, mode,
+                    out, mu, rsigma, static_cast<cudaStream_t>(stream));
+}
+
+rn_status rn_rmsnorm_fwd(const void* x, rn_dtype x_dtype, const float* gamma, int64_t N, int64_t H,
+                         float eps, int zero_centered_gamma, int sm_margin, rn_quant_mode mode,
+                         const rn_output* out, float* rsigma, void* stream) {
+  return fwd_common(kRms, x, x_dtype, gamma, nullptr, N, H, eps, zero_centered_gamma, sm_margin,
+                    mode, out, nullptr, rsigma, static_cast<cudaStream_t>(stream));
+}
+
+rn_status rn_layernorm_bwd(const void* dz, const void* x, rn_dtype dtype, const float* mu,
+                           const float* rsigma, const float* gamma, int64_t N, int64_t H,
+                           int zero_centered_gamma, int sm_margin, void* dx, float* dgamma,
+                           float* dbeta, void* workspace, size_t* workspace_bytes, void* stream) {
+  return bwd_common(true, dz, x, dtype, mu, rsigma, gamma, N, H, zero_centered_gamma, sm_margin, dx,
+                    dgamma, dbeta, workspace, workspace_bytes, static_cast<cudaStream_t>(stream));
+}
+
+rn_status rn_rmsnorm_bwd(const void* dz, const void* x, rn_dtype dtype, const float* rsigma,
+                         const float* gamma, int64_t N, int64_t H, int zero_centered_gamma,
+                         int sm_margin, void* dx, float* dgamma, void* workspace,
+                         size_t* workspace_bytes, void* stream) {
+  return bwd_common(false, dz, x, dtype, nullptr, rsigma, gamma, N, H, zero_centered_gamma,
+                    sm_margin, dx, dgamma, nullptr, workspace, workspace_bytes,
+                    static_cast<cudaStream_t>(stream));
+}
+
+rn_status rn_quantize_only(const float* y, int64_t N, int64_t H, rn_quant_mode mode,
+                           const rn_output* out, void* stream) {
+  if (mode != RN_QUANT_FP8_DELAYED && mode != RN_QUANT_FP8_CURRENT && mode != RN_QUANT_MXFP8)
+    return RN_ERR_INVALID;
+  return fwd_common(kIdentity, y, RN_F32, nullptr, nullptr, N, H, 0.0f, 0, 0, mode, out, nullptr,
+                    nullptr, static_cast<cudaStream_t>(stream));
+}
+
+const char* rn_status_str(rn_status s) {
+  switch (s) {
+    case RN_OK: return "ok";
+    case RN_ERR_INVALID: return "invalid argument";
+    case RN_ERR_UNSUPPORTED: return "unsupported shape, dtype or alignment";
+    case RN_ERR_WORKSPACE: return "workspace missing or too small";
+    case RN_ERR_CUDA: return "CUDA runtime error";
+    default: return "unknown status";
+  }
+}
+
+rn_status rn_device_error(unsigned int* code) {
+  if (code == nullptr) return RN_ERR_INVALID;
+  if (cudaDeviceSynchronize() != cudaSuccess) return RN_ERR_CUDA;
+  unsigned a = 0, b = 0, c = 0;
+  rn_status st;
+  if ((st = read_clear_error_fwd(&a)) != RN_OK) return st;
+  if ((st = read_clear_error_mx(&b)) != RN_OK) return st;
+  if ((st = read_clear_error_bwd(&c)) != RN_OK) return st;
+  *code = a ? a : (b ? b : c);
+  return RN_OK;
+}
+
+int rn_abi_version(void) { return 1; }
+
+}  // extern "C"

@@ -1,0 +1,184 @@
+// Device-side building blocks shared by the normalization kernels:
+// mbarrier + bulk-copy (TMA engine, non-tensor form) pipeline primitives with
+// bounded waits, numeric conversions (bf16, E4M3, E8M0) and reductions.
+//
+// Every wait here has a time limit: on expiry the kernel records an error
+// code in its translation unit's device error word and carries on, so that a
+// logic error can never hang the GPU.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace rn {
+
+// error codes recorded in the device error word
+enum : unsigned {
+  kErrFullWait = 1,   // a consumer gave up waiting for a row to land
+  kErrEmptyWait = 2,  // the producer gave up waiting for a slot to free
+  kErrDrainWait = 3,  // the producer gave up waiting for its last copies
+};
+
+constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s
+
+__device__ __forceinline__ unsigned long long global_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_barrier_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Wait until the phase with `parity` of barrier `bar` has completed, for at
+// most kWaitLimitNs; on expiry record `code` in *err and return false.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigned* err,
+                                          unsigned code) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = global_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (global_ns() - t0 > kWaitLimitNs) {
+      atomicCAS(err, 0u, code);
+      return false;
+    }
+  }
+  return true;
+}
+
+// One contiguous global -> shared copy by the bulk-copy engine; completion
+// is signalled on `bar` as `bytes` transaction bytes.  dst, src 16-byte
+// aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes,
+                                         uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          dst),
+      "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
+// named barrier over the consumer warps only (id 1; id 0 is __syncthreads)
+__device__ __forceinline__ void consumer_sync(int nthreads) {
+  asm volatile("bar.sync 1, %0;" ::"r"(nthreads) : "memory");
+}
+
+// ------------------------------------------------------------ conversions
+// 8 bf16 (one 16-byte chunk) -> fp32; exact.
+__device__ __forceinline__ void bf16x8_to_f32(const uint4& v, float* f) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    f[2 * i] = __uint_as_float(w[i] << 16);
+    f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+  }
+}
+
+__device__ __forceinline__ void bf16x4_to_f32(const uint2& v, float* f) {
+  f[0] = __uint_as_float(v.x << 16);
+  f[1] = __uint_as_float(v.x & 0xFFFF0000u);
+  f[2] = __uint_as_float(v.y << 16);
+  f[3] = __uint_as_float(v.y & 0xFFFF0000u);
+}
+
+// two fp32 -> packed bf16x2 (round to nearest even); lo in the low half
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// two fp32 -> two E4M3 codes (nearest even, saturating); lo in the low byte
+__device__ __forceinline__ uint32_t pack_e4m3x2(float lo, float hi) {
+  unsigned short r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// four fp32 -> four E4M3 codes in one word, element 0 in the low byte
+__device__ __forceinline__ uint32_t pack_e4m3x4(float a, float b, float c, float d) {
+  return pack_e4m3x2(a, b) | (pack_e4m3x2(c, d) << 16);
+}
+
+// |v| as ordered bits: for non-negative floats and NaN the unsigned order of
+// the bit patterns is the numeric order, with NaN above +inf.
+__device__ __forceinline__ uint32_t abs_bits(float v) {
+  return __float_as_uint(v) & 0x7FFFFFFFu;
+}
+
+// max that lets NaN win (max.NaN), on magnitudes
+__device__ __forceinline__ float amax_acc(float acc, float v) {
+  float r;
+  asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(acc), "f"(fabsf(v)));
+  return r;
+}
+
+// E8M0 shared-scale code of a block with absolute maximum `amax`
+// (OCP MX v1.0 rule for E4M3 elements): e = floor(log2 amax) - 8 clamped to
+// [-127, 127], code = e + 127.  floor(log2) of a normal fp32 is its biased
+// exponent field minus 127, so code = field - 8, clamped to [0, 254]; zero
+// and subnormal amax give 0; NaN gives 0xFF; +inf (field 255) gives 247.
+__device__ __forceinline__ uint32_t e8m0_code(float amax) {
+  const uint32_t b = __float_as_uint(amax) & 0x7FFFFFFFu;
+  if (b > 0x7F800000u) return 0xFFu;
+  const int field = static_cast<int>(b >> 23);
+  const int c = field - 8;
+  return static_cast<uint32_t>(c < 0 ? 0 : c);
+}
+
+// 2^-e for an E8M0 code (e = code - 127), as the fp32 with exponent field
+// 254 - code; codes 0..247 give normal values 2^127 .. 2^-120.  NaN code
+// gives NaN so that the whole block quantizes to NaN.
+__device__ __forceinline__ float e8m0_inv_scale(uint32_t code) {
+  if (code == 0xFFu) return __uint_as_float(0x7FC00000u);
+  return __uint_as_float((254u - code) << 23);
+}
+
+// ------------------------------------------------------------- reductions
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+  return v;
+}
+
+__device__ __forceinline__ uint32_t warp_umax(uint32_t v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = max(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+  return v;
+}
+
+}  // namespace rn

@@ -1,0 +1,119 @@
+// Host-side plumbing shared by the translation units of the library: kernel
+// parameter blocks, launch plans and the per-unit launch functions.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "../../include/rn.h"
+
+namespace rn {
+
+// what a kernel does before quantizing: normalize (RMSNorm / LayerNorm) or
+// take its fp32 input as y already (the stand-alone quantize entry point)
+enum NormKind : int { kRms = 0, kLn = 1, kIdentity = 2 };
+
+// quantization variants of the row-wise forward kernel
+enum FwdQuant : int {
+  kQNone = 0,       // bf16 or fp32 output
+  kQDelayed = 1,    // E4M3 with a given scale, + amax
+  kQCurAmax = 2,    // current scaling, pass 1: statistics + amax, no output
+  kQCurQuant = 3,   // current scaling, pass 2: quantize with 448/amax
+};
+
+struct FwdParams {
+  const void* x;
+  const float* gamma;
+  const float* beta;
+  void* out;            // [N, H] (bf16/fp32 or E4M3 codes)
+  float* mu;            // LayerNorm: written (pass 1) or read (kQCurQuant)
+  float* rsigma;
+  const float* scale;   // kQDelayed
+  float* amax;          // kQDelayed, kQCurAmax: reduced into; kQCurQuant: read
+  float* scale_inv;     // kQDelayed, kQCurQuant
+  float* scale_out;     // kQCurQuant
+  int N, H;
+  float eps;
+  int zcg;              // zero-centered gamma
+  int out_f32;          // kQNone: 1 = fp32 output, 0 = bf16
+  int T;                // rows per tile
+  int wpr;              // warps sharing one row in phase 1
+  int Q;                // ring slots (rows)
+  int n_tiles;
+  int reverse;          // walk the tiles from the last one
+};
+
+struct MxParams {
+  const void* x;
+  const float* gamma;
+  const float* beta;
+  uint8_t* data;        // rowwise codes [N, H] or NULL
+  uint8_t* row_scales;  // [N, H/32]
+  uint8_t* col_data;    // [H, N] or NULL
+  uint8_t* col_scales;  // [H, N/32]
+  float* mu;
+  float* rsigma;
+  int N, H;
+  float eps;
+  int zcg;
+  int Q;
+  int n_tiles;          // N / 32
+};
+
+struct BwdParams {
+  const void* dz;
+  const void* x;
+  const float* mu;
+  const float* rsigma;
+  const float* gamma;
+  void* dx;
+  float* part;          // workspace partials [C][nacc][H]
+  int N, H;
+  int zcg;
+  int T;                // rows per tile
+  int wpr;              // warps sharing one row in phase 1
+  int tiles_per_chunk;  // chunk = tiles_per_chunk * T rows
+  int Q;
+  int n_tiles;
+  int n_chunks;
+};
+
+struct ColReduceParams {
+  const float* part;    // [C][nacc][H]
+  float* dgamma;
+  float* dbeta;
+  int H;
+  int n_chunks;
+  int nacc;
+};
+
+// launch shape shared by the persistent kernels
+struct Launch {
+  int grid;
+  int threads;          // consumer threads + one producer warp
+  size_t smem;
+};
+
+// per-device limits, queried once
+struct DeviceInfo {
+  int sms;
+  int smem_optin;
+};
+rn_status device_info(DeviceInfo* out);
+
+// launch functions (one per translation unit family)
+rn_status launch_fwd(int nk, bool bf16, int ng, int qmode, const FwdParams& p, const Launch& l,
+                     cudaStream_t s);
+rn_status launch_mx(int nk, bool bf16, int ng, const MxParams& p, const Launch& l,
+                    cudaStream_t s);
+rn_status launch_bwd(bool ln, bool bf16, int ng, const BwdParams& p, const Launch& l,
+                     cudaStream_t s);
+rn_status launch_colreduce(const ColReduceParams& p, cudaStream_t s);
+
+// device error words, one per translation unit
+rn_status read_clear_error_fwd(unsigned* code);
+rn_status read_clear_error_mx(unsigned* code);
+rn_status read_clear_error_bwd(unsigned* code);
+
+}  // namespace rn

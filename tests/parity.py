@@ -1,0 +1,133 @@
+"""Element-wise comparison of kernel outputs with the oracle.
+
+Tolerances (from the stated targets; where a target leaves the measure open
+the reading is given here and in the design notes):
+
+* rsigma: relative error <= 1e-5.
+* mu: error <= 1e-5 * mean(|x|) of the row.  A mean can be ~0 while its
+  summands are not, so its relative error is measured against the mean of
+  the magnitudes that were summed (the same normalisation as dgamma below).
+* bf16 outputs: within 1 bf16 ulp of the oracle's correctly rounded value,
+  plus the fp32 evaluation bound 2**-20 * w, where w is the magnitude of the
+  terms that form y (``term_magnitude``); the bound only matters where y
+  cancels to near zero.
+* FP8 codes: equal, except that a code may differ by one step (adjacent
+  values, including +-0) when the oracle's pre-quantization value p lies
+  within 1e-6 * (s * w) of a rounding boundary; such exemptions may cover at
+  most 0.1 % of the elements.  "1e-6 relative" is read relative to the terms
+  whose fp32 sum forms p (s * w), which covers cancellation.
+* MXFP8 E8M0 codes: equal, except where the oracle's block maximum lies
+  within 1e-6 * (block max of w) of a power of two; such blocks are checked
+  only for their exponent being one of the two neighbours.
+* amax (fused): |amax_gpu - amax_ref| <= 1e-6 * max(w); bit-exact in the
+  stand-alone quantizer (identical inputs).
+* dx: fp32 |dx - ref| <= 2e-3 * max(|ref|, rms_row(ref)); bf16 within one bf16
+  ulp of the oracle's rounded value or 2e-3 * rms_row(ref), and every row's
+  norm-wise relative error <= 2e-3.
+* dgamma / dbeta: |err_j| <= 1e-3 * sum_i |dz_ij * xhat_ij| (dbeta:
+  sum_i |dz_ij|), the sum over all N rows ("normalised by the row count").
+"""
+from __future__ import annotations
+
+import numpy as np
+
+import oracle
+
+_MAGS = oracle.e4m3_magnitudes()
+_MIDS = (_MAGS[:-1] + _MAGS[1:]) / 2
+# boundaries of E4M3 rounding in |p|: the midpoints, plus 0 (sign)
+_BOUNDS = np.concatenate([[0.0], _MIDS])
+
+
+def term_magnitude(x64, m, r, gamma, beta, zcg):
+    """w = (|x| + |m|) * r * |g| + |beta| (RMSNorm: |x| * r * |g|), fp64."""
+    g = np.abs(1.0 + gamma.astype(np.float64) if zcg else gamma.astype(np.float64))
+    r = np.asarray(r, np.float64)[:, None]
+    if m is None:
+        w = np.abs(x64) * r * g
+    else:
+        w = (np.abs(x64) + np.abs(np.asarray(m, np.float64))[:, None]) * r * g
+    if beta is not None:
+        w = w + np.abs(beta.astype(np.float64))
+    return w
+
+
+def bf16_ulp(v):
+    a = np.abs(np.asarray(v, np.float64))
+    _, k = np.frexp(np.where(a == 0, 1.0, a))
+    e = np.maximum(k - 1, -126)
+    return np.ldexp(1.0, (e - 7).astype(np.int32))
+
+
+def check_stats(mu_gpu, rs_gpu, x64_rows, mu_ref=None, rs_ref=None):
+    rs_ref = np.asarray(rs_ref, np.float64)
+    rel = np.abs(rs_gpu.astype(np.float64) - rs_ref) / rs_ref
+    assert np.all(rel <= 1e-5), f"rsigma rel err {rel.max():.3e}"
+    if mu_ref is not None:
+        scale = np.mean(np.abs(x64_rows), axis=1)
+        err = np.abs(mu_gpu.astype(np.float64) - np.asarray(mu_ref, np.float64))
+        bad = err > 1e-5 * np.maximum(scale, 1e-300)
+        assert not bad.any(), f"mu err {err[bad][:4]} vs scale {scale[bad][:4]}"
+
+
+def check_bf16(bits_gpu, y_ref64, w):
+    got = (bits_gpu.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    ref = oracle.round_to_bf16(y_ref64)
+    tol = bf16_ulp(ref) + 2.0 ** -20 * w
+    err = np.abs(got - ref)
+    bad = err > tol
+    assert not bad.any(), f"{bad.sum()} bf16 outputs off: max err/tol {np.max(err / tol):.3f}"
+
+
+def _ord(codes):
+    c = codes.astype(np.int64)
+    mag = c & 0x7F
+    return np.where(c & 0x80, -mag, mag)
+
+
+def near_boundary(p_abs, window):
+    idx = np.searchsorted(_BOUNDS, p_abs)
+    lo = _BOUNDS[np.clip(idx - 1, 0, len(_BOUNDS) - 1)]
+    hi = _BOUNDS[np.clip(idx, 0, len(_BOUNDS) - 1)]
+    d = np.minimum(np.abs(p_abs - lo), np.abs(hi - p_abs))
+    return d <= window
+
+
+def check_fp8_codes(codes_gpu, codes_ref, p_ref, window, what="fp8", max_frac=1e-3):
+    """codes equal except one-step misses at rounding boundaries (<= max_frac)."""
+    codes_gpu = np.asarray(codes_gpu, np.uint8)
+    codes_ref = np.asarray(codes_ref, np.uint8)
+    diff = codes_gpu != codes_ref
+    n = int(diff.sum())
+    if n == 0:
+        return 0
+    step = np.abs(_ord(codes_gpu[diff]) - _ord(codes_ref[diff]))
+    ok = (step <= 1) & near_boundary(np.abs(p_ref[diff]), window[diff] if np.ndim(window) else window)
+    assert ok.all(), (f"{what}: {int((~ok).sum())} code mismatches not at a rounding boundary; "
+                      f"e.g. gpu={codes_gpu[diff][~ok][:5]} ref={codes_ref[diff][~ok][:5]} "
+                      f"p={p_ref[diff][~ok][:5]}")
+    assert n <= max_frac * codes_gpu.size, f"{what}: {n} boundary mismatches > {max_frac:.1%}"
+    return n
+
+
+def check_mx(gpu_q, gpu_s, y32_ref, w, what):
+    """One direction of MXFP8 ([rows, H] blocks of 32 along the last axis)."""
+    ref_q, ref_s = oracle.norm.mx_blocks_1d(y32_ref)
+    n, h = y32_ref.shape
+    nb = h // 32
+    A = np.abs(y32_ref.astype(np.float64)).reshape(n, nb, 32).max(axis=2)
+    wb = w.reshape(n, nb, 32).max(axis=2)
+    sdiff = gpu_s != ref_s
+    if sdiff.any():
+        # allowed only when the block max sits at a power of two (within window)
+        lg = np.log2(np.where(A == 0, 1.0, A))
+        pw = np.exp2(np.round(lg))
+        near = np.abs(A - pw) <= 1e-6 * wb
+        ok = near[sdiff] & (np.abs(gpu_s[sdiff].astype(int) - ref_s[sdiff].astype(int)) == 1)
+        assert ok.all(), f"{what}: {int((~ok).sum())} E8M0 scale mismatches"
+    same = np.repeat(~sdiff, 32, axis=1)
+    e = ref_s.astype(np.int64) - 127
+    inv = np.repeat(np.exp2(-e.astype(np.float64)), 32, axis=1)
+    p = y32_ref.astype(np.float64) * inv
+    win = 1e-6 * w * inv
+    return check_fp8_codes(gpu_q[same], ref_q[same], p[same], win[same], what)
