@@ -66,13 +66,16 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 }
 
 // Wait until the phase with `parity` of barrier `bar` has completed, for at
-// most kWaitLimitNs; on expiry record `code` in *err and return false.
+// most kWaitLimitNs; on expiry record `code` in *err and return false.  Once
+// an error is recorded, later waits that do not succeed at once give up
+// immediately, so a kernel that lost its pipeline finishes quickly (its
+// results are then meaningless; the host reads the error word).
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigned* err,
                                           unsigned code) {
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = global_ns();
   while (!mbar_try_wait(bar, parity)) {
-    if (global_ns() - t0 > kWaitLimitNs) {
+    if (*reinterpret_cast<volatile unsigned*>(err) != 0u || global_ns() - t0 > kWaitLimitNs) {
       atomicCAS(err, 0u, code);
       return false;
     }
