@@ -296,9 +296,14 @@ def run_rn(args):
 
     l2 = torch.cuda.get_device_properties(local).L2_cache_size
     flush_buf = torch.empty(2 * l2, dtype=torch.uint8, device="cuda")
+    read_buf = torch.ones(2 * l2 // 4, dtype=torch.float32, device="cuda")
 
     def flush():
+        # write 2x L2, then read another 2x L2: the write evicts everything,
+        # the read evicts the dirty lines of the write, so the timed call
+        # starts with an L2 holding only clean, unrelated lines
         flush_buf.fill_(1)
+        read_buf.sum()
 
     peak, peak_kind, peak_key = hbm_peak()
 

@@ -200,7 +200,8 @@ rn_status check_margin(int sm_margin, const DeviceInfo& di) {
 rn_status fwd_common(int nk, const void* x, rn_dtype dt, const float* gamma, const float* beta,
                      int64_t N, int64_t H, float eps, int zcg, int sm_margin, rn_quant_mode mode,
                      const rn_output* out, float* mu, float* rsigma, cudaStream_t stream) {
-  if (x == nullptr || !dtype_ok(dt) || N < 0 || H < 1 || N > INT32_MAX || H > INT32_MAX)
+  if ((x == nullptr && N > 0) || !dtype_ok(dt) || N < 0 || H < 1 || N > INT32_MAX ||
+      H > INT32_MAX)
     return RN_ERR_INVALID;
   if (nk != kIdentity && (gamma == nullptr || rsigma == nullptr)) return RN_ERR_INVALID;
   if (nk == kLn && mu == nullptr) return RN_ERR_INVALID;
@@ -297,10 +298,11 @@ rn_status bwd_common(bool ln, const void* dz, const void* x, rn_dtype dt, const 
     *ws_bytes = need;
     return RN_OK;
   }
-  if (dz == nullptr || x == nullptr || rsigma == nullptr || gamma == nullptr || dx == nullptr ||
-      dgamma == nullptr)
+  // with N == 0 the row tensors are empty and may be NULL
+  if (((dz == nullptr || x == nullptr || rsigma == nullptr || dx == nullptr) && N > 0) ||
+      gamma == nullptr || dgamma == nullptr)
     return RN_ERR_INVALID;
-  if (ln && (mu == nullptr || dbeta == nullptr)) return RN_ERR_INVALID;
+  if (ln && ((mu == nullptr && N > 0) || dbeta == nullptr)) return RN_ERR_INVALID;
   if (ws_bytes == nullptr || *ws_bytes < need) return RN_ERR_WORKSPACE;
   if (!aligned(dz, 16) || !aligned(x, 16) || !aligned(dx, 16) || !aligned(ws, 16) ||
       !aligned(gamma, 4) || !aligned(rsigma, 4) || (mu && !aligned(mu, 4)) ||

@@ -93,15 +93,16 @@ def _mx_sweep_values():
             blk[rng.integers(0, 32)] = amax * (1 if rng.random() < 0.5 else -1)
             rows.append(blk)
     rows.append(np.zeros(32, np.float32))
+    rows.append((rng.uniform(-1, 1, 32) * 2.0 ** -140).astype(np.float32))   # subnormal block
     arr = np.concatenate(rows)
-    arr = np.concatenate([arr, np.zeros((-arr.size) % (32 * 64), np.float32)])
-    return arr.reshape(-1, 64 * 32)[:, :]        # H = 2048, blocks of 32 along rows
+    H = 256
+    arr = np.concatenate([arr, np.zeros((-arr.size) % (32 * H), np.float32)])
+    return arr.reshape(-1, H)                     # [128, 256]: N and H multiples of 32
 
 
 def test_quantize_only_mxfp8_bit_exact():
     y = _mx_sweep_values()
-    n = y.shape[0] - y.shape[0] % 32
-    y = np.ascontiguousarray(y[:n])
+    assert y.shape[0] % 32 == 0 and y.shape[0] >= 32
     r = rn.quantize_only(to_dev(y, "f32"), "mxfp8")
     ref = oracle.quantize(y, "mxfp8")
     for k in ("data", "row_scales", "col_data", "col_scales"):
