@@ -84,10 +84,12 @@ rn_status plan_fwd(int H, int esz, int N, int sm_margin, const DeviceInfo& di, R
   const int w = th / 32;
   const size_t row_bytes = (size_t)H * esz;
   // worst-case fixed part: stats [2][32] float2, slice partials [32] float4,
-  // amax scratch, alignment slack
+  // amax scratch, alignment slack; per slot: the row, its (mu, rsigma) and
+  // two mbarriers
   const size_t fixed = 2 * 32 * sizeof(float2) + 32 * 16 + 32 * sizeof(uint32_t) + 64;
+  const size_t per_slot = row_bytes + sizeof(float2) + 16;
   const size_t avail = (size_t)di.smem_optin > fixed ? di.smem_optin - fixed : 0;
-  int Q = (int)(avail / (row_bytes + 16));
+  int Q = (int)(avail / per_slot);
   if (Q > 128) Q = 128;
   if (Q < 2) return RN_ERR_UNSUPPORTED;
   const int T = pick_tile(w, Q);
@@ -96,7 +98,7 @@ rn_status plan_fwd(int H, int esz, int N, int sm_margin, const DeviceInfo& di, R
   pl->wpr = w > T ? w / T : 1;
   pl->Q = Q;
   pl->l.threads = th + 32;
-  pl->l.smem = (size_t)Q * row_bytes + fixed + (size_t)Q * 16;
+  pl->l.smem = (size_t)Q * per_slot + fixed;
   const int n_tiles = (N + T - 1) / T;
   const int g = di.sms - sm_margin;
   pl->l.grid = n_tiles < g ? (n_tiles > 0 ? n_tiles : 1) : g;
@@ -136,7 +138,7 @@ struct BwdShape {
 rn_status bwd_shape(int64_t N, int64_t H, int esz, BwdShape* s) {
   const int vec = 16 / esz;
   const int nchunks = (int)(H / vec);
-  const int ng = pick_ng(nchunks, 256, 4);
+  const int ng = pick_ng(nchunks, kMaxConsumers, 4);
   if (ng == 0) return RN_ERR_UNSUPPORTED;
   s->ng = ng;
   s->th = round_up((nchunks + ng - 1) / ng, 32);
@@ -203,8 +205,8 @@ rn_status fwd_common(int nk, const void* x, rn_dtype dt, const float* gamma, con
   if ((x == nullptr && N > 0) || !dtype_ok(dt) || N < 0 || H < 1 || N > INT32_MAX ||
       H > INT32_MAX)
     return RN_ERR_INVALID;
-  if (nk != kIdentity && (gamma == nullptr || rsigma == nullptr)) return RN_ERR_INVALID;
-  if (nk == kLn && mu == nullptr) return RN_ERR_INVALID;
+  if (nk != kIdentity && (gamma == nullptr || (rsigma == nullptr && N > 0))) return RN_ERR_INVALID;
+  if (nk == kLn && mu == nullptr && N > 0) return RN_ERR_INVALID;
   if (nk == kIdentity && mode == RN_QUANT_NONE) return RN_ERR_INVALID;
   rn_status st = check_out(mode, out, N, H);
   if (st != RN_OK) return st;
@@ -319,10 +321,13 @@ rn_status bwd_common(bool ln, const void* dz, const void* x, rn_dtype dt, const 
   }
   const int esz = elem_size(dt);
   const size_t row_bytes = (size_t)H * esz;
+  // fixed: g [H], stats [2][8] float4, slice partials [32] float2, slack;
+  // per slot: the x and dz rows, (mu, rsigma), two mbarriers
   const size_t fixed = (size_t)H * sizeof(float) + 2 * kBwdTileRows * sizeof(float4) +
                        32 * sizeof(float2) + 64;
+  const size_t per_slot = 2 * row_bytes + sizeof(float2) + 16;
   const size_t avail = (size_t)di.smem_optin > fixed ? di.smem_optin - fixed : 0;
-  int Q = (int)(avail / (2 * row_bytes + 16));
+  int Q = (int)(avail / per_slot);
   if (Q > 64) Q = 64;
   if (Q < 2) return RN_ERR_UNSUPPORTED;
   const int w = sh.th / 32;
@@ -330,7 +335,7 @@ rn_status bwd_common(bool ln, const void* dz, const void* x, rn_dtype dt, const 
   while (T > 1 && 3 * T > Q) T /= 2;
   Launch l;
   l.threads = sh.th + 32;
-  l.smem = (size_t)Q * 2 * row_bytes + fixed + (size_t)Q * 16;
+  l.smem = (size_t)Q * per_slot + fixed;
   const int g = di.sms - sm_margin;
   l.grid = sh.n_chunks < g ? sh.n_chunks : g;
 

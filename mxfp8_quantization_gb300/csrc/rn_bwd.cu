@@ -14,7 +14,8 @@
 //   phase 1  the two row means mean(dy), mean(dy * xhat): WPR warps share a
 //            row (one when rows are short), each summing an interleaved slice
 //            of its chunks; the slices are added in slice order (g is read
-//            from a shared-memory copy);
+//            from a shared-memory copy; mu / rsigma arrive with the row, by
+//            4-byte cp.async on the row's barrier);
 //   phase 2  each thread owns fixed 16-byte column chunks: dx for every row
 //            of the tile, plus running per-column sums of dz * xhat and dz
 //            in registers.
@@ -22,8 +23,9 @@
 // of a chunk its column sums are written to the workspace as one fp32
 // partial row.  The chunk size depends on N and H only, and each partial is
 // summed in row order, so the partials do not depend on the grid.
-// Kernel 2 adds the partials of each column in chunk order (a fixed tree:
-// 32 strided sequential sums, then the 32 results in order).
+// Kernel 2 adds the partials of each column in a fixed order that depends
+// on the chunk count only.  Arithmetic is on element pairs (f32x2), with
+// bf16 inputs entering through the mixed-precision forms.
 #include <cuda_runtime.h>
 
 #include "rn_device.cuh"
@@ -37,37 +39,25 @@ __device__ unsigned g_err_bwd;
 constexpr int kMaxThreads = 512 + 32;
 
 template <typename TIn>
-struct BChunk;
+__device__ __forceinline__ void store_dx(void* base, size_t elem, const float2* d);
 
 template <>
-struct BChunk<uint16_t> {
-  static constexpr int VEC = 8;
-  __device__ __forceinline__ static void load(const unsigned char* p, int c, float* f) {
-    bf16x8_to_f32(*reinterpret_cast<const uint4*>(p + (size_t)c * 16), f);
-  }
-  __device__ __forceinline__ static void store(void* base, size_t elem, const float* y) {
-    *reinterpret_cast<uint4*>(static_cast<uint16_t*>(base) + elem) =
-        make_uint4(pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3]), pack_bf16x2(y[4], y[5]),
-                   pack_bf16x2(y[6], y[7]));
-  }
-};
+__device__ __forceinline__ void store_dx<uint16_t>(void* base, size_t elem, const float2* d) {
+  *reinterpret_cast<uint4*>(static_cast<uint16_t*>(base) + elem) =
+      make_uint4(pack_bf16x2(d[0].x, d[0].y), pack_bf16x2(d[1].x, d[1].y),
+                 pack_bf16x2(d[2].x, d[2].y), pack_bf16x2(d[3].x, d[3].y));
+}
 
 template <>
-struct BChunk<float> {
-  static constexpr int VEC = 4;
-  __device__ __forceinline__ static void load(const unsigned char* p, int c, float* f) {
-    const float4 v = *reinterpret_cast<const float4*>(p + (size_t)c * 16);
-    f[0] = v.x; f[1] = v.y; f[2] = v.z; f[3] = v.w;
-  }
-  __device__ __forceinline__ static void store(void* base, size_t elem, const float* y) {
-    *reinterpret_cast<float4*>(static_cast<float*>(base) + elem) = make_float4(y[0], y[1], y[2], y[3]);
-  }
-};
+__device__ __forceinline__ void store_dx<float>(void* base, size_t elem, const float2* d) {
+  *reinterpret_cast<float4*>(static_cast<float*>(base) + elem) = make_float4(d[0].x, d[0].y, d[1].x, d[1].y);
+}
 
 template <typename TIn, int NG, bool LN>
 __global__ void __launch_bounds__(kMaxThreads, 1) rn_bwd_kernel(const BwdParams p) {
-  using C = BChunk<TIn>;
-  constexpr int VEC = C::VEC;
+  constexpr int VEC = 16 / (int)sizeof(TIn);
+  using V = Vec<TIn, VEC>;
+  constexpr int PAIRS = V::PAIRS;
   extern __shared__ __align__(128) unsigned char smem[];
 
   const int TH = blockDim.x - 32;
@@ -76,19 +66,21 @@ __global__ void __launch_bounds__(kMaxThreads, 1) rn_bwd_kernel(const BwdParams 
   const int nchunks = H / VEC;
   const uint32_t row_bytes = (uint32_t)H * sizeof(TIn);
   const uint32_t slot_bytes = 2 * row_bytes;  // x row, then dz row
-  const int Q = p.Q;
+  const uint32_t Q = (uint32_t)p.Q;
+  const int T = p.T;
   const int WPR = p.wpr;
 
   unsigned char* ring = smem;
   float* gs = reinterpret_cast<float*>(smem + (size_t)Q * slot_bytes);  // g, [H]
   float4* stats = reinterpret_cast<float4*>(gs + H);                     // [2][T]
-  float2* part = reinterpret_cast<float2*>(stats + 2 * p.T);             // [T * WPR]
-  uint64_t* full = reinterpret_cast<uint64_t*>(part + p.T * p.wpr);
+  float2* part = reinterpret_cast<float2*>(stats + 2 * T);               // [T * WPR]
+  float2* meta = part + T * WPR;                                         // [Q] (mu, rsigma)
+  uint64_t* full = reinterpret_cast<uint64_t*>(meta + Q);
   uint64_t* empty = full + Q;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < Q; ++i) {
-      mbar_init(smem_u32(&full[i]), 1);
+    for (uint32_t i = 0; i < Q; ++i) {
+      mbar_init(smem_u32(&full[i]), 2);  // bulk copies + the mu/rsigma cp.async
       mbar_init(smem_u32(&empty[i]), W);
     }
     fence_barrier_init();
@@ -108,101 +100,90 @@ __global__ void __launch_bounds__(kMaxThreads, 1) rn_bwd_kernel(const BwdParams 
     if (lane == 0) {
       const unsigned char* xb = static_cast<const unsigned char*>(p.x);
       const unsigned char* db = static_cast<const unsigned char*>(p.dz);
-      uint32_t q = 0;
+      RingPos pos{0u, 0u};
+      uint32_t issued = 0;
       for (int c = blockIdx.x; c < p.n_chunks; c += G) {
         const int t1 = min((c + 1) * tpc, p.n_tiles);
         for (int tt = c * tpc; tt < t1; ++tt) {
-          const int r0 = tt * p.T;
-          const int r1 = min(r0 + p.T, p.N);
-          for (int r = r0; r < r1; ++r, ++q) {
-            const uint32_t s = q % Q, use = q / Q;
-            if (use > 0) mbar_wait(smem_u32(&empty[s]), (use - 1) & 1, &g_err_bwd, kErrEmptyWait);
+          const int r0 = tt * T;
+          const int r1 = min(r0 + T, p.N);
+          for (int r = r0; r < r1; ++r, ++issued) {
+            const uint32_t s = pos.slot;
+            if (issued >= Q) mbar_wait(smem_u32(&empty[s]), pos.phase ^ 1u, &g_err_bwd, kErrEmptyWait);
             const uint32_t bar = smem_u32(&full[s]);
+            if (LN) cp_async4(smem_u32(&meta[s].x), p.mu + r);
+            cp_async4(smem_u32(&meta[s].y), p.rsigma + r);
+            cp_async_arrive(bar);
             mbar_arrive_expect_tx(bar, slot_bytes);
             const uint32_t dst = smem_u32(ring + (size_t)s * slot_bytes);
             bulk_g2s(dst, xb + (size_t)r * row_bytes, row_bytes, bar);
             bulk_g2s(dst + row_bytes, db + (size_t)r * row_bytes, row_bytes, bar);
+            pos.advance(1, Q);
           }
         }
       }
-      for (uint32_t k = q > (uint32_t)Q ? q - Q : 0; k < q; ++k)
-        mbar_wait(smem_u32(&full[k % Q]), (k / Q) & 1, &g_err_bwd, kErrDrainWait);
+      const uint32_t first = issued > Q ? issued - Q : 0;
+      for (uint32_t k = first; k < issued; ++k)
+        mbar_wait(smem_u32(&full[k % Q]), (k / Q) & 1u, &g_err_bwd, kErrDrainWait);
     }
     return;
   }
 
   const int t = threadIdx.x;
-  float gv[NG][VEC];
+  float2 g2[NG][PAIRS];
 #pragma unroll
   for (int g = 0; g < NG; ++g) {
     const int v = g * TH + t;
 #pragma unroll
-    for (int i = 0; i < VEC; ++i) gv[g][i] = (v < nchunks) ? gs[v * VEC + i] : 0.f;
+    for (int i = 0; i < PAIRS; ++i)
+      g2[g][i] = (v < nchunks) ? make_float2(gs[v * VEC + 2 * i], gs[v * VEC + 2 * i + 1])
+                               : make_float2(0.f, 0.f);
   }
   const float hf = (float)H;
   const int nacc = LN ? 2 : 1;
 
-  uint32_t q = 0;
+  RingPos pos{0u, 0u};
   int it = 0;
   for (int c = blockIdx.x; c < p.n_chunks; c += G) {
-    float adg[NG][VEC], adb[NG][VEC];
+    float2 adg[NG][PAIRS], adb[NG][PAIRS];
 #pragma unroll
     for (int g = 0; g < NG; ++g)
 #pragma unroll
-      for (int i = 0; i < VEC; ++i) {
-        adg[g][i] = 0.f;
-        adb[g][i] = 0.f;
+      for (int i = 0; i < PAIRS; ++i) {
+        adg[g][i] = make_float2(0.f, 0.f);
+        adb[g][i] = make_float2(0.f, 0.f);
       }
     const int t1 = min((c + 1) * tpc, p.n_tiles);
     for (int tt = c * tpc; tt < t1; ++tt, ++it) {
-      const int r0 = tt * p.T;
-      const int nrows = min(p.T, p.N - r0);
-      float4* st = stats + (it & 1) * p.T;
+      const int r0 = tt * T;
+      const int nrows = min(T, p.N - r0);
+      float4* st = stats + (it & 1) * T;
 
       // ------------------------------------------- phase 1: row reductions
       // WPR warps share a row: warp (k, j) sums chunks j*32 + lane + i*32*WPR
+      // of sum(dy) and sum(dy * (x - mu)) (RMSNorm: sum(dy * x))
       for (int item = warp; item < nrows * WPR; item += W) {
         const int k = item / WPR, j = item - k * WPR;
-        const uint32_t qq = q + k;
-        const uint32_t s = qq % Q;
-        mbar_wait(smem_u32(&full[s]), (qq / Q) & 1, &g_err_bwd, kErrFullWait);
-        const unsigned char* xr = ring + (size_t)s * slot_bytes;
+        const RingPos rp = pos.ahead(k, Q);
+        mbar_wait(smem_u32(&full[rp.slot]), rp.phase, &g_err_bwd, kErrFullWait);
+        const unsigned char* xr = ring + (size_t)rp.slot * slot_bytes;
         const unsigned char* dr = xr + row_bytes;
-        const float mu = LN ? p.mu[r0 + k] : 0.f;
-        const float rs = p.rsigma[r0 + k];
-        float s1[VEC], s2[VEC];
-#pragma unroll
-        for (int i = 0; i < VEC; ++i) {
-          s1[i] = 0.f;
-          s2[i] = 0.f;
-        }
+        const float mu = LN ? meta[rp.slot].x : 0.f;
+        float2 s1 = make_float2(0.f, 0.f), s2 = make_float2(0.f, 0.f);
         for (int cc = j * 32 + lane; cc < nchunks; cc += 32 * WPR) {
-          float xf[VEC], df[VEC];
-          C::load(xr, cc, xf);
-          C::load(dr, cc, df);
-          const float4* gp = reinterpret_cast<const float4*>(gs + cc * VEC);
+          const typename V::Raw xw = V::load(xr, cc);
+          const typename V::Raw dw = V::load(dr, cc);
+          const float2* gp = reinterpret_cast<const float2*>(gs + cc * VEC);
 #pragma unroll
-          for (int jj = 0; jj < VEC / 4; ++jj) {
-            const float4 g4 = gp[jj];
-            const float gg[4] = {g4.x, g4.y, g4.z, g4.w};
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              const int e = 4 * jj + i;
-              const float xh = (LN ? xf[e] - mu : xf[e]) * rs;
-              const float dy = df[e] * gg[i];
-              s1[e] += dy;
-              s2[e] = fmaf(dy, xh, s2[e]);
-            }
+          for (int i = 0; i < PAIRS; ++i) {
+            const float2 d = LN ? V::sub(xw, i, mu) : V::f32(xw, i);
+            const float2 dy = mul2(V::f32(dw, i), gp[i]);
+            s1 = add2(s1, dy);
+            s2 = fma2(dy, d, s2);
           }
         }
-        float a1 = 0.f, a2 = 0.f;
-#pragma unroll
-        for (int i = 0; i < VEC; ++i) {
-          a1 += s1[i];
-          a2 += s2[i];
-        }
-        a1 = warp_sum(a1);
-        a2 = warp_sum(a2);
+        const float a1 = warp_sum(s1.x + s1.y);
+        const float a2 = warp_sum(s2.x + s2.y);
         if (lane == 0) part[k * WPR + j] = make_float2(a1, a2);
       }
       consumer_sync(TH);
@@ -214,41 +195,46 @@ __global__ void __launch_bounds__(kMaxThreads, 1) rn_bwd_kernel(const BwdParams 
           a1 += pj.x;
           a2 += pj.y;
         }
-        st[k] = make_float4(LN ? p.mu[r0 + k] : 0.f, p.rsigma[r0 + k],
-                            LN ? __fdiv_rn(a1, hf) : 0.f, __fdiv_rn(a2, hf));
+        const float2 m = meta[pos.ahead(k, Q).slot];
+        const float rs = m.y;
+        // c1 = mean(dy), c2 = mean(dy * xhat) = rsigma * mean(dy * (x - mu))
+        st[k] = make_float4(LN ? m.x : 0.f, rs, LN ? __fdiv_rn(a1, hf) : 0.f,
+                            rs * __fdiv_rn(a2, hf));
       }
       consumer_sync(TH);
 
       // ------------------------------------------------- phase 2: dx, sums
+      RingPos rp = pos;
       for (int k = 0; k < nrows; ++k) {
-        const uint32_t qq = q + k;
-        const uint32_t s = qq % Q;
-        mbar_wait(smem_u32(&full[s]), (qq / Q) & 1, &g_err_bwd, kErrFullWait);
+        mbar_wait(smem_u32(&full[rp.slot]), rp.phase, &g_err_bwd, kErrFullWait);
         const float4 m = st[k];
-        const unsigned char* xr = ring + (size_t)s * slot_bytes;
+        const unsigned char* xr = ring + (size_t)rp.slot * slot_bytes;
         const unsigned char* dr = xr + row_bytes;
+        const size_t rowe = (size_t)(r0 + k) * H;
 #pragma unroll
         for (int g = 0; g < NG; ++g) {
           const int v = g * TH + t;
           if (v < nchunks) {
-            float xf[VEC], df[VEC], dx[VEC];
-            C::load(xr, v, xf);
-            C::load(dr, v, df);
+            const typename V::Raw xw = V::load(xr, v);
+            const typename V::Raw dw = V::load(dr, v);
+            float2 dx[PAIRS];
 #pragma unroll
-            for (int i = 0; i < VEC; ++i) {
-              const float xh = (LN ? xf[i] - m.x : xf[i]) * m.y;
-              const float dy = df[i] * gv[g][i];
-              dx[i] = (dy - fmaf(xh, m.w, m.z)) * m.y;
-              adg[g][i] = fmaf(df[i], xh, adg[g][i]);
-              if (LN) adb[g][i] += df[i];
+            for (int i = 0; i < PAIRS; ++i) {
+              const float2 xh = mul2(LN ? V::sub(xw, i, m.x) : V::f32(xw, i), splat2(m.y));
+              const float2 dzf = V::f32(dw, i);
+              const float2 dy = mul2(dzf, g2[g][i]);
+              dx[i] = mul2(sub2(dy, fma2(xh, splat2(m.w), splat2(m.z))), splat2(m.y));
+              adg[g][i] = fma2(dzf, xh, adg[g][i]);
+              if (LN) adb[g][i] = add2(adb[g][i], dzf);
             }
-            C::store(p.dx, (size_t)(r0 + k) * H + (size_t)v * VEC, dx);
+            store_dx<TIn>(p.dx, rowe + (size_t)v * VEC, dx);
           }
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&empty[s]));
+        if (lane == 0) mbar_arrive(smem_u32(&empty[rp.slot]));
+        rp.advance(1, Q);
       }
-      q += nrows;
+      pos = rp;
     }
     // chunk finished: write its partial column sums
     float* prow = p.part + (size_t)c * nacc * H;
@@ -257,12 +243,12 @@ __global__ void __launch_bounds__(kMaxThreads, 1) rn_bwd_kernel(const BwdParams 
       const int v = g * TH + t;
       if (v < nchunks) {
 #pragma unroll
-        for (int j = 0; j < VEC / 4; ++j) {
+        for (int j = 0; j < PAIRS / 2; ++j) {
           reinterpret_cast<float4*>(prow + (size_t)v * VEC)[j] =
-              make_float4(adg[g][4 * j], adg[g][4 * j + 1], adg[g][4 * j + 2], adg[g][4 * j + 3]);
+              make_float4(adg[g][2 * j].x, adg[g][2 * j].y, adg[g][2 * j + 1].x, adg[g][2 * j + 1].y);
           if (LN)
             reinterpret_cast<float4*>(prow + H + (size_t)v * VEC)[j] =
-                make_float4(adb[g][4 * j], adb[g][4 * j + 1], adb[g][4 * j + 2], adb[g][4 * j + 3]);
+                make_float4(adb[g][2 * j].x, adb[g][2 * j].y, adb[g][2 * j + 1].x, adb[g][2 * j + 1].y);
         }
       }
     }
@@ -271,36 +257,58 @@ __global__ void __launch_bounds__(kMaxThreads, 1) rn_bwd_kernel(const BwdParams 
 
 // dgamma[j] (a = 0) / dbeta[j] (a = 1) = sum over chunks of part[c][a][j].
 // Block: 32 warps x 32 lanes; lane owns 4 adjacent columns of a 128-column
-// slice; warp w sums chunks w, w+32, ... in order; then thread j of the
-// first 128 adds the 32 warp sums in warp order.  Fixed order throughout.
+// slice; warp w sums chunks w, w+32, w+64, ... into four interleaved
+// accumulators (chunk index / 32 mod 4), adds them as (a0+a1)+(a2+a3), then
+// thread j of the first 128 adds the 32 warp sums in warp order.  The order
+// depends on the chunk count only.
 __global__ void __launch_bounds__(1024) rn_colreduce_kernel(const ColReduceParams p) {
   __shared__ float4 red[32][33];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int a = blockIdx.y;
   const int col = blockIdx.x * 128 + lane * 4;
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  float4 acc[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
   if (col < p.H) {
     const float* base = p.part + (size_t)a * p.H + col;
     const size_t stride = (size_t)p.nacc * p.H;
-    for (int c = warp; c < p.n_chunks; c += 32) {
+    int c = warp;
+    for (; c + 96 < p.n_chunks; c += 128) {
+      float4 v[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) v[i] = *reinterpret_cast<const float4*>(base + (size_t)(c + 32 * i) * stride);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        acc[i].x += v[i].x;
+        acc[i].y += v[i].y;
+        acc[i].z += v[i].z;
+        acc[i].w += v[i].w;
+      }
+    }
+    for (int i = 0; c < p.n_chunks; c += 32, ++i) {
       const float4 v = *reinterpret_cast<const float4*>(base + (size_t)c * stride);
-      acc.x += v.x;
-      acc.y += v.y;
-      acc.z += v.z;
-      acc.w += v.w;
+      acc[i].x += v.x;
+      acc[i].y += v.y;
+      acc[i].z += v.z;
+      acc[i].w += v.w;
     }
   }
-  red[warp][lane] = acc;
+  float4 s;
+  s.x = (acc[0].x + acc[1].x) + (acc[2].x + acc[3].x);
+  s.y = (acc[0].y + acc[1].y) + (acc[2].y + acc[3].y);
+  s.z = (acc[0].z + acc[1].z) + (acc[2].z + acc[3].z);
+  s.w = (acc[0].w + acc[1].w) + (acc[2].w + acc[3].w);
+  red[warp][lane] = s;
   __syncthreads();
   if (threadIdx.x < 128) {
     const int l = threadIdx.x >> 2, e = threadIdx.x & 3;
     const int j = blockIdx.x * 128 + threadIdx.x;
-    float s = 0.f;
+    float r = 0.f;
     for (int w = 0; w < 32; ++w) {
       const float4 v = red[w][l];
-      s += (e == 0) ? v.x : (e == 1) ? v.y : (e == 2) ? v.z : v.w;
+      r += (e == 0) ? v.x : (e == 1) ? v.y : (e == 2) ? v.z : v.w;
     }
-    if (j < p.H) (a == 0 ? p.dgamma : p.dbeta)[j] = s;
+    if (j < p.H) (a == 0 ? p.dgamma : p.dbeta)[j] = r;
   }
 }
 

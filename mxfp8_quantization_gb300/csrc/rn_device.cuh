@@ -95,6 +95,37 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
       : "memory");
 }
 
+// 4-byte asynchronous global -> shared copy (cp.async); completion is
+// tracked by cp_async_arrive on an mbarrier
+__device__ __forceinline__ void cp_async4(uint32_t dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
+}
+
+// the barrier receives one arrival once every cp.async this thread issued
+// so far has landed (the arrival is counted in the barrier's init count)
+__device__ __forceinline__ void cp_async_arrive(uint32_t bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+
+// Position in a ring of q slots: slot index and the parity of its use.
+// Advancing by n <= q rows needs no division.
+struct RingPos {
+  uint32_t slot, phase;
+  __device__ __forceinline__ void advance(uint32_t n, uint32_t q) {
+    slot += n;
+    if (slot >= q) {
+      slot -= q;
+      phase ^= 1u;
+    }
+  }
+  // position k rows ahead (k < q)
+  __device__ __forceinline__ RingPos ahead(uint32_t k, uint32_t q) const {
+    RingPos r = *this;
+    r.advance(k, q);
+    return r;
+  }
+};
+
 // named barrier over the consumer warps only (id 1; id 0 is __syncthreads)
 __device__ __forceinline__ void consumer_sync(int nthreads) {
   asm volatile("bar.sync 1, %0;" ::"r"(nthreads) : "memory");
@@ -170,6 +201,158 @@ __device__ __forceinline__ float e8m0_inv_scale(uint32_t code) {
   if (code == 0xFFu) return __uint_as_float(0x7FC00000u);
   return __uint_as_float((254u - code) << 23);
 }
+
+// ------------------------------------------------- packed fp32 pairs (f32x2)
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
+  float2 d;
+  asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\tmov.b64 rc, {%6, %7};\n\t"
+      "fma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+  return d;
+}
+
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) {
+  float2 d;
+  asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+      "mul.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
+}
+
+__device__ __forceinline__ float2 add2(float2 a, float2 b) {
+  float2 d;
+  asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+      "add.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
+}
+
+__device__ __forceinline__ float2 sub2(float2 a, float2 b) {
+  float2 d;
+  asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+      "sub.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
+}
+
+__device__ __forceinline__ float2 splat2(float v) { return make_float2(v, v); }
+
+// ------------------------------------- bf16 pairs with fp32 arithmetic
+// A 32-bit word holds two bf16 values, element 0 in the low half.  The
+// mixed-precision forms take the bf16 operands directly; every result is the
+// same single-rounded fp32 value as converting first (bf16 -> fp32 is exact).
+
+// exact fp32 values of the pair
+__device__ __forceinline__ float2 bf16x2_f32(uint32_t w) {
+  return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+}
+
+// (x0 - m, x1 - m), each rounded once
+__device__ __forceinline__ float2 bf16x2_sub(uint32_t w, float m) {
+  float2 d;
+  asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
+      "sub.rn.f32.bf16 %0, l, %3;\n\tsub.rn.f32.bf16 %1, h, %3;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "r"(w), "f"(m));
+  return d;
+}
+
+// acc += (x0, x1)
+__device__ __forceinline__ void bf16x2_acc(float2& acc, uint32_t w) {
+  asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
+      "add.rn.f32.bf16 %0, l, %0;\n\tadd.rn.f32.bf16 %1, h, %1;\n\t}"
+      : "+f"(acc.x), "+f"(acc.y)
+      : "r"(w));
+}
+
+// acc += (x0 * x0, x1 * x1)  (the products are exact in fp32)
+__device__ __forceinline__ void bf16x2_sq_acc(float2& acc, uint32_t w) {
+  asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
+      "fma.rn.f32.bf16 %0, l, l, %0;\n\tfma.rn.f32.bf16 %1, h, h, %1;\n\t}"
+      : "+f"(acc.x), "+f"(acc.y)
+      : "r"(w));
+}
+
+// running max of magnitudes over two more values; NaN wins
+__device__ __forceinline__ float amax_acc2(float acc, float2 v) {
+  float r;
+  asm("max.NaN.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(acc), "f"(fabsf(v.x)), "f"(fabsf(v.y)));
+  return r;
+}
+
+// ------------------------------------------------------- row chunks
+// A chunk is VEC consecutive elements of a row (VEC/2 pairs), loaded from
+// shared memory with one vector load.
+template <typename TIn, int VEC>
+struct Vec;
+
+template <>
+struct Vec<uint16_t, 8> {  // bf16, 16 bytes
+  static constexpr int PAIRS = 4;
+  struct Raw {
+    uint32_t w[4];
+  };
+  __device__ __forceinline__ static Raw load(const unsigned char* p, int c) {
+    const uint4 v = *reinterpret_cast<const uint4*>(p + (size_t)c * 16);
+    return Raw{{v.x, v.y, v.z, v.w}};
+  }
+  __device__ __forceinline__ static float2 f32(const Raw& r, int i) { return bf16x2_f32(r.w[i]); }
+  __device__ __forceinline__ static float2 sub(const Raw& r, int i, float m) {
+    return bf16x2_sub(r.w[i], m);
+  }
+  __device__ __forceinline__ static void acc(float2& a, const Raw& r, int i) { bf16x2_acc(a, r.w[i]); }
+  __device__ __forceinline__ static void sq_acc(float2& a, const Raw& r, int i) {
+    bf16x2_sq_acc(a, r.w[i]);
+  }
+};
+
+template <>
+struct Vec<uint16_t, 4> {  // bf16, 8 bytes
+  static constexpr int PAIRS = 2;
+  struct Raw {
+    uint32_t w[2];
+  };
+  __device__ __forceinline__ static Raw load(const unsigned char* p, int c) {
+    const uint2 v = *reinterpret_cast<const uint2*>(p + (size_t)c * 8);
+    return Raw{{v.x, v.y}};
+  }
+  __device__ __forceinline__ static float2 f32(const Raw& r, int i) { return bf16x2_f32(r.w[i]); }
+  __device__ __forceinline__ static float2 sub(const Raw& r, int i, float m) {
+    return bf16x2_sub(r.w[i], m);
+  }
+  __device__ __forceinline__ static void acc(float2& a, const Raw& r, int i) { bf16x2_acc(a, r.w[i]); }
+  __device__ __forceinline__ static void sq_acc(float2& a, const Raw& r, int i) {
+    bf16x2_sq_acc(a, r.w[i]);
+  }
+};
+
+template <>
+struct Vec<float, 4> {  // fp32, 16 bytes
+  static constexpr int PAIRS = 2;
+  struct Raw {
+    float2 p[2];
+  };
+  __device__ __forceinline__ static Raw load(const unsigned char* p, int c) {
+    const float4 v = *reinterpret_cast<const float4*>(p + (size_t)c * 16);
+    return Raw{{make_float2(v.x, v.y), make_float2(v.z, v.w)}};
+  }
+  __device__ __forceinline__ static float2 f32(const Raw& r, int i) { return r.p[i]; }
+  __device__ __forceinline__ static float2 sub(const Raw& r, int i, float m) {
+    return sub2(r.p[i], splat2(m));
+  }
+  __device__ __forceinline__ static void acc(float2& a, const Raw& r, int i) { a = add2(a, r.p[i]); }
+  __device__ __forceinline__ static void sq_acc(float2& a, const Raw& r, int i) {
+    a = fma2(r.p[i], r.p[i], a);
+  }
+};
 
 // ------------------------------------------------------------- reductions
 __device__ __forceinline__ float warp_sum(float v) {

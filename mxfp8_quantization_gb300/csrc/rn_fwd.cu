@@ -8,6 +8,8 @@
 //     into a ring of Q shared-memory slots with the bulk-copy engine
 //     (cp.async.bulk, completion on a per-slot "full" mbarrier) and refills a
 //     slot as soon as every consumer warp has released it ("empty" mbarrier);
+//     when a pass needs the saved mu / rsigma of a row, the same lane fetches
+//     them into the slot with 4-byte cp.async tracked by the same barrier;
 //   * consumer warps 0..W-1 take tiles of T rows:
 //       phase 1  the row statistics from shared memory: WPR warps share a
 //                row (one when rows are short), each taking an interleaved
@@ -20,13 +22,15 @@
 //                (gamma / beta live in its registers for the whole kernel) and
 //                forms y = (x-mu)*rsigma*g + beta (RMSNorm: x*rsigma*g) for
 //                each row of the tile, then stores bf16/fp32 or E4M3 codes;
+//   * arithmetic is done on pairs of elements with the packed fp32 (f32x2)
+//     instructions, and bf16 inputs enter through the mixed-precision
+//     add/sub/fma forms, which round exactly like convert-then-operate;
 //   * the per-tensor amax is reduced per thread, per CTA, then with one
 //     atomicMax on the fp32 bit pattern (ordered like the values for
 //     non-negative numbers, NaN above +inf).
 // Current scaling runs the kernel twice: pass 1 (statistics + amax, no
-// output) and pass 2 (quantize with 448/amax, reading mu/rsigma back), the
-// second walking the tiles backwards so that it starts on the rows that
-// pass 1 left in L2.
+// output) and pass 2 (quantize with 448/amax), the second walking the tiles
+// backwards so that it starts on the rows pass 1 left in L2.
 #include <cuda_runtime.h>
 
 #include "rn_device.cuh"
@@ -39,78 +43,51 @@ __device__ unsigned g_err_fwd;
 
 constexpr int kMaxThreads = 512 + 32;
 
-template <typename TIn>
-struct Chunk;
-
-template <>
-struct Chunk<uint16_t> {  // bf16 storage
-  static constexpr int VEC = 8;
-  __device__ __forceinline__ static void load(const unsigned char* p, int c, float* f) {
-    const uint4 v = *reinterpret_cast<const uint4*>(p + (size_t)c * 16);
-    bf16x8_to_f32(v, f);
-  }
-};
-
-template <>
-struct Chunk<float> {
-  static constexpr int VEC = 4;
-  __device__ __forceinline__ static void load(const unsigned char* p, int c, float* f) {
-    const float4 v = *reinterpret_cast<const float4*>(p + (size_t)c * 16);
-    f[0] = v.x; f[1] = v.y; f[2] = v.z; f[3] = v.w;
-  }
-};
-
-template <int VEC>
-__device__ __forceinline__ float tree_sum(const float* a) {
-  float s[VEC];
-#pragma unroll
-  for (int i = 0; i < VEC; ++i) s[i] = a[i];
-#pragma unroll
-  for (int w = VEC / 2; w > 0; w >>= 1)
-#pragma unroll
-    for (int i = 0; i < w; ++i) s[i] += s[i + w];
-  return s[0];
-}
-
-// store VEC outputs of one chunk
-template <int VEC, int QM>
-__device__ __forceinline__ void store_chunk(const FwdParams& p, size_t elem, const float* y,
+// store the PAIRS y pairs of one chunk in the output format
+template <int PAIRS, int QM>
+__device__ __forceinline__ void store_chunk(const FwdParams& p, size_t elem, const float2* y,
                                             float scale) {
   if constexpr (QM == kQNone) {
     if (p.out_f32) {
       float4* o = reinterpret_cast<float4*>(static_cast<float*>(p.out) + elem);
 #pragma unroll
-      for (int i = 0; i < VEC / 4; ++i)
-        o[i] = make_float4(y[4 * i], y[4 * i + 1], y[4 * i + 2], y[4 * i + 3]);
+      for (int i = 0; i < PAIRS / 2; ++i)
+        o[i] = make_float4(y[2 * i].x, y[2 * i].y, y[2 * i + 1].x, y[2 * i + 1].y);
     } else {
       uint16_t* o = static_cast<uint16_t*>(p.out) + elem;
-      if constexpr (VEC == 8) {
+      if constexpr (PAIRS == 4) {
         *reinterpret_cast<uint4*>(o) =
-            make_uint4(pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3]), pack_bf16x2(y[4], y[5]),
-                       pack_bf16x2(y[6], y[7]));
+            make_uint4(pack_bf16x2(y[0].x, y[0].y), pack_bf16x2(y[1].x, y[1].y),
+                       pack_bf16x2(y[2].x, y[2].y), pack_bf16x2(y[3].x, y[3].y));
       } else {
-        *reinterpret_cast<uint2*>(o) = make_uint2(pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3]));
+        *reinterpret_cast<uint2*>(o) =
+            make_uint2(pack_bf16x2(y[0].x, y[0].y), pack_bf16x2(y[1].x, y[1].y));
       }
     }
   } else {
     uint8_t* o = static_cast<uint8_t*>(p.out) + elem;
-    float s[VEC];
+    uint32_t c[PAIRS];
 #pragma unroll
-    for (int i = 0; i < VEC; ++i) s[i] = y[i] * scale;
-    if constexpr (VEC == 8) {
-      *reinterpret_cast<uint2*>(o) =
-          make_uint2(pack_e4m3x4(s[0], s[1], s[2], s[3]), pack_e4m3x4(s[4], s[5], s[6], s[7]));
-    } else {
-      *reinterpret_cast<uint32_t*>(o) = pack_e4m3x4(s[0], s[1], s[2], s[3]);
+    for (int i = 0; i < PAIRS; ++i) {
+      const float2 s = mul2(y[i], splat2(scale));
+      c[i] = pack_e4m3x2(s.x, s.y);
     }
+    if constexpr (PAIRS == 4)
+      *reinterpret_cast<uint2*>(o) = make_uint2(c[0] | (c[1] << 16), c[2] | (c[3] << 16));
+    else
+      *reinterpret_cast<uint32_t*>(o) = c[0] | (c[1] << 16);
   }
 }
 
 template <typename TIn, int NG, int NK, int QM>
 __global__ void __launch_bounds__(kMaxThreads, 1) rn_fwd_kernel(const FwdParams p) {
-  using C = Chunk<TIn>;
-  constexpr int VEC = C::VEC;
+  constexpr int VEC = 16 / (int)sizeof(TIn);
+  using V = Vec<TIn, VEC>;
+  constexpr int PAIRS = V::PAIRS;
   constexpr bool LN = (NK == kLn);
+  // pass 2 of current scaling gets mu / rsigma with each row
+  constexpr bool META = (QM == kQCurQuant && NK != kIdentity);
+  constexpr bool STATS = (QM != kQCurQuant && NK != kIdentity);
   extern __shared__ __align__(128) unsigned char smem[];
 
   const int TH = blockDim.x - 32;  // consumer threads
@@ -118,19 +95,21 @@ __global__ void __launch_bounds__(kMaxThreads, 1) rn_fwd_kernel(const FwdParams 
   const int H = p.H;
   const int nchunks = H / VEC;
   const uint32_t row_bytes = (uint32_t)H * sizeof(TIn);
-  const int Q = p.Q;
+  const uint32_t Q = (uint32_t)p.Q;
+  const int T = p.T;
   const int WPR = p.wpr;
 
   unsigned char* ring = smem;
-  float2* stats = reinterpret_cast<float2*>(smem + (size_t)Q * row_bytes);
-  float4* part = reinterpret_cast<float4*>(stats + 2 * p.T);   // [T * WPR]
-  uint32_t* red = reinterpret_cast<uint32_t*>(part + p.T * p.wpr);
-  uint64_t* full = reinterpret_cast<uint64_t*>(red + 32);
+  float2* stats = reinterpret_cast<float2*>(smem + (size_t)Q * row_bytes);  // [2][T]
+  float4* part = reinterpret_cast<float4*>(stats + 2 * T);                  // [T * WPR]
+  uint32_t* red = reinterpret_cast<uint32_t*>(part + T * WPR);              // [32]
+  float2* meta = reinterpret_cast<float2*>(red + 32);                       // [Q]
+  uint64_t* full = reinterpret_cast<uint64_t*>(meta + Q);
   uint64_t* empty = full + Q;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < Q; ++i) {
-      mbar_init(smem_u32(&full[i]), 1);
+    for (uint32_t i = 0; i < Q; ++i) {
+      mbar_init(smem_u32(&full[i]), META ? 2 : 1);
       mbar_init(smem_u32(&empty[i]), W);
     }
     fence_barrier_init();
@@ -145,51 +124,58 @@ __global__ void __launch_bounds__(kMaxThreads, 1) rn_fwd_kernel(const FwdParams 
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       const unsigned char* xb = static_cast<const unsigned char*>(p.x);
-      uint32_t q = 0;
-      for (int t = blockIdx.x; t < p.n_tiles; t += G) {
-        const int tt = p.reverse ? p.n_tiles - 1 - t : t;
-        const int r0 = tt * p.T;
-        const int r1 = min(r0 + p.T, p.N);
-        for (int r = r0; r < r1; ++r, ++q) {
-          const uint32_t s = q % Q, use = q / Q;
-          if (use > 0) mbar_wait(smem_u32(&empty[s]), (use - 1) & 1, &g_err_fwd, kErrEmptyWait);
-          mbar_arrive_expect_tx(smem_u32(&full[s]), row_bytes);
-          bulk_g2s(smem_u32(ring + (size_t)s * row_bytes), xb + (size_t)r * row_bytes, row_bytes,
-                   smem_u32(&full[s]));
+      RingPos pos{0u, 0u};
+      uint32_t issued = 0;
+      for (int tk = blockIdx.x; tk < p.n_tiles; tk += G) {
+        const int tt = p.reverse ? p.n_tiles - 1 - tk : tk;
+        const int r0 = tt * T;
+        const int r1 = min(r0 + T, p.N);
+        for (int r = r0; r < r1; ++r, ++issued) {
+          const uint32_t s = pos.slot;
+          if (issued >= Q) mbar_wait(smem_u32(&empty[s]), pos.phase ^ 1u, &g_err_fwd, kErrEmptyWait);
+          const uint32_t bar = smem_u32(&full[s]);
+          if constexpr (META) {
+            if (LN) cp_async4(smem_u32(&meta[s].x), p.mu + r);
+            cp_async4(smem_u32(&meta[s].y), p.rsigma + r);
+            cp_async_arrive(bar);
+          }
+          mbar_arrive_expect_tx(bar, row_bytes);
+          bulk_g2s(smem_u32(ring + (size_t)s * row_bytes), xb + (size_t)r * row_bytes, row_bytes, bar);
+          pos.advance(1, Q);
         }
       }
       // every copy this CTA issued must have landed before it exits
-      for (uint32_t k = q > (uint32_t)Q ? q - Q : 0; k < q; ++k)
-        mbar_wait(smem_u32(&full[k % Q]), (k / Q) & 1, &g_err_fwd, kErrDrainWait);
+      const uint32_t first = issued > Q ? issued - Q : 0;
+      for (uint32_t k = first; k < issued; ++k)
+        mbar_wait(smem_u32(&full[k % Q]), (k / Q) & 1u, &g_err_fwd, kErrDrainWait);
     }
     return;
   }
 
   // -------------------------------------------------------------- consumers
   const int t = threadIdx.x;
-  float gv[NG][VEC], bv[NG][VEC];
+  float2 g2[NG][PAIRS], b2[NG][PAIRS];
 #pragma unroll
   for (int g = 0; g < NG; ++g) {
     const int v = g * TH + t;
 #pragma unroll
-    for (int i = 0; i < VEC; ++i) {
-      gv[g][i] = 0.f;
-      bv[g][i] = 0.f;
-    }
-    if (v < nchunks) {
-#pragma unroll
-      for (int i = 0; i < VEC; ++i) {
-        if constexpr (NK != kIdentity) {
-          const float gam = p.gamma[v * VEC + i];
-          gv[g][i] = p.zcg ? 1.0f + gam : gam;
-        }
-        if constexpr (LN) bv[g][i] = p.beta ? p.beta[v * VEC + i] : 0.0f;
+    for (int i = 0; i < PAIRS; ++i) {
+      g2[g][i] = make_float2(0.f, 0.f);
+      b2[g][i] = make_float2(0.f, 0.f);
+      if (NK != kIdentity && v < nchunks) {
+        const int c = v * VEC + 2 * i;
+        const float ga = p.gamma[c], gb = p.gamma[c + 1];
+        g2[g][i] = p.zcg ? make_float2(1.0f + ga, 1.0f + gb) : make_float2(ga, gb);
+        if (LN && p.beta != nullptr) b2[g][i] = make_float2(p.beta[c], p.beta[c + 1]);
       }
     }
   }
 
   float scale = 1.0f;
-  if constexpr (QM == kQDelayed) scale = *p.scale;
+  if constexpr (QM == kQDelayed) {
+    scale = *p.scale;
+    if (blockIdx.x == 0 && t == 0) *p.scale_inv = __fdiv_rn(1.0f, scale);
+  }
   if constexpr (QM == kQCurQuant) {
     const float am = *p.amax;
     scale = (am == 0.0f) ? 1.0f : __fdiv_rn(448.0f, am);
@@ -198,70 +184,70 @@ __global__ void __launch_bounds__(kMaxThreads, 1) rn_fwd_kernel(const FwdParams 
       *p.scale_inv = __fdiv_rn(1.0f, scale);
     }
   }
-  if constexpr (QM == kQDelayed) {
-    if (blockIdx.x == 0 && t == 0) *p.scale_inv = __fdiv_rn(1.0f, scale);
-  }
   float amax_t = 0.0f;
-  const float inv_h_num = (float)H;
+  const float hf = (float)H;
 
-  uint32_t q = 0;
+  RingPos pos{0u, 0u};  // ring position of the current tile's first row
   int it = 0;
   for (int tk = blockIdx.x; tk < p.n_tiles; tk += G, ++it) {
     const int tt = p.reverse ? p.n_tiles - 1 - tk : tk;
-    const int r0 = tt * p.T;
-    const int nrows = min(p.T, p.N - r0);
-    float2* st = stats + (it & 1) * p.T;
+    const int r0 = tt * T;
+    const int nrows = min(T, p.N - r0);
+    float2* st = stats + (it & 1) * T;
 
-    if constexpr (QM != kQCurQuant && NK != kIdentity) {
+    if constexpr (STATS) {
       // ---------------------------------------------- phase 1: statistics
-      // WPR warps share a row; warp (k, j) takes chunks j*32 + lane + i*32*WPR
-      // of row k and leaves (mean, M2, n) of its slice (LayerNorm; exact
-      // two-pass within the slice) or its sum of squares (RMSNorm)
       for (int item = warp; item < nrows * WPR; item += W) {
         const int k = item / WPR, j = item - k * WPR;
-        const uint32_t qq = q + k;
-        const uint32_t s = qq % Q;
-        mbar_wait(smem_u32(&full[s]), (qq / Q) & 1, &g_err_fwd, kErrFullWait);
-        const unsigned char* rowp = ring + (size_t)s * row_bytes;
-        float acc[VEC];
+        const RingPos rp = pos.ahead(k, Q);
+        mbar_wait(smem_u32(&full[rp.slot]), rp.phase, &g_err_fwd, kErrFullWait);
+        const unsigned char* rowp = ring + (size_t)rp.slot * row_bytes;
         float smean = 0.0f, cnt = 0.0f;
+        float2 a[PAIRS];
         if constexpr (LN) {
 #pragma unroll
-          for (int i = 0; i < VEC; ++i) acc[i] = 0.0f;
+          for (int i = 0; i < PAIRS; ++i) a[i] = make_float2(0.f, 0.f);
           for (int c = j * 32 + lane; c < nchunks; c += 32 * WPR) {
-            float xf[VEC];
-            C::load(rowp, c, xf);
+            const typename V::Raw raw = V::load(rowp, c);
 #pragma unroll
-            for (int i = 0; i < VEC; ++i) acc[i] += xf[i];
+            for (int i = 0; i < PAIRS; ++i) V::acc(a[i], raw, i);
             cnt += (float)VEC;
           }
+          float s = 0.f;
+#pragma unroll
+          for (int i = 0; i < PAIRS; ++i) s += a[i].x + a[i].y;
           cnt = warp_sum(cnt);
-          smean = cnt > 0.0f ? __fdiv_rn(warp_sum(tree_sum<VEC>(acc)), cnt) : 0.0f;
+          smean = cnt > 0.0f ? __fdiv_rn(warp_sum(s), cnt) : 0.0f;
         }
 #pragma unroll
-        for (int i = 0; i < VEC; ++i) acc[i] = 0.0f;
+        for (int i = 0; i < PAIRS; ++i) a[i] = make_float2(0.f, 0.f);
         for (int c = j * 32 + lane; c < nchunks; c += 32 * WPR) {
-          float xf[VEC];
-          C::load(rowp, c, xf);
+          const typename V::Raw raw = V::load(rowp, c);
 #pragma unroll
-          for (int i = 0; i < VEC; ++i) {
-            const float d = LN ? xf[i] - smean : xf[i];
-            acc[i] = fmaf(d, d, acc[i]);
+          for (int i = 0; i < PAIRS; ++i) {
+            if constexpr (LN) {
+              const float2 d = V::sub(raw, i, smean);
+              a[i] = fma2(d, d, a[i]);
+            } else {
+              V::sq_acc(a[i], raw, i);
+            }
           }
         }
-        const float m2 = warp_sum(tree_sum<VEC>(acc));
+        float m2 = 0.f;
+#pragma unroll
+        for (int i = 0; i < PAIRS; ++i) m2 += a[i].x + a[i].y;
+        m2 = warp_sum(m2);
         if (lane == 0) part[k * WPR + j] = make_float4(smean, m2, cnt, 0.0f);
       }
       consumer_sync(TH);
       // merge the slices of each row in slice order (Chan et al.)
       if (t < nrows) {
         const int k = t;
-        float mean = 0.0f, m2, n;
         const float4 p0 = part[k * WPR];
+        float mean = 0.0f, m2 = p0.y;
         if constexpr (LN) {
           mean = p0.x;
-          m2 = p0.y;
-          n = p0.z;
+          float n = p0.z;
           for (int j = 1; j < WPR; ++j) {
             const float4 pj = part[k * WPR + j];
             if (pj.z > 0.0f) {
@@ -273,10 +259,9 @@ __global__ void __launch_bounds__(kMaxThreads, 1) rn_fwd_kernel(const FwdParams 
             }
           }
         } else {
-          m2 = p0.y;
           for (int j = 1; j < WPR; ++j) m2 += part[k * WPR + j].y;
         }
-        const float rs = __frsqrt_rn(__fdiv_rn(m2, inv_h_num) + p.eps);
+        const float rs = __frsqrt_rn(__fdiv_rn(m2, hf) + p.eps);
         st[k] = make_float2(mean, rs);
         if constexpr (LN) p.mu[r0 + k] = mean;
         p.rsigma[r0 + k] = rs;
@@ -285,46 +270,46 @@ __global__ void __launch_bounds__(kMaxThreads, 1) rn_fwd_kernel(const FwdParams 
     }
 
     // ------------------------------------------- phase 2: apply + output
+    RingPos rp = pos;
     for (int k = 0; k < nrows; ++k) {
-      const uint32_t qq = q + k;
-      const uint32_t s = qq % Q;
-      mbar_wait(smem_u32(&full[s]), (qq / Q) & 1, &g_err_fwd, kErrFullWait);
+      mbar_wait(smem_u32(&full[rp.slot]), rp.phase, &g_err_fwd, kErrFullWait);
       float mean = 0.0f, rs = 1.0f;
-      if constexpr (NK == kIdentity) {
-      } else if constexpr (QM == kQCurQuant) {
-        rs = p.rsigma[r0 + k];
-        mean = LN ? p.mu[r0 + k] : 0.0f;
-      } else {
+      if constexpr (META) {
+        const float2 m = meta[rp.slot];
+        mean = LN ? m.x : 0.0f;
+        rs = m.y;
+      } else if constexpr (STATS) {
         const float2 m = st[k];
         mean = m.x;
         rs = m.y;
       }
-      const unsigned char* rowp = ring + (size_t)s * row_bytes;
+      const unsigned char* rowp = ring + (size_t)rp.slot * row_bytes;
+      const size_t rowe = (size_t)(r0 + k) * H;
 #pragma unroll
       for (int g = 0; g < NG; ++g) {
         const int v = g * TH + t;
         if (v < nchunks) {
-          float y[VEC];
-          C::load(rowp, v, y);
+          const typename V::Raw raw = V::load(rowp, v);
+          float2 y[PAIRS];
 #pragma unroll
-          for (int i = 0; i < VEC; ++i) {
-            if constexpr (LN)
-              y[i] = fmaf((y[i] - mean) * rs, gv[g][i], bv[g][i]);
-            else if constexpr (NK == kRms)
-              y[i] = (y[i] * rs) * gv[g][i];
+          for (int i = 0; i < PAIRS; ++i) {
+            if constexpr (LN) {
+              y[i] = fma2(mul2(V::sub(raw, i, mean), splat2(rs)), g2[g][i], b2[g][i]);
+            } else if constexpr (NK == kRms) {
+              y[i] = mul2(mul2(V::f32(raw, i), splat2(rs)), g2[g][i]);
+            } else {
+              y[i] = V::f32(raw, i);
+            }
+            if constexpr (QM == kQDelayed || QM == kQCurAmax) amax_t = amax_acc2(amax_t, y[i]);
           }
-          if constexpr (QM == kQDelayed || QM == kQCurAmax) {
-#pragma unroll
-            for (int i = 0; i < VEC; ++i) amax_t = amax_acc(amax_t, y[i]);
-          }
-          if constexpr (QM != kQCurAmax)
-            store_chunk<VEC, QM>(p, (size_t)(r0 + k) * H + (size_t)v * VEC, y, scale);
+          if constexpr (QM != kQCurAmax) store_chunk<PAIRS, QM>(p, rowe + (size_t)v * VEC, y, scale);
         }
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&empty[s]));
+      if (lane == 0) mbar_arrive(smem_u32(&empty[rp.slot]));
+      rp.advance(1, Q);
     }
-    q += nrows;
+    pos = rp;
   }
 
   if constexpr (QM == kQDelayed || QM == kQCurAmax) {

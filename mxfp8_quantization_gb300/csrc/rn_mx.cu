@@ -21,6 +21,8 @@
 // y is recomputed in pass B from the bf16/fp32 row still in shared memory
 // (cheaper than keeping 32x4 fp32 values per thread), with the same
 // instructions as in pass A so both directions quantize identical y32.
+// Arithmetic is on element pairs (f32x2); bf16 inputs enter through the
+// mixed-precision forms.
 #include <cuda_runtime.h>
 
 #include "rn_device.cuh"
@@ -34,34 +36,26 @@ __device__ unsigned g_err_mx;
 constexpr int kMaxThreads = 512 + 32;
 constexpr int kTile = 32;
 
-template <typename TIn>
-__device__ __forceinline__ void load4(const unsigned char* rowp, int v, float* f);
-
-template <>
-__device__ __forceinline__ void load4<uint16_t>(const unsigned char* rowp, int v, float* f) {
-  bf16x4_to_f32(*reinterpret_cast<const uint2*>(rowp + (size_t)v * 8), f);
-}
-
-template <>
-__device__ __forceinline__ void load4<float>(const unsigned char* rowp, int v, float* f) {
-  const float4 a = *reinterpret_cast<const float4*>(rowp + (size_t)v * 16);
-  f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w;
-}
-
-template <int NK>
-__device__ __forceinline__ void apply4(float* y, float mean, float rs, const float* g,
-                                       const float* b) {
+// y of the 4 columns (two pairs) of chunk v in one row
+template <typename TIn, int NK>
+__device__ __forceinline__ void y4(const unsigned char* rowp, int v, float mean, float rs,
+                                   const float2* g, const float2* b, float2* y) {
+  using V = Vec<TIn, 4>;
+  const typename V::Raw raw = V::load(rowp, v);
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
+  for (int i = 0; i < 2; ++i) {
     if constexpr (NK == kLn)
-      y[i] = fmaf((y[i] - mean) * rs, g[i], b[i]);
+      y[i] = fma2(mul2(V::sub(raw, i, mean), splat2(rs)), g[i], b[i]);
     else if constexpr (NK == kRms)
-      y[i] = (y[i] * rs) * g[i];
+      y[i] = mul2(mul2(V::f32(raw, i), splat2(rs)), g[i]);
+    else
+      y[i] = V::f32(raw, i);
   }
 }
 
 template <typename TIn, int NG, int NK>
 __global__ void __launch_bounds__(kMaxThreads, 1) rn_mx_kernel(const MxParams p) {
+  using V = Vec<TIn, 4>;
   extern __shared__ __align__(128) unsigned char smem[];
   const int TH = blockDim.x - 32;
   const int W = TH >> 5;
@@ -69,15 +63,15 @@ __global__ void __launch_bounds__(kMaxThreads, 1) rn_mx_kernel(const MxParams p)
   const int N = p.N;
   const int nchunks = H >> 2;
   const uint32_t row_bytes = (uint32_t)H * sizeof(TIn);
-  const int Q = p.Q;
+  const uint32_t Q = (uint32_t)p.Q;
 
   unsigned char* ring = smem;
-  float2* stats = reinterpret_cast<float2*>(smem + (size_t)Q * row_bytes);
+  float2* stats = reinterpret_cast<float2*>(smem + (size_t)Q * row_bytes);  // [2][32]
   uint64_t* full = reinterpret_cast<uint64_t*>(stats + 2 * kTile);
   uint64_t* empty = full + Q;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < Q; ++i) {
+    for (uint32_t i = 0; i < Q; ++i) {
       mbar_init(smem_u32(&full[i]), 1);
       mbar_init(smem_u32(&empty[i]), W);
     }
@@ -92,36 +86,40 @@ __global__ void __launch_bounds__(kMaxThreads, 1) rn_mx_kernel(const MxParams p)
   if (warp == W) {
     if (lane == 0) {
       const unsigned char* xb = static_cast<const unsigned char*>(p.x);
-      uint32_t q = 0;
+      RingPos pos{0u, 0u};
+      uint32_t issued = 0;
       for (int t = blockIdx.x; t < p.n_tiles; t += G) {
-        for (int k = 0; k < kTile; ++k, ++q) {
+        for (int k = 0; k < kTile; ++k, ++issued) {
           const int r = t * kTile + k;
-          const uint32_t s = q % Q, use = q / Q;
-          if (use > 0) mbar_wait(smem_u32(&empty[s]), (use - 1) & 1, &g_err_mx, kErrEmptyWait);
+          const uint32_t s = pos.slot;
+          if (issued >= Q) mbar_wait(smem_u32(&empty[s]), pos.phase ^ 1u, &g_err_mx, kErrEmptyWait);
           mbar_arrive_expect_tx(smem_u32(&full[s]), row_bytes);
           bulk_g2s(smem_u32(ring + (size_t)s * row_bytes), xb + (size_t)r * row_bytes, row_bytes,
                    smem_u32(&full[s]));
+          pos.advance(1, Q);
         }
       }
-      for (uint32_t k = q > (uint32_t)Q ? q - Q : 0; k < q; ++k)
-        mbar_wait(smem_u32(&full[k % Q]), (k / Q) & 1, &g_err_mx, kErrDrainWait);
+      const uint32_t first = issued > Q ? issued - Q : 0;
+      for (uint32_t k = first; k < issued; ++k)
+        mbar_wait(smem_u32(&full[k % Q]), (k / Q) & 1u, &g_err_mx, kErrDrainWait);
     }
     return;
   }
 
   const int t = threadIdx.x;
-  float gv[NG][4], bv[NG][4];
+  float2 g2[NG][2], b2[NG][2];
 #pragma unroll
   for (int g = 0; g < NG; ++g) {
     const int v = g * TH + t;
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      gv[g][i] = 0.f;
-      bv[g][i] = 0.f;
+    for (int i = 0; i < 2; ++i) {
+      g2[g][i] = make_float2(0.f, 0.f);
+      b2[g][i] = make_float2(0.f, 0.f);
       if (NK != kIdentity && v < nchunks) {
-        const float gam = p.gamma[v * 4 + i];
-        gv[g][i] = p.zcg ? 1.0f + gam : gam;
-        if (NK == kLn && p.beta) bv[g][i] = p.beta[v * 4 + i];
+        const int c = v * 4 + 2 * i;
+        const float ga = p.gamma[c], gb = p.gamma[c + 1];
+        g2[g][i] = p.zcg ? make_float2(1.0f + ga, 1.0f + gb) : make_float2(ga, gb);
+        if (NK == kLn && p.beta) b2[g][i] = make_float2(p.beta[c], p.beta[c + 1]);
       }
     }
   }
@@ -129,44 +127,53 @@ __global__ void __launch_bounds__(kMaxThreads, 1) rn_mx_kernel(const MxParams p)
   const int hs = H >> 5;   // row scales per row
   const int ns = N >> 5;   // column scales per column
 
-  uint32_t q = 0;
+  RingPos pos{0u, 0u};
   int it = 0;
   for (int tile = blockIdx.x; tile < p.n_tiles; tile += G, ++it) {
     const int r0 = tile * kTile;
     float2* st = stats + (it & 1) * kTile;
+    // the ring slot of each row of the tile: slot0 + k, wrapping once
+    const uint32_t slot0 = pos.slot;
+    auto slot_of = [&](int k) -> uint32_t {
+      const uint32_t s = slot0 + (uint32_t)k;
+      return s >= Q ? s - Q : s;
+    };
 
     // every consumer warp waits for all 32 rows of the tile once
-    for (int k = 0; k < kTile; ++k) {
-      const uint32_t qq = q + k;
-      mbar_wait(smem_u32(&full[qq % Q]), (qq / Q) & 1, &g_err_mx, kErrFullWait);
+    {
+      RingPos rp = pos;
+      for (int k = 0; k < kTile; ++k) {
+        mbar_wait(smem_u32(&full[rp.slot]), rp.phase, &g_err_mx, kErrFullWait);
+        rp.advance(1, Q);
+      }
     }
 
     if constexpr (NK != kIdentity) {
       for (int k = warp; k < kTile; k += W) {
-        const unsigned char* rowp = ring + (size_t)((q + k) % Q) * row_bytes;
-        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        const unsigned char* rowp = ring + (size_t)slot_of(k) * row_bytes;
+        float2 a0 = make_float2(0.f, 0.f), a1 = make_float2(0.f, 0.f);
         float mean = 0.f;
         if constexpr (NK == kLn) {
           for (int c = lane; c < nchunks; c += 32) {
-            float xf[4];
-            load4<TIn>(rowp, c, xf);
-#pragma unroll
-            for (int i = 0; i < 4; ++i) acc[i] += xf[i];
+            const typename V::Raw raw = V::load(rowp, c);
+            V::acc(a0, raw, 0);
+            V::acc(a1, raw, 1);
           }
-          mean = __fdiv_rn(warp_sum((acc[0] + acc[2]) + (acc[1] + acc[3])), hf);
-#pragma unroll
-          for (int i = 0; i < 4; ++i) acc[i] = 0.f;
+          mean = __fdiv_rn(warp_sum((a0.x + a0.y) + (a1.x + a1.y)), hf);
+          a0 = a1 = make_float2(0.f, 0.f);
         }
         for (int c = lane; c < nchunks; c += 32) {
-          float xf[4];
-          load4<TIn>(rowp, c, xf);
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const float d = (NK == kLn) ? xf[i] - mean : xf[i];
-            acc[i] = fmaf(d, d, acc[i]);
+          const typename V::Raw raw = V::load(rowp, c);
+          if constexpr (NK == kLn) {
+            const float2 d0 = V::sub(raw, 0, mean), d1 = V::sub(raw, 1, mean);
+            a0 = fma2(d0, d0, a0);
+            a1 = fma2(d1, d1, a1);
+          } else {
+            V::sq_acc(a0, raw, 0);
+            V::sq_acc(a1, raw, 1);
           }
         }
-        const float var = __fdiv_rn(warp_sum((acc[0] + acc[2]) + (acc[1] + acc[3])), hf);
+        const float var = __fdiv_rn(warp_sum((a0.x + a0.y) + (a1.x + a1.y)), hf);
         const float rs = __frsqrt_rn(var + p.eps);
         if (lane == 0) {
           st[k] = make_float2(mean, rs);
@@ -181,75 +188,75 @@ __global__ void __launch_bounds__(kMaxThreads, 1) rn_mx_kernel(const MxParams p)
     for (int g = 0; g < NG; ++g) {
       const int v = g * TH + t;
       const bool valid = v < nchunks;
-      float cmax[4] = {0.f, 0.f, 0.f, 0.f};
+      float cm[4] = {0.f, 0.f, 0.f, 0.f};
       // ------------------------------------------------------------ pass A
-      for (int k = 0; k < kTile; ++k) {
-        const unsigned char* rowp = ring + (size_t)((q + k) % Q) * row_bytes;
-        float mean = 0.f, rs = 1.f;
-        if constexpr (NK != kIdentity) {
-          const float2 m = st[k];
-          mean = m.x;
-          rs = m.y;
-        }
-        float y[4] = {0.f, 0.f, 0.f, 0.f};
-        if (valid) {
-          load4<TIn>(rowp, v, y);
-          apply4<NK>(y, mean, rs, gv[g], bv[g]);
-        }
-        if (p.data != nullptr) {
-          float m = 0.f;
+      for (int k = 0; k < kTile; k += 2) {
+        float2 y[2][2];
 #pragma unroll
-          for (int i = 0; i < 4; ++i) m = amax_acc(m, y[i]);
-          uint32_t mb = abs_bits(m);
-          mb = max(mb, __shfl_xor_sync(0xFFFFFFFFu, mb, 1));
-          mb = max(mb, __shfl_xor_sync(0xFFFFFFFFu, mb, 2));
-          mb = max(mb, __shfl_xor_sync(0xFFFFFFFFu, mb, 4));
-          const uint32_t code = e8m0_code(__uint_as_float(mb));
-          const float inv = e8m0_inv_scale(code);
-          if (valid) {
-            const size_t row = (size_t)(r0 + k);
-            *reinterpret_cast<uint32_t*>(p.data + row * H + (size_t)v * 4) =
-                pack_e4m3x4(y[0] * inv, y[1] * inv, y[2] * inv, y[3] * inv);
-            if ((t & 7) == 0) p.row_scales[row * hs + (v >> 3)] = (uint8_t)code;
+        for (int kk = 0; kk < 2; ++kk) {
+          float mean = 0.f, rs = 1.f;
+          if constexpr (NK != kIdentity) {
+            const float2 m = st[k + kk];
+            mean = m.x;
+            rs = m.y;
+          }
+          y[kk][0] = y[kk][1] = make_float2(0.f, 0.f);
+          if (valid)
+            y4<TIn, NK>(ring + (size_t)slot_of(k + kk) * row_bytes, v, mean, rs, g2[g], b2[g], y[kk]);
+          if (p.data != nullptr) {
+            uint32_t mb = abs_bits(amax_acc2(amax_acc2(0.f, y[kk][0]), y[kk][1]));
+            mb = max(mb, __shfl_xor_sync(0xFFFFFFFFu, mb, 1));
+            mb = max(mb, __shfl_xor_sync(0xFFFFFFFFu, mb, 2));
+            mb = max(mb, __shfl_xor_sync(0xFFFFFFFFu, mb, 4));
+            const uint32_t code = e8m0_code(__uint_as_float(mb));
+            const float2 inv = splat2(e8m0_inv_scale(code));
+            if (valid) {
+              const size_t row = (size_t)(r0 + k + kk);
+              const float2 q0 = mul2(y[kk][0], inv), q1 = mul2(y[kk][1], inv);
+              *reinterpret_cast<uint32_t*>(p.data + row * H + (size_t)v * 4) =
+                  pack_e4m3x2(q0.x, q0.y) | (pack_e4m3x2(q1.x, q1.y) << 16);
+              if ((t & 7) == 0) p.row_scales[row * hs + (v >> 3)] = (uint8_t)code;
+            }
           }
         }
-#pragma unroll
-        for (int i = 0; i < 4; ++i) cmax[i] = amax_acc(cmax[i], y[i]);
+        cm[0] = amax_acc2(cm[0], make_float2(y[0][0].x, y[1][0].x));
+        cm[1] = amax_acc2(cm[1], make_float2(y[0][0].y, y[1][0].y));
+        cm[2] = amax_acc2(cm[2], make_float2(y[0][1].x, y[1][1].x));
+        cm[3] = amax_acc2(cm[3], make_float2(y[0][1].y, y[1][1].y));
       }
       // ------------------------------------------------------------ pass B
       if (p.col_data != nullptr) {
-        float cinv[4];
         uint32_t ccode[4];
+        float cinv[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-          ccode[i] = e8m0_code(cmax[i]);
+          ccode[i] = e8m0_code(cm[i]);
           cinv[i] = e8m0_inv_scale(ccode[i]);
         }
+        const float2 ci01 = make_float2(cinv[0], cinv[1]), ci23 = make_float2(cinv[2], cinv[3]);
         uint32_t cq[4][8];
 #pragma unroll
         for (int k4 = 0; k4 < 8; ++k4) {
-          float y4[4][4];
+          float2 q[4][2];  // [row][pair] scaled by the column scales
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
             const int k = 4 * k4 + kk;
-            const unsigned char* rowp = ring + (size_t)((q + k) % Q) * row_bytes;
             float mean = 0.f, rs = 1.f;
             if constexpr (NK != kIdentity) {
               const float2 m = st[k];
               mean = m.x;
               rs = m.y;
             }
-#pragma unroll
-            for (int i = 0; i < 4; ++i) y4[kk][i] = 0.f;
-            if (valid) {
-              load4<TIn>(rowp, v, y4[kk]);
-              apply4<NK>(y4[kk], mean, rs, gv[g], bv[g]);
-            }
+            float2 y[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+            if (valid)
+              y4<TIn, NK>(ring + (size_t)slot_of(k) * row_bytes, v, mean, rs, g2[g], b2[g], y);
+            q[kk][0] = mul2(y[0], ci01);
+            q[kk][1] = mul2(y[1], ci23);
           }
-#pragma unroll
-          for (int i = 0; i < 4; ++i)
-            cq[i][k4] = pack_e4m3x4(y4[0][i] * cinv[i], y4[1][i] * cinv[i], y4[2][i] * cinv[i],
-                                    y4[3][i] * cinv[i]);
+          cq[0][k4] = pack_e4m3x2(q[0][0].x, q[1][0].x) | (pack_e4m3x2(q[2][0].x, q[3][0].x) << 16);
+          cq[1][k4] = pack_e4m3x2(q[0][0].y, q[1][0].y) | (pack_e4m3x2(q[2][0].y, q[3][0].y) << 16);
+          cq[2][k4] = pack_e4m3x2(q[0][1].x, q[1][1].x) | (pack_e4m3x2(q[2][1].x, q[3][1].x) << 16);
+          cq[3][k4] = pack_e4m3x2(q[0][1].y, q[1][1].y) | (pack_e4m3x2(q[2][1].y, q[3][1].y) << 16);
         }
         if (valid) {
 #pragma unroll
@@ -265,9 +272,14 @@ __global__ void __launch_bounds__(kMaxThreads, 1) rn_mx_kernel(const MxParams p)
     }
     // release the tile's slots
     __syncwarp();
-    if (lane == 0)
-      for (int k = 0; k < kTile; ++k) mbar_arrive(smem_u32(&empty[(q + k) % Q]));
-    q += kTile;
+    if (lane == 0) {
+      RingPos rp = pos;
+      for (int k = 0; k < kTile; ++k) {
+        mbar_arrive(smem_u32(&empty[rp.slot]));
+        rp.advance(1, Q);
+      }
+    }
+    pos.advance(kTile, Q);
   }
 }
 

@@ -10,7 +10,7 @@ the reading is given here and in the design notes):
 * bf16 outputs: within 1 bf16 ulp of the oracle's correctly rounded value,
   plus the fp32 evaluation bound 2**-20 * w, where w is the magnitude of the
   terms that form y (``term_magnitude``); the bound only matters where y
-  cancels to near zero.
+  cancels to near zero.  fp32 outputs: within 2**-20 * w.
 * FP8 codes: equal, except that a code may differ by one step (adjacent
   values, including +-0) when the oracle's pre-quantization value p lies
   within 1e-6 * (s * w) of a rounding boundary; such exemptions may cover at
@@ -40,13 +40,17 @@ _BOUNDS = np.concatenate([[0.0], _MIDS])
 
 
 def term_magnitude(x64, m, r, gamma, beta, zcg):
-    """w = (|x| + |m|) * r * |g| + |beta| (RMSNorm: |x| * r * |g|), fp64."""
+    """w = (|x| + mean_row|x|) * r * |g| + |beta| (RMSNorm: |x| * r * |g|), fp64.
+
+    For LayerNorm the centring x - mu involves mu, a sum of the whole row
+    whose rounding error scales with mean|x| (not with |mu|), so mean|x|
+    stands in for the magnitude of mu."""
     g = np.abs(1.0 + gamma.astype(np.float64) if zcg else gamma.astype(np.float64))
     r = np.asarray(r, np.float64)[:, None]
     if m is None:
         w = np.abs(x64) * r * g
     else:
-        w = (np.abs(x64) + np.abs(np.asarray(m, np.float64))[:, None]) * r * g
+        w = (np.abs(x64) + np.mean(np.abs(x64), axis=1, keepdims=True)) * r * g
     if beta is not None:
         w = w + np.abs(beta.astype(np.float64))
     return w
