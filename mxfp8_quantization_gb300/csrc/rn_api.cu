@@ -13,6 +13,7 @@ namespace {
 constexpr int kMaxDevices = 64;
 std::atomic<int> g_sms[kMaxDevices];
 std::atomic<int> g_smem[kMaxDevices];
+std::atomic<int> g_smem_sm[kMaxDevices];
 
 constexpr int kMaxConsumers = 512;
 constexpr int kBwdTileRows = 8;
@@ -44,16 +45,22 @@ rn_status device_info(DeviceInfo* out) {
   if (dev < 0 || dev >= kMaxDevices) return RN_ERR_UNSUPPORTED;
   int sms = g_sms[dev].load(std::memory_order_relaxed);
   int smem = g_smem[dev].load(std::memory_order_relaxed);
-  if (sms <= 0 || smem <= 0) {
+  int smem_sm = g_smem_sm[dev].load(std::memory_order_relaxed);
+  if (sms <= 0 || smem <= 0 || smem_sm <= 0) {
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
       return RN_ERR_CUDA;
     if (cudaDeviceGetAttribute(&smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
       return RN_ERR_CUDA;
+    if (cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) !=
+        cudaSuccess)
+      return RN_ERR_CUDA;
     g_sms[dev].store(sms, std::memory_order_relaxed);
     g_smem[dev].store(smem, std::memory_order_relaxed);
+    g_smem_sm[dev].store(smem_sm, std::memory_order_relaxed);
   }
   out->sms = sms;
   out->smem_optin = smem;
+  out->smem_per_sm = smem_sm;
   return RN_OK;
 }
 
@@ -74,35 +81,48 @@ int pick_tile(int w, int q) {
   return T;
 }
 
-// row-wise forward: ring of Q row slots, tiles of T rows
+// shared memory one CTA may use when per_sm CTAs share an SM (the runtime
+// reserves 1 KB per CTA)
+size_t cta_smem_budget(const DeviceInfo& di, int per_sm) {
+  const long long b = ((long long)di.smem_per_sm - 1024LL * per_sm) / per_sm;
+  const long long cap = di.smem_optin;
+  return (size_t)(b < cap ? b : cap);
+}
+
+// row-wise forward: ring of Q row slots, tiles of T rows.  Two CTAs of at
+// most 256 consumer threads per SM when each still holds a ring of >= 6 rows
+// (their tile barriers then overlap), else one CTA of up to 512.
 rn_status plan_fwd(int H, int esz, int N, int sm_margin, const DeviceInfo& di, RowPlan* pl) {
   const int vec = 16 / esz;
   const int nchunks = H / vec;
-  const int ng = pick_ng(nchunks, kMaxConsumers, 4);
-  if (ng == 0) return RN_ERR_UNSUPPORTED;
-  const int th = round_up((nchunks + ng - 1) / ng, 32);
-  const int w = th / 32;
   const size_t row_bytes = (size_t)H * esz;
   // worst-case fixed part: stats [2][32] float2, slice partials [32] float4,
   // amax scratch, alignment slack; per slot: the row, its (mu, rsigma) and
   // two mbarriers
   const size_t fixed = 2 * 32 * sizeof(float2) + 32 * 16 + 32 * sizeof(uint32_t) + 64;
   const size_t per_slot = row_bytes + sizeof(float2) + 16;
-  const size_t avail = (size_t)di.smem_optin > fixed ? di.smem_optin - fixed : 0;
-  int Q = (int)(avail / per_slot);
-  if (Q > 128) Q = 128;
-  if (Q < 2) return RN_ERR_UNSUPPORTED;
-  const int T = pick_tile(w, Q);
-  pl->ng = ng;
-  pl->T = T;
-  pl->wpr = w > T ? w / T : 1;
-  pl->Q = Q;
-  pl->l.threads = th + 32;
-  pl->l.smem = (size_t)Q * per_slot + fixed;
-  const int n_tiles = (N + T - 1) / T;
-  const int g = di.sms - sm_margin;
-  pl->l.grid = n_tiles < g ? (n_tiles > 0 ? n_tiles : 1) : g;
-  return RN_OK;
+  for (int per_sm = 2; per_sm >= 1; --per_sm) {
+    const int ng = pick_ng(nchunks, per_sm == 2 ? 256 : kMaxConsumers, 4);
+    if (ng == 0) continue;
+    const size_t budget = cta_smem_budget(di, per_sm);
+    int Q = budget > fixed ? (int)((budget - fixed) / per_slot) : 0;
+    if (Q > 128) Q = 128;
+    if (Q < (per_sm == 2 ? 6 : 2)) continue;
+    const int th = round_up((nchunks + ng - 1) / ng, 32);
+    const int w = th / 32;
+    const int T = pick_tile(w, Q);
+    pl->ng = ng;
+    pl->T = T;
+    pl->wpr = w > T ? w / T : 1;
+    pl->Q = Q;
+    pl->l.threads = th + 32;
+    pl->l.smem = (size_t)Q * per_slot + fixed;
+    pl->l.work = (N + T - 1) / T;
+    pl->l.sms = di.sms - sm_margin;
+    pl->l.per_sm = per_sm;
+    return RN_OK;
+  }
+  return RN_ERR_UNSUPPORTED;
 }
 
 rn_status plan_mx(int H, int esz, int N, int sm_margin, const DeviceInfo& di, RowPlan* pl) {
@@ -121,9 +141,9 @@ rn_status plan_mx(int H, int esz, int N, int sm_margin, const DeviceInfo& di, Ro
   pl->Q = Q;
   pl->l.threads = th + 32;
   pl->l.smem = (size_t)Q * row_bytes + fixed + (size_t)Q * 16;
-  const int n_tiles = N / 32;
-  const int g = di.sms - sm_margin;
-  pl->l.grid = n_tiles < g ? (n_tiles > 0 ? n_tiles : 1) : g;
+  pl->l.work = N / 32;
+  pl->l.sms = di.sms - sm_margin;
+  pl->l.per_sm = 1;
   return RN_OK;
 }
 
@@ -132,16 +152,11 @@ rn_status plan_mx(int H, int esz, int N, int sm_margin, const DeviceInfo& di, Ro
 // and their sum are independent of sm_margin; a tile (T rows, T | 8) never
 // straddles two chunks
 struct BwdShape {
-  int ng, th, chunk_rows, n_chunks;
+  int chunk_rows, n_chunks;
 };
 
 rn_status bwd_shape(int64_t N, int64_t H, int esz, BwdShape* s) {
-  const int vec = 16 / esz;
-  const int nchunks = (int)(H / vec);
-  const int ng = pick_ng(nchunks, kMaxConsumers, 4);
-  if (ng == 0) return RN_ERR_UNSUPPORTED;
-  s->ng = ng;
-  s->th = round_up((nchunks + ng - 1) / ng, 32);
+  if (pick_ng((int)(H * esz / 16), kMaxConsumers, 4) == 0) return RN_ERR_UNSUPPORTED;
   const int64_t m = N / (int64_t)(kBwdTileRows * kBwdTargetChunks);
   s->chunk_rows = kBwdTileRows * (int)(m < 1 ? 1 : m);
   s->n_chunks = (int)((N + s->chunk_rows - 1) / s->chunk_rows);
@@ -163,6 +178,17 @@ bool out_fields_only(const rn_output* o, bool data, bool rs, bool cd, bool cs, b
 
 rn_status check_out(rn_quant_mode mode, const rn_output* o, int64_t N, int64_t H) {
   if (o == nullptr) return RN_ERR_INVALID;
+  if (N == 0) {
+    // empty row tensors may have NULL data; only the scalar outputs matter
+    if (mode == RN_QUANT_FP8_DELAYED)
+      return (o->scale && o->scale_inv && o->amax) ? RN_OK : RN_ERR_INVALID;
+    if (mode == RN_QUANT_FP8_CURRENT)
+      return (o->scale_out && o->scale_inv && o->amax) ? RN_OK : RN_ERR_INVALID;
+    if (mode == RN_QUANT_NONE)
+      return (o->out_dtype == RN_BF16 || o->out_dtype == RN_F32) ? RN_OK : RN_ERR_INVALID;
+    if (mode == RN_QUANT_MXFP8) return (H % 32 == 0) ? RN_OK : RN_ERR_UNSUPPORTED;
+    return RN_ERR_INVALID;
+  }
   switch (mode) {
     case RN_QUANT_NONE:
       if (!out_fields_only(o, true, false, false, false, false, false, false, false))
@@ -321,23 +347,34 @@ rn_status bwd_common(bool ln, const void* dz, const void* x, rn_dtype dt, const 
   }
   const int esz = elem_size(dt);
   const size_t row_bytes = (size_t)H * esz;
-  // fixed: g [H], stats [2][8] float4, slice partials [32] float2, slack;
-  // per slot: the x and dz rows, (mu, rsigma), two mbarriers
+  // fixed: g [H] (as float4 parts of each chunk), stats [2][8] float4,
+  // slice partials [32] float2, slack; per slot: the x and dz rows,
+  // (mu, rsigma), two mbarriers.  Two CTAs (<= 256 consumer threads) per SM
+  // when each holds >= 6 slots, else one CTA of up to 512.
   const size_t fixed = (size_t)H * sizeof(float) + 2 * kBwdTileRows * sizeof(float4) +
                        32 * sizeof(float2) + 64;
   const size_t per_slot = 2 * row_bytes + sizeof(float2) + 16;
-  const size_t avail = (size_t)di.smem_optin > fixed ? di.smem_optin - fixed : 0;
-  int Q = (int)(avail / per_slot);
-  if (Q > 64) Q = 64;
-  if (Q < 2) return RN_ERR_UNSUPPORTED;
-  const int w = sh.th / 32;
+  int Q = 0, per_sm = 2, ng = 0;
+  for (; per_sm >= 1; --per_sm) {
+    ng = pick_ng((int)(H * esz / 16), per_sm == 2 ? 256 : kMaxConsumers, 4);
+    if (ng == 0) continue;
+    const size_t budget = cta_smem_budget(di, per_sm);
+    Q = budget > fixed ? (int)((budget - fixed) / per_slot) : 0;
+    if (Q > 64) Q = 64;
+    if (Q >= (per_sm == 2 ? 6 : 2)) break;
+  }
+  if (per_sm < 1) return RN_ERR_UNSUPPORTED;
+  const int nch = (int)(H * esz / 16);
+  const int th = round_up((nch + ng - 1) / ng, 32);
+  const int w = th / 32;
   int T = kBwdTileRows;                   // divides every chunk
   while (T > 1 && 3 * T > Q) T /= 2;
   Launch l;
-  l.threads = sh.th + 32;
+  l.threads = th + 32;
   l.smem = (size_t)Q * per_slot + fixed;
-  const int g = di.sms - sm_margin;
-  l.grid = sh.n_chunks < g ? sh.n_chunks : g;
+  l.work = sh.n_chunks;
+  l.sms = di.sms - sm_margin;
+  l.per_sm = per_sm;
 
   BwdParams p{};
   p.dz = dz;
@@ -356,7 +393,7 @@ rn_status bwd_common(bool ln, const void* dz, const void* x, rn_dtype dt, const 
   p.Q = Q;
   p.n_tiles = (int)((N + T - 1) / T);
   p.n_chunks = sh.n_chunks;
-  if ((st = launch_bwd(ln, dt == RN_BF16, sh.ng, p, l, stream)) != RN_OK) return st;
+  if ((st = launch_bwd(ln, dt == RN_BF16, ng, p, l, stream)) != RN_OK) return st;
   ColReduceParams c{};
   c.part = p.part;
   c.dgamma = dgamma;

@@ -71,8 +71,10 @@ __global__ void __launch_bounds__(kMaxThreads, 1) rn_bwd_kernel(const BwdParams 
   const int WPR = p.wpr;
 
   unsigned char* ring = smem;
-  float* gs = reinterpret_cast<float*>(smem + (size_t)Q * slot_bytes);  // g, [H]
-  float4* stats = reinterpret_cast<float4*>(gs + H);                     // [2][T]
+  // g as [VEC/4][nchunks] float4: part j of chunk c at gsv[j * nchunks + c],
+  // so that 32 lanes reading 32 consecutive chunks touch consecutive 16 bytes
+  float4* gsv = reinterpret_cast<float4*>(smem + (size_t)Q * slot_bytes);
+  float4* stats = gsv + (size_t)(VEC / 4) * nchunks;                      // [2][T]
   float2* part = reinterpret_cast<float2*>(stats + 2 * T);               // [T * WPR]
   float2* meta = part + T * WPR;                                         // [Q] (mu, rsigma)
   uint64_t* full = reinterpret_cast<uint64_t*>(meta + Q);
@@ -85,9 +87,11 @@ __global__ void __launch_bounds__(kMaxThreads, 1) rn_bwd_kernel(const BwdParams 
     }
     fence_barrier_init();
   }
-  for (int j = threadIdx.x; j < H; j += blockDim.x) {
-    const float gam = p.gamma[j];
-    gs[j] = p.zcg ? 1.0f + gam : gam;
+  for (int j = threadIdx.x; j < H / 4; j += blockDim.x) {
+    float4 g4 = make_float4(p.gamma[4 * j], p.gamma[4 * j + 1], p.gamma[4 * j + 2], p.gamma[4 * j + 3]);
+    if (p.zcg) g4 = make_float4(1.0f + g4.x, 1.0f + g4.y, 1.0f + g4.z, 1.0f + g4.w);
+    const int c = j / (VEC / 4), part_j = j % (VEC / 4);
+    gsv[part_j * nchunks + c] = g4;
   }
   __syncthreads();
 
@@ -135,11 +139,13 @@ __global__ void __launch_bounds__(kMaxThreads, 1) rn_bwd_kernel(const BwdParams 
   for (int g = 0; g < NG; ++g) {
     const int v = g * TH + t;
 #pragma unroll
-    for (int i = 0; i < PAIRS; ++i)
-      g2[g][i] = (v < nchunks) ? make_float2(gs[v * VEC + 2 * i], gs[v * VEC + 2 * i + 1])
-                               : make_float2(0.f, 0.f);
+    for (int i = 0; i < PAIRS; i += 2) {
+      const float4 g4 = (v < nchunks) ? gsv[(i / 2) * nchunks + v] : make_float4(0.f, 0.f, 0.f, 0.f);
+      g2[g][i] = make_float2(g4.x, g4.y);
+      g2[g][i + 1] = make_float2(g4.z, g4.w);
+    }
   }
-  const float hf = (float)H;
+  const float inv_h = 1.0f / (float)H;
   const int nacc = LN ? 2 : 1;
 
   RingPos pos{0u, 0u};
@@ -173,7 +179,13 @@ __global__ void __launch_bounds__(kMaxThreads, 1) rn_bwd_kernel(const BwdParams 
         for (int cc = j * 32 + lane; cc < nchunks; cc += 32 * WPR) {
           const typename V::Raw xw = V::load(xr, cc);
           const typename V::Raw dw = V::load(dr, cc);
-          const float2* gp = reinterpret_cast<const float2*>(gs + cc * VEC);
+          float2 gp[PAIRS];
+#pragma unroll
+          for (int i = 0; i < PAIRS; i += 2) {
+            const float4 g4 = gsv[(i / 2) * nchunks + cc];
+            gp[i] = make_float2(g4.x, g4.y);
+            gp[i + 1] = make_float2(g4.z, g4.w);
+          }
 #pragma unroll
           for (int i = 0; i < PAIRS; ++i) {
             const float2 d = LN ? V::sub(xw, i, mu) : V::f32(xw, i);
@@ -198,8 +210,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) rn_bwd_kernel(const BwdParams 
         const float2 m = meta[pos.ahead(k, Q).slot];
         const float rs = m.y;
         // c1 = mean(dy), c2 = mean(dy * xhat) = rsigma * mean(dy * (x - mu))
-        st[k] = make_float4(LN ? m.x : 0.f, rs, LN ? __fdiv_rn(a1, hf) : 0.f,
-                            rs * __fdiv_rn(a2, hf));
+        st[k] = make_float4(LN ? m.x : 0.f, rs, LN ? a1 * inv_h : 0.f, rs * (a2 * inv_h));
       }
       consumer_sync(TH);
 
@@ -318,7 +329,9 @@ rn_status launch_t(const BwdParams& p, const Launch& l, cudaStream_t s) {
   if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)l.smem) !=
       cudaSuccess)
     return RN_ERR_CUDA;
-  k<<<l.grid, l.threads, l.smem, s>>>(p);
+  int grid = 1;
+  if (persistent_grid(k, l, &grid) != RN_OK) return RN_ERR_CUDA;
+  k<<<grid, l.threads, l.smem, s>>>(p);
   return cudaGetLastError() == cudaSuccess ? RN_OK : RN_ERR_CUDA;
 }
 

@@ -90,7 +90,9 @@ struct ColReduceParams {
 
 // launch shape shared by the persistent kernels
 struct Launch {
-  int grid;
+  int work;             // independent work items (tiles / chunks): grid upper bound
+  int sms;              // SMs the grid may use (SMs - sm_margin)
+  int per_sm;           // CTAs per SM the shared-memory plan was sized for
   int threads;          // consumer threads + one producer warp
   size_t smem;
 };
@@ -98,9 +100,24 @@ struct Launch {
 // per-device limits, queried once
 struct DeviceInfo {
   int sms;
-  int smem_optin;
+  int smem_optin;       // per CTA
+  int smem_per_sm;      // per SM
 };
 rn_status device_info(DeviceInfo* out);
+
+// Grid of a persistent kernel: min(work, sms * CTAs per SM), where CTAs per
+// SM is the planned count capped by what the kernel's resources allow.
+template <class Kernel>
+rn_status persistent_grid(Kernel k, const Launch& l, int* grid) {
+  int occ = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k, l.threads, l.smem) != cudaSuccess)
+    return RN_ERR_CUDA;
+  const int per = occ < 1 ? 1 : (occ < l.per_sm ? occ : l.per_sm);
+  const long long g = (long long)l.sms * per;
+  int n = (int)(g < l.work ? g : l.work);
+  *grid = n < 1 ? 1 : n;
+  return RN_OK;
+}
 
 // launch functions (one per translation unit family)
 rn_status launch_fwd(int nk, bool bf16, int ng, int qmode, const FwdParams& p, const Launch& l,

@@ -289,7 +289,9 @@ rn_status launch_t(const MxParams& p, const Launch& l, cudaStream_t s) {
   if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)l.smem) !=
       cudaSuccess)
     return RN_ERR_CUDA;
-  k<<<l.grid, l.threads, l.smem, s>>>(p);
+  int grid = 1;
+  if (persistent_grid(k, l, &grid) != RN_OK) return RN_ERR_CUDA;
+  k<<<grid, l.threads, l.smem, s>>>(p);
   return cudaGetLastError() == cudaSuccess ? RN_OK : RN_ERR_CUDA;
 }
 
