@@ -162,6 +162,35 @@ rn_status rn_rmsnorm_bwd(const void* dz, const void* x, rn_dtype dtype,
                          size_t* workspace_bytes, void* stream);
 
 /*
+ * LayerNorm backward that allocates nothing (the pages have no counterpart:
+ * this is an addition for callers that cannot allocate device memory where
+ * they run the backward, e.g. code that must not call cudaMalloc because it
+ * may synchronize the device, or that runs without an allocator of its own).
+ * Same arguments, arithmetic and results as rn_layernorm_bwd, minus the
+ * workspace: the dgamma/dbeta partial sums go to a fixed 16 MiB array that
+ * the library image places in the memory of every device that loads it and
+ * that stays there until the process exits.
+ *   - Limit: problems whose partials exceed 16 MiB (chunks * 2 * H * 4 bytes;
+ *     e.g. N = 3000, H = 5120 fits, N = 8192, H = 4096 does not) return
+ *     RN_ERR_WORKSPACE before anything is enqueued.
+ *   - The first call on each device looks up the array's device address
+ *     (with that device current); make that first call before any stream
+ *     capture.
+ *   - Every call on a device shares the one array, which keeps the last
+ *     call's contents; nothing in it needs to start at zero (each call
+ *     overwrites every partial it reads).  Calls whose kernels may overlap on
+ *     the GPU (different streams, or host threads without ordering) race on
+ *     the array and must be serialized by the caller.
+ * No cudaMalloc / cudaFree or other allocating call is made.
+ */
+rn_status rn_layernorm_bwd_noalloc(const void* dz, const void* x, rn_dtype dtype,
+                                   const float* mu, const float* rsigma,
+                                   const float* gamma, int64_t N, int64_t H,
+                                   int zero_centered_gamma, int sm_margin,
+                                   void* dx, float* dgamma, float* dbeta,
+                                   void* stream);
+
+/*
  * Quantization stage alone on caller-given fp32 values y [N, H] (the
  * page's UNFUSED path: norm, then a separate quantize).  Same output
  * descriptor and arithmetic as the fused forward for `mode`

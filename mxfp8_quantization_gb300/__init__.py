@@ -31,6 +31,7 @@ import torch
 
 __all__ = [
     "layernorm_fwd", "rmsnorm_fwd", "layernorm_bwd", "rmsnorm_bwd", "quantize_only",
+    "layernorm_bwd_noalloc",
     "bwd_workspace_bytes", "device_error", "Fp8Output", "MXFP8Output", "lib_path", "RNError",
     "QUANT_MODES",
 ]
@@ -82,11 +83,12 @@ def _load():
     lib.rn_layernorm_bwd.argtypes = [vp, vp, i32, vp, vp, vp, i64, i64, i32, i32, vp, vp, vp, vp, szp, vp]
     lib.rn_rmsnorm_bwd.argtypes = [vp, vp, i32, vp, vp, i64, i64, i32, i32, vp, vp, vp, szp, vp]
     lib.rn_quantize_only.argtypes = [vp, i64, i64, i32, outp, vp]
+    lib.rn_layernorm_bwd_noalloc.argtypes = [vp, vp, i32, vp, vp, vp, i64, i64, i32, i32, vp, vp, vp, vp]
     lib.rn_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint)]
     lib.rn_status_str.argtypes = [i32]
     lib.rn_status_str.restype = ctypes.c_char_p
     for f in ("rn_layernorm_fwd", "rn_rmsnorm_fwd", "rn_layernorm_bwd", "rn_rmsnorm_bwd",
-              "rn_quantize_only", "rn_device_error", "rn_abi_version"):
+              "rn_quantize_only", "rn_device_error", "rn_abi_version", "rn_layernorm_bwd_noalloc"):
         getattr(lib, f).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -281,6 +283,28 @@ def rmsnorm_bwd(dz, x, rsigma, gamma, sm_margin=0, zero_centered_gamma=False, wo
                             _ptr(ws), ctypes.byref(n), _stream())
     _check(st, "rn_rmsnorm_bwd")
     return dx, dgamma
+
+
+def layernorm_bwd_noalloc(dz, x, mu, rsigma, gamma, sm_margin=0, zero_centered_gamma=False):
+    """LayerNorm backward -> (dx, dgamma, dbeta) without a workspace: the
+    library's fixed per-device scratch array holds the partial sums (for
+    callers that cannot allocate device memory; see include/rn.h for its size
+    limit and the rule that overlapping calls race)."""
+    lib = _load()
+    _need(x, "x")
+    N, H = x.shape
+    _need(dz, "dz", x.dtype, (N, H))
+    _need(mu, "mu", torch.float32, (N,))
+    _need(rsigma, "rsigma", torch.float32, (N,))
+    _need(gamma, "gamma", torch.float32, (H,))
+    dx = torch.empty_like(x)
+    dgamma = torch.empty(H, dtype=torch.float32, device=x.device)
+    dbeta = torch.empty(H, dtype=torch.float32, device=x.device)
+    st = lib.rn_layernorm_bwd_noalloc(_ptr(dz), _ptr(x), _dtype_code(x), _ptr(mu), _ptr(rsigma),
+                                      _ptr(gamma), N, H, int(bool(zero_centered_gamma)),
+                                      int(sm_margin), _ptr(dx), _ptr(dgamma), _ptr(dbeta), _stream())
+    _check(st, "rn_layernorm_bwd_noalloc")
+    return dx, dgamma, dbeta
 
 
 def quantize_only(y, quant, scale=None, rowwise=True, colwise=True):

@@ -477,3 +477,57 @@ rn_status rn_device_error(unsigned int* code) {
 int rn_abi_version(void) { return 1; }
 
 }  // extern "C"
+
+// ------------------------------------------ LayerNorm backward, no allocation
+// rn_layernorm_bwd needs a caller-allocated workspace for its dgamma/dbeta
+// partial sums.  Callers that cannot allocate device memory where they run
+// the backward get rn_layernorm_bwd_noalloc instead: the partials live in a
+// fixed array that is part of the library's device image.
+namespace rn {
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = size_t(16) << 20;  // 16 MiB per device
+
+// Loaded with the library on every device that runs its kernels and held
+// until the process exits.  Host code must not pass this symbol to a kernel:
+// on the host it is only a stand-in; the device address comes from
+// cudaGetSymbolAddress below.
+__device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+std::atomic<void*> g_noalloc_addr[kMaxDevices];
+
+// Device address of the scratch array on the current device, looked up once
+// per device (with that device current) and cached.
+rn_status noalloc_scratch(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return RN_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return RN_ERR_UNSUPPORTED;
+  void* p = g_noalloc_addr[dev].load(std::memory_order_acquire);
+  if (p == nullptr) {
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr)
+      return RN_ERR_CUDA;
+    g_noalloc_addr[dev].store(p, std::memory_order_release);
+  }
+  *out = p;
+  return RN_OK;
+}
+
+}  // namespace
+}  // namespace rn
+
+extern "C" rn_status rn_layernorm_bwd_noalloc(const void* dz, const void* x, rn_dtype dtype,
+                                              const float* mu, const float* rsigma,
+                                              const float* gamma, int64_t N, int64_t H,
+                                              int zero_centered_gamma, int sm_margin, void* dx,
+                                              float* dgamma, float* dbeta, void* stream) {
+  size_t need = 0;
+  rn_status st = bwd_common(true, nullptr, nullptr, dtype, nullptr, nullptr, nullptr, N, H, 0, 0,
+                            nullptr, nullptr, nullptr, nullptr, &need, nullptr);
+  if (st != RN_OK) return st;
+  if (need > kNoAllocScratchBytes) return RN_ERR_WORKSPACE;
+  void* scratch = nullptr;
+  if ((st = noalloc_scratch(&scratch)) != RN_OK) return st;
+  size_t cap = kNoAllocScratchBytes;
+  return bwd_common(true, dz, x, dtype, mu, rsigma, gamma, N, H, zero_centered_gamma, sm_margin,
+                    dx, dgamma, dbeta, scratch, &cap, static_cast<cudaStream_t>(stream));
+}
