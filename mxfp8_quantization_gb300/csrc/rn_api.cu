@@ -69,17 +69,9 @@ namespace {
 // ---------------------------------------------------------------- planning
 struct RowPlan {
   int ng, T, wpr, Q;
+  int apply_warps, stats_warps;
   Launch l;
 };
-
-// rows per tile: start from one row per consumer warp (at least 8) and
-// halve while the tile would take more than a third of the ring, so that
-// rows keep streaming in while a tile is being worked on
-int pick_tile(int w, int q) {
-  int T = w > 8 ? w : 8;
-  while (T > 1 && 3 * T > q) T /= 2;
-  return T;
-}
 
 // shared memory one CTA may use when per_sm CTAs share an SM (the runtime
 // reserves 1 KB per CTA)
@@ -89,58 +81,96 @@ size_t cta_smem_budget(const DeviceInfo& di, int per_sm) {
   return (size_t)(b < cap ? b : cap);
 }
 
-// row-wise forward: ring of Q row slots, tiles of T rows.  Two CTAs of at
-// most 256 consumer threads per SM when each still holds a ring of >= 6 rows
-// (their tile barriers then overlap), else one CTA of up to 512.
-rn_status plan_fwd(int H, int esz, int N, int sm_margin, const DeviceInfo& di, RowPlan* pl) {
-  const int vec = 16 / esz;
-  const int nchunks = H / vec;
-  const size_t row_bytes = (size_t)H * esz;
-  // worst-case fixed part: stats [2][32] float2, slice partials [32] float4,
-  // amax scratch, alignment slack; per slot: the row, its (mu, rsigma) and
-  // two mbarriers
-  const size_t fixed = 2 * 32 * sizeof(float2) + 32 * 16 + 32 * sizeof(uint32_t) + 64;
-  const size_t per_slot = row_bytes + sizeof(float2) + 16;
-  for (int per_sm = 2; per_sm >= 1; --per_sm) {
-    const int ng = pick_ng(nchunks, per_sm == 2 ? 256 : kMaxConsumers, 4);
-    if (ng == 0) continue;
-    const size_t budget = cta_smem_budget(di, per_sm);
+// Warp roles of the row kernels: A apply warps (each thread owning NG
+// 16-byte chunks of every row), S = max(2, A/2) stats warps, one producer.
+// Compact shape: NG <= 2, A <= 8, two CTAs per SM when each still holds a
+// ring of >= 6 slots.  Otherwise the wide shape: one CTA per SM, NG in
+// {2, 4, 8}, A <= 16.
+struct Roles {
+  int ng, A, S, per_sm, Q;
+};
+
+rn_status plan_roles(int nchunks, size_t per_slot, size_t fixed, const DeviceInfo& di, int q_cap,
+                     Roles* r) {
+  if (nchunks <= 512) {
+    const int ng = nchunks <= 256 ? 1 : 2;
+    const size_t budget = cta_smem_budget(di, 2);
     int Q = budget > fixed ? (int)((budget - fixed) / per_slot) : 0;
-    if (Q > 128) Q = 128;
-    if (Q < (per_sm == 2 ? 6 : 2)) continue;
-    const int th = round_up((nchunks + ng - 1) / ng, 32);
-    const int w = th / 32;
-    const int T = pick_tile(w, Q);
-    pl->ng = ng;
-    pl->T = T;
-    pl->wpr = w > T ? w / T : 1;
-    pl->Q = Q;
-    pl->l.threads = th + 32;
-    pl->l.smem = (size_t)Q * per_slot + fixed;
-    pl->l.work = (N + T - 1) / T;
-    pl->l.sms = di.sms - sm_margin;
-    pl->l.per_sm = per_sm;
-    return RN_OK;
+    if (Q > q_cap) Q = q_cap;
+    if (Q >= 6) {
+      r->ng = ng;
+      r->A = round_up((nchunks + ng - 1) / ng, 32) / 32;
+      r->S = r->A / 2 > 2 ? r->A / 2 : 2;
+      r->per_sm = 2;
+      r->Q = Q;
+      return RN_OK;
+    }
   }
-  return RN_ERR_UNSUPPORTED;
+  int ng = pick_ng(nchunks, 512, 8);
+  if (ng == 0) return RN_ERR_UNSUPPORTED;
+  if (ng < 2) ng = 2;
+  const size_t budget = cta_smem_budget(di, 1);
+  int Q = budget > fixed ? (int)((budget - fixed) / per_slot) : 0;
+  if (Q > q_cap) Q = q_cap;
+  if (Q < 2) return RN_ERR_UNSUPPORTED;
+  r->ng = ng;
+  r->A = round_up((nchunks + ng - 1) / ng, 32) / 32;
+  r->S = r->A / 2 > 2 ? r->A / 2 : 2;
+  r->per_sm = 1;
+  r->Q = Q;
+  return RN_OK;
 }
 
+// row-wise forward; T (rows per tile) is only the unit CTAs take turns on
+constexpr int kFwdTileRows = 4;
+
+rn_status plan_fwd(int H, int esz, int N, int sm_margin, const DeviceInfo& di, RowPlan* pl) {
+  const int nchunks = H * esz / 16;
+  // fixed: amax scratch + slack; per slot: the row, (mean, rsigma), three
+  // mbarriers
+  const size_t fixed = 32 * sizeof(uint32_t) + 64;
+  const size_t per_slot = (size_t)H * esz + sizeof(float2) + 24;
+  Roles r;
+  const rn_status st = plan_roles(nchunks, per_slot, fixed, di, 128, &r);
+  if (st != RN_OK) return st;
+  pl->ng = r.ng;
+  pl->T = kFwdTileRows;
+  pl->wpr = 1;
+  pl->apply_warps = r.A;
+  pl->stats_warps = r.S;
+  pl->Q = r.Q;
+  pl->l.threads = 32 * (r.A + r.S + 1);
+  pl->l.smem = (size_t)r.Q * per_slot + fixed;
+  pl->l.work = (N + kFwdTileRows - 1) / kFwdTileRows;
+  pl->l.sms = di.sms - sm_margin;
+  pl->l.per_sm = r.per_sm;
+  return RN_OK;
+}
+
+// MXFP8: apply threads own 8 columns each (A = H/256 warps, at most 12),
+// S = max(2, A/2) stats warps (fewer when A + S would pass 15), a producer;
+// one CTA per SM with a ring of at least 33 rows (a 32-row tile plus
+// look-ahead).
 rn_status plan_mx(int H, int esz, int N, int sm_margin, const DeviceInfo& di, RowPlan* pl) {
-  const int nchunks = H / 4;
-  const int ng = pick_ng(nchunks, kMaxConsumers, 2);
-  if (ng == 0) return RN_ERR_UNSUPPORTED;
-  const int th = round_up((nchunks + ng - 1) / ng, 32);
+  const int nchunks = H / 8;
+  const int A = (nchunks + 31) / 32;
+  if (A > 12) return RN_ERR_UNSUPPORTED;
+  int S = A / 2 > 2 ? A / 2 : 2;
+  if (A + S > 15) S = 15 - A;
   const size_t row_bytes = (size_t)H * esz;
-  const size_t fixed = 2 * 32 * sizeof(float2) + 64;
-  const size_t avail = (size_t)di.smem_optin > fixed ? di.smem_optin - fixed : 0;
-  int Q = (int)(avail / (row_bytes + 16));
+  const size_t fixed = 64;
+  const size_t per_slot = row_bytes + sizeof(float2) + 24;
+  const size_t budget = cta_smem_budget(di, 1);
+  int Q = budget > fixed ? (int)((budget - fixed) / per_slot) : 0;
   if (Q > 128) Q = 128;
   if (Q < 33) return RN_ERR_UNSUPPORTED;
-  pl->ng = ng;
+  pl->ng = 1;
   pl->T = 32;
   pl->Q = Q;
-  pl->l.threads = th + 32;
-  pl->l.smem = (size_t)Q * row_bytes + fixed + (size_t)Q * 16;
+  pl->apply_warps = A;
+  pl->stats_warps = S;
+  pl->l.threads = 32 * (A + S + 1);
+  pl->l.smem = (size_t)Q * per_slot + fixed;
   pl->l.work = N / 32;
   pl->l.sms = di.sms - sm_margin;
   pl->l.per_sm = 1;
@@ -266,6 +296,8 @@ rn_status fwd_common(int nk, const void* x, rn_dtype dt, const float* gamma, con
     p.eps = eps;
     p.zcg = zcg ? 1 : 0;
     p.Q = pl.Q;
+    p.apply_warps = pl.apply_warps;
+    p.stats_warps = pl.stats_warps;
     p.n_tiles = (int)(N / 32);
     return launch_mx(nk, bf16, pl.ng, p, pl.l, stream);
   }
@@ -289,7 +321,8 @@ rn_status fwd_common(int nk, const void* x, rn_dtype dt, const float* gamma, con
   p.zcg = zcg ? 1 : 0;
   p.out_f32 = (mode == RN_QUANT_NONE && out->out_dtype == RN_F32) ? 1 : 0;
   p.T = pl.T;
-  p.wpr = pl.wpr;
+  p.apply_warps = pl.apply_warps;
+  p.stats_warps = pl.stats_warps;
   p.Q = pl.Q;
   p.n_tiles = (int)((N + pl.T - 1) / pl.T);
   p.reverse = 0;
@@ -347,34 +380,21 @@ rn_status bwd_common(bool ln, const void* dz, const void* x, rn_dtype dt, const 
   }
   const int esz = elem_size(dt);
   const size_t row_bytes = (size_t)H * esz;
-  // fixed: g [H] (as float4 parts of each chunk), stats [2][8] float4,
-  // slice partials [32] float2, slack; per slot: the x and dz rows,
-  // (mu, rsigma), two mbarriers.  Two CTAs (<= 256 consumer threads) per SM
-  // when each holds >= 6 slots, else one CTA of up to 512.
-  const size_t fixed = (size_t)H * sizeof(float) + 2 * kBwdTileRows * sizeof(float4) +
-                       32 * sizeof(float2) + 64;
-  const size_t per_slot = 2 * row_bytes + sizeof(float2) + 16;
-  int Q = 0, per_sm = 2, ng = 0;
-  for (; per_sm >= 1; --per_sm) {
-    ng = pick_ng((int)(H * esz / 16), per_sm == 2 ? 256 : kMaxConsumers, 4);
-    if (ng == 0) continue;
-    const size_t budget = cta_smem_budget(di, per_sm);
-    Q = budget > fixed ? (int)((budget - fixed) / per_slot) : 0;
-    if (Q > 64) Q = 64;
-    if (Q >= (per_sm == 2 ? 6 : 2)) break;
-  }
-  if (per_sm < 1) return RN_ERR_UNSUPPORTED;
+  // roles as in the forward (plan_roles).  fixed: g [H] (as float4 parts of
+  // each chunk) + slack; per slot: the x and dz rows, (mu, rsigma) as
+  // loaded, (mu, rsigma, c1, c2), three mbarriers.
   const int nch = (int)(H * esz / 16);
-  const int th = round_up((nch + ng - 1) / ng, 32);
-  const int w = th / 32;
-  int T = kBwdTileRows;                   // divides every chunk
-  while (T > 1 && 3 * T > Q) T /= 2;
+  const size_t fixed = (size_t)H * sizeof(float) + 64;
+  const size_t per_slot = 2 * row_bytes + sizeof(float2) + sizeof(float4) + 24;
+  Roles ro;
+  if ((st = plan_roles(nch, per_slot, fixed, di, 64, &ro)) != RN_OK) return st;
+  const int ng = ro.ng, A = ro.A, S = ro.S, Q = ro.Q;
   Launch l;
-  l.threads = th + 32;
+  l.threads = 32 * (A + S + 1);
   l.smem = (size_t)Q * per_slot + fixed;
   l.work = sh.n_chunks;
   l.sms = di.sms - sm_margin;
-  l.per_sm = per_sm;
+  l.per_sm = ro.per_sm;
 
   BwdParams p{};
   p.dz = dz;
@@ -387,11 +407,10 @@ rn_status bwd_common(bool ln, const void* dz, const void* x, rn_dtype dt, const 
   p.N = (int)N;
   p.H = (int)H;
   p.zcg = zcg ? 1 : 0;
-  p.T = T;
-  p.wpr = w > T ? w / T : 1;
-  p.tiles_per_chunk = sh.chunk_rows / T;
+  p.chunk_rows = sh.chunk_rows;
+  p.apply_warps = A;
+  p.stats_warps = S;
   p.Q = Q;
-  p.n_tiles = (int)((N + T - 1) / T);
   p.n_chunks = sh.n_chunks;
   if ((st = launch_bwd(ln, dt == RN_BF16, ng, p, l, stream)) != RN_OK) return st;
   ColReduceParams c{};

@@ -8,21 +8,21 @@
 //   RMSNorm    dx = rsigma * (dy - xhat * mean(dy * xhat))
 //   dgamma = sum_rows dz * xhat,  dbeta = sum_rows dz.
 //
-// Kernel 1 (persistent, warp-specialized like the forward): the producer
-// lane streams the x row and the dz row of each row into one shared-memory
-// slot with two bulk copies; the consumers take tiles of T rows:
-//   phase 1  the two row means mean(dy), mean(dy * xhat): WPR warps share a
-//            row (one when rows are short), each summing an interleaved slice
-//            of its chunks; the slices are added in slice order (g is read
-//            from a shared-memory copy; mu / rsigma arrive with the row, by
-//            4-byte cp.async on the row's barrier);
-//   phase 2  each thread owns fixed 16-byte column chunks: dx for every row
-//            of the tile, plus running per-column sums of dz * xhat and dz
-//            in registers.
-// Rows are grouped in fixed chunks of tiles_per_chunk * T rows; at the end
-// of a chunk its column sums are written to the workspace as one fp32
-// partial row.  The chunk size depends on N and H only, and each partial is
-// summed in row order, so the partials do not depend on the grid.
+// Kernel 1 (persistent, warp-specialized like the forward, no CTA-wide
+// barrier on the row path): the producer lane streams the x row and the dz
+// row of each row into one shared-memory slot with two bulk copies, and its
+// saved mu / rsigma with 4-byte cp.async, all on the slot's "full" barrier;
+//   stats warps  take rows in turn and form the two row means mean(dy) and
+//                mean(dy * xhat) (g from a shared-memory copy laid out for
+//                conflict-free reads), published on the slot's "ready"
+//                barrier;
+//   apply warps  own fixed 16-byte column chunks: dx for every row in order,
+//                plus running per-column sums of dz * xhat and dz in
+//                registers; they release the slot ("empty").
+// Rows are grouped in fixed chunks of chunk_rows rows; at the end of a chunk
+// its column sums are written to the workspace as one fp32 partial row.  The
+// chunk size depends on N only, and each partial is summed in row order, so
+// the partials do not depend on the grid.
 // Kernel 2 adds the partials of each column in a fixed order that depends
 // on the chunk count only.  Arithmetic is on element pairs (f32x2), with
 // bf16 inputs entering through the mixed-precision forms.
@@ -36,7 +36,10 @@ namespace {
 
 __device__ unsigned g_err_bwd;
 
-constexpr int kMaxThreads = 512 + 32;
+// compact shape: at most 8 apply + 4 stats warps + the producer, two CTAs
+// per SM; wide shape: up to 16 apply + 8 stats warps + the producer, one CTA
+constexpr int kMaxThreads = 416;
+constexpr int kMaxThreadsWide = 800;
 
 template <typename TIn>
 __device__ __forceinline__ void store_dx(void* base, size_t elem, const float2* d);
@@ -53,37 +56,38 @@ __device__ __forceinline__ void store_dx<float>(void* base, size_t elem, const f
   *reinterpret_cast<float4*>(static_cast<float*>(base) + elem) = make_float4(d[0].x, d[0].y, d[1].x, d[1].y);
 }
 
-template <typename TIn, int NG, bool LN>
-__global__ void __launch_bounds__(kMaxThreads, 1) rn_bwd_kernel(const BwdParams p) {
+template <typename TIn, int NG, bool LN, bool WIDE>
+__global__ void __launch_bounds__(WIDE ? kMaxThreadsWide : kMaxThreads, WIDE ? 1 : 2)
+    rn_bwd_kernel(const BwdParams p) {
   constexpr int VEC = 16 / (int)sizeof(TIn);
   using V = Vec<TIn, VEC>;
   constexpr int PAIRS = V::PAIRS;
   extern __shared__ __align__(128) unsigned char smem[];
 
-  const int TH = blockDim.x - 32;
-  const int W = TH >> 5;
+  const int A = p.apply_warps;          // warps 0 .. A-1
+  const int S = p.stats_warps;          // warps A .. A+S-1; producer: A+S
+  const int TH = A * 32;
   const int H = p.H;
   const int nchunks = H / VEC;
   const uint32_t row_bytes = (uint32_t)H * sizeof(TIn);
   const uint32_t slot_bytes = 2 * row_bytes;  // x row, then dz row
   const uint32_t Q = (uint32_t)p.Q;
-  const int T = p.T;
-  const int WPR = p.wpr;
 
   unsigned char* ring = smem;
   // g as [VEC/4][nchunks] float4: part j of chunk c at gsv[j * nchunks + c],
   // so that 32 lanes reading 32 consecutive chunks touch consecutive 16 bytes
   float4* gsv = reinterpret_cast<float4*>(smem + (size_t)Q * slot_bytes);
-  float4* stats = gsv + (size_t)(VEC / 4) * nchunks;                      // [2][T]
-  float2* part = reinterpret_cast<float2*>(stats + 2 * T);               // [T * WPR]
-  float2* meta = part + T * WPR;                                         // [Q] (mu, rsigma)
+  float4* rstat = gsv + (size_t)(VEC / 4) * nchunks;   // [Q] (mu, rsigma, c1, c2)
+  float2* meta = reinterpret_cast<float2*>(rstat + Q);  // [Q] (mu, rsigma) as loaded
   uint64_t* full = reinterpret_cast<uint64_t*>(meta + Q);
-  uint64_t* empty = full + Q;
+  uint64_t* ready = full + Q;
+  uint64_t* empty = ready + Q;
 
   if (threadIdx.x == 0) {
     for (uint32_t i = 0; i < Q; ++i) {
       mbar_init(smem_u32(&full[i]), 2);  // bulk copies + the mu/rsigma cp.async
-      mbar_init(smem_u32(&empty[i]), W);
+      mbar_init(smem_u32(&ready[i]), 1);
+      mbar_init(smem_u32(&empty[i]), A);
     }
     fence_barrier_init();
   }
@@ -98,32 +102,29 @@ __global__ void __launch_bounds__(kMaxThreads, 1) rn_bwd_kernel(const BwdParams 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int G = gridDim.x;
-  const int tpc = p.tiles_per_chunk;
+  const int R = p.chunk_rows;
 
-  if (warp == W) {
+  if (warp == A + S) {
+    // ------------------------------------------------------------ producer
     if (lane == 0) {
       const unsigned char* xb = static_cast<const unsigned char*>(p.x);
       const unsigned char* db = static_cast<const unsigned char*>(p.dz);
       RingPos pos{0u, 0u};
       uint32_t issued = 0;
       for (int c = blockIdx.x; c < p.n_chunks; c += G) {
-        const int t1 = min((c + 1) * tpc, p.n_tiles);
-        for (int tt = c * tpc; tt < t1; ++tt) {
-          const int r0 = tt * T;
-          const int r1 = min(r0 + T, p.N);
-          for (int r = r0; r < r1; ++r, ++issued) {
-            const uint32_t s = pos.slot;
-            if (issued >= Q) mbar_wait(smem_u32(&empty[s]), pos.phase ^ 1u, &g_err_bwd, kErrEmptyWait);
-            const uint32_t bar = smem_u32(&full[s]);
-            if (LN) cp_async4(smem_u32(&meta[s].x), p.mu + r);
-            cp_async4(smem_u32(&meta[s].y), p.rsigma + r);
-            cp_async_arrive(bar);
-            mbar_arrive_expect_tx(bar, slot_bytes);
-            const uint32_t dst = smem_u32(ring + (size_t)s * slot_bytes);
-            bulk_g2s(dst, xb + (size_t)r * row_bytes, row_bytes, bar);
-            bulk_g2s(dst + row_bytes, db + (size_t)r * row_bytes, row_bytes, bar);
-            pos.advance(1, Q);
-          }
+        const int r1 = min((c + 1) * R, p.N);
+        for (int r = c * R; r < r1; ++r, ++issued) {
+          const uint32_t s = pos.slot;
+          if (issued >= Q) mbar_wait(smem_u32(&empty[s]), pos.phase ^ 1u, &g_err_bwd, kErrEmptyWait);
+          const uint32_t bar = smem_u32(&full[s]);
+          if (LN) cp_async4(smem_u32(&meta[s].x), p.mu + r);
+          cp_async4(smem_u32(&meta[s].y), p.rsigma + r);
+          cp_async_arrive(bar);
+          mbar_arrive_expect_tx(bar, slot_bytes);
+          const uint32_t dst = smem_u32(ring + (size_t)s * slot_bytes);
+          bulk_g2s(dst, xb + (size_t)r * row_bytes, row_bytes, bar);
+          bulk_g2s(dst + row_bytes, db + (size_t)r * row_bytes, row_bytes, bar);
+          pos.advance(1, Q);
         }
       }
       const uint32_t first = issued > Q ? issued - Q : 0;
@@ -133,6 +134,58 @@ __global__ void __launch_bounds__(kMaxThreads, 1) rn_bwd_kernel(const BwdParams 
     return;
   }
 
+  if (warp >= A) {
+    // --------------------------------------------------------- stats warps
+    // stats warp j takes rows j, j + S, ... of the CTA's sequence: the two
+    // row sums of dy = dz * g and dy * (x - mu) (RMSNorm: dy * x), giving
+    // c1 = mean(dy) and c2 = mean(dy * xhat) = rsigma * mean(dy * (x - mu))
+    const int j = warp - A;
+    const float inv_h = 1.0f / (float)H;
+    RingPos pos{0u, 0u};
+    int q = 0;
+    for (int c = blockIdx.x; c < p.n_chunks; c += G) {
+      const int r1 = min((c + 1) * R, p.N);
+      for (int r = c * R; r < r1; ++r, ++q) {
+        if (q % S == j) {
+          const uint32_t s = pos.slot;
+          mbar_wait(smem_u32(&full[s]), pos.phase, &g_err_bwd, kErrStatsWait);
+          const unsigned char* xr = ring + (size_t)s * slot_bytes;
+          const unsigned char* dr = xr + row_bytes;
+          const float2 m = meta[s];
+          const float mu = LN ? m.x : 0.f;
+          float2 s1 = make_float2(0.f, 0.f), s2 = make_float2(0.f, 0.f);
+          for (int cc = lane; cc < nchunks; cc += 32) {
+            const typename V::Raw xw = V::load(xr, cc);
+            const typename V::Raw dw = V::load(dr, cc);
+            float2 gp[PAIRS];
+#pragma unroll
+            for (int i = 0; i < PAIRS; i += 2) {
+              const float4 g4 = gsv[(i / 2) * nchunks + cc];
+              gp[i] = make_float2(g4.x, g4.y);
+              gp[i + 1] = make_float2(g4.z, g4.w);
+            }
+#pragma unroll
+            for (int i = 0; i < PAIRS; ++i) {
+              const float2 d = LN ? V::sub(xw, i, mu) : V::f32(xw, i);
+              const float2 dy = mul2(V::f32(dw, i), gp[i]);
+              s1 = add2(s1, dy);
+              s2 = fma2(dy, d, s2);
+            }
+          }
+          const float a1 = warp_sum(s1.x + s1.y);
+          const float a2 = warp_sum(s2.x + s2.y);
+          if (lane == 0) {
+            rstat[s] = make_float4(mu, m.y, LN ? a1 * inv_h : 0.f, m.y * (a2 * inv_h));
+            mbar_arrive(smem_u32(&ready[s]));
+          }
+        }
+        pos.advance(1, Q);
+      }
+    }
+    return;
+  }
+
+  // ---------------------------------------------------------- apply warps
   const int t = threadIdx.x;
   float2 g2[NG][PAIRS];
 #pragma unroll
@@ -145,11 +198,9 @@ __global__ void __launch_bounds__(kMaxThreads, 1) rn_bwd_kernel(const BwdParams 
       g2[g][i + 1] = make_float2(g4.z, g4.w);
     }
   }
-  const float inv_h = 1.0f / (float)H;
   const int nacc = LN ? 2 : 1;
 
   RingPos pos{0u, 0u};
-  int it = 0;
   for (int c = blockIdx.x; c < p.n_chunks; c += G) {
     float2 adg[NG][PAIRS], adb[NG][PAIRS];
 #pragma unroll
@@ -159,93 +210,37 @@ __global__ void __launch_bounds__(kMaxThreads, 1) rn_bwd_kernel(const BwdParams 
         adg[g][i] = make_float2(0.f, 0.f);
         adb[g][i] = make_float2(0.f, 0.f);
       }
-    const int t1 = min((c + 1) * tpc, p.n_tiles);
-    for (int tt = c * tpc; tt < t1; ++tt, ++it) {
-      const int r0 = tt * T;
-      const int nrows = min(T, p.N - r0);
-      float4* st = stats + (it & 1) * T;
-
-      // ------------------------------------------- phase 1: row reductions
-      // WPR warps share a row: warp (k, j) sums chunks j*32 + lane + i*32*WPR
-      // of sum(dy) and sum(dy * (x - mu)) (RMSNorm: sum(dy * x))
-      for (int item = warp; item < nrows * WPR; item += W) {
-        const int k = item / WPR, j = item - k * WPR;
-        const RingPos rp = pos.ahead(k, Q);
-        mbar_wait(smem_u32(&full[rp.slot]), rp.phase, &g_err_bwd, kErrFullWait);
-        const unsigned char* xr = ring + (size_t)rp.slot * slot_bytes;
-        const unsigned char* dr = xr + row_bytes;
-        const float mu = LN ? meta[rp.slot].x : 0.f;
-        float2 s1 = make_float2(0.f, 0.f), s2 = make_float2(0.f, 0.f);
-        for (int cc = j * 32 + lane; cc < nchunks; cc += 32 * WPR) {
-          const typename V::Raw xw = V::load(xr, cc);
-          const typename V::Raw dw = V::load(dr, cc);
-          float2 gp[PAIRS];
+    const int r1 = min((c + 1) * R, p.N);
+    for (int r = c * R; r < r1; ++r) {
+      const uint32_t s = pos.slot;
+      mbar_wait(smem_u32(&full[s]), pos.phase, &g_err_bwd, kErrFullWait);
+      mbar_wait(smem_u32(&ready[s]), pos.phase, &g_err_bwd, kErrReadyWait);
+      const float4 m = rstat[s];
+      const unsigned char* xr = ring + (size_t)s * slot_bytes;
+      const unsigned char* dr = xr + row_bytes;
+      const size_t rowe = (size_t)r * H;
 #pragma unroll
-          for (int i = 0; i < PAIRS; i += 2) {
-            const float4 g4 = gsv[(i / 2) * nchunks + cc];
-            gp[i] = make_float2(g4.x, g4.y);
-            gp[i + 1] = make_float2(g4.z, g4.w);
-          }
+      for (int g = 0; g < NG; ++g) {
+        const int v = g * TH + t;
+        if (v < nchunks) {
+          const typename V::Raw xw = V::load(xr, v);
+          const typename V::Raw dw = V::load(dr, v);
+          float2 dx[PAIRS];
 #pragma unroll
           for (int i = 0; i < PAIRS; ++i) {
-            const float2 d = LN ? V::sub(xw, i, mu) : V::f32(xw, i);
-            const float2 dy = mul2(V::f32(dw, i), gp[i]);
-            s1 = add2(s1, dy);
-            s2 = fma2(dy, d, s2);
+            const float2 xh = mul2(LN ? V::sub(xw, i, m.x) : V::f32(xw, i), splat2(m.y));
+            const float2 dzf = V::f32(dw, i);
+            const float2 dy = mul2(dzf, g2[g][i]);
+            dx[i] = mul2(sub2(dy, fma2(xh, splat2(m.w), splat2(m.z))), splat2(m.y));
+            adg[g][i] = fma2(dzf, xh, adg[g][i]);
+            if (LN) adb[g][i] = add2(adb[g][i], dzf);
           }
+          store_dx<TIn>(p.dx, rowe + (size_t)v * VEC, dx);
         }
-        const float a1 = warp_sum(s1.x + s1.y);
-        const float a2 = warp_sum(s2.x + s2.y);
-        if (lane == 0) part[k * WPR + j] = make_float2(a1, a2);
       }
-      consumer_sync(TH);
-      if (t < nrows) {
-        const int k = t;
-        float a1 = 0.f, a2 = 0.f;
-        for (int j = 0; j < WPR; ++j) {
-          const float2 pj = part[k * WPR + j];
-          a1 += pj.x;
-          a2 += pj.y;
-        }
-        const float2 m = meta[pos.ahead(k, Q).slot];
-        const float rs = m.y;
-        // c1 = mean(dy), c2 = mean(dy * xhat) = rsigma * mean(dy * (x - mu))
-        st[k] = make_float4(LN ? m.x : 0.f, rs, LN ? a1 * inv_h : 0.f, rs * (a2 * inv_h));
-      }
-      consumer_sync(TH);
-
-      // ------------------------------------------------- phase 2: dx, sums
-      RingPos rp = pos;
-      for (int k = 0; k < nrows; ++k) {
-        mbar_wait(smem_u32(&full[rp.slot]), rp.phase, &g_err_bwd, kErrFullWait);
-        const float4 m = st[k];
-        const unsigned char* xr = ring + (size_t)rp.slot * slot_bytes;
-        const unsigned char* dr = xr + row_bytes;
-        const size_t rowe = (size_t)(r0 + k) * H;
-#pragma unroll
-        for (int g = 0; g < NG; ++g) {
-          const int v = g * TH + t;
-          if (v < nchunks) {
-            const typename V::Raw xw = V::load(xr, v);
-            const typename V::Raw dw = V::load(dr, v);
-            float2 dx[PAIRS];
-#pragma unroll
-            for (int i = 0; i < PAIRS; ++i) {
-              const float2 xh = mul2(LN ? V::sub(xw, i, m.x) : V::f32(xw, i), splat2(m.y));
-              const float2 dzf = V::f32(dw, i);
-              const float2 dy = mul2(dzf, g2[g][i]);
-              dx[i] = mul2(sub2(dy, fma2(xh, splat2(m.w), splat2(m.z))), splat2(m.y));
-              adg[g][i] = fma2(dzf, xh, adg[g][i]);
-              if (LN) adb[g][i] = add2(adb[g][i], dzf);
-            }
-            store_dx<TIn>(p.dx, rowe + (size_t)v * VEC, dx);
-          }
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&empty[rp.slot]));
-        rp.advance(1, Q);
-      }
-      pos = rp;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&empty[s]));
+      pos.advance(1, Q);
     }
     // chunk finished: write its partial column sums
     float* prow = p.part + (size_t)c * nacc * H;
@@ -254,12 +249,12 @@ __global__ void __launch_bounds__(kMaxThreads, 1) rn_bwd_kernel(const BwdParams 
       const int v = g * TH + t;
       if (v < nchunks) {
 #pragma unroll
-        for (int j = 0; j < PAIRS / 2; ++j) {
-          reinterpret_cast<float4*>(prow + (size_t)v * VEC)[j] =
-              make_float4(adg[g][2 * j].x, adg[g][2 * j].y, adg[g][2 * j + 1].x, adg[g][2 * j + 1].y);
+        for (int jj = 0; jj < PAIRS / 2; ++jj) {
+          reinterpret_cast<float4*>(prow + (size_t)v * VEC)[jj] =
+              make_float4(adg[g][2 * jj].x, adg[g][2 * jj].y, adg[g][2 * jj + 1].x, adg[g][2 * jj + 1].y);
           if (LN)
-            reinterpret_cast<float4*>(prow + H + (size_t)v * VEC)[j] =
-                make_float4(adb[g][2 * j].x, adb[g][2 * j].y, adb[g][2 * j + 1].x, adb[g][2 * j + 1].y);
+            reinterpret_cast<float4*>(prow + H + (size_t)v * VEC)[jj] =
+                make_float4(adb[g][2 * jj].x, adb[g][2 * jj].y, adb[g][2 * jj + 1].x, adb[g][2 * jj + 1].y);
         }
       }
     }
@@ -323,9 +318,9 @@ __global__ void __launch_bounds__(1024) rn_colreduce_kernel(const ColReduceParam
   }
 }
 
-template <typename TIn, int NG, bool LN>
+template <typename TIn, int NG, bool LN, bool WIDE>
 rn_status launch_t(const BwdParams& p, const Launch& l, cudaStream_t s) {
-  auto k = rn_bwd_kernel<TIn, NG, LN>;
+  auto k = rn_bwd_kernel<TIn, NG, LN, WIDE>;
   if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)l.smem) !=
       cudaSuccess)
     return RN_ERR_CUDA;
@@ -335,12 +330,22 @@ rn_status launch_t(const BwdParams& p, const Launch& l, cudaStream_t s) {
   return cudaGetLastError() == cudaSuccess ? RN_OK : RN_ERR_CUDA;
 }
 
+// compact shape for NG 1 and 2; wide shape for NG 2, 4 and 8
 template <typename TIn, bool LN>
 rn_status launch_ng(int ng, const BwdParams& p, const Launch& l, cudaStream_t s) {
+  const bool wide = l.threads > kMaxThreads || l.per_sm == 1;
+  if (!wide) {
+    switch (ng) {
+      case 1: return launch_t<TIn, 1, LN, false>(p, l, s);
+      case 2: return launch_t<TIn, 2, LN, false>(p, l, s);
+      default: return RN_ERR_UNSUPPORTED;
+    }
+  }
+  if (l.threads > kMaxThreadsWide) return RN_ERR_UNSUPPORTED;
   switch (ng) {
-    case 1: return launch_t<TIn, 1, LN>(p, l, s);
-    case 2: return launch_t<TIn, 2, LN>(p, l, s);
-    case 4: return launch_t<TIn, 4, LN>(p, l, s);
+    case 2: return launch_t<TIn, 2, LN, true>(p, l, s);
+    case 4: return launch_t<TIn, 4, LN, true>(p, l, s);
+    case 8: return launch_t<TIn, 8, LN, true>(p, l, s);
     default: return RN_ERR_UNSUPPORTED;
   }
 }

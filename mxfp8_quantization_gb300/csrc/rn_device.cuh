@@ -14,18 +14,16 @@ namespace rn {
 
 // error codes recorded in the device error word
 enum : unsigned {
-  kErrFullWait = 1,   // a consumer gave up waiting for a row to land
-  kErrEmptyWait = 2,  // the producer gave up waiting for a slot to free
-  kErrDrainWait = 3,  // the producer gave up waiting for its last copies
+  kErrFullWait = 1,    // an apply warp gave up waiting for a row to land
+  kErrEmptyWait = 2,   // the producer gave up waiting for a slot to free
+  kErrDrainWait = 3,   // the producer gave up waiting for its last copies
+  kErrReadyWait = 4,   // an apply warp gave up waiting for a row's statistics
+  kErrStatsWait = 5,   // a stats warp gave up waiting for a row to land
 };
 
-constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s
-
-__device__ __forceinline__ unsigned long long global_ns() {
-  unsigned long long t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
+// wait limit in SM clock cycles (about 4 s at 1 GHz, 2 s at 2 GHz); the
+// per-SM cycle counter is monotonic, unlike a wall-clock timer
+constexpr long long kWaitLimitCycles = 4000000000ll;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -66,16 +64,16 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 }
 
 // Wait until the phase with `parity` of barrier `bar` has completed, for at
-// most kWaitLimitNs; on expiry record `code` in *err and return false.  Once
+// most kWaitLimitCycles; on expiry record `code` in *err and return false.  Once
 // an error is recorded, later waits that do not succeed at once give up
 // immediately, so a kernel that lost its pipeline finishes quickly (its
 // results are then meaningless; the host reads the error word).
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigned* err,
                                           unsigned code) {
   if (mbar_try_wait(bar, parity)) return true;
-  const unsigned long long t0 = global_ns();
+  const long long t0 = clock64();
   while (!mbar_try_wait(bar, parity)) {
-    if (*reinterpret_cast<volatile unsigned*>(err) != 0u || global_ns() - t0 > kWaitLimitNs) {
+    if (*reinterpret_cast<volatile unsigned*>(err) != 0u || clock64() - t0 > kWaitLimitCycles) {
       atomicCAS(err, 0u, code);
       return false;
     }
@@ -343,6 +341,28 @@ struct Vec<float, 4> {  // fp32, 16 bytes
   __device__ __forceinline__ static Raw load(const unsigned char* p, int c) {
     const float4 v = *reinterpret_cast<const float4*>(p + (size_t)c * 16);
     return Raw{{make_float2(v.x, v.y), make_float2(v.z, v.w)}};
+  }
+  __device__ __forceinline__ static float2 f32(const Raw& r, int i) { return r.p[i]; }
+  __device__ __forceinline__ static float2 sub(const Raw& r, int i, float m) {
+    return sub2(r.p[i], splat2(m));
+  }
+  __device__ __forceinline__ static void acc(float2& a, const Raw& r, int i) { a = add2(a, r.p[i]); }
+  __device__ __forceinline__ static void sq_acc(float2& a, const Raw& r, int i) {
+    a = fma2(r.p[i], r.p[i], a);
+  }
+};
+
+template <>
+struct Vec<float, 8> {  // fp32, 32 bytes
+  static constexpr int PAIRS = 4;
+  struct Raw {
+    float2 p[4];
+  };
+  __device__ __forceinline__ static Raw load(const unsigned char* p, int c) {
+    const float4* q = reinterpret_cast<const float4*>(p + (size_t)c * 32);
+    const float4 a = q[0], b = q[1];
+    return Raw{{make_float2(a.x, a.y), make_float2(a.z, a.w), make_float2(b.x, b.y),
+                make_float2(b.z, b.w)}};
   }
   __device__ __forceinline__ static float2 f32(const Raw& r, int i) { return r.p[i]; }
   __device__ __forceinline__ static float2 sub(const Raw& r, int i, float m) {

@@ -3,25 +3,24 @@
 // section "Description": the fully fused delayed-scaling path and both
 // passes of the norm+amax-then-quantize current-scaling path).
 //
-// Design (one persistent CTA per SM, warp-specialized):
-//   * warp W (the last one) is the producer: one lane streams whole rows of x
-//     into a ring of Q shared-memory slots with the bulk-copy engine
-//     (cp.async.bulk, completion on a per-slot "full" mbarrier) and refills a
-//     slot as soon as every consumer warp has released it ("empty" mbarrier);
-//     when a pass needs the saved mu / rsigma of a row, the same lane fetches
-//     them into the slot with 4-byte cp.async tracked by the same barrier;
-//   * consumer warps 0..W-1 take tiles of T rows:
-//       phase 1  the row statistics from shared memory: WPR warps share a
-//                row (one when rows are short), each taking an interleaved
-//                slice of its 16-byte chunks; LayerNorm slices are reduced
-//                exactly in two passes (slice mean, then centred sum of
-//                squares) and merged in slice order with Chan's pairwise
-//                update; RMSNorm slices give sums of squares, added in
-//                order; then mu / rsigma are written;
-//       phase 2  every consumer thread owns fixed 16-byte column chunks
-//                (gamma / beta live in its registers for the whole kernel) and
-//                forms y = (x-mu)*rsigma*g + beta (RMSNorm: x*rsigma*g) for
-//                each row of the tile, then stores bf16/fp32 or E4M3 codes;
+// Design (persistent CTAs, one or two per SM; warp-specialized, with no
+// CTA-wide barrier on the row path):
+//   * producer warp: one lane streams whole rows of x into a ring of Q
+//     shared-memory slots with the bulk-copy engine (cp.async.bulk,
+//     completion on the slot's "full" mbarrier) and refills a slot as soon as
+//     the apply warps have released it ("empty"); when a pass needs the saved
+//     mu / rsigma of a row, the same lane fetches them into the slot with
+//     4-byte cp.async tracked by the same barrier;
+//   * stats warps: warp j of S takes rows j, j+S, ... of the CTA's sequence
+//     and computes its statistics from shared memory (LayerNorm: two passes,
+//     mean then centred sum of squares; RMSNorm: sum of squares), writes
+//     mu / rsigma and publishes (mean, rsigma) on the slot's "ready"
+//     mbarrier;
+//   * apply warps: every thread owns fixed 16-byte column chunks (gamma /
+//     beta in registers for the whole kernel); for each row in order it waits
+//     for "ready", forms y = (x-mu)*rsigma*g + beta (RMSNorm: x*rsigma*g),
+//     stores bf16/fp32 or E4M3 codes, and releases the slot;
+//   so statistics of later rows are computed while earlier rows are applied.
 //   * arithmetic is done on pairs of elements with the packed fp32 (f32x2)
 //     instructions, and bf16 inputs enter through the mixed-precision
 //     add/sub/fma forms, which round exactly like convert-then-operate;
@@ -29,8 +28,9 @@
 //     atomicMax on the fp32 bit pattern (ordered like the values for
 //     non-negative numbers, NaN above +inf).
 // Current scaling runs the kernel twice: pass 1 (statistics + amax, no
-// output) and pass 2 (quantize with 448/amax), the second walking the tiles
-// backwards so that it starts on the rows pass 1 left in L2.
+// output) and pass 2 (quantize with 448/amax, no stats warps), the second
+// walking the tiles backwards so that it starts on the rows pass 1 left in
+// L2.
 #include <cuda_runtime.h>
 
 #include "rn_device.cuh"
@@ -41,7 +41,10 @@ namespace {
 
 __device__ unsigned g_err_fwd;
 
-constexpr int kMaxThreads = 512 + 32;
+// compact shape: at most 8 apply + 4 stats warps + the producer, two CTAs
+// per SM; wide shape: up to 16 apply + 8 stats warps + the producer, one CTA
+constexpr int kMaxThreads = 416;
+constexpr int kMaxThreadsWide = 800;
 
 // store the PAIRS y pairs of one chunk in the output format
 template <int PAIRS, int QM>
@@ -79,38 +82,55 @@ __device__ __forceinline__ void store_chunk(const FwdParams& p, size_t elem, con
   }
 }
 
-template <typename TIn, int NG, int NK, int QM>
-__global__ void __launch_bounds__(kMaxThreads, 1) rn_fwd_kernel(const FwdParams p) {
+// Enumerates the rows of this CTA in the order every role visits them:
+// tiles blockIdx.x, blockIdx.x + gridDim.x, ... (walked from the last tile
+// when reverse), T rows each.
+struct RowWalk {
+  int tk, r, r1;
+  __device__ __forceinline__ bool next(const FwdParams& p) {
+    if (++r < r1) return true;
+    tk = (tk < 0) ? (int)blockIdx.x : tk + (int)gridDim.x;
+    if (tk >= p.n_tiles) return false;
+    const int tt = p.reverse ? p.n_tiles - 1 - tk : tk;
+    r = tt * p.T;
+    r1 = min(r + p.T, p.N);
+    return true;
+  }
+};
+
+template <typename TIn, int NG, int NK, int QM, bool WIDE>
+__global__ void __launch_bounds__(WIDE ? kMaxThreadsWide : kMaxThreads, WIDE ? 1 : 2)
+    rn_fwd_kernel(const FwdParams p) {
   constexpr int VEC = 16 / (int)sizeof(TIn);
   using V = Vec<TIn, VEC>;
   constexpr int PAIRS = V::PAIRS;
   constexpr bool LN = (NK == kLn);
   // pass 2 of current scaling gets mu / rsigma with each row
   constexpr bool META = (QM == kQCurQuant && NK != kIdentity);
+  // rows whose statistics stats warps compute
   constexpr bool STATS = (QM != kQCurQuant && NK != kIdentity);
   extern __shared__ __align__(128) unsigned char smem[];
 
-  const int TH = blockDim.x - 32;  // consumer threads
-  const int W = TH >> 5;           // consumer warps
+  const int A = p.apply_warps;           // warps 0 .. A-1
+  const int S = STATS ? p.stats_warps : 0;  // warps A .. A+S-1; producer: A+S
+  const int TH = A * 32;                 // apply threads
   const int H = p.H;
   const int nchunks = H / VEC;
   const uint32_t row_bytes = (uint32_t)H * sizeof(TIn);
   const uint32_t Q = (uint32_t)p.Q;
-  const int T = p.T;
-  const int WPR = p.wpr;
 
   unsigned char* ring = smem;
-  float2* stats = reinterpret_cast<float2*>(smem + (size_t)Q * row_bytes);  // [2][T]
-  float4* part = reinterpret_cast<float4*>(stats + 2 * T);                  // [T * WPR]
-  uint32_t* red = reinterpret_cast<uint32_t*>(part + T * WPR);              // [32]
-  float2* meta = reinterpret_cast<float2*>(red + 32);                       // [Q]
-  uint64_t* full = reinterpret_cast<uint64_t*>(meta + Q);
-  uint64_t* empty = full + Q;
+  float2* rstat = reinterpret_cast<float2*>(smem + (size_t)Q * row_bytes);  // [Q] (mean, rsigma)
+  uint32_t* red = reinterpret_cast<uint32_t*>(rstat + Q);                   // [32]
+  uint64_t* full = reinterpret_cast<uint64_t*>(red + 32);                   // row landed
+  uint64_t* ready = full + Q;                                               // statistics written
+  uint64_t* empty = ready + Q;                                              // slot released
 
   if (threadIdx.x == 0) {
     for (uint32_t i = 0; i < Q; ++i) {
       mbar_init(smem_u32(&full[i]), META ? 2 : 1);
-      mbar_init(smem_u32(&empty[i]), W);
+      mbar_init(smem_u32(&ready[i]), 1);
+      mbar_init(smem_u32(&empty[i]), A);
     }
     fence_barrier_init();
   }
@@ -118,31 +138,28 @@ __global__ void __launch_bounds__(kMaxThreads, 1) rn_fwd_kernel(const FwdParams 
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int G = gridDim.x;
 
-  if (warp == W) {
+  if (warp == A + S) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       const unsigned char* xb = static_cast<const unsigned char*>(p.x);
       RingPos pos{0u, 0u};
       uint32_t issued = 0;
-      for (int tk = blockIdx.x; tk < p.n_tiles; tk += G) {
-        const int tt = p.reverse ? p.n_tiles - 1 - tk : tk;
-        const int r0 = tt * T;
-        const int r1 = min(r0 + T, p.N);
-        for (int r = r0; r < r1; ++r, ++issued) {
-          const uint32_t s = pos.slot;
-          if (issued >= Q) mbar_wait(smem_u32(&empty[s]), pos.phase ^ 1u, &g_err_fwd, kErrEmptyWait);
-          const uint32_t bar = smem_u32(&full[s]);
-          if constexpr (META) {
-            if (LN) cp_async4(smem_u32(&meta[s].x), p.mu + r);
-            cp_async4(smem_u32(&meta[s].y), p.rsigma + r);
-            cp_async_arrive(bar);
-          }
-          mbar_arrive_expect_tx(bar, row_bytes);
-          bulk_g2s(smem_u32(ring + (size_t)s * row_bytes), xb + (size_t)r * row_bytes, row_bytes, bar);
-          pos.advance(1, Q);
+      RowWalk wk{-1, 0, 0};
+      while (wk.next(p)) {
+        const int r = wk.r;
+        const uint32_t s = pos.slot;
+        if (issued >= Q) mbar_wait(smem_u32(&empty[s]), pos.phase ^ 1u, &g_err_fwd, kErrEmptyWait);
+        const uint32_t bar = smem_u32(&full[s]);
+        if constexpr (META) {
+          if (LN) cp_async4(smem_u32(&rstat[s].x), p.mu + r);
+          cp_async4(smem_u32(&rstat[s].y), p.rsigma + r);
+          cp_async_arrive(bar);
         }
+        mbar_arrive_expect_tx(bar, row_bytes);
+        bulk_g2s(smem_u32(ring + (size_t)s * row_bytes), xb + (size_t)r * row_bytes, row_bytes, bar);
+        pos.advance(1, Q);
+        ++issued;
       }
       // every copy this CTA issued must have landed before it exits
       const uint32_t first = issued > Q ? issued - Q : 0;
@@ -152,7 +169,69 @@ __global__ void __launch_bounds__(kMaxThreads, 1) rn_fwd_kernel(const FwdParams 
     return;
   }
 
-  // -------------------------------------------------------------- consumers
+  if (warp >= A) {
+    // --------------------------------------------------------- stats warps
+    // stats warp j takes rows j, j + S, j + 2S, ... of the CTA's sequence;
+    // LayerNorm: two passes over the row in shared memory (mean, then the
+    // centred sum of squares); RMSNorm: one pass (sum of squares)
+    if constexpr (STATS) {
+      const int j = warp - A;
+      const float inv_h = 1.0f / (float)H;
+      RingPos pos{0u, 0u};
+      RowWalk wk{-1, 0, 0};
+      int q = 0;
+      while (wk.next(p)) {
+        if (q++ % S == j) {
+          const uint32_t s = pos.slot;
+          mbar_wait(smem_u32(&full[s]), pos.phase, &g_err_fwd, kErrStatsWait);
+          const unsigned char* rowp = ring + (size_t)s * row_bytes;
+          float2 a[PAIRS];
+          float mean = 0.0f;
+          if constexpr (LN) {
+#pragma unroll
+            for (int i = 0; i < PAIRS; ++i) a[i] = make_float2(0.f, 0.f);
+            for (int c = lane; c < nchunks; c += 32) {
+              const typename V::Raw raw = V::load(rowp, c);
+#pragma unroll
+              for (int i = 0; i < PAIRS; ++i) V::acc(a[i], raw, i);
+            }
+            float sum = 0.f;
+#pragma unroll
+            for (int i = 0; i < PAIRS; ++i) sum += a[i].x + a[i].y;
+            mean = warp_sum(sum) * inv_h;
+          }
+#pragma unroll
+          for (int i = 0; i < PAIRS; ++i) a[i] = make_float2(0.f, 0.f);
+          for (int c = lane; c < nchunks; c += 32) {
+            const typename V::Raw raw = V::load(rowp, c);
+#pragma unroll
+            for (int i = 0; i < PAIRS; ++i) {
+              if constexpr (LN) {
+                const float2 d = V::sub(raw, i, mean);
+                a[i] = fma2(d, d, a[i]);
+              } else {
+                V::sq_acc(a[i], raw, i);
+              }
+            }
+          }
+          float m2 = 0.f;
+#pragma unroll
+          for (int i = 0; i < PAIRS; ++i) m2 += a[i].x + a[i].y;
+          const float rs = __frsqrt_rn(warp_sum(m2) * inv_h + p.eps);
+          if (lane == 0) {
+            rstat[s] = make_float2(mean, rs);
+            if constexpr (LN) p.mu[wk.r] = mean;
+            p.rsigma[wk.r] = rs;
+            mbar_arrive(smem_u32(&ready[s]));
+          }
+        }
+        pos.advance(1, Q);
+      }
+    }
+    return;
+  }
+
+  // ---------------------------------------------------------- apply warps
   const int t = threadIdx.x;
   float2 g2[NG][PAIRS], b2[NG][PAIRS];
 #pragma unroll
@@ -185,131 +264,44 @@ __global__ void __launch_bounds__(kMaxThreads, 1) rn_fwd_kernel(const FwdParams 
     }
   }
   float amax_t = 0.0f;
-  const float hf = (float)H;
 
-  RingPos pos{0u, 0u};  // ring position of the current tile's first row
-  int it = 0;
-  for (int tk = blockIdx.x; tk < p.n_tiles; tk += G, ++it) {
-    const int tt = p.reverse ? p.n_tiles - 1 - tk : tk;
-    const int r0 = tt * T;
-    const int nrows = min(T, p.N - r0);
-    float2* st = stats + (it & 1) * T;
-
-    if constexpr (STATS) {
-      // ---------------------------------------------- phase 1: statistics
-      for (int item = warp; item < nrows * WPR; item += W) {
-        const int k = item / WPR, j = item - k * WPR;
-        const RingPos rp = pos.ahead(k, Q);
-        mbar_wait(smem_u32(&full[rp.slot]), rp.phase, &g_err_fwd, kErrFullWait);
-        const unsigned char* rowp = ring + (size_t)rp.slot * row_bytes;
-        float smean = 0.0f, cnt = 0.0f;
-        float2 a[PAIRS];
-        if constexpr (LN) {
-#pragma unroll
-          for (int i = 0; i < PAIRS; ++i) a[i] = make_float2(0.f, 0.f);
-          for (int c = j * 32 + lane; c < nchunks; c += 32 * WPR) {
-            const typename V::Raw raw = V::load(rowp, c);
-#pragma unroll
-            for (int i = 0; i < PAIRS; ++i) V::acc(a[i], raw, i);
-            cnt += (float)VEC;
-          }
-          float s = 0.f;
-#pragma unroll
-          for (int i = 0; i < PAIRS; ++i) s += a[i].x + a[i].y;
-          cnt = warp_sum(cnt);
-          smean = cnt > 0.0f ? __fdiv_rn(warp_sum(s), cnt) : 0.0f;
-        }
-#pragma unroll
-        for (int i = 0; i < PAIRS; ++i) a[i] = make_float2(0.f, 0.f);
-        for (int c = j * 32 + lane; c < nchunks; c += 32 * WPR) {
-          const typename V::Raw raw = V::load(rowp, c);
-#pragma unroll
-          for (int i = 0; i < PAIRS; ++i) {
-            if constexpr (LN) {
-              const float2 d = V::sub(raw, i, smean);
-              a[i] = fma2(d, d, a[i]);
-            } else {
-              V::sq_acc(a[i], raw, i);
-            }
-          }
-        }
-        float m2 = 0.f;
-#pragma unroll
-        for (int i = 0; i < PAIRS; ++i) m2 += a[i].x + a[i].y;
-        m2 = warp_sum(m2);
-        if (lane == 0) part[k * WPR + j] = make_float4(smean, m2, cnt, 0.0f);
-      }
-      consumer_sync(TH);
-      // merge the slices of each row in slice order (Chan et al.)
-      if (t < nrows) {
-        const int k = t;
-        const float4 p0 = part[k * WPR];
-        float mean = 0.0f, m2 = p0.y;
-        if constexpr (LN) {
-          mean = p0.x;
-          float n = p0.z;
-          for (int j = 1; j < WPR; ++j) {
-            const float4 pj = part[k * WPR + j];
-            if (pj.z > 0.0f) {
-              const float n2 = n + pj.z;
-              const float delta = pj.x - mean;
-              mean = fmaf(delta, __fdiv_rn(pj.z, n2), mean);
-              m2 = m2 + pj.y + delta * delta * __fdiv_rn(n * pj.z, n2);
-              n = n2;
-            }
-          }
-        } else {
-          for (int j = 1; j < WPR; ++j) m2 += part[k * WPR + j].y;
-        }
-        const float rs = __frsqrt_rn(__fdiv_rn(m2, hf) + p.eps);
-        st[k] = make_float2(mean, rs);
-        if constexpr (LN) p.mu[r0 + k] = mean;
-        p.rsigma[r0 + k] = rs;
-      }
-      consumer_sync(TH);
+  RingPos pos{0u, 0u};
+  RowWalk wk{-1, 0, 0};
+  while (wk.next(p)) {
+    const uint32_t s = pos.slot;
+    mbar_wait(smem_u32(&full[s]), pos.phase, &g_err_fwd, kErrFullWait);
+    if constexpr (STATS) mbar_wait(smem_u32(&ready[s]), pos.phase, &g_err_fwd, kErrReadyWait);
+    float mean = 0.0f, rs = 1.0f;
+    if constexpr (STATS || META) {
+      const float2 m = rstat[s];
+      mean = LN ? m.x : 0.0f;
+      rs = m.y;
     }
-
-    // ------------------------------------------- phase 2: apply + output
-    RingPos rp = pos;
-    for (int k = 0; k < nrows; ++k) {
-      mbar_wait(smem_u32(&full[rp.slot]), rp.phase, &g_err_fwd, kErrFullWait);
-      float mean = 0.0f, rs = 1.0f;
-      if constexpr (META) {
-        const float2 m = meta[rp.slot];
-        mean = LN ? m.x : 0.0f;
-        rs = m.y;
-      } else if constexpr (STATS) {
-        const float2 m = st[k];
-        mean = m.x;
-        rs = m.y;
-      }
-      const unsigned char* rowp = ring + (size_t)rp.slot * row_bytes;
-      const size_t rowe = (size_t)(r0 + k) * H;
+    const unsigned char* rowp = ring + (size_t)s * row_bytes;
+    const size_t rowe = (size_t)wk.r * H;
 #pragma unroll
-      for (int g = 0; g < NG; ++g) {
-        const int v = g * TH + t;
-        if (v < nchunks) {
-          const typename V::Raw raw = V::load(rowp, v);
-          float2 y[PAIRS];
+    for (int g = 0; g < NG; ++g) {
+      const int v = g * TH + t;
+      if (v < nchunks) {
+        const typename V::Raw raw = V::load(rowp, v);
+        float2 y[PAIRS];
 #pragma unroll
-          for (int i = 0; i < PAIRS; ++i) {
-            if constexpr (LN) {
-              y[i] = fma2(mul2(V::sub(raw, i, mean), splat2(rs)), g2[g][i], b2[g][i]);
-            } else if constexpr (NK == kRms) {
-              y[i] = mul2(mul2(V::f32(raw, i), splat2(rs)), g2[g][i]);
-            } else {
-              y[i] = V::f32(raw, i);
-            }
-            if constexpr (QM == kQDelayed || QM == kQCurAmax) amax_t = amax_acc2(amax_t, y[i]);
+        for (int i = 0; i < PAIRS; ++i) {
+          if constexpr (LN) {
+            y[i] = fma2(mul2(V::sub(raw, i, mean), splat2(rs)), g2[g][i], b2[g][i]);
+          } else if constexpr (NK == kRms) {
+            y[i] = mul2(mul2(V::f32(raw, i), splat2(rs)), g2[g][i]);
+          } else {
+            y[i] = V::f32(raw, i);
           }
-          if constexpr (QM != kQCurAmax) store_chunk<PAIRS, QM>(p, rowe + (size_t)v * VEC, y, scale);
+          if constexpr (QM == kQDelayed || QM == kQCurAmax) amax_t = amax_acc2(amax_t, y[i]);
         }
+        if constexpr (QM != kQCurAmax) store_chunk<PAIRS, QM>(p, rowe + (size_t)v * VEC, y, scale);
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&empty[rp.slot]));
-      rp.advance(1, Q);
     }
-    pos = rp;
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_u32(&empty[s]));
+    pos.advance(1, Q);
   }
 
   if constexpr (QM == kQDelayed || QM == kQCurAmax) {
@@ -318,15 +310,15 @@ __global__ void __launch_bounds__(kMaxThreads, 1) rn_fwd_kernel(const FwdParams 
     consumer_sync(TH);
     if (t == 0) {
       uint32_t m = 0;
-      for (int w = 0; w < W; ++w) m = max(m, red[w]);
+      for (int w = 0; w < A; ++w) m = max(m, red[w]);
       atomicMax(reinterpret_cast<unsigned int*>(p.amax), m);
     }
   }
 }
 
-template <typename TIn, int NG, int NK, int QM>
+template <typename TIn, int NG, int NK, int QM, bool WIDE>
 rn_status launch_t(const FwdParams& p, const Launch& l, cudaStream_t s) {
-  auto k = rn_fwd_kernel<TIn, NG, NK, QM>;
+  auto k = rn_fwd_kernel<TIn, NG, NK, QM, WIDE>;
   if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)l.smem) !=
       cudaSuccess)
     return RN_ERR_CUDA;
@@ -336,12 +328,22 @@ rn_status launch_t(const FwdParams& p, const Launch& l, cudaStream_t s) {
   return cudaGetLastError() == cudaSuccess ? RN_OK : RN_ERR_CUDA;
 }
 
+// compact shape for NG 1 and 2; wide shape for NG 2, 4 and 8
 template <typename TIn, int NK, int QM>
 rn_status launch_ng(int ng, const FwdParams& p, const Launch& l, cudaStream_t s) {
+  const bool wide = l.threads > kMaxThreads || l.per_sm == 1;
+  if (!wide) {
+    switch (ng) {
+      case 1: return launch_t<TIn, 1, NK, QM, false>(p, l, s);
+      case 2: return launch_t<TIn, 2, NK, QM, false>(p, l, s);
+      default: return RN_ERR_UNSUPPORTED;
+    }
+  }
+  if (l.threads > kMaxThreadsWide) return RN_ERR_UNSUPPORTED;
   switch (ng) {
-    case 1: return launch_t<TIn, 1, NK, QM>(p, l, s);
-    case 2: return launch_t<TIn, 2, NK, QM>(p, l, s);
-    case 4: return launch_t<TIn, 4, NK, QM>(p, l, s);
+    case 2: return launch_t<TIn, 2, NK, QM, true>(p, l, s);
+    case 4: return launch_t<TIn, 4, NK, QM, true>(p, l, s);
+    case 8: return launch_t<TIn, 8, NK, QM, true>(p, l, s);
     default: return RN_ERR_UNSUPPORTED;
   }
 }

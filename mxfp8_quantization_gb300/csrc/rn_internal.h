@@ -37,8 +37,9 @@ struct FwdParams {
   float eps;
   int zcg;              // zero-centered gamma
   int out_f32;          // kQNone: 1 = fp32 output, 0 = bf16
-  int T;                // rows per tile
-  int wpr;              // warps sharing one row in phase 1
+  int T;                // rows per tile (the unit CTAs take turns on)
+  int apply_warps;      // warps that apply and store
+  int stats_warps;      // warps that compute row statistics
   int Q;                // ring slots (rows)
   int n_tiles;
   int reverse;          // walk the tiles from the last one
@@ -57,6 +58,8 @@ struct MxParams {
   int N, H;
   float eps;
   int zcg;
+  int apply_warps;
+  int stats_warps;
   int Q;
   int n_tiles;          // N / 32
 };
@@ -71,11 +74,10 @@ struct BwdParams {
   float* part;          // workspace partials [C][nacc][H]
   int N, H;
   int zcg;
-  int T;                // rows per tile
-  int wpr;              // warps sharing one row in phase 1
-  int tiles_per_chunk;  // chunk = tiles_per_chunk * T rows
+  int chunk_rows;       // rows per dgamma/dbeta partial
+  int apply_warps;
+  int stats_warps;
   int Q;
-  int n_tiles;
   int n_chunks;
 };
 
