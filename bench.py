@@ -286,6 +286,20 @@ def run_rn(args):
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     torch.cuda.set_device(local)
+    if args.only is not None:
+        _build.build()
+        lib = rn._load()
+        l2 = torch.cuda.get_device_properties(local).L2_cache_size
+        fb = torch.empty(2 * l2, dtype=torch.uint8, device="cuda")
+        rb = torch.ones(2 * l2 // 4, dtype=torch.float32, device="cuda")
+
+        def flush_only():
+            fb.fill_(1)
+            rb.sum()
+        res = run_other_workloads(torch, rn, lib, rn_inputs, flush_only, hbm_peak()[0], args.steps,
+                                  args.warmup, only=args.only)
+        print(json.dumps({"only": args.only, "workloads": res}))
+        return
     if world > 1:
         dist.init_process_group("nccl")
     if rank == 0 or world == 1:
@@ -440,8 +454,13 @@ def run_e2e(torch, lib, P, fwd, bwd, w, steps, step_bytes):
             "ms_per_step": round(ms, 4), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
 
 
-def run_other_workloads(torch, rn, lib, rn_inputs, flush, peak, steps, warmup):
+def run_other_workloads(torch, rn, lib, rn_inputs, flush, peak, steps, warmup, only=None):
+    """Full-size timing of the other workloads; ``only`` restricts the run to
+    one group ("rms_small", "rms_current", "mxfp8", "bwd_f32", "bwd_bf16")."""
     res = {}
+
+    def want(name):
+        return only is None or only == name
 
     def report(name, kind, N, H, esz, ln, ms, launches):
         b = algorithmic_bytes(kind, N, H, esz, ln)
@@ -450,6 +469,43 @@ def run_other_workloads(torch, rn, lib, rn_inputs, flush, peak, steps, warmup):
                      "frac_of_peak": round(gbs / peak, 4), "pct_of_8TBps": round(gbs / 80.0, 2),
                      "algorithmic_bytes": b, "kernels_per_call": launches}
 
+    if want("rms_small"):
+        _small(torch, rn, lib, rn_inputs, flush, steps, warmup, report)
+    if want("rms_current"):
+        w = rn_inputs.make("rms_current")
+        P = Prepared(rn, torch, w, ln=False)
+        t = time_calls(torch, lib, [("cur", P.fwd_args("fp8_current"))], steps, warmup, flush)
+        report("rms_16384x8192_fwd_fp8_current", "fwd_fp8_current", w.N, w.H, 2, False,
+               statistics.mean(t["cur"]), 2)
+        del P, w
+    if want("mxfp8"):
+        w = rn_inputs.make("mxfp8")
+        for ln in (True, False):
+            P = Prepared(rn, torch, w, ln=ln)
+            t = time_calls(torch, lib, [("mx", P.fwd_args("mxfp8"))], steps, warmup, flush)
+            report(f"{'ln' if ln else 'rms'}_65536x2048_fwd_mxfp8", "fwd_mxfp8", w.N, w.H, 2, ln,
+                   statistics.mean(t["mx"]), 1)
+            del P
+        del w
+    for name in ("bwd_f32", "bwd_bf16"):
+        if not want(name):
+            continue
+        w = rn_inputs.make(name)
+        esz = 4 if w.dtype == "f32" else 2
+        for ln in (True, False):
+            P = Prepared(rn, torch, w, ln=ln)
+            call(lib, P.fwd_args("none"), P.stream())      # mu / rsigma for the backward
+            for margin in (0, 16):
+                t = time_calls(torch, lib, [("b", P.bwd_args(margin))], steps, warmup, flush)
+                report(f"{'ln' if ln else 'rms'}_{w.N}x{w.H}_{w.dtype}_bwd_margin{margin}", "bwd",
+                       w.N, w.H, esz, ln, statistics.mean(t["b"]), 2)
+            del P
+        del w
+    torch.cuda.synchronize()
+    return res
+
+
+def _small(torch, rn, lib, rn_inputs, flush, steps, warmup, report):
     w = rn_inputs.make("rms_small")
     P = Prepared(rn, torch, w, ln=False)
     calls = [("none", P.fwd_args("none"))]
@@ -460,38 +516,6 @@ def run_other_workloads(torch, rn, lib, rn_inputs, flush, peak, steps, warmup):
     report("rms_256x1024_fwd_fp8_delayed", "fwd_fp8", w.N, w.H, 2, False, statistics.mean(t["dl"]), 1)
     report("rms_256x1024_bwd", "bwd", w.N, w.H, 2, False, statistics.mean(t["bwd"]), 2)
     del P
-
-    w = rn_inputs.make("rms_current")
-    P = Prepared(rn, torch, w, ln=False)
-    t = time_calls(torch, lib, [("cur", P.fwd_args("fp8_current"))], steps, warmup, flush)
-    report("rms_16384x8192_fwd_fp8_current", "fwd_fp8_current", w.N, w.H, 2, False,
-           statistics.mean(t["cur"]), 2)
-    del P, w
-
-    w = rn_inputs.make("mxfp8")
-    for ln in (True, False):
-        P = Prepared(rn, torch, w, ln=ln)
-        t = time_calls(torch, lib, [("mx", P.fwd_args("mxfp8"))], steps, warmup, flush)
-        report(f"{'ln' if ln else 'rms'}_65536x2048_fwd_mxfp8", "fwd_mxfp8", w.N, w.H, 2, ln,
-               statistics.mean(t["mx"]), 1)
-        del P
-    del w
-
-    for name in ("bwd_f32", "bwd_bf16"):
-        w = rn_inputs.make(name)
-        esz = 4 if w.dtype == "f32" else 2
-        for ln in (True, False):
-            P = Prepared(rn, torch, w, ln=ln)
-            P.fwd_args("none")
-            call(lib, P.fwd_args("none"), P.stream())      # mu / rsigma for the backward
-            for margin in (0, 16):
-                t = time_calls(torch, lib, [("b", P.bwd_args(margin))], steps, warmup, flush)
-                report(f"{'ln' if ln else 'rms'}_{w.N}x{w.H}_{w.dtype}_bwd_margin{margin}", "bwd",
-                       w.N, w.H, esz, ln, statistics.mean(t["b"]), 2)
-            del P
-        del w
-    torch.cuda.synchronize()
-    return res
 
 
 def cpu_baseline(w, step_bytes):
@@ -559,6 +583,9 @@ def main():
     ap.add_argument("--impl", default="rn", choices=["rn", "reference"])
     ap.add_argument("--quick", action="store_true", help="headline workload only")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    ap.add_argument("--only", default=None,
+                    choices=["rms_small", "rms_current", "mxfp8", "bwd_f32", "bwd_bf16"],
+                    help="time only this workload group (prints its results; for profiling)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
