@@ -82,7 +82,8 @@ size_t cta_smem_budget(const DeviceInfo& di, int per_sm) {
 }
 
 // Warp roles of the row kernels: A apply warps (each thread owning NG
-// 16-byte chunks of every row), S = max(2, A/2) stats warps, one producer.
+// 16-byte chunks of every row), S = max(2, A/2) stats warps (fewer than the
+// ring's slots, which their pacing on slot releases relies on), one producer.
 // Compact shape: NG <= 2, A <= 8, two CTAs per SM when each still holds a
 // ring of >= 6 slots.  Otherwise the wide shape: one CTA per SM, NG in
 // {2, 4, 8}, A <= 16.
@@ -101,6 +102,7 @@ rn_status plan_roles(int nchunks, size_t per_slot, size_t fixed, const DeviceInf
       r->ng = ng;
       r->A = round_up((nchunks + ng - 1) / ng, 32) / 32;
       r->S = r->A / 2 > 2 ? r->A / 2 : 2;
+      if (r->S > Q - 1) r->S = Q - 1;  // stats warps must be fewer than slots
       r->per_sm = 2;
       r->Q = Q;
       return RN_OK;
@@ -116,6 +118,7 @@ rn_status plan_roles(int nchunks, size_t per_slot, size_t fixed, const DeviceInf
   r->ng = ng;
   r->A = round_up((nchunks + ng - 1) / ng, 32) / 32;
   r->S = r->A / 2 > 2 ? r->A / 2 : 2;
+  if (r->S > Q - 1) r->S = Q - 1;  // stats warps must be fewer than slots
   r->per_sm = 1;
   r->Q = Q;
   return RN_OK;
@@ -147,14 +150,13 @@ rn_status plan_fwd(int H, int esz, int N, int sm_margin, const DeviceInfo& di, R
   return RN_OK;
 }
 
-// MXFP8: apply threads own 8 columns each (A = H/256 warps, at most 12),
-// S = max(2, A/2) stats warps (fewer when A + S would pass 15), a producer;
-// one CTA per SM with a ring of at least 33 rows (a 32-row tile plus
-// look-ahead).
+// MXFP8: apply warps take 64-column sub-tiles of each 32-row tile
+// (A = min(H/64, 10) warps), S = max(2, A/2) stats warps (fewer when A + S
+// would pass 15), a producer; one CTA per SM with a ring of at least 33 rows
+// (a 32-row tile plus look-ahead).
 rn_status plan_mx(int H, int esz, int N, int sm_margin, const DeviceInfo& di, RowPlan* pl) {
-  const int nchunks = H / 8;
-  const int A = (nchunks + 31) / 32;
-  if (A > 12) return RN_ERR_UNSUPPORTED;
+  const int nsub = (H + 63) / 64;
+  const int A = nsub < 10 ? nsub : 10;
   int S = A / 2 > 2 ? A / 2 : 2;
   if (A + S > 15) S = 15 - A;
   const size_t row_bytes = (size_t)H * esz;

@@ -148,6 +148,10 @@ __global__ void __launch_bounds__(WIDE ? kMaxThreadsWide : kMaxThreads, WIDE ? 1
       for (int r = c * R; r < r1; ++r, ++q) {
         if (q % S == j) {
           const uint32_t s = pos.slot;
+          // not paced by the apply warps: wait for the previous use of the
+          // slot to be released first, so that the parity wait below cannot
+          // match a phase one lap old (alias-free as stats warps < slots)
+          if (q >= (int)Q) mbar_wait(smem_u32(&empty[s]), pos.phase ^ 1u, &g_err_bwd, kErrStatsWait);
           mbar_wait(smem_u32(&full[s]), pos.phase, &g_err_bwd, kErrStatsWait);
           const unsigned char* xr = ring + (size_t)s * slot_bytes;
           const unsigned char* dr = xr + row_bytes;

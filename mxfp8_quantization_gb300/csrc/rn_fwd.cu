@@ -183,6 +183,11 @@ __global__ void __launch_bounds__(WIDE ? kMaxThreadsWide : kMaxThreads, WIDE ? 1
       while (wk.next(p)) {
         if (q++ % S == j) {
           const uint32_t s = pos.slot;
+          // a stats warp is not paced by the apply warps: before waiting for
+          // this use of the slot it waits for the previous use to be
+          // released, so that the parity wait below cannot match a phase
+          // one lap old (alias-free because stats warps are fewer than slots)
+          if (q > (int)Q) mbar_wait(smem_u32(&empty[s]), pos.phase ^ 1u, &g_err_fwd, kErrStatsWait);
           mbar_wait(smem_u32(&full[s]), pos.phase, &g_err_fwd, kErrStatsWait);
           const unsigned char* rowp = ring + (size_t)s * row_bytes;
           float2 a[PAIRS];

@@ -10,23 +10,21 @@
 //   stats warps  take rows in turn: mean / rsigma from shared memory
 //                (LayerNorm: two passes), published on the slot's "ready"
 //                mbarrier and written to mu / rsigma;
-//   apply warps  work on tiles of 32 rows (the height of a column block);
-//                every thread owns 8 consecutive columns (gamma / beta in
-//                registers):
-//       pass A   for every row of the tile: y, the 1x32 row-block maximum (4
-//                lanes x 8 columns, 2 shuffle steps), its E8M0 code, the
-//                rowwise E4M3 codes; and the running maximum of each of the
-//                thread's 8 columns;
-//       pass B   the 8 column-block codes, then y again for the 32 rows,
-//                quantized with the column scales, in two sweeps of 16 rows;
-//                each column's 16 codes of a sweep are packed in registers and
-//                written as 16 contiguous bytes of the transposed [H, N]
-//                columnwise array;
+//   apply warps  work on tiles of 32 rows (the height of a column block),
+//                each warp on 64-column sub-tiles: every thread holds y for
+//                an 8-row x 8-column block in registers, computed once
+//                (gamma / beta for its columns from the L1-cached global
+//                copies).  From those registers it forms
+//       rowwise  the 1x32 row-block maxima (4 lanes, 2 shuffle steps), their
+//                E8M0 codes and the rowwise E4M3 codes;
+//       colwise  the 32x1 column-block maxima (4 row groups, 2 shuffle
+//                steps), their codes, and the columnwise codes, 8 per column
+//                per thread, stored as 8 contiguous bytes of the transposed
+//                [H, N] array;
 //   then the tile's 32 slots are released ("empty").
-// y is recomputed in pass B from the row still in shared memory (cheaper
-// than keeping 32x8 fp32 values per thread), with the same instructions as
-// in pass A so both directions quantize identical y32.  Arithmetic is on
-// element pairs (f32x2); bf16 inputs enter through the mixed-precision forms.
+// Both directions quantize the same y32 (one computation per element).
+// Arithmetic is on element pairs (f32x2); bf16 inputs enter through the
+// mixed-precision forms.
 #include <cuda_runtime.h>
 
 #include "rn_device.cuh"
@@ -126,6 +124,10 @@ __global__ void __launch_bounds__(kMaxThreads, 1) rn_mx_kernel(const MxParams p)
         for (int k = 0; k < kTile; ++k, ++q) {
           if (q % S == j) {
             const uint32_t s = pos.slot;
+            // not paced by the apply warps: wait for the previous use of the
+            // slot to be released first, so that the parity wait below
+            // cannot match a phase one lap old (stats warps < slots)
+            if (q >= (int)Q) mbar_wait(smem_u32(&empty[s]), pos.phase ^ 1u, &g_err_mx, kErrStatsWait);
             mbar_wait(smem_u32(&full[s]), pos.phase, &g_err_mx, kErrStatsWait);
             const unsigned char* rowp = ring + (size_t)s * row_bytes;
             float2 a[4];
@@ -174,131 +176,131 @@ __global__ void __launch_bounds__(kMaxThreads, 1) rn_mx_kernel(const MxParams p)
   }
 
   // ---------------------------------------------------------- apply warps
-  const int t = threadIdx.x;
-  const int v = t;  // this thread's chunk of 8 columns
-  const bool valid = v < nchunks;
-  float2 g2[4], b2[4];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    g2[i] = make_float2(0.f, 0.f);
-    b2[i] = make_float2(0.f, 0.f);
-    if (NK != kIdentity && valid) {
-      const int c = v * 8 + 2 * i;
-      const float ga = p.gamma[c], gb = p.gamma[c + 1];
-      g2[i] = p.zcg ? make_float2(1.0f + ga, 1.0f + gb) : make_float2(ga, gb);
-      if (NK == kLn && p.beta) b2[i] = make_float2(p.beta[c], p.beta[c + 1]);
-    }
-  }
+  // Each apply warp takes 64-column sub-tiles of the 32-row tile (w, w + A,
+  // ...).  Lane = hb*16 + rg*4 + cc: the thread holds y of rows 8rg..8rg+7
+  // and columns 64*sub + 32*hb + 8*cc .. +7 in registers.  A row block (32
+  // columns) spans the 4 lanes cc = 0..3 (shuffles xor 1, 2); a column block
+  // (32 rows) spans the 4 lanes rg = 0..3 (shuffles xor 4, 8).
+  const int hb = lane >> 4, rg = (lane >> 2) & 3, cc = lane & 3;
+  const int nsub = (nchunks + 7) >> 3;
   const int hs = H >> 5;   // row scales per row
   const int ns = N >> 5;   // column scales per column
 
   RingPos pos{0u, 0u};
   for (int tile = blockIdx.x; tile < p.n_tiles; tile += G) {
     const int r0 = tile * kTile;
-    const uint32_t slot0 = pos.slot;
-    // ------------------------------------------------------------ pass A
-    float cm[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) cm[i] = 0.f;
+    // this lane's 8 rows: wait until they have landed and have statistics
     {
-      RingPos rp = pos;
-      for (int k = 0; k < kTile; k += 2) {
-        float2 y[2][4];
-#pragma unroll
-        for (int kk = 0; kk < 2; ++kk) {
-          const uint32_t s = rp.slot;
-          mbar_wait(smem_u32(&full[s]), rp.phase, &g_err_mx, kErrFullWait);
-          float mean = 0.f, rs = 1.f;
-          if constexpr (STATS) {
-            mbar_wait(smem_u32(&ready[s]), rp.phase, &g_err_mx, kErrReadyWait);
-            const float2 m = rstat[s];
-            mean = m.x;
-            rs = m.y;
-          }
-          rp.advance(1, Q);
-#pragma unroll
-          for (int i = 0; i < 4; ++i) y[kk][i] = make_float2(0.f, 0.f);
-          if (valid) y8<TIn, NK>(ring + (size_t)s * row_bytes, v, mean, rs, g2, b2, y[kk]);
-          if (p.data != nullptr) {
-            float m = amax_acc2(amax_acc2(0.f, y[kk][0]), y[kk][1]);
-            m = amax_acc2(amax_acc2(m, y[kk][2]), y[kk][3]);
-            uint32_t mb = abs_bits(m);
-            mb = max(mb, __shfl_xor_sync(0xFFFFFFFFu, mb, 1));
-            mb = max(mb, __shfl_xor_sync(0xFFFFFFFFu, mb, 2));
-            const uint32_t code = e8m0_code(__uint_as_float(mb));
-            const float2 inv = splat2(e8m0_inv_scale(code));
-            if (valid) {
-              const size_t row = (size_t)(r0 + k + kk);
-              uint32_t c[4];
-#pragma unroll
-              for (int i = 0; i < 4; ++i) {
-                const float2 q = mul2(y[kk][i], inv);
-                c[i] = pack_e4m3x2(q.x, q.y);
-              }
-              *reinterpret_cast<uint2*>(p.data + row * H + (size_t)v * 8) =
-                  make_uint2(c[0] | (c[1] << 16), c[2] | (c[3] << 16));
-              if ((t & 3) == 0) p.row_scales[row * hs + (v >> 2)] = (uint8_t)code;
-            }
-          }
-        }
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          cm[2 * i] = amax_acc2(cm[2 * i], make_float2(y[0][i].x, y[1][i].x));
-          cm[2 * i + 1] = amax_acc2(cm[2 * i + 1], make_float2(y[0][i].y, y[1][i].y));
-        }
+      RingPos rp = pos.ahead(8 * rg, Q);
+      for (int j = 0; j < 8; ++j) {
+        mbar_wait(smem_u32(&full[rp.slot]), rp.phase, &g_err_mx, kErrFullWait);
+        if constexpr (STATS) mbar_wait(smem_u32(&ready[rp.slot]), rp.phase, &g_err_mx, kErrReadyWait);
+        rp.advance(1, Q);
       }
     }
-    // ------------------------------------------------------------ pass B
-    if (p.col_data != nullptr) {
-      uint32_t ccode[8];
-      float cinv[8];
+    uint32_t slot[8];
+    float2 st8[8];
+    {
+      RingPos rp = pos.ahead(8 * rg, Q);
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        ccode[i] = e8m0_code(cm[i]);
-        cinv[i] = e8m0_inv_scale(ccode[i]);
+      for (int j = 0; j < 8; ++j) {
+        slot[j] = rp.slot;
+        st8[j] = STATS ? rstat[rp.slot] : make_float2(0.f, 1.f);
+        rp.advance(1, Q);
       }
-      // two sweeps of 16 rows; each row's y is formed once for all 8 columns
+    }
+    for (int sub = warp; sub < nsub; sub += A) {
+      const int v = sub * 8 + hb * 4 + cc;  // chunk of 8 columns
+      const bool valid = v < nchunks;
+      float2 g2[4], b2[4];
 #pragma unroll
-      for (int sweep = 0; sweep < 2; ++sweep) {
-        uint32_t cq[8][4];  // [column][word]: codes of rows 16*sweep + 4*word .. +3
+      for (int i = 0; i < 4; ++i) {
+        g2[i] = make_float2(0.f, 0.f);
+        b2[i] = make_float2(0.f, 0.f);
+        if (NK != kIdentity && valid) {
+          const int c = v * 8 + 2 * i;
+          const float ga = __ldg(p.gamma + c), gb = __ldg(p.gamma + c + 1);
+          g2[i] = p.zcg ? make_float2(1.0f + ga, 1.0f + gb) : make_float2(ga, gb);
+          if (NK == kLn && p.beta) b2[i] = make_float2(__ldg(p.beta + c), __ldg(p.beta + c + 1));
+        }
+      }
+      float2 y[8][4];
 #pragma unroll
-        for (int k4 = 0; k4 < 4; ++k4) {
-          float2 q[4][4];  // [row][pair] scaled by the column scales
+      for (int j = 0; j < 8; ++j) {
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            const int k = 16 * sweep + 4 * k4 + kk;
-            uint32_t s = slot0 + (uint32_t)k;
-            s = s >= Q ? s - Q : s;
-            float mean = 0.f, rs = 1.f;
-            if constexpr (STATS) {
-              const float2 m = rstat[s];
-              mean = m.x;
-              rs = m.y;
+        for (int i = 0; i < 4; ++i) y[j][i] = make_float2(0.f, 0.f);
+        if (valid) y8<TIn, NK>(ring + (size_t)slot[j] * row_bytes, v, st8[j].x, st8[j].y, g2, b2, y[j]);
+      }
+      // ------------------------------------------------- rowwise 1x32 blocks
+      if (p.data != nullptr) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          float m = amax_acc2(amax_acc2(0.f, y[j][0]), y[j][1]);
+          m = amax_acc2(amax_acc2(m, y[j][2]), y[j][3]);
+          uint32_t mb = abs_bits(m);
+          mb = max(mb, __shfl_xor_sync(0xFFFFFFFFu, mb, 1));
+          mb = max(mb, __shfl_xor_sync(0xFFFFFFFFu, mb, 2));
+          const uint32_t code = e8m0_code(__uint_as_float(mb));
+          const float2 inv = splat2(e8m0_inv_scale(code));
+          if (valid) {
+            const size_t row = (size_t)(r0 + 8 * rg + j);
+            uint32_t c[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const float2 q = mul2(y[j][i], inv);
+              c[i] = pack_e4m3x2(q.x, q.y);
             }
-            float2 y[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
-                           make_float2(0.f, 0.f)};
-            if (valid) y8<TIn, NK>(ring + (size_t)s * row_bytes, v, mean, rs, g2, b2, y);
-#pragma unroll
-            for (int i = 0; i < 4; ++i) q[kk][i] = mul2(y[i], make_float2(cinv[2 * i], cinv[2 * i + 1]));
+            *reinterpret_cast<uint2*>(p.data + row * H + (size_t)v * 8) =
+                make_uint2(c[0] | (c[1] << 16), c[2] | (c[3] << 16));
+            if (cc == 0) p.row_scales[row * hs + (v >> 2)] = (uint8_t)code;
           }
+        }
+      }
+      // ---------------------------------------------- columnwise 32x1 blocks
+      if (p.col_data != nullptr) {
+        float cm[8];
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            cq[2 * i][k4] = pack_e4m3x2(q[0][i].x, q[1][i].x) | (pack_e4m3x2(q[2][i].x, q[3][i].x) << 16);
-            cq[2 * i + 1][k4] = pack_e4m3x2(q[0][i].y, q[1][i].y) | (pack_e4m3x2(q[2][i].y, q[3][i].y) << 16);
+        for (int i = 0; i < 4; ++i) {
+          float a = 0.f, b = 0.f;
+#pragma unroll
+          for (int j = 0; j < 8; j += 2) {
+            a = amax_acc2(a, make_float2(y[j][i].x, y[j + 1][i].x));
+            b = amax_acc2(b, make_float2(y[j][i].y, y[j + 1][i].y));
           }
+          cm[2 * i] = a;
+          cm[2 * i + 1] = b;
+        }
+        float cinv[8];
+        uint32_t ccode[8];
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          uint32_t mb = abs_bits(cm[c]);
+          mb = max(mb, __shfl_xor_sync(0xFFFFFFFFu, mb, 4));
+          mb = max(mb, __shfl_xor_sync(0xFFFFFFFFu, mb, 8));
+          ccode[c] = e8m0_code(__uint_as_float(mb));
+          cinv[c] = e8m0_inv_scale(ccode[c]);
         }
         if (valid) {
 #pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const size_t col = (size_t)v * 8 + i;
-            *reinterpret_cast<uint4*>(p.col_data + col * N + (size_t)r0 + 16 * sweep) =
-                make_uint4(cq[i][0], cq[i][1], cq[i][2], cq[i][3]);
+          for (int i = 0; i < 4; ++i) {
+            const float2 ci = make_float2(cinv[2 * i], cinv[2 * i + 1]);
+            float2 q[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) q[j] = mul2(y[j][i], ci);
+            const uint32_t lo0 = pack_e4m3x2(q[0].x, q[1].x) | (pack_e4m3x2(q[2].x, q[3].x) << 16);
+            const uint32_t hi0 = pack_e4m3x2(q[4].x, q[5].x) | (pack_e4m3x2(q[6].x, q[7].x) << 16);
+            const uint32_t lo1 = pack_e4m3x2(q[0].y, q[1].y) | (pack_e4m3x2(q[2].y, q[3].y) << 16);
+            const uint32_t hi1 = pack_e4m3x2(q[4].y, q[5].y) | (pack_e4m3x2(q[6].y, q[7].y) << 16);
+            const size_t col = (size_t)v * 8 + 2 * i;
+            *reinterpret_cast<uint2*>(p.col_data + col * N + (size_t)(r0 + 8 * rg)) = make_uint2(lo0, hi0);
+            *reinterpret_cast<uint2*>(p.col_data + (col + 1) * N + (size_t)(r0 + 8 * rg)) =
+                make_uint2(lo1, hi1);
+          }
+          if (rg == 0) {
+#pragma unroll
+            for (int c = 0; c < 8; ++c) p.col_scales[((size_t)v * 8 + c) * ns + tile] = (uint8_t)ccode[c];
           }
         }
-      }
-      if (valid) {
-#pragma unroll
-        for (int i = 0; i < 8; ++i) p.col_scales[((size_t)v * 8 + i) * ns + tile] = (uint8_t)ccode[i];
       }
     }
     // release the tile's slots
