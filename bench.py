@@ -147,6 +147,20 @@ class ClockSampler:
                 "samples": len(rows)}
 
 
+def aggregate_ranks(ms_per_step, bytes_per_step, dist=None, device="cpu"):
+    """Whole-job figures of a replicas run: the slowest rank's time per step
+    (max over ranks) and the bytes of all ranks over it.  Returns
+    (max_ms, GB/s).  Without a process group: this rank alone."""
+    import torch
+    world = 1
+    if dist is not None and dist.is_available() and dist.is_initialized():
+        world = dist.get_world_size()
+        t = torch.tensor([float(ms_per_step)], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_per_step = float(t.item())
+    return ms_per_step, world * bytes_per_step / (ms_per_step * 1e-3) / 1e9
+
+
 # ---------------------------------------------------------------- our arm
 class Prepared:
     """Device buffers and ctypes argument lists for repeated C-ABI calls."""
@@ -338,15 +352,14 @@ def run_rn(args):
     clocks = sampler.stop()
     fwd_ms = statistics.mean(times["fwd"])
     bwd_ms = statistics.mean(times["bwd"])
-    ms_step = fwd_ms + bwd_ms
-    if world > 1:
-        t = torch.tensor([ms_step, fwd_ms, bwd_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_step, fwd_ms, bwd_ms = (float(v) for v in t.tolist())
     b_fwd = algorithmic_bytes("fwd_fp8", N, H, 2, True)
     b_bwd = algorithmic_bytes("bwd", N, H, 2, True)
     step_bytes = b_fwd + b_bwd
-    value = world * step_bytes / (ms_step * 1e-3) / 1e9
+    ms_step, value = aggregate_ranks(fwd_ms + bwd_ms, step_bytes, dist if world > 1 else None, "cuda")
+    if world > 1:
+        t = torch.tensor([fwd_ms, bwd_ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        fwd_ms, bwd_ms = (float(v) for v in t.tolist())
 
     # ------------------------------------------------ end to end, host data
     e2e = None
