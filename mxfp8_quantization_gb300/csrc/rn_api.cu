@@ -151,12 +151,14 @@ rn_status plan_fwd(int H, int esz, int N, int sm_margin, const DeviceInfo& di, R
 }
 
 // MXFP8: apply warps take 64-column sub-tiles of each 32-row tile
-// (A = min(H/64, 10) warps), S = max(2, A/2) stats warps (fewer when A + S
+// (A <= 10 warps, as few as give the same sub-tiles per warp), S = max(2, A/2) stats warps (fewer when A + S
 // would pass 15), a producer; one CTA per SM with a ring of at least 33 rows
 // (a 32-row tile plus look-ahead).
 rn_status plan_mx(int H, int esz, int N, int sm_margin, const DeviceInfo& di, RowPlan* pl) {
   const int nsub = (H + 63) / 64;
-  const int A = nsub < 10 ? nsub : 10;
+  // the largest A <= 10 that spreads the sub-tiles evenly
+  int A = nsub < 10 ? nsub : 10;
+  while (A > 1 && (nsub % A) != 0 && (nsub + A - 1) / A == (nsub + A - 2) / (A - 1)) --A;
   int S = A / 2 > 2 ? A / 2 : 2;
   if (A + S > 15) S = 15 - A;
   const size_t row_bytes = (size_t)H * esz;

@@ -217,7 +217,7 @@ __global__ void __launch_bounds__(WIDE ? kMaxThreadsWide : kMaxThreads, WIDE ? 1
     const int r1 = min((c + 1) * R, p.N);
     for (int r = c * R; r < r1; ++r) {
       const uint32_t s = pos.slot;
-      mbar_wait(smem_u32(&full[s]), pos.phase, &g_err_bwd, kErrFullWait);
+      // "ready" is published after the stats warp saw the row land
       mbar_wait(smem_u32(&ready[s]), pos.phase, &g_err_bwd, kErrReadyWait);
       const float4 m = rstat[s];
       const unsigned char* xr = ring + (size_t)s * slot_bytes;
@@ -266,57 +266,44 @@ __global__ void __launch_bounds__(WIDE ? kMaxThreadsWide : kMaxThreads, WIDE ? 1
 }
 
 // dgamma[j] (a = 0) / dbeta[j] (a = 1) = sum over chunks of part[c][a][j].
-// Block: 32 warps x 32 lanes; lane owns 4 adjacent columns of a 128-column
-// slice; warp w sums chunks w, w+32, w+64, ... into four interleaved
-// accumulators (chunk index / 32 mod 4), adds them as (a0+a1)+(a2+a3), then
-// thread j of the first 128 adds the 32 warp sums in warp order.  The order
-// depends on the chunk count only.
+// Block: 32 warps x 32 lanes; lane owns 2 adjacent columns of a 64-column
+// slice; warp w sums chunks w, w+32, w+64, ... into eight interleaved
+// accumulators (chunk index / 32 mod 8, eight loads in flight), adds them
+// pairwise in a fixed tree, then thread j of the first 64 adds the 32 warp
+// sums in warp order.  The order depends on the chunk count only.
 __global__ void __launch_bounds__(1024) rn_colreduce_kernel(const ColReduceParams p) {
-  __shared__ float4 red[32][33];
+  __shared__ float2 red[32][33];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int a = blockIdx.y;
-  const int col = blockIdx.x * 128 + lane * 4;
-  float4 acc[4];
+  const int col = blockIdx.x * 64 + lane * 2;
+  float2 acc[8];
 #pragma unroll
-  for (int i = 0; i < 4; ++i) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int i = 0; i < 8; ++i) acc[i] = make_float2(0.f, 0.f);
   if (col < p.H) {
     const float* base = p.part + (size_t)a * p.H + col;
     const size_t stride = (size_t)p.nacc * p.H;
     int c = warp;
-    for (; c + 96 < p.n_chunks; c += 128) {
-      float4 v[4];
+    for (; c + 224 < p.n_chunks; c += 256) {
+      float2 v[8];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) v[i] = *reinterpret_cast<const float4*>(base + (size_t)(c + 32 * i) * stride);
+      for (int i = 0; i < 8; ++i) v[i] = *reinterpret_cast<const float2*>(base + (size_t)(c + 32 * i) * stride);
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        acc[i].x += v[i].x;
-        acc[i].y += v[i].y;
-        acc[i].z += v[i].z;
-        acc[i].w += v[i].w;
-      }
+      for (int i = 0; i < 8; ++i) acc[i] = add2(acc[i], v[i]);
     }
-    for (int i = 0; c < p.n_chunks; c += 32, ++i) {
-      const float4 v = *reinterpret_cast<const float4*>(base + (size_t)c * stride);
-      acc[i].x += v.x;
-      acc[i].y += v.y;
-      acc[i].z += v.z;
-      acc[i].w += v.w;
-    }
+    for (int i = 0; c < p.n_chunks; c += 32, ++i)
+      acc[i] = add2(acc[i], *reinterpret_cast<const float2*>(base + (size_t)c * stride));
   }
-  float4 s;
-  s.x = (acc[0].x + acc[1].x) + (acc[2].x + acc[3].x);
-  s.y = (acc[0].y + acc[1].y) + (acc[2].y + acc[3].y);
-  s.z = (acc[0].z + acc[1].z) + (acc[2].z + acc[3].z);
-  s.w = (acc[0].w + acc[1].w) + (acc[2].w + acc[3].w);
+  const float2 s = add2(add2(add2(acc[0], acc[1]), add2(acc[2], acc[3])),
+                        add2(add2(acc[4], acc[5]), add2(acc[6], acc[7])));
   red[warp][lane] = s;
   __syncthreads();
-  if (threadIdx.x < 128) {
-    const int l = threadIdx.x >> 2, e = threadIdx.x & 3;
-    const int j = blockIdx.x * 128 + threadIdx.x;
+  if (threadIdx.x < 64) {
+    const int l = threadIdx.x >> 1, e = threadIdx.x & 1;
+    const int j = blockIdx.x * 64 + threadIdx.x;
     float r = 0.f;
     for (int w = 0; w < 32; ++w) {
-      const float4 v = red[w][l];
-      r += (e == 0) ? v.x : (e == 1) ? v.y : (e == 2) ? v.z : v.w;
+      const float2 v = red[w][l];
+      r += e ? v.y : v.x;
     }
     if (j < p.H) (a == 0 ? p.dgamma : p.dbeta)[j] = r;
   }
@@ -363,7 +350,7 @@ rn_status launch_bwd(bool ln, bool bf16, int ng, const BwdParams& p, const Launc
 }
 
 rn_status launch_colreduce(const ColReduceParams& p, cudaStream_t s) {
-  dim3 grid((p.H + 127) / 128, p.nacc);
+  dim3 grid((p.H + 63) / 64, p.nacc);
   rn_colreduce_kernel<<<grid, 1024, 0, s>>>(p);
   return cudaGetLastError() == cudaSuccess ? RN_OK : RN_ERR_CUDA;
 }

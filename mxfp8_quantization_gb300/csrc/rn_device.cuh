@@ -69,16 +69,21 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 }
 
 // Wait until the phase with `parity` of barrier `bar` has completed, for at
-// most kWaitLimitCycles; on expiry record `code` in *err and return false.  Once
-// an error is recorded, later waits that do not succeed at once give up
-// immediately, so a kernel that lost its pipeline finishes quickly (its
+// most kWaitLimitCycles; on expiry record `code` in *err and return false.
+// Once an error is recorded (checked only after kErrorCheckCycles of
+// waiting, so that the spin itself touches no global memory), later waits
+// give up too, so a kernel that lost its pipeline finishes quickly (its
 // results are then meaningless; the host reads the error word).
+constexpr long long kErrorCheckCycles = 100000;
+
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigned* err,
                                           unsigned code) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   while (!mbar_try_wait(bar, parity)) {
-    if (*reinterpret_cast<volatile unsigned*>(err) != 0u || clock64() - t0 > kWaitLimitCycles) {
+    const long long dt = clock64() - t0;
+    if (dt > kErrorCheckCycles &&
+        (dt > kWaitLimitCycles || *reinterpret_cast<volatile unsigned*>(err) != 0u)) {
       atomicCAS(err, 0u, code);
       return false;
     }
@@ -282,6 +287,19 @@ __device__ __forceinline__ void bf16x2_sq_acc(float2& acc, uint32_t w) {
       "fma.rn.f32.bf16 %0, l, l, %0;\n\tfma.rn.f32.bf16 %1, h, h, %1;\n\t}"
       : "+f"(acc.x), "+f"(acc.y)
       : "r"(w));
+}
+
+// running maximum and minimum over two more values (3-input forms); NaN
+// wins.  max|y| = max(hi, -lo) at the end.
+__device__ __forceinline__ float max3(float acc, float2 v) {
+  float r;
+  asm("max.NaN.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(acc), "f"(v.x), "f"(v.y));
+  return r;
+}
+__device__ __forceinline__ float min3(float acc, float2 v) {
+  float r;
+  asm("min.NaN.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(acc), "f"(v.x), "f"(v.y));
+  return r;
 }
 
 // running max of magnitudes over two more values; NaN wins

@@ -268,14 +268,18 @@ __global__ void __launch_bounds__(WIDE ? kMaxThreadsWide : kMaxThreads, WIDE ? 1
       *p.scale_inv = __fdiv_rn(1.0f, scale);
     }
   }
-  float amax_t = 0.0f;
+  float ymax = 0.0f, ymin = 0.0f;  // amax = max(ymax, -ymin)
 
   RingPos pos{0u, 0u};
   RowWalk wk{-1, 0, 0};
   while (wk.next(p)) {
     const uint32_t s = pos.slot;
-    mbar_wait(smem_u32(&full[s]), pos.phase, &g_err_fwd, kErrFullWait);
-    if constexpr (STATS) mbar_wait(smem_u32(&ready[s]), pos.phase, &g_err_fwd, kErrReadyWait);
+    // "ready" is published by a stats warp after it saw the row land, so it
+    // implies "full"
+    if constexpr (STATS)
+      mbar_wait(smem_u32(&ready[s]), pos.phase, &g_err_fwd, kErrReadyWait);
+    else
+      mbar_wait(smem_u32(&full[s]), pos.phase, &g_err_fwd, kErrFullWait);
     float mean = 0.0f, rs = 1.0f;
     if constexpr (STATS || META) {
       const float2 m = rstat[s];
@@ -299,7 +303,10 @@ __global__ void __launch_bounds__(WIDE ? kMaxThreadsWide : kMaxThreads, WIDE ? 1
           } else {
             y[i] = V::f32(raw, i);
           }
-          if constexpr (QM == kQDelayed || QM == kQCurAmax) amax_t = amax_acc2(amax_t, y[i]);
+          if constexpr (QM == kQDelayed || QM == kQCurAmax) {
+            ymax = max3(ymax, y[i]);
+            ymin = min3(ymin, y[i]);
+          }
         }
         if constexpr (QM != kQCurAmax) store_chunk<PAIRS, QM>(p, rowe + (size_t)v * VEC, y, scale);
       }
@@ -310,6 +317,8 @@ __global__ void __launch_bounds__(WIDE ? kMaxThreadsWide : kMaxThreads, WIDE ? 1
   }
 
   if constexpr (QM == kQDelayed || QM == kQCurAmax) {
+    float amax_t;
+    asm("max.NaN.f32 %0, %1, %2;" : "=f"(amax_t) : "f"(ymax), "f"(-ymin));
     const uint32_t b = warp_umax(abs_bits(amax_t));
     if (lane == 0) red[warp] = b;
     consumer_sync(TH);

@@ -189,12 +189,15 @@ __global__ void __launch_bounds__(kMaxThreads, 1) rn_mx_kernel(const MxParams p)
   RingPos pos{0u, 0u};
   for (int tile = blockIdx.x; tile < p.n_tiles; tile += G) {
     const int r0 = tile * kTile;
-    // this lane's 8 rows: wait until they have landed and have statistics
+    // the whole warp waits for the tile's 32 rows (warp-uniform waits; "ready"
+    // implies the row has landed)
     {
-      RingPos rp = pos.ahead(8 * rg, Q);
-      for (int j = 0; j < 8; ++j) {
-        mbar_wait(smem_u32(&full[rp.slot]), rp.phase, &g_err_mx, kErrFullWait);
-        if constexpr (STATS) mbar_wait(smem_u32(&ready[rp.slot]), rp.phase, &g_err_mx, kErrReadyWait);
+      RingPos rp = pos;
+      for (int k = 0; k < kTile; ++k) {
+        if constexpr (STATS)
+          mbar_wait(smem_u32(&ready[rp.slot]), rp.phase, &g_err_mx, kErrReadyWait);
+        else
+          mbar_wait(smem_u32(&full[rp.slot]), rp.phase, &g_err_mx, kErrFullWait);
         rp.advance(1, Q);
       }
     }
