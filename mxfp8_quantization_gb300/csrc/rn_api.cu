@@ -124,29 +124,59 @@ rn_status plan_roles(int nchunks, size_t per_slot, size_t fixed, const DeviceInf
   return RN_OK;
 }
 
-// row-wise forward; T (rows per tile) is only the unit CTAs take turns on
-constexpr int kFwdTileRows = 4;
+// Row-wise forward: rows are taken by groups of G warps, the fewest that
+// hold a row with <= 16 chunks of 16 bytes a lane (NC = 4 chunks for short
+// rows); every chunk keeps its bounds test (the kernel's FULL variants,
+// without them, need more than the 128 registers a thread of a 512-thread
+// CTA has).  Threads a CTA follow from NC (512 for NC = 16, 1024 for 4: the
+// registers of the row part); W = every warp but the producer, in whole
+// groups, at most 14 groups of G >= 2; one CTA per SM; a ring of Q > W / G
+// rows.
+struct FwdPlan {
+  FwdShape sh;
+  int workers, Q;
+  Launch l;
+};
 
-rn_status plan_fwd(int H, int esz, int N, int sm_margin, const DeviceInfo& di, RowPlan* pl) {
+int fwd_max_threads(int nc) { return nc >= 16 ? 512 : (nc >= 8 ? 768 : 1024); }
+
+rn_status plan_fwd(int nk, int H, int esz, int N, int sm_margin, const DeviceInfo& di,
+                   FwdPlan* pl) {
   const int nchunks = H * esz / 16;
-  // fixed: amax scratch + slack; per slot: the row, (mean, rsigma), three
-  // mbarriers
-  const size_t fixed = 32 * sizeof(uint32_t) + 64;
-  const size_t per_slot = (size_t)H * esz + sizeof(float2) + 24;
-  Roles r;
-  const rn_status st = plan_roles(nchunks, per_slot, fixed, di, 128, &r);
-  if (st != RN_OK) return st;
-  pl->ng = r.ng;
-  pl->T = kFwdTileRows;
-  pl->wpr = 1;
-  pl->apply_warps = r.A;
-  pl->stats_warps = r.S;
-  pl->Q = r.Q;
-  pl->l.threads = 32 * (r.A + r.S + 1);
-  pl->l.smem = (size_t)r.Q * per_slot + fixed;
-  pl->l.work = (N + kFwdTileRows - 1) / kFwdTileRows;
+  FwdShape sh{1, 16, false};
+  while (sh.g <= 8 && nchunks > 32 * sh.g * 16) sh.g *= 2;
+  if (sh.g > 8) return RN_ERR_UNSUPPORTED;
+  if (sh.g == 1 && nchunks <= 32 * 4) sh.nc = 4;
+  const int g = sh.g;
+  // gamma (and beta) staged in shared memory for G <= 2, read through L1
+  // for longer rows
+  const size_t gb =
+      (nk != kIdentity && g <= 2) ? (size_t)H * sizeof(float) * (nk == kLn ? 2 : 1) : 0;
+  // fixed: gamma/beta, group exchange (14 groups x 4 x 8 floats), amax words
+  // (32), slack; per slot: the row, (mu, rsigma), two mbarriers
+  const size_t fixed = gb + 14 * 4 * 8 * sizeof(float) + 32 * sizeof(uint32_t) + 64;
+  const size_t per_slot = (size_t)H * esz + sizeof(float2) + 16;
+  const size_t budget = cta_smem_budget(di, 1);
+  int Q = budget > fixed ? (int)((budget - fixed) / per_slot) : 0;
+  if (Q > 64) Q = 64;
+  if (g >= 4) {
+    // leave L1 room for gamma / beta
+    const int qmax = (int)((size_t(128) << 10) / per_slot);
+    if (Q > qmax) Q = qmax;
+  }
+  int W = (fwd_max_threads(sh.nc) / 32 - 1) / g * g;
+  // groups of several warps: at most 14 (their named barriers are 1 .. 14)
+  if (g > 1 && W / g > 14) W = 14 * g;
+  while (W > g && W / g >= Q) W -= g;
+  if (W / g >= Q) return RN_ERR_UNSUPPORTED;
+  pl->sh = sh;
+  pl->workers = W;
+  pl->Q = Q;
+  pl->l.threads = 32 * (W + 1);
+  pl->l.smem = (size_t)Q * per_slot + fixed;
+  pl->l.work = N;
   pl->l.sms = di.sms - sm_margin;
-  pl->l.per_sm = r.per_sm;
+  pl->l.per_sm = 1;
   return RN_OK;
 }
 
@@ -271,7 +301,7 @@ rn_status fwd_common(int nk, const void* x, rn_dtype dt, const float* gamma, con
   rn_status st = check_out(mode, out, N, H);
   if (st != RN_OK) return st;
   if (!row_ok(H, dt) || !aligned(x, 16)) return RN_ERR_UNSUPPORTED;
-  if ((gamma && !aligned(gamma, 4)) || (beta && !aligned(beta, 4)) ||
+  if ((gamma && !aligned(gamma, 16)) || (beta && !aligned(beta, 16)) ||
       (mu && !aligned(mu, 4)) || (rsigma && !aligned(rsigma, 4)))
     return RN_ERR_UNSUPPORTED;
   DeviceInfo di;
@@ -306,8 +336,8 @@ rn_status fwd_common(int nk, const void* x, rn_dtype dt, const float* gamma, con
     return launch_mx(nk, bf16, pl.ng, p, pl.l, stream);
   }
 
-  RowPlan pl;
-  if ((st = plan_fwd((int)H, esz, (int)N, sm_margin, di, &pl)) != RN_OK) return st;
+  FwdPlan pl;
+  if ((st = plan_fwd(nk, (int)H, esz, (int)N, sm_margin, di, &pl)) != RN_OK) return st;
   FwdParams p{};
   p.x = x;
   p.gamma = gamma;
@@ -324,24 +354,22 @@ rn_status fwd_common(int nk, const void* x, rn_dtype dt, const float* gamma, con
   p.eps = eps;
   p.zcg = zcg ? 1 : 0;
   p.out_f32 = (mode == RN_QUANT_NONE && out->out_dtype == RN_F32) ? 1 : 0;
-  p.T = pl.T;
-  p.apply_warps = pl.apply_warps;
-  p.stats_warps = pl.stats_warps;
+  p.workers = pl.workers;
   p.Q = pl.Q;
-  p.n_tiles = (int)((N + pl.T - 1) / pl.T);
   p.reverse = 0;
 
   switch (mode) {
     case RN_QUANT_NONE:
-      return launch_fwd(nk, bf16, pl.ng, kQNone, p, pl.l, stream);
+      return launch_fwd(nk, bf16, pl.sh, kQNone, p, pl.l, false, stream);
     case RN_QUANT_FP8_DELAYED:
-      if (cudaMemsetAsync(out->amax, 0, sizeof(float), stream) != cudaSuccess) return RN_ERR_CUDA;
-      return launch_fwd(nk, bf16, pl.ng, kQDelayed, p, pl.l, stream);
+      if ((st = launch_fwd_init(out->amax, out->scale, out->scale_inv, stream)) != RN_OK) return st;
+      return launch_fwd(nk, bf16, pl.sh, kQDelayed, p, pl.l, true, stream);
     case RN_QUANT_FP8_CURRENT:
-      if (cudaMemsetAsync(out->amax, 0, sizeof(float), stream) != cudaSuccess) return RN_ERR_CUDA;
-      if ((st = launch_fwd(nk, bf16, pl.ng, kQCurAmax, p, pl.l, stream)) != RN_OK) return st;
+      if ((st = launch_fwd_init(out->amax, nullptr, nullptr, stream)) != RN_OK) return st;
+      if ((st = launch_fwd(nk, bf16, pl.sh, kQCurAmax, p, pl.l, true, stream)) != RN_OK)
+        return st;
       p.reverse = 1;
-      return launch_fwd(nk, bf16, pl.ng, kQCurQuant, p, pl.l, stream);
+      return launch_fwd(nk, bf16, pl.sh, kQCurQuant, p, pl.l, true, stream);
     default:
       return RN_ERR_INVALID;
   }

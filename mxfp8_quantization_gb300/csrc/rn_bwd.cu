@@ -63,6 +63,9 @@ __global__ void __launch_bounds__(WIDE ? kMaxThreadsWide : kMaxThreads, WIDE ? 1
   using V = Vec<TIn, VEC>;
   constexpr int PAIRS = V::PAIRS;
   extern __shared__ __align__(128) unsigned char smem[];
+  // the column reduction (launched next, as a programmatic dependent) may be
+  // placed on SMs as soon as this grid's CTAs retire
+  if (threadIdx.x == 0) pdl_launch_dependents();
 
   const int A = p.apply_warps;          // warps 0 .. A-1
   const int S = p.stats_warps;          // warps A .. A+S-1; producer: A+S
@@ -109,6 +112,7 @@ __global__ void __launch_bounds__(WIDE ? kMaxThreadsWide : kMaxThreads, WIDE ? 1
     if (lane == 0) {
       const unsigned char* xb = static_cast<const unsigned char*>(p.x);
       const unsigned char* db = static_cast<const unsigned char*>(p.dz);
+      const uint64_t stream_pol = l2_evict_first();
       RingPos pos{0u, 0u};
       uint32_t issued = 0;
       for (int c = blockIdx.x; c < p.n_chunks; c += G) {
@@ -122,8 +126,10 @@ __global__ void __launch_bounds__(WIDE ? kMaxThreadsWide : kMaxThreads, WIDE ? 1
           cp_async_arrive(bar);
           mbar_arrive_expect_tx(bar, slot_bytes);
           const uint32_t dst = smem_u32(ring + (size_t)s * slot_bytes);
-          bulk_g2s(dst, xb + (size_t)r * row_bytes, row_bytes, bar);
-          bulk_g2s(dst + row_bytes, db + (size_t)r * row_bytes, row_bytes, bar);
+          // x and dz are read once here: let them leave L2 first, so that the
+          // dgamma/dbeta partials stay there for the column reduction
+          bulk_g2s_hint(dst, xb + (size_t)r * row_bytes, row_bytes, bar, stream_pol);
+          bulk_g2s_hint(dst + row_bytes, db + (size_t)r * row_bytes, row_bytes, bar, stream_pol);
           pos.advance(1, Q);
         }
       }
@@ -203,6 +209,7 @@ __global__ void __launch_bounds__(WIDE ? kMaxThreadsWide : kMaxThreads, WIDE ? 1
     }
   }
   const int nacc = LN ? 2 : 1;
+  const uint64_t keep_pol = l2_evict_last();
 
   RingPos pos{0u, 0u};
   for (int c = blockIdx.x; c < p.n_chunks; c += G) {
@@ -246,7 +253,8 @@ __global__ void __launch_bounds__(WIDE ? kMaxThreadsWide : kMaxThreads, WIDE ? 1
       if (lane == 0) mbar_arrive(smem_u32(&empty[s]));
       pos.advance(1, Q);
     }
-    // chunk finished: write its partial column sums
+    // chunk finished: write its partial column sums (kept in L2 for the
+    // column reduction)
     float* prow = p.part + (size_t)c * nacc * H;
 #pragma unroll
     for (int g = 0; g < NG; ++g) {
@@ -254,11 +262,15 @@ __global__ void __launch_bounds__(WIDE ? kMaxThreadsWide : kMaxThreads, WIDE ? 1
       if (v < nchunks) {
 #pragma unroll
         for (int jj = 0; jj < PAIRS / 2; ++jj) {
-          reinterpret_cast<float4*>(prow + (size_t)v * VEC)[jj] =
-              make_float4(adg[g][2 * jj].x, adg[g][2 * jj].y, adg[g][2 * jj + 1].x, adg[g][2 * jj + 1].y);
+          st_hint_f4(prow + (size_t)v * VEC + 4 * jj,
+                     make_float4(adg[g][2 * jj].x, adg[g][2 * jj].y, adg[g][2 * jj + 1].x,
+                                 adg[g][2 * jj + 1].y),
+                     keep_pol);
           if (LN)
-            reinterpret_cast<float4*>(prow + H + (size_t)v * VEC)[jj] =
-                make_float4(adb[g][2 * jj].x, adb[g][2 * jj].y, adb[g][2 * jj + 1].x, adb[g][2 * jj + 1].y);
+            st_hint_f4(prow + H + (size_t)v * VEC + 4 * jj,
+                       make_float4(adb[g][2 * jj].x, adb[g][2 * jj].y, adb[g][2 * jj + 1].x,
+                                   adb[g][2 * jj + 1].y),
+                       keep_pol);
         }
       }
     }
@@ -273,6 +285,7 @@ __global__ void __launch_bounds__(WIDE ? kMaxThreadsWide : kMaxThreads, WIDE ? 1
 // sums in warp order.  The order depends on the chunk count only.
 __global__ void __launch_bounds__(1024) rn_colreduce_kernel(const ColReduceParams p) {
   __shared__ float2 red[32][33];
+  pdl_wait();  // the partials come from the backward kernel
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int a = blockIdx.y;
   const int col = blockIdx.x * 64 + lane * 2;
@@ -282,16 +295,18 @@ __global__ void __launch_bounds__(1024) rn_colreduce_kernel(const ColReduceParam
   if (col < p.H) {
     const float* base = p.part + (size_t)a * p.H + col;
     const size_t stride = (size_t)p.nacc * p.H;
+    // the partials are read once here; the bwd kernel kept them in L2
+    const uint64_t pol = l2_evict_first();
     int c = warp;
     for (; c + 224 < p.n_chunks; c += 256) {
       float2 v[8];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) v[i] = *reinterpret_cast<const float2*>(base + (size_t)(c + 32 * i) * stride);
+      for (int i = 0; i < 8; ++i) v[i] = ld_hint_f2(base + (size_t)(c + 32 * i) * stride, pol);
 #pragma unroll
       for (int i = 0; i < 8; ++i) acc[i] = add2(acc[i], v[i]);
     }
     for (int i = 0; c < p.n_chunks; c += 32, ++i)
-      acc[i] = add2(acc[i], *reinterpret_cast<const float2*>(base + (size_t)c * stride));
+      acc[i] = add2(acc[i], ld_hint_f2(base + (size_t)c * stride, pol));
   }
   const float2 s = add2(add2(add2(acc[0], acc[1]), add2(acc[2], acc[3])),
                         add2(add2(acc[4], acc[5]), add2(acc[6], acc[7])));
@@ -349,9 +364,21 @@ rn_status launch_bwd(bool ln, bool bf16, int ng, const BwdParams& p, const Launc
   return ln ? launch_ng<float, true>(ng, p, l, s) : launch_ng<float, false>(ng, p, l, s);
 }
 
+// launched as a programmatic dependent of the backward kernel: its CTAs are
+// placed as the backward's CTAs retire and wait (griddepcontrol.wait) for
+// the partials
 rn_status launch_colreduce(const ColReduceParams& p, cudaStream_t s) {
-  dim3 grid((p.H + 63) / 64, p.nacc);
-  rn_colreduce_kernel<<<grid, 1024, 0, s>>>(p);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)((p.H + 63) / 64), (unsigned)p.nacc);
+  cfg.blockDim = dim3(1024);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, rn_colreduce_kernel, p) != cudaSuccess) return RN_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? RN_OK : RN_ERR_CUDA;
 }
 

@@ -103,6 +103,52 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
       : "memory");
 }
 
+// L2 eviction-priority policies (createpolicy), used as cache hints
+__device__ __forceinline__ uint64_t l2_evict_first() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+__device__ __forceinline__ uint64_t l2_evict_last() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
+// bulk copy as bulk_g2s, with an L2 cache-eviction hint for the source
+__device__ __forceinline__ void bulk_g2s_hint(uint32_t dst, const void* src, uint32_t bytes,
+                                              uint32_t bar, uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
+          dst),
+      "l"(src), "r"(bytes), "r"(bar), "l"(pol)
+      : "memory");
+}
+
+// 16-byte global store with an L2 cache-eviction hint
+__device__ __forceinline__ void st_hint_f4(float* p, float4 v, uint64_t pol) {
+  asm volatile("st.global.L2::cache_hint.v4.f32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(p), "f"(v.x),
+               "f"(v.y), "f"(v.z), "f"(v.w), "l"(pol)
+               : "memory");
+}
+
+// 8-byte global load with an L2 cache-eviction hint
+__device__ __forceinline__ float2 ld_hint_f2(const float* p, uint64_t pol) {
+  float2 v;
+  asm volatile("ld.global.L2::cache_hint.v2.f32 {%0, %1}, [%2], %3;" : "=f"(v.x), "=f"(v.y) : "l"(p), "l"(pol));
+  return v;
+}
+
+// Programmatic dependent launch: a kernel launched with programmatic stream
+// serialization may start while the previous kernel of its stream still
+// runs; griddepcontrol.wait blocks until that kernel has completed and its
+// memory operations are visible.  launch_dependents lets the next such
+// kernel start before this one ends.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // 4-byte asynchronous global -> shared copy (cp.async); completion is
 // tracked by cp_async_arrive on an mbarrier
 __device__ __forceinline__ void cp_async4(uint32_t dst, const void* src) {
@@ -273,6 +319,16 @@ __device__ __forceinline__ float2 bf16x2_sub(uint32_t w, float m) {
   return d;
 }
 
+// (x0 + c, x1 + c), each rounded once
+__device__ __forceinline__ float2 bf16x2_add(uint32_t w, float c) {
+  float2 d;
+  asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
+      "add.rn.f32.bf16 %0, l, %3;\n\tadd.rn.f32.bf16 %1, h, %3;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "r"(w), "f"(c));
+  return d;
+}
+
 // acc += (x0, x1)
 __device__ __forceinline__ void bf16x2_acc(float2& acc, uint32_t w) {
   asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
@@ -329,6 +385,9 @@ struct Vec<uint16_t, 8> {  // bf16, 16 bytes
   __device__ __forceinline__ static float2 sub(const Raw& r, int i, float m) {
     return bf16x2_sub(r.w[i], m);
   }
+  __device__ __forceinline__ static float2 add(const Raw& r, int i, float c) {
+    return bf16x2_add(r.w[i], c);
+  }
   __device__ __forceinline__ static void acc(float2& a, const Raw& r, int i) { bf16x2_acc(a, r.w[i]); }
   __device__ __forceinline__ static void sq_acc(float2& a, const Raw& r, int i) {
     bf16x2_sq_acc(a, r.w[i]);
@@ -349,6 +408,9 @@ struct Vec<uint16_t, 4> {  // bf16, 8 bytes
   __device__ __forceinline__ static float2 sub(const Raw& r, int i, float m) {
     return bf16x2_sub(r.w[i], m);
   }
+  __device__ __forceinline__ static float2 add(const Raw& r, int i, float c) {
+    return bf16x2_add(r.w[i], c);
+  }
   __device__ __forceinline__ static void acc(float2& a, const Raw& r, int i) { bf16x2_acc(a, r.w[i]); }
   __device__ __forceinline__ static void sq_acc(float2& a, const Raw& r, int i) {
     bf16x2_sq_acc(a, r.w[i]);
@@ -368,6 +430,9 @@ struct Vec<float, 4> {  // fp32, 16 bytes
   __device__ __forceinline__ static float2 f32(const Raw& r, int i) { return r.p[i]; }
   __device__ __forceinline__ static float2 sub(const Raw& r, int i, float m) {
     return sub2(r.p[i], splat2(m));
+  }
+  __device__ __forceinline__ static float2 add(const Raw& r, int i, float c) {
+    return add2(r.p[i], splat2(c));
   }
   __device__ __forceinline__ static void acc(float2& a, const Raw& r, int i) { a = add2(a, r.p[i]); }
   __device__ __forceinline__ static void sq_acc(float2& a, const Raw& r, int i) {
@@ -390,6 +455,9 @@ struct Vec<float, 8> {  // fp32, 32 bytes
   __device__ __forceinline__ static float2 f32(const Raw& r, int i) { return r.p[i]; }
   __device__ __forceinline__ static float2 sub(const Raw& r, int i, float m) {
     return sub2(r.p[i], splat2(m));
+  }
+  __device__ __forceinline__ static float2 add(const Raw& r, int i, float c) {
+    return add2(r.p[i], splat2(c));
   }
   __device__ __forceinline__ static void acc(float2& a, const Raw& r, int i) { a = add2(a, r.p[i]); }
   __device__ __forceinline__ static void sq_acc(float2& a, const Raw& r, int i) {

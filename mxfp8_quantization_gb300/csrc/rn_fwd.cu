@@ -3,72 +3,93 @@
 // section "Description": the fully fused delayed-scaling path and both
 // passes of the norm+amax-then-quantize current-scaling path).
 //
-// Design (persistent CTAs, one or two per SM; warp-specialized, with no
-// CTA-wide barrier on the row path):
+// Design (one persistent CTA per SM, rows b, b + grid, b + 2 grid, ... for
+// CTA b):
 //   * producer warp: one lane streams whole rows of x into a ring of Q
 //     shared-memory slots with the bulk-copy engine (cp.async.bulk,
 //     completion on the slot's "full" mbarrier) and refills a slot as soon as
-//     the apply warps have released it ("empty"); when a pass needs the saved
+//     its row has been read out ("empty"); when a pass needs the saved
 //     mu / rsigma of a row, the same lane fetches them into the slot with
 //     4-byte cp.async tracked by the same barrier;
-//   * stats warps: warp j of S takes rows j, j+S, ... of the CTA's sequence
-//     and computes its statistics from shared memory (LayerNorm: two passes,
-//     mean then centred sum of squares; RMSNorm: sum of squares), writes
-//     mu / rsigma and publishes (mean, rsigma) on the slot's "ready"
-//     mbarrier;
-//   * apply warps: every thread owns fixed 16-byte column chunks (gamma /
-//     beta in registers for the whole kernel); for each row in order it waits
-//     for "ready", forms y = (x-mu)*rsigma*g + beta (RMSNorm: x*rsigma*g),
-//     stores bf16/fp32 or E4M3 codes, and releases the slot;
-//   so statistics of later rows are computed while earlier rows are applied.
+//   * worker warps, in groups of G warps (G = 1 up to H = 4096 bf16 /
+//     2048 fp32, larger G for longer rows): a group takes every (W/G)-th row
+//     of the CTA's sequence, copies it from its slot into registers (each
+//     lane up to 16 chunks of 16 bytes), releases the slot at once, computes
+//     the row statistics with warp shuffles (LayerNorm: mean, then the
+//     centred sum of squares; RMSNorm: sum of squares; a group of several
+//     warps adds its warp sums in warp order through shared memory), then
+//     forms y = (x-mu)*rsigma*g + beta (RMSNorm: x*rsigma*g) and stores
+//     bf16/fp32 or E4M3 codes.  gamma (+1 when zero-centred) and beta are
+//     staged in shared memory once per CTA (read from global memory for the
+//     longest rows, where they would not fit beside the ring);
+//   so there is no hand-off between warps inside a row, and the per-row cost
+//   (waits, reductions, addressing) is spread over up to 128 elements a lane.
 //   * arithmetic is done on pairs of elements with the packed fp32 (f32x2)
 //     instructions, and bf16 inputs enter through the mixed-precision
-//     add/sub/fma forms, which round exactly like convert-then-operate;
+//     add/sub forms, which round exactly like convert-then-operate;
 //   * the per-tensor amax is reduced per thread, per CTA, then with one
 //     atomicMax on the fp32 bit pattern (ordered like the values for
-//     non-negative numbers, NaN above +inf).
+//     non-negative numbers, NaN above +inf).  A one-thread kernel launched
+//     just before zeroes amax; the forward is launched as its programmatic
+//     dependent and waits for it (griddepcontrol.wait) only before that
+//     atomicMax.
 // Current scaling runs the kernel twice: pass 1 (statistics + amax, no
-// output) and pass 2 (quantize with 448/amax, no stats warps), the second
-// walking the tiles backwards so that it starts on the rows pass 1 left in
-// L2.
+// output) and pass 2 (quantize with 448/amax from the saved mu / rsigma), the
+// second launched as a programmatic dependent of the first and walking the
+// rows backwards so that it starts on the rows pass 1 left in L2.
 #include <cuda_runtime.h>
 
 #include "rn_device.cuh"
 #include "rn_internal.h"
+
+// the (G, NC, FULL) row shapes compiled in
+#ifndef RN_FWD_SHAPES
+#define RN_FWD_SHAPES                                                            \
+  RN_FWD_SHAPE(1, 4, false) RN_FWD_SHAPE(1, 16, false) RN_FWD_SHAPE(2, 16, false) \
+  RN_FWD_SHAPE(4, 16, false) RN_FWD_SHAPE(8, 16, false)
+#endif
 
 namespace rn {
 namespace {
 
 __device__ unsigned g_err_fwd;
 
-// compact shape: at most 8 apply + 4 stats warps + the producer, two CTAs
-// per SM; wide shape: up to 16 apply + 8 stats warps + the producer, one CTA
-constexpr int kMaxThreads = 416;
-constexpr int kMaxThreadsWide = 800;
+// threads a CTA: the row part a lane holds (NC chunks of 16 bytes) sets the
+// registers a thread needs: NC = 16 -> 512 threads (128 registers),
+// NC = 8 -> 768 (80), NC = 4 -> 1024 (64)
+template <int NC>
+constexpr int max_threads() {
+  return NC >= 16 ? 512 : (NC >= 8 ? 768 : 1024);
+}
+// named barriers: 1 .. kMaxGroups for the worker groups (G >= 2), 15 for
+// all workers
+constexpr int kMaxGroups = 14;
+constexpr int kBarWorkers = 15;
 
-// store the PAIRS y pairs of one chunk in the output format
+__device__ __forceinline__ void named_sync(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// store the PAIRS y pairs of one chunk in the output format; o points at the
+// chunk's first output byte
 template <int PAIRS, int QM>
-__device__ __forceinline__ void store_chunk(const FwdParams& p, size_t elem, const float2* y,
+__device__ __forceinline__ void store_chunk(unsigned char* o, int out_f32, const float2* y,
                                             float scale) {
   if constexpr (QM == kQNone) {
-    if (p.out_f32) {
-      float4* o = reinterpret_cast<float4*>(static_cast<float*>(p.out) + elem);
+    if (out_f32) {
+      float4* q = reinterpret_cast<float4*>(o);
 #pragma unroll
       for (int i = 0; i < PAIRS / 2; ++i)
-        o[i] = make_float4(y[2 * i].x, y[2 * i].y, y[2 * i + 1].x, y[2 * i + 1].y);
+        q[i] = make_float4(y[2 * i].x, y[2 * i].y, y[2 * i + 1].x, y[2 * i + 1].y);
+    } else if constexpr (PAIRS == 4) {
+      *reinterpret_cast<uint4*>(o) =
+          make_uint4(pack_bf16x2(y[0].x, y[0].y), pack_bf16x2(y[1].x, y[1].y),
+                     pack_bf16x2(y[2].x, y[2].y), pack_bf16x2(y[3].x, y[3].y));
     } else {
-      uint16_t* o = static_cast<uint16_t*>(p.out) + elem;
-      if constexpr (PAIRS == 4) {
-        *reinterpret_cast<uint4*>(o) =
-            make_uint4(pack_bf16x2(y[0].x, y[0].y), pack_bf16x2(y[1].x, y[1].y),
-                       pack_bf16x2(y[2].x, y[2].y), pack_bf16x2(y[3].x, y[3].y));
-      } else {
-        *reinterpret_cast<uint2*>(o) =
-            make_uint2(pack_bf16x2(y[0].x, y[0].y), pack_bf16x2(y[1].x, y[1].y));
-      }
+      *reinterpret_cast<uint2*>(o) =
+          make_uint2(pack_bf16x2(y[0].x, y[0].y), pack_bf16x2(y[1].x, y[1].y));
     }
   } else {
-    uint8_t* o = static_cast<uint8_t*>(p.out) + elem;
     uint32_t c[PAIRS];
 #pragma unroll
     for (int i = 0; i < PAIRS; ++i) {
@@ -82,74 +103,99 @@ __device__ __forceinline__ void store_chunk(const FwdParams& p, size_t elem, con
   }
 }
 
-// Enumerates the rows of this CTA in the order every role visits them:
-// tiles blockIdx.x, blockIdx.x + gridDim.x, ... (walked from the last tile
-// when reverse), T rows each.
-struct RowWalk {
-  int tk, r, r1;
-  __device__ __forceinline__ bool next(const FwdParams& p) {
-    if (++r < r1) return true;
-    tk = (tk < 0) ? (int)blockIdx.x : tk + (int)gridDim.x;
-    if (tk >= p.n_tiles) return false;
-    const int tt = p.reverse ? p.n_tiles - 1 - tk : tk;
-    r = tt * p.T;
-    r1 = min(r + p.T, p.N);
-    return true;
+// The rows of this CTA: b, b + g, b + 2g, ... (b = blockIdx.x, g = gridDim.x),
+// from the last one when reverse.
+struct RowSeq {
+  int first, step, count;
+  __device__ __forceinline__ explicit RowSeq(const FwdParams& p) {
+    const int b = blockIdx.x, g = gridDim.x;
+    count = b < p.N ? (p.N - b + g - 1) / g : 0;
+    first = p.reverse ? b + (count - 1) * g : b;
+    step = p.reverse ? -g : g;
   }
+  __device__ __forceinline__ int row(int i) const { return first + i * step; }
 };
 
-template <typename TIn, int NG, int NK, int QM, bool WIDE>
-__global__ void __launch_bounds__(WIDE ? kMaxThreadsWide : kMaxThreads, WIDE ? 1 : 2)
-    rn_fwd_kernel(const FwdParams p) {
+// sum of one value per warp over the G warps of a group, added in warp
+// order (the same on every warp of the group); buf selects one of four
+// exchange buffers so that consecutive exchanges never overwrite a value a
+// slower warp of the group has yet to read
+template <int G>
+__device__ __forceinline__ float group_sum(float v, float* red, int group, int wg, int lane,
+                                           int buf) {
+  if constexpr (G == 1) {
+    return v;
+  } else {
+    float* b = red + (group * 4 + buf) * 8;
+    if (lane == 0) b[wg] = v;
+    named_sync(1 + group, 32 * G);
+    float s = b[0];
+#pragma unroll
+    for (int w = 1; w < G; ++w) s += b[w];
+    return s;
+  }
+}
+
+// FULL: every lane holds exactly NC chunks of every row (H = NC * 32 * G
+// chunks), so no chunk needs a bounds test
+template <typename TIn, int NK, int QM, int G, int NC, bool FULL>
+__global__ void __launch_bounds__(max_threads<NC>(), 1) rn_fwd_kernel(const FwdParams p) {
   constexpr int VEC = 16 / (int)sizeof(TIn);
   using V = Vec<TIn, VEC>;
+  using Raw = typename V::Raw;
   constexpr int PAIRS = V::PAIRS;
+  constexpr int F4 = VEC / 4;  // float4 of gamma per chunk
   constexpr bool LN = (NK == kLn);
+  constexpr bool NORM = (NK != kIdentity);
   // pass 2 of current scaling gets mu / rsigma with each row
-  constexpr bool META = (QM == kQCurQuant && NK != kIdentity);
-  // rows whose statistics stats warps compute
-  constexpr bool STATS = (QM != kQCurQuant && NK != kIdentity);
+  constexpr bool META = (QM == kQCurQuant && NORM);
+  constexpr bool STATS = (QM != kQCurQuant && NORM);
+  constexpr bool AMAX = (QM == kQDelayed || QM == kQCurAmax);
+  constexpr bool GB_SMEM = NORM && G <= 2;
   extern __shared__ __align__(128) unsigned char smem[];
 
-  const int A = p.apply_warps;           // warps 0 .. A-1
-  const int S = STATS ? p.stats_warps : 0;  // warps A .. A+S-1; producer: A+S
-  const int TH = A * 32;                 // apply threads
+  const int W = p.workers;  // warps 0 .. W-1; producer: W
   const int H = p.H;
   const int nchunks = H / VEC;
   const uint32_t row_bytes = (uint32_t)H * sizeof(TIn);
   const uint32_t Q = (uint32_t)p.Q;
+  const size_t gb_bytes = GB_SMEM ? (size_t)H * sizeof(float) * (LN ? 2 : 1) : 0;
 
-  unsigned char* ring = smem;
-  float2* rstat = reinterpret_cast<float2*>(smem + (size_t)Q * row_bytes);  // [Q] (mean, rsigma)
-  uint32_t* red = reinterpret_cast<uint32_t*>(rstat + Q);                   // [32]
-  uint64_t* full = reinterpret_cast<uint64_t*>(red + 32);                   // row landed
-  uint64_t* ready = full + Q;                                               // statistics written
-  uint64_t* empty = ready + Q;                                              // slot released
+  float4* gsm = reinterpret_cast<float4*>(smem);  // [F4][nchunks]: g of chunk c, part j
+  float4* bsm = gsm + (size_t)F4 * nchunks;       // same for beta (LayerNorm)
+  unsigned char* ring = smem + gb_bytes;
+  float2* rstat = reinterpret_cast<float2*>(ring + (size_t)Q * row_bytes);  // [Q] (mu, rsigma)
+  float* red = reinterpret_cast<float*>(rstat + Q);                   // [kMaxGroups][4][8]
+  uint32_t* red2 = reinterpret_cast<uint32_t*>(red + kMaxGroups * 4 * 8);  // [32]
+  uint64_t* full = reinterpret_cast<uint64_t*>(red2 + 32);                  // row landed
+  uint64_t* empty = full + Q;                                               // row read out
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  if (QM == kQCurAmax && threadIdx.x == 0) pdl_launch_dependents();
 
   if (threadIdx.x == 0) {
     for (uint32_t i = 0; i < Q; ++i) {
       mbar_init(smem_u32(&full[i]), META ? 2 : 1);
-      mbar_init(smem_u32(&ready[i]), 1);
-      mbar_init(smem_u32(&empty[i]), A);
+      mbar_init(smem_u32(&empty[i]), G);
     }
     fence_barrier_init();
   }
   __syncthreads();
 
-  const int warp = threadIdx.x >> 5;
-  const int lane = threadIdx.x & 31;
+  const RowSeq seq(p);
 
-  if (warp == A + S) {
+  if (warp == W) {
     // ------------------------------------------------------------ producer
+    // (starts streaming rows while the workers stage gamma / beta)
     if (lane == 0) {
+      if constexpr (META) pdl_wait();  // mu / rsigma come from pass 1
       const unsigned char* xb = static_cast<const unsigned char*>(p.x);
       RingPos pos{0u, 0u};
-      uint32_t issued = 0;
-      RowWalk wk{-1, 0, 0};
-      while (wk.next(p)) {
-        const int r = wk.r;
+      for (int i = 0; i < seq.count; ++i) {
+        const int r = seq.row(i);
         const uint32_t s = pos.slot;
-        if (issued >= Q) mbar_wait(smem_u32(&empty[s]), pos.phase ^ 1u, &g_err_fwd, kErrEmptyWait);
+        if (i >= (int)Q) mbar_wait(smem_u32(&empty[s]), pos.phase ^ 1u, &g_err_fwd, kErrEmptyWait);
         const uint32_t bar = smem_u32(&full[s]);
         if constexpr (META) {
           if (LN) cp_async4(smem_u32(&rstat[s].x), p.mu + r);
@@ -157,235 +203,278 @@ __global__ void __launch_bounds__(WIDE ? kMaxThreadsWide : kMaxThreads, WIDE ? 1
           cp_async_arrive(bar);
         }
         mbar_arrive_expect_tx(bar, row_bytes);
-        bulk_g2s(smem_u32(ring + (size_t)s * row_bytes), xb + (size_t)r * row_bytes, row_bytes, bar);
+        bulk_g2s(smem_u32(ring + (size_t)s * row_bytes), xb + (size_t)r * row_bytes, row_bytes,
+                 bar);
         pos.advance(1, Q);
-        ++issued;
       }
       // every copy this CTA issued must have landed before it exits
-      const uint32_t first = issued > Q ? issued - Q : 0;
-      for (uint32_t k = first; k < issued; ++k)
-        mbar_wait(smem_u32(&full[k % Q]), (k / Q) & 1u, &g_err_fwd, kErrDrainWait);
+      const int first = seq.count > (int)Q ? seq.count - (int)Q : 0;
+      for (int k = first; k < seq.count; ++k)
+        mbar_wait(smem_u32(&full[k % Q]), (uint32_t)(k / Q) & 1u, &g_err_fwd, kErrDrainWait);
     }
     return;
   }
 
-  if (warp >= A) {
-    // --------------------------------------------------------- stats warps
-    // stats warp j takes rows j, j + S, j + 2S, ... of the CTA's sequence;
-    // LayerNorm: two passes over the row in shared memory (mean, then the
-    // centred sum of squares); RMSNorm: one pass (sum of squares)
-    if constexpr (STATS) {
-      const int j = warp - A;
-      const float inv_h = 1.0f / (float)H;
-      RingPos pos{0u, 0u};
-      RowWalk wk{-1, 0, 0};
-      int q = 0;
-      while (wk.next(p)) {
-        if (q++ % S == j) {
-          const uint32_t s = pos.slot;
-          // a stats warp is not paced by the apply warps: before waiting for
-          // this use of the slot it waits for the previous use to be
-          // released, so that the parity wait below cannot match a phase
-          // one lap old (alias-free because stats warps are fewer than slots)
-          if (q > (int)Q) mbar_wait(smem_u32(&empty[s]), pos.phase ^ 1u, &g_err_fwd, kErrStatsWait);
-          mbar_wait(smem_u32(&full[s]), pos.phase, &g_err_fwd, kErrStatsWait);
-          const unsigned char* rowp = ring + (size_t)s * row_bytes;
-          float2 a[PAIRS];
-          float mean = 0.0f;
-          if constexpr (LN) {
-#pragma unroll
-            for (int i = 0; i < PAIRS; ++i) a[i] = make_float2(0.f, 0.f);
-            for (int c = lane; c < nchunks; c += 32) {
-              const typename V::Raw raw = V::load(rowp, c);
-#pragma unroll
-              for (int i = 0; i < PAIRS; ++i) V::acc(a[i], raw, i);
-            }
-            float sum = 0.f;
-#pragma unroll
-            for (int i = 0; i < PAIRS; ++i) sum += a[i].x + a[i].y;
-            mean = warp_sum(sum) * inv_h;
-          }
-#pragma unroll
-          for (int i = 0; i < PAIRS; ++i) a[i] = make_float2(0.f, 0.f);
-          for (int c = lane; c < nchunks; c += 32) {
-            const typename V::Raw raw = V::load(rowp, c);
-#pragma unroll
-            for (int i = 0; i < PAIRS; ++i) {
-              if constexpr (LN) {
-                const float2 d = V::sub(raw, i, mean);
-                a[i] = fma2(d, d, a[i]);
-              } else {
-                V::sq_acc(a[i], raw, i);
-              }
-            }
-          }
-          float m2 = 0.f;
-#pragma unroll
-          for (int i = 0; i < PAIRS; ++i) m2 += a[i].x + a[i].y;
-          const float rs = __frsqrt_rn(warp_sum(m2) * inv_h + p.eps);
-          if (lane == 0) {
-            rstat[s] = make_float2(mean, rs);
-            if constexpr (LN) p.mu[wk.r] = mean;
-            p.rsigma[wk.r] = rs;
-            mbar_arrive(smem_u32(&ready[s]));
-          }
-        }
-        pos.advance(1, Q);
-      }
+  if constexpr (GB_SMEM) {
+    // chunk c's gamma as F4 float4, part j at gsm[j * nchunks + c], so that a
+    // warp's 16-byte reads of consecutive chunks are contiguous
+    const int n4 = H / 4;
+    for (int u = threadIdx.x; u < n4; u += 32 * W) {
+      const int c = u / F4, j = u - c * F4;
+      const float4 gv = reinterpret_cast<const float4*>(p.gamma)[u];
+      gsm[j * nchunks + c] =
+          p.zcg ? make_float4(1.0f + gv.x, 1.0f + gv.y, 1.0f + gv.z, 1.0f + gv.w) : gv;
+      if (LN)
+        bsm[j * nchunks + c] = p.beta ? reinterpret_cast<const float4*>(p.beta)[u]
+                                      : make_float4(0.f, 0.f, 0.f, 0.f);
     }
-    return;
+    named_sync(kBarWorkers, 32 * W);
   }
 
-  // ---------------------------------------------------------- apply warps
-  const int t = threadIdx.x;
-  float2 g2[NG][PAIRS], b2[NG][PAIRS];
-#pragma unroll
-  for (int g = 0; g < NG; ++g) {
-    const int v = g * TH + t;
-#pragma unroll
-    for (int i = 0; i < PAIRS; ++i) {
-      g2[g][i] = make_float2(0.f, 0.f);
-      b2[g][i] = make_float2(0.f, 0.f);
-      if (NK != kIdentity && v < nchunks) {
-        const int c = v * VEC + 2 * i;
-        const float ga = p.gamma[c], gb = p.gamma[c + 1];
-        g2[g][i] = p.zcg ? make_float2(1.0f + ga, 1.0f + gb) : make_float2(ga, gb);
-        if (LN && p.beta != nullptr) b2[g][i] = make_float2(p.beta[c], p.beta[c + 1]);
-      }
-    }
-  }
+  // ---------------------------------------------------------- worker warps
+  const int group = warp / G, wg = warp - group * G;
+  const int NGR = W / G;  // groups; NGR < Q, NGR <= kMaxGroups when G > 1
+  // this lane's chunks: cbase + k * CSTEP for k < nvalid
+  const int cbase = wg * 32 + lane;
+  constexpr int CSTEP = 32 * G;
+  const int nv = cbase < nchunks ? (nchunks - cbase + CSTEP - 1) / CSTEP : 0;
+  const int nvalid = FULL ? NC : (nv < NC ? nv : NC);
+  // the apply loop keeps a (then always true) test per chunk even for full
+  // rows: with the chunks in one straight block the scheduler overlaps the
+  // gamma / beta reads of many chunks and runs out of registers
+  int nvalid_apply;
+  asm volatile("mov.b32 %0, %1;" : "=r"(nvalid_apply) : "r"(nvalid));
+  const float inv_h = 1.0f / (float)H;
+  const int oesz = (QM == kQNone) ? (p.out_f32 ? 4 : 2) : 1;  // output bytes per element
+  const size_t ostep = (size_t)CSTEP * VEC * oesz;              // output bytes from k to k + 1
 
   float scale = 1.0f;
-  if constexpr (QM == kQDelayed) {
-    scale = *p.scale;
-    if (blockIdx.x == 0 && t == 0) *p.scale_inv = __fdiv_rn(1.0f, scale);
-  }
+  if constexpr (QM == kQDelayed) scale = *p.scale;
   if constexpr (QM == kQCurQuant) {
+    pdl_wait();  // amax comes from pass 1
     const float am = *p.amax;
     scale = (am == 0.0f) ? 1.0f : __fdiv_rn(448.0f, am);
-    if (blockIdx.x == 0 && t == 0) {
+    if (blockIdx.x == 0 && threadIdx.x == 0) {
       *p.scale_out = scale;
       *p.scale_inv = __fdiv_rn(1.0f, scale);
     }
   }
   float ymax = 0.0f, ymin = 0.0f;  // amax = max(ymax, -ymin)
 
-  RingPos pos{0u, 0u};
-  RowWalk wk{-1, 0, 0};
-  while (wk.next(p)) {
+  RingPos pos{(uint32_t)group, 0u};
+  int par = 0;
+  for (int i = group; i < seq.count; i += NGR) {
     const uint32_t s = pos.slot;
-    // "ready" is published by a stats warp after it saw the row land, so it
-    // implies "full"
-    if constexpr (STATS)
-      mbar_wait(smem_u32(&ready[s]), pos.phase, &g_err_fwd, kErrReadyWait);
-    else
-      mbar_wait(smem_u32(&full[s]), pos.phase, &g_err_fwd, kErrFullWait);
+    // before waiting for this use of the slot, wait for the previous use to
+    // be released: that use has then landed, so the parity wait below cannot
+    // match a phase one lap old (alias-free since NGR < Q)
+    if (i >= (int)Q) mbar_wait(smem_u32(&empty[s]), pos.phase ^ 1u, &g_err_fwd, kErrStatsWait);
+    mbar_wait(smem_u32(&full[s]), pos.phase, &g_err_fwd, kErrFullWait);
+    const unsigned char* rowp = ring + (size_t)s * row_bytes;
+    Raw raw[NC];
+#pragma unroll
+    for (int k = 0; k < NC; ++k)
+      if (k < nvalid) raw[k] = V::load(rowp, cbase + k * CSTEP);
     float mean = 0.0f, rs = 1.0f;
-    if constexpr (STATS || META) {
+    if constexpr (META) {
       const float2 m = rstat[s];
       mean = LN ? m.x : 0.0f;
       rs = m.y;
     }
-    const unsigned char* rowp = ring + (size_t)s * row_bytes;
-    const size_t rowe = (size_t)wk.r * H;
-#pragma unroll
-    for (int g = 0; g < NG; ++g) {
-      const int v = g * TH + t;
-      if (v < nchunks) {
-        const typename V::Raw raw = V::load(rowp, v);
-        float2 y[PAIRS];
-#pragma unroll
-        for (int i = 0; i < PAIRS; ++i) {
-          if constexpr (LN) {
-            y[i] = fma2(mul2(V::sub(raw, i, mean), splat2(rs)), g2[g][i], b2[g][i]);
-          } else if constexpr (NK == kRms) {
-            y[i] = mul2(mul2(V::f32(raw, i), splat2(rs)), g2[g][i]);
-          } else {
-            y[i] = V::f32(raw, i);
-          }
-          if constexpr (QM == kQDelayed || QM == kQCurAmax) {
-            ymax = max3(ymax, y[i]);
-            ymin = min3(ymin, y[i]);
-          }
-        }
-        if constexpr (QM != kQCurAmax) store_chunk<PAIRS, QM>(p, rowe + (size_t)v * VEC, y, scale);
-      }
-    }
     __syncwarp();
     if (lane == 0) mbar_arrive(smem_u32(&empty[s]));
-    pos.advance(1, Q);
+    pos.advance((uint32_t)NGR, Q);
+    const int r = seq.row(i);
+
+    if constexpr (STATS) {
+      float2 a[PAIRS];
+      if constexpr (LN) {
+#pragma unroll
+        for (int j = 0; j < PAIRS; ++j) a[j] = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int k = 0; k < NC; ++k)
+          if (k < nvalid) {
+#pragma unroll
+            for (int j = 0; j < PAIRS; ++j) V::acc(a[j], raw[k], j);
+          }
+        float sum = 0.f;
+#pragma unroll
+        for (int j = 0; j < PAIRS; ++j) sum += a[j].x + a[j].y;
+        mean = group_sum<G>(warp_sum(sum), red, group, wg, lane, 2 * par) * inv_h;
+      }
+#pragma unroll
+      for (int j = 0; j < PAIRS; ++j) a[j] = make_float2(0.f, 0.f);
+#pragma unroll
+      for (int k = 0; k < NC; ++k)
+        if (k < nvalid) {
+#pragma unroll
+          for (int j = 0; j < PAIRS; ++j) {
+            if constexpr (LN) {
+              const float2 d = V::sub(raw[k], j, mean);
+              a[j] = fma2(d, d, a[j]);
+            } else {
+              V::sq_acc(a[j], raw[k], j);
+            }
+          }
+        }
+      float m2 = 0.f;
+#pragma unroll
+      for (int j = 0; j < PAIRS; ++j) m2 += a[j].x + a[j].y;
+      m2 = group_sum<G>(warp_sum(m2), red, group, wg, lane, 2 * par + 1);
+      rs = __frsqrt_rn(m2 * inv_h + p.eps);
+      if (wg == 0 && lane == 0) {
+        if constexpr (LN) p.mu[r] = mean;
+        p.rsigma[r] = rs;
+      }
+      par ^= 1;
+    }
+
+    unsigned char* orow =
+        static_cast<unsigned char*>(p.out) + ((size_t)r * H + (size_t)cbase * VEC) * oesz;
+    const float2 rs2 = splat2(rs);
+#pragma unroll
+    for (int k = 0; k < NC; ++k) {
+      if (k < nvalid_apply) {
+        const int c = cbase + k * CSTEP;
+        float4 gv[F4], bv[F4];
+        if constexpr (NORM) {
+#pragma unroll
+          for (int j = 0; j < F4; ++j) {
+            if constexpr (GB_SMEM) {
+              gv[j] = gsm[j * nchunks + c];
+              if (LN) bv[j] = bsm[j * nchunks + c];
+            } else {
+              gv[j] = __ldg(reinterpret_cast<const float4*>(p.gamma) + c * F4 + j);
+              if (p.zcg)
+                gv[j] = make_float4(1.0f + gv[j].x, 1.0f + gv[j].y, 1.0f + gv[j].z, 1.0f + gv[j].w);
+              if (LN)
+                bv[j] = p.beta ? __ldg(reinterpret_cast<const float4*>(p.beta) + c * F4 + j)
+                               : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+          }
+        }
+        float2 y[PAIRS];
+#pragma unroll
+        for (int j = 0; j < PAIRS; ++j) {
+          if constexpr (NORM) {
+            const float4& g4 = gv[j / 2];
+            const float2 gp = (j & 1) ? make_float2(g4.z, g4.w) : make_float2(g4.x, g4.y);
+            if constexpr (LN) {
+              const float4& b4 = bv[j / 2];
+              const float2 bp = (j & 1) ? make_float2(b4.z, b4.w) : make_float2(b4.x, b4.y);
+              // x + (-mean): the same value as x - mean, written differently
+              // so that the compiler does not keep the variance pass's
+              // differences alive (128 registers) to reuse them here
+              y[j] = fma2(mul2(V::add(raw[k], j, -mean), rs2), gp, bp);
+            } else {
+              y[j] = mul2(mul2(V::f32(raw[k], j), rs2), gp);
+            }
+          } else {
+            y[j] = V::f32(raw[k], j);
+          }
+          if constexpr (AMAX) {
+            ymax = max3(ymax, y[j]);
+            ymin = min3(ymin, y[j]);
+          }
+        }
+        if constexpr (QM != kQCurAmax)
+          store_chunk<PAIRS, QM>(orow + (size_t)k * ostep, p.out_f32, y, scale);
+      }
+    }
   }
 
-  if constexpr (QM == kQDelayed || QM == kQCurAmax) {
+  if constexpr (AMAX) {
     float amax_t;
     asm("max.NaN.f32 %0, %1, %2;" : "=f"(amax_t) : "f"(ymax), "f"(-ymin));
     const uint32_t b = warp_umax(abs_bits(amax_t));
-    if (lane == 0) red[warp] = b;
-    consumer_sync(TH);
-    if (t == 0) {
+    if (lane == 0) red2[warp] = b;
+    named_sync(kBarWorkers, 32 * W);
+    if (threadIdx.x == 0) {
       uint32_t m = 0;
-      for (int w = 0; w < A; ++w) m = max(m, red[w]);
+      for (int w = 0; w < W; ++w) m = max(m, red2[w]);
+      pdl_wait();  // amax was zeroed by the kernel this one depends on
       atomicMax(reinterpret_cast<unsigned int*>(p.amax), m);
     }
   }
 }
 
-template <typename TIn, int NG, int NK, int QM, bool WIDE>
-rn_status launch_t(const FwdParams& p, const Launch& l, cudaStream_t s) {
-  auto k = rn_fwd_kernel<TIn, NG, NK, QM, WIDE>;
+// zeroes amax (and forms scale_inv = 1/scale for delayed scaling) ahead of
+// the forward, which is launched as its programmatic dependent
+__global__ void rn_fwd_init_kernel(float* amax, const float* scale, float* scale_inv) {
+  pdl_launch_dependents();
+  *amax = 0.0f;
+  if (scale != nullptr) *scale_inv = __fdiv_rn(1.0f, *scale);
+}
+
+template <typename TIn, int NK, int QM, int G, int NC, bool FULL>
+rn_status launch_t(const FwdParams& p, const Launch& l, bool pdl, cudaStream_t s) {
+  auto k = rn_fwd_kernel<TIn, NK, QM, G, NC, FULL>;
+  // the shared-memory exchange buffers and named barriers exist for at most
+  // kMaxGroups groups of G >= 2 warps and 31 worker warps
+  const int workers = l.threads / 32 - 1;
+  if (l.threads > max_threads<NC>() || workers != p.workers || workers % G != 0 || workers > 31 ||
+      (G > 1 && workers / G > kMaxGroups))
+    return RN_ERR_UNSUPPORTED;
   if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)l.smem) !=
       cudaSuccess)
     return RN_ERR_CUDA;
   int grid = 1;
   if (persistent_grid(k, l, &grid) != RN_OK) return RN_ERR_CUDA;
-  k<<<grid, l.threads, l.smem, s>>>(p);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3((unsigned)l.threads);
+  cfg.dynamicSmemBytes = l.smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  if (cudaLaunchKernelEx(&cfg, k, p) != cudaSuccess) return RN_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? RN_OK : RN_ERR_CUDA;
 }
 
-// compact shape for NG 1 and 2; wide shape for NG 2, 4 and 8
+// row shapes (G, NC, FULL); the planner picks one of these
 template <typename TIn, int NK, int QM>
-rn_status launch_ng(int ng, const FwdParams& p, const Launch& l, cudaStream_t s) {
-  const bool wide = l.threads > kMaxThreads || l.per_sm == 1;
-  if (!wide) {
-    switch (ng) {
-      case 1: return launch_t<TIn, 1, NK, QM, false>(p, l, s);
-      case 2: return launch_t<TIn, 2, NK, QM, false>(p, l, s);
-      default: return RN_ERR_UNSUPPORTED;
-    }
-  }
-  if (l.threads > kMaxThreadsWide) return RN_ERR_UNSUPPORTED;
-  switch (ng) {
-    case 2: return launch_t<TIn, 2, NK, QM, true>(p, l, s);
-    case 4: return launch_t<TIn, 4, NK, QM, true>(p, l, s);
-    case 8: return launch_t<TIn, 8, NK, QM, true>(p, l, s);
-    default: return RN_ERR_UNSUPPORTED;
-  }
+rn_status launch_shape(const FwdShape& sh, const FwdParams& p, const Launch& l, bool pdl,
+                       cudaStream_t s) {
+#define RN_FWD_SHAPE(G_, NC_, FULL_) \
+  if (sh.g == G_ && sh.nc == NC_ && sh.full == FULL_) return launch_t<TIn, NK, QM, G_, NC_, FULL_>(p, l, pdl, s);
+  RN_FWD_SHAPES
+#undef RN_FWD_SHAPE
+  return RN_ERR_UNSUPPORTED;
 }
 
 template <typename TIn, int NK>
-rn_status launch_q(int ng, int qmode, const FwdParams& p, const Launch& l, cudaStream_t s) {
+rn_status launch_q(const FwdShape& sh, int qmode, const FwdParams& p, const Launch& l, bool pdl,
+                   cudaStream_t s) {
   switch (qmode) {
     case kQNone:
       if constexpr (NK == kIdentity) return RN_ERR_UNSUPPORTED;
-      else return launch_ng<TIn, NK, kQNone>(ng, p, l, s);
-    case kQDelayed: return launch_ng<TIn, NK, kQDelayed>(ng, p, l, s);
-    case kQCurAmax: return launch_ng<TIn, NK, kQCurAmax>(ng, p, l, s);
-    case kQCurQuant: return launch_ng<TIn, NK, kQCurQuant>(ng, p, l, s);
+      else return launch_shape<TIn, NK, kQNone>(sh, p, l, pdl, s);
+    case kQDelayed: return launch_shape<TIn, NK, kQDelayed>(sh, p, l, pdl, s);
+    case kQCurAmax: return launch_shape<TIn, NK, kQCurAmax>(sh, p, l, pdl, s);
+    case kQCurQuant: return launch_shape<TIn, NK, kQCurQuant>(sh, p, l, pdl, s);
     default: return RN_ERR_INVALID;
   }
 }
 
 }  // namespace
 
-rn_status launch_fwd(int nk, bool bf16, int ng, int qmode, const FwdParams& p, const Launch& l,
-                     cudaStream_t s) {
+rn_status launch_fwd_init(float* amax, const float* scale, float* scale_inv, cudaStream_t s) {
+  rn_fwd_init_kernel<<<1, 1, 0, s>>>(amax, scale, scale_inv);
+  return cudaGetLastError() == cudaSuccess ? RN_OK : RN_ERR_CUDA;
+}
+
+rn_status launch_fwd(int nk, bool bf16, const FwdShape& sh, int qmode, const FwdParams& p,
+                     const Launch& l, bool pdl, cudaStream_t s) {
   if (nk == kIdentity)
-    return bf16 ? RN_ERR_UNSUPPORTED : launch_q<float, kIdentity>(ng, qmode, p, l, s);
+    return bf16 ? RN_ERR_UNSUPPORTED : launch_q<float, kIdentity>(sh, qmode, p, l, pdl, s);
   if (bf16)
-    return nk == kLn ? launch_q<uint16_t, kLn>(ng, qmode, p, l, s)
-                     : launch_q<uint16_t, kRms>(ng, qmode, p, l, s);
-  return nk == kLn ? launch_q<float, kLn>(ng, qmode, p, l, s)
-                   : launch_q<float, kRms>(ng, qmode, p, l, s);
+    return nk == kLn ? launch_q<uint16_t, kLn>(sh, qmode, p, l, pdl, s)
+                     : launch_q<uint16_t, kRms>(sh, qmode, p, l, pdl, s);
+  return nk == kLn ? launch_q<float, kLn>(sh, qmode, p, l, pdl, s)
+                   : launch_q<float, kRms>(sh, qmode, p, l, pdl, s);
 }
 
 rn_status read_clear_error_fwd(unsigned* code) {

@@ -24,25 +24,22 @@ enum FwdQuant : int {
 
 struct FwdParams {
   const void* x;
-  const float* gamma;
+  const float* gamma;   // 16-byte aligned
   const float* beta;
   void* out;            // [N, H] (bf16/fp32 or E4M3 codes)
   float* mu;            // LayerNorm: written (pass 1) or read (kQCurQuant)
   float* rsigma;
   const float* scale;   // kQDelayed
   float* amax;          // kQDelayed, kQCurAmax: reduced into; kQCurQuant: read
-  float* scale_inv;     // kQDelayed, kQCurQuant
+  float* scale_inv;     // kQCurQuant (kQDelayed: written by the init kernel)
   float* scale_out;     // kQCurQuant
   int N, H;
   float eps;
   int zcg;              // zero-centered gamma
   int out_f32;          // kQNone: 1 = fp32 output, 0 = bf16
-  int T;                // rows per tile (the unit CTAs take turns on)
-  int apply_warps;      // warps that apply and store
-  int stats_warps;      // warps that compute row statistics
-  int Q;                // ring slots (rows)
-  int n_tiles;
-  int reverse;          // walk the tiles from the last one
+  int workers;          // worker warps (a multiple of the row group size)
+  int Q;                // ring slots (rows); more than workers / group size
+  int reverse;          // walk the rows from the last one
 };
 
 struct MxParams {
@@ -122,8 +119,17 @@ rn_status persistent_grid(Kernel k, const Launch& l, int* grid) {
 }
 
 // launch functions (one per translation unit family)
-rn_status launch_fwd(int nk, bool bf16, int ng, int qmode, const FwdParams& p, const Launch& l,
-                     cudaStream_t s);
+// row shape of the forward: G warps per row, NC 16-byte chunks per lane,
+// full = every lane holds exactly NC chunks (H * esz == 16 * 32 * G * NC)
+struct FwdShape {
+  int g, nc;
+  bool full;
+};
+// pdl: launch as a programmatic dependent of the previous kernel
+rn_status launch_fwd(int nk, bool bf16, const FwdShape& sh, int qmode, const FwdParams& p,
+                     const Launch& l, bool pdl, cudaStream_t s);
+// one-thread kernel: amax = 0 and, when scale != NULL, scale_inv = 1/scale
+rn_status launch_fwd_init(float* amax, const float* scale, float* scale_inv, cudaStream_t s);
 rn_status launch_mx(int nk, bool bf16, int ng, const MxParams& p, const Launch& l,
                     cudaStream_t s);
 rn_status launch_bwd(bool ln, bool bf16, int ng, const BwdParams& p, const Launch& l,
