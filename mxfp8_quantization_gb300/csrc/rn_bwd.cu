@@ -40,6 +40,8 @@ __device__ unsigned g_err_bwd;
 // per SM; wide shape: up to 16 apply + 8 stats warps + the producer, one CTA
 constexpr int kMaxThreads = 416;
 constexpr int kMaxThreadsWide = 800;
+// rows the producer issues before waiting for the first one to land
+constexpr uint32_t kStartRows = 2;
 
 template <typename TIn>
 __device__ __forceinline__ void store_dx(void* base, size_t elem, const float2* d);
@@ -86,12 +88,10 @@ __global__ void __launch_bounds__(WIDE ? kMaxThreadsWide : kMaxThreads, WIDE ? 1
   uint64_t* ready = full + Q;
   uint64_t* empty = ready + Q;
 
-  if (threadIdx.x == 0) {
-    for (uint32_t i = 0; i < Q; ++i) {
-      mbar_init(smem_u32(&full[i]), 2);  // bulk copies + the mu/rsigma cp.async
-      mbar_init(smem_u32(&ready[i]), 1);
-      mbar_init(smem_u32(&empty[i]), A);
-    }
+  for (uint32_t i = threadIdx.x; i < Q; i += blockDim.x) {
+    mbar_init(smem_u32(&full[i]), 2);  // bulk copies + the mu/rsigma cp.async
+    mbar_init(smem_u32(&ready[i]), 1);
+    mbar_init(smem_u32(&empty[i]), A);
     fence_barrier_init();
   }
   for (int j = threadIdx.x; j < H / 4; j += blockDim.x) {
@@ -119,6 +119,10 @@ __global__ void __launch_bounds__(WIDE ? kMaxThreadsWide : kMaxThreads, WIDE ? 1
         const int r1 = min((c + 1) * R, p.N);
         for (int r = c * R; r < r1; ++r, ++issued) {
           const uint32_t s = pos.slot;
+          // the first kStartRows rows go out alone, the rest of the ring once
+          // row 0 is in (a start-up burst of whole rings from every SM lands
+          // all at once, late)
+          if (issued == kStartRows) mbar_wait(smem_u32(&full[0]), 0u, &g_err_bwd, kErrFullWait);
           if (issued >= Q) mbar_wait(smem_u32(&empty[s]), pos.phase ^ 1u, &g_err_bwd, kErrEmptyWait);
           const uint32_t bar = smem_u32(&full[s]);
           if (LN) cp_async4(smem_u32(&meta[s].x), p.mu + r);

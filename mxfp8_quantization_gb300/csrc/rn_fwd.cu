@@ -65,6 +65,8 @@ constexpr int max_threads() {
 // all workers
 constexpr int kMaxGroups = 14;
 constexpr int kBarWorkers = 15;
+// rows the producer issues before waiting for the first one to land
+constexpr int kStartRows = 2;
 
 __device__ __forceinline__ void named_sync(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
@@ -174,11 +176,9 @@ __global__ void __launch_bounds__(max_threads<NC>(), 1) rn_fwd_kernel(const FwdP
   const int lane = threadIdx.x & 31;
   if (QM == kQCurAmax && threadIdx.x == 0) pdl_launch_dependents();
 
-  if (threadIdx.x == 0) {
-    for (uint32_t i = 0; i < Q; ++i) {
-      mbar_init(smem_u32(&full[i]), META ? 2 : 1);
-      mbar_init(smem_u32(&empty[i]), G);
-    }
+  for (uint32_t i = threadIdx.x; i < Q; i += blockDim.x) {
+    mbar_init(smem_u32(&full[i]), META ? 2 : 1);
+    mbar_init(smem_u32(&empty[i]), G);
     fence_barrier_init();
   }
   __syncthreads();
@@ -195,6 +195,10 @@ __global__ void __launch_bounds__(max_threads<NC>(), 1) rn_fwd_kernel(const FwdP
       for (int i = 0; i < seq.count; ++i) {
         const int r = seq.row(i);
         const uint32_t s = pos.slot;
+        // a start-up burst of whole rings from every SM lands all at once,
+        // late; instead the first kStartRows rows go out alone and the rest
+        // of the ring once row 0 is in, so that the workers start early
+        if (i == kStartRows) mbar_wait(smem_u32(&full[0]), 0u, &g_err_fwd, kErrFullWait);
         if (i >= (int)Q) mbar_wait(smem_u32(&empty[s]), pos.phase ^ 1u, &g_err_fwd, kErrEmptyWait);
         const uint32_t bar = smem_u32(&full[s]);
         if constexpr (META) {
