@@ -412,22 +412,7 @@ rn_status bwd_common(bool ln, const void* dz, const void* x, rn_dtype dt, const 
   }
   const int esz = elem_size(dt);
   const size_t row_bytes = (size_t)H * esz;
-  // roles as in the forward (plan_roles).  fixed: g [H] (as float4 parts of
-  // each chunk) + slack; per slot: the x and dz rows, (mu, rsigma) as
-  // loaded, (mu, rsigma, c1, c2), three mbarriers.
   const int nch = (int)(H * esz / 16);
-  const size_t fixed = (size_t)H * sizeof(float) + 64;
-  const size_t per_slot = 2 * row_bytes + sizeof(float2) + sizeof(float4) + 24;
-  Roles ro;
-  if ((st = plan_roles(nch, per_slot, fixed, di, 64, &ro)) != RN_OK) return st;
-  const int ng = ro.ng, A = ro.A, S = ro.S, Q = ro.Q;
-  Launch l;
-  l.threads = 32 * (A + S + 1);
-  l.smem = (size_t)Q * per_slot + fixed;
-  l.work = sh.n_chunks;
-  l.sms = di.sms - sm_margin;
-  l.per_sm = ro.per_sm;
-
   BwdParams p{};
   p.dz = dz;
   p.x = x;
@@ -440,11 +425,61 @@ rn_status bwd_common(bool ln, const void* dz, const void* x, rn_dtype dt, const 
   p.H = (int)H;
   p.zcg = zcg ? 1 : 0;
   p.chunk_rows = sh.chunk_rows;
-  p.apply_warps = A;
-  p.stats_warps = S;
-  p.Q = Q;
   p.n_chunks = sh.n_chunks;
-  if ((st = launch_bwd(ln, dt == RN_BF16, ng, p, l, stream)) != RN_OK) return st;
+  Launch l;
+  l.work = sh.n_chunks;
+  l.sms = di.sms - sm_margin;
+
+  // fp32 rows that 16 warps cover with 16 elements (4 chunks) a thread take
+  // the kernel without stats or producer warps: A warps, up to 8 with as
+  // many CTAs per SM (<= 4) as keep a ring of >= 6 slots and 128 registers a
+  // thread, else one CTA per SM with up to 16.  (bf16 rows stay with the
+  // stats-warp kernel: with its more warps per SM it is the faster of the
+  // two there, 44.5 vs 47.3 us for 8192 x 4096.)  per slot: the x and dz
+  // rows, (mu, rsigma), an mbarrier; fixed: the warp-sum exchange (2 x 16
+  // float2) + slack.
+  const int ngf = 4;
+  const int Af = (nch + 32 * ngf - 1) / (32 * ngf);
+  if (dt == RN_F32 && Af <= 16) {
+    const size_t per_slot = 2 * row_bytes + sizeof(float2) + 8;
+    const size_t fixed = 32 * sizeof(float2) + 64;
+    const bool big = Af > 8;
+    int per_sm = 0, Q = 0;
+    for (int k = big ? 1 : 4; k >= 1 && per_sm == 0; --k) {
+      if (k * 32 * Af > 512 && k > 1) continue;
+      const size_t b = cta_smem_budget(di, k);
+      int q = b > fixed ? (int)((b - fixed) / per_slot) : 0;
+      if (q > 64) q = 64;
+      if (q >= (k > 1 ? 6 : 3)) {
+        per_sm = k;
+        Q = q;
+      }
+    }
+    if (per_sm == 0) return RN_ERR_UNSUPPORTED;
+    p.apply_warps = Af;
+    p.stats_warps = 0;
+    p.Q = Q;
+    l.threads = 32 * Af;
+    l.smem = (size_t)Q * per_slot + fixed;
+    l.per_sm = per_sm;
+    if ((st = launch_bwd_fused(ln, big, p, l, stream)) != RN_OK) return st;
+  } else {
+    // longer rows: stats warps + apply warps (roles as in plan_roles).
+    // fixed: g [H] (as float4 parts of each chunk) + slack; per slot: the x
+    // and dz rows, (mu, rsigma) as loaded, (mu, rsigma, c1, c2), three
+    // mbarriers.
+    const size_t fixed = (size_t)H * sizeof(float) + 64;
+    const size_t per_slot = 2 * row_bytes + sizeof(float2) + sizeof(float4) + 24;
+    Roles ro;
+    if ((st = plan_roles(nch, per_slot, fixed, di, 64, &ro)) != RN_OK) return st;
+    p.apply_warps = ro.A;
+    p.stats_warps = ro.S;
+    p.Q = ro.Q;
+    l.threads = 32 * (ro.A + ro.S + 1);
+    l.smem = (size_t)ro.Q * per_slot + fixed;
+    l.per_sm = ro.per_sm;
+    if ((st = launch_bwd(ln, dt == RN_BF16, ro.ng, p, l, stream)) != RN_OK) return st;
+  }
   ColReduceParams c{};
   c.part = p.part;
   c.dgamma = dgamma;

@@ -43,6 +43,10 @@ constexpr int kMaxThreadsWide = 800;
 // rows the producer issues before waiting for the first one to land
 constexpr uint32_t kStartRows = 2;
 
+__device__ __forceinline__ void named_sync(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
 template <typename TIn>
 __device__ __forceinline__ void store_dx(void* base, size_t elem, const float2* d);
 
@@ -281,6 +285,236 @@ __global__ void __launch_bounds__(WIDE ? kMaxThreadsWide : kMaxThreads, WIDE ? 1
   }
 }
 
+// ------------------------------------------------------------ fused kernel
+// fp32 rows of up to 16 warps x 32 threads x 16 elements (H <= 8192): no
+// stats warps and no producer warp.  Every thread owns NG fixed
+// 16-byte chunks (16 elements of each row; gamma and the dgamma / dbeta sums
+// in registers).  Per row it reads its chunks out of the ring slot, forms
+// d = x - mu (RMSNorm: x), dz and dy = dz * g in registers and its share of
+// the two row sums sum(dy) and sum(dy * d); the warps exchange their sums
+// through shared memory around one CTA barrier and add them in a fixed order
+// (a butterfly over the warp sums, identical on every thread); then
+//   dx = rsigma * dy + P * d + B,  P = -rsigma^2 * c2,  B = -rsigma * c1,
+// with c1 = mean(dy) and c2 = mean(dy * xhat) = rsigma * mean(dy * d), which
+// is rsigma * (dy - c1 - xhat * c2) regrouped.
+// The barrier also frees the row's slot (every thread has read it), so lane 0
+// of warp 0 refills it right there with the row Q places ahead (bulk copies
+// of x and dz, cp.async of mu / rsigma, on the slot's "full" mbarrier); the
+// first rows go out one by one at the start so that row 0 lands early.
+constexpr int kFusedCompact = 256;  // <= 8 warps, 2+ CTAs per SM (128 registers)
+constexpr int kFusedBig = 512;      // <= 16 warps, 1 CTA per SM (128 registers)
+
+// the rows of this CTA, chunk by chunk (chunks blockIdx.x + k * gridDim.x)
+struct ChunkRows {
+  int c, r, r1;
+  __device__ __forceinline__ bool next(const BwdParams& p) {
+    if (++r < r1) return true;
+    c = (c < 0) ? (int)blockIdx.x : c + (int)gridDim.x;
+    if (c >= p.n_chunks) return false;
+    r = c * p.chunk_rows;
+    r1 = min(r + p.chunk_rows, p.N);
+    return true;
+  }
+};
+
+template <bool LN>
+__device__ __forceinline__ void issue_row(const BwdParams& p, unsigned char* ring, float2* meta,
+                                          uint64_t* full, uint32_t s, int r, uint32_t row_bytes,
+                                          uint64_t pol) {
+  const uint32_t bar = smem_u32(&full[s]);
+  if (LN) cp_async4(smem_u32(&meta[s].x), p.mu + r);
+  cp_async4(smem_u32(&meta[s].y), p.rsigma + r);
+  cp_async_arrive(bar);
+  mbar_arrive_expect_tx(bar, 2 * row_bytes);
+  const uint32_t dst = smem_u32(ring + (size_t)s * 2 * row_bytes);
+  bulk_g2s_hint(dst, static_cast<const unsigned char*>(p.x) + (size_t)r * row_bytes, row_bytes,
+                bar, pol);
+  bulk_g2s_hint(dst + row_bytes, static_cast<const unsigned char*>(p.dz) + (size_t)r * row_bytes,
+                row_bytes, bar, pol);
+}
+
+template <typename TIn, int NG, bool LN, bool BIG>
+__global__ void __launch_bounds__(BIG ? kFusedBig : kFusedCompact, BIG ? 1 : 2)
+    rn_bwd_fused_kernel(const BwdParams p) {
+  constexpr int VEC = 16 / (int)sizeof(TIn);
+  using V = Vec<TIn, VEC>;
+  constexpr int PAIRS = V::PAIRS;
+  extern __shared__ __align__(128) unsigned char smem[];
+  if (threadIdx.x == 0) pdl_launch_dependents();
+
+  const int A = p.apply_warps;  // warps of the CTA (<= 16)
+  const int TH = A * 32;
+  const int H = p.H;
+  const int nchunks = H / VEC;
+  const uint32_t row_bytes = (uint32_t)H * sizeof(TIn);
+  const uint32_t slot_bytes = 2 * row_bytes;  // x row, then dz row
+  const uint32_t Q = (uint32_t)p.Q;
+
+  unsigned char* ring = smem;
+  float2* meta = reinterpret_cast<float2*>(smem + (size_t)Q * slot_bytes);  // [Q] (mu, rsigma)
+  float2* red = meta + Q;                                                   // [2][16] warp sums
+  uint64_t* full = reinterpret_cast<uint64_t*>(red + 32);
+
+  for (uint32_t i = threadIdx.x; i < Q; i += blockDim.x) {
+    mbar_init(smem_u32(&full[i]), 2);  // bulk copies + the mu/rsigma cp.async
+    fence_barrier_init();
+  }
+  __syncthreads();
+
+  const int t = threadIdx.x;
+  const int warp = t >> 5;
+  const int lane = t & 31;
+  const bool issuer = (t == 0);
+  const uint64_t stream_pol = l2_evict_first();
+
+  // issue cursor (thread 0): rows handed to the copy engine so far
+  ChunkRows iw{-1, 0, 0};
+  uint32_t issued = 0;
+  bool more = true;
+  RingPos ipos{0u, 0u};
+  if (issuer) {
+    while (issued < (uint32_t)kStartRows && issued < Q && (more = iw.next(p))) {
+      issue_row<LN>(p, ring, meta, full, ipos.slot, iw.r, row_bytes, stream_pol);
+      ipos.advance(1, Q);
+      ++issued;
+    }
+  }
+
+  float2 g2[NG][PAIRS];
+#pragma unroll
+  for (int g = 0; g < NG; ++g) {
+    const int v = g * TH + t;
+#pragma unroll
+    for (int i = 0; i < PAIRS; ++i) {
+      g2[g][i] = make_float2(0.f, 0.f);
+      if (v < nchunks) {
+        const int e = v * VEC + 2 * i;
+        const float ga = p.gamma[e], gb = p.gamma[e + 1];
+        g2[g][i] = p.zcg ? make_float2(1.0f + ga, 1.0f + gb) : make_float2(ga, gb);
+      }
+    }
+  }
+  const float inv_h = 1.0f / (float)H;
+  const int nacc = LN ? 2 : 1;
+  const uint64_t keep_pol = l2_evict_last();
+
+  RingPos pos{0u, 0u};
+  uint32_t q = 0;
+  for (int c = blockIdx.x; c < p.n_chunks; c += (int)gridDim.x) {
+    float2 adg[NG][PAIRS], adb[NG][PAIRS];
+#pragma unroll
+    for (int g = 0; g < NG; ++g)
+#pragma unroll
+      for (int i = 0; i < PAIRS; ++i) {
+        adg[g][i] = make_float2(0.f, 0.f);
+        adb[g][i] = make_float2(0.f, 0.f);
+      }
+    const int r1 = min((c + 1) * p.chunk_rows, p.N);
+    for (int r = c * p.chunk_rows; r < r1; ++r, ++q) {
+      const uint32_t s = pos.slot;
+      // every thread read the slot's previous row before the barrier that
+      // let it be refilled, so this parity wait cannot match an older phase
+      mbar_wait(smem_u32(&full[s]), pos.phase, &g_err_bwd, kErrFullWait);
+      const unsigned char* xr = ring + (size_t)s * slot_bytes;
+      const unsigned char* dr = xr + row_bytes;
+      const float2 m = meta[s];
+      const float mu = LN ? m.x : 0.0f;
+      const float rs = m.y;
+
+      // this thread's share of sum(dy) and sum(dy * d)
+      float2 d[NG][PAIRS], dzf[NG][PAIRS];
+      float2 s1 = make_float2(0.f, 0.f), s2 = make_float2(0.f, 0.f);
+#pragma unroll
+      for (int g = 0; g < NG; ++g) {
+        const int v = g * TH + t;
+        const bool ok = v < nchunks;
+        typename V::Raw xw, dw;
+        if (ok) {
+          xw = V::load(xr, v);
+          dw = V::load(dr, v);
+        }
+#pragma unroll
+        for (int i = 0; i < PAIRS; ++i) {
+          d[g][i] = make_float2(0.f, 0.f);
+          dzf[g][i] = make_float2(0.f, 0.f);
+          if (ok) {
+            d[g][i] = LN ? V::sub(xw, i, mu) : V::f32(xw, i);
+            dzf[g][i] = V::f32(dw, i);
+            const float2 dy = mul2(dzf[g][i], g2[g][i]);
+            s1 = add2(s1, dy);
+            s2 = fma2(dy, d[g][i], s2);
+          }
+        }
+      }
+      const float a1 = LN ? warp_sum(s1.x + s1.y) : 0.0f;
+      const float a2 = warp_sum(s2.x + s2.y);
+      float2* rb = red + (q & 1u) * 16;
+      if (lane == 0) rb[warp] = make_float2(a1, a2);
+      // rb[q & 1] is rewritten two rows later, after every thread has passed
+      // the next row's barrier (and so has read it)
+      __syncthreads();
+      pos.advance(1, Q);
+      if (issuer) {
+        // slot s is free: refill it (and, at the start, the rest of the ring)
+        fence_proxy_async();
+        const uint32_t target = q + Q;  // rows issued after this: all up to q + Q
+        while (more && issued <= target && (more = iw.next(p))) {
+          issue_row<LN>(p, ring, meta, full, ipos.slot, iw.r, row_bytes, stream_pol);
+          ipos.advance(1, Q);
+          ++issued;
+        }
+      }
+      float2 tot = (lane < A) ? rb[lane] : make_float2(0.f, 0.f);
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1)
+        tot = add2(tot, make_float2(__shfl_xor_sync(0xFFFFFFFFu, tot.x, o),
+                                    __shfl_xor_sync(0xFFFFFFFFu, tot.y, o)));
+      const float c1 = tot.x * inv_h;         // mean(dy)
+      const float c2 = rs * (tot.y * inv_h);  // mean(dy * xhat)
+      const float2 P2 = splat2(-(rs * rs) * c2);
+      const float2 B2 = splat2(LN ? -rs * c1 : 0.0f);
+      const float2 rs2 = splat2(rs);
+      const size_t rowe = (size_t)r * H;
+#pragma unroll
+      for (int g = 0; g < NG; ++g) {
+        const int v = g * TH + t;
+        if (v < nchunks) {
+          float2 dx[PAIRS];
+#pragma unroll
+          for (int i = 0; i < PAIRS; ++i) {
+            const float2 dy = mul2(dzf[g][i], g2[g][i]);
+            dx[i] = fma2(dy, rs2, fma2(d[g][i], P2, B2));
+            adg[g][i] = fma2(dzf[g][i], mul2(d[g][i], rs2), adg[g][i]);
+            if (LN) adb[g][i] = add2(adb[g][i], dzf[g][i]);
+          }
+          store_dx<TIn>(p.dx, rowe + (size_t)v * VEC, dx);
+        }
+      }
+    }
+    // chunk finished: write its partial column sums (kept in L2 for the
+    // column reduction)
+    float* prow = p.part + (size_t)c * nacc * H;
+#pragma unroll
+    for (int g = 0; g < NG; ++g) {
+      const int v = g * TH + t;
+      if (v < nchunks) {
+#pragma unroll
+        for (int jj = 0; jj < PAIRS / 2; ++jj) {
+          st_hint_f4(prow + (size_t)v * VEC + 4 * jj,
+                     make_float4(adg[g][2 * jj].x, adg[g][2 * jj].y, adg[g][2 * jj + 1].x,
+                                 adg[g][2 * jj + 1].y),
+                     keep_pol);
+          if (LN)
+            st_hint_f4(prow + H + (size_t)v * VEC + 4 * jj,
+                       make_float4(adb[g][2 * jj].x, adb[g][2 * jj].y, adb[g][2 * jj + 1].x,
+                                   adb[g][2 * jj + 1].y),
+                       keep_pol);
+        }
+      }
+    }
+  }
+}
+
 // dgamma[j] (a = 0) / dbeta[j] (a = 1) = sum over chunks of part[c][a][j].
 // Block: 32 warps x 32 lanes; lane owns 2 adjacent columns of a 64-column
 // slice; warp w sums chunks w, w+32, w+64, ... into eight interleaved
@@ -361,6 +595,33 @@ rn_status launch_ng(int ng, const BwdParams& p, const Launch& l, cudaStream_t s)
 }
 
 }  // namespace
+
+namespace {
+
+template <typename TIn, int NG, bool LN, bool BIG>
+rn_status launch_fused_t(const BwdParams& p, const Launch& l, cudaStream_t s) {
+  auto k = rn_bwd_fused_kernel<TIn, NG, LN, BIG>;
+  if (l.threads > (BIG ? kFusedBig : kFusedCompact) || p.apply_warps > 16 ||
+      l.threads != 32 * p.apply_warps || p.Q < 2)
+    return RN_ERR_UNSUPPORTED;
+  if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)l.smem) !=
+      cudaSuccess)
+    return RN_ERR_CUDA;
+  int grid = 1;
+  if (persistent_grid(k, l, &grid) != RN_OK) return RN_ERR_CUDA;
+  k<<<grid, l.threads, l.smem, s>>>(p);
+  return cudaGetLastError() == cudaSuccess ? RN_OK : RN_ERR_CUDA;
+}
+
+}  // namespace
+
+// fp32 rows: 4 chunks (16 elements) a thread
+rn_status launch_bwd_fused(bool ln, bool big, const BwdParams& p, const Launch& l, cudaStream_t s) {
+  if (ln) return big ? launch_fused_t<float, 4, true, true>(p, l, s)
+                     : launch_fused_t<float, 4, true, false>(p, l, s);
+  return big ? launch_fused_t<float, 4, false, true>(p, l, s)
+             : launch_fused_t<float, 4, false, false>(p, l, s);
+}
 
 rn_status launch_bwd(bool ln, bool bf16, int ng, const BwdParams& p, const Launch& l,
                      cudaStream_t s) {

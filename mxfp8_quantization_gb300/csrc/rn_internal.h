@@ -132,8 +132,14 @@ rn_status launch_fwd(int nk, bool bf16, const FwdShape& sh, int qmode, const Fwd
 rn_status launch_fwd_init(float* amax, const float* scale, float* scale_inv, cudaStream_t s);
 rn_status launch_mx(int nk, bool bf16, int ng, const MxParams& p, const Launch& l,
                     cudaStream_t s);
+// backward with stats warps (rows of any length)
 rn_status launch_bwd(bool ln, bool bf16, int ng, const BwdParams& p, const Launch& l,
                      cudaStream_t s);
+// backward without stats or producer warps, fp32 rows of up to 16 warps x
+// 32 threads x 16 elements (big: one CTA per SM, up to 16 warps; otherwise
+// up to 8 warps, several CTAs per SM)
+rn_status launch_bwd_fused(bool ln, bool big, const BwdParams& p, const Launch& l,
+                           cudaStream_t s);
 rn_status launch_colreduce(const ColReduceParams& p, cudaStream_t s);
 
 // device error words, one per translation unit
