@@ -67,11 +67,6 @@ rn_status device_info(DeviceInfo* out) {
 namespace {
 
 // ---------------------------------------------------------------- planning
-struct RowPlan {
-  int ng, T, wpr, Q;
-  int apply_warps, stats_warps;
-  Launch l;
-};
 
 // shared memory one CTA may use when per_sm CTAs share an SM (the runtime
 // reserves 1 KB per CTA)
@@ -180,11 +175,18 @@ rn_status plan_fwd(int nk, int H, int esz, int N, int sm_margin, const DeviceInf
   return RN_OK;
 }
 
-// MXFP8: apply warps take 64-column sub-tiles of each 32-row tile
-// (A <= 10 warps, as few as give the same sub-tiles per warp), S = max(2, A/2) stats warps (fewer when A + S
-// would pass 15), a producer; one CTA per SM with a ring of at least 33 rows
-// (a 32-row tile plus look-ahead).
-rn_status plan_mx(int H, int esz, int N, int sm_margin, const DeviceInfo& di, RowPlan* pl) {
+// MXFP8: apply warps take 64-column sub-tiles of each 32-row tile (A <= 10
+// warps, as few as give the same sub-tiles per warp), S = max(2, A/2) stats
+// warps (fewer when A + S would pass 15), a producer; one CTA per SM with a
+// ring of at least 33 rows (a 32-row tile plus look-ahead) and gamma / beta
+// staged in shared memory.
+struct MxPlan {
+  int Q, n_tbar, apply_warps, stats_warps;
+  Launch l;
+};
+
+rn_status plan_mx(int nk, int H, int esz, int N, int sm_margin, const DeviceInfo& di,
+                  MxPlan* pl) {
   const int nsub = (H + 63) / 64;
   // the largest A <= 10 that spreads the sub-tiles evenly
   int A = nsub < 10 ? nsub : 10;
@@ -192,15 +194,17 @@ rn_status plan_mx(int H, int esz, int N, int sm_margin, const DeviceInfo& di, Ro
   int S = A / 2 > 2 ? A / 2 : 2;
   if (A + S > 15) S = 15 - A;
   const size_t row_bytes = (size_t)H * esz;
-  const size_t fixed = 64;
-  const size_t per_slot = row_bytes + sizeof(float2) + 24;
+  const size_t gb = nk == kIdentity ? 0 : (size_t)H * sizeof(float) * (nk == kLn ? 2 : 1);
+  // per slot: the row, (mean, rsigma), two mbarriers; fixed: gamma / beta,
+  // the tile barriers (at most 8), slack
+  const size_t per_slot = row_bytes + sizeof(float2) + 16;
+  const size_t fixed = gb + 8 * sizeof(uint64_t) + 64;
   const size_t budget = cta_smem_budget(di, 1);
   int Q = budget > fixed ? (int)((budget - fixed) / per_slot) : 0;
   if (Q > 128) Q = 128;
   if (Q < 33) return RN_ERR_UNSUPPORTED;
-  pl->ng = 1;
-  pl->T = 32;
   pl->Q = Q;
+  pl->n_tbar = (Q + 31) / 32 + 2;  // <= 8
   pl->apply_warps = A;
   pl->stats_warps = S;
   pl->l.threads = 32 * (A + S + 1);
@@ -313,8 +317,8 @@ rn_status fwd_common(int nk, const void* x, rn_dtype dt, const float* gamma, con
   const int esz = elem_size(dt);
 
   if (mode == RN_QUANT_MXFP8) {
-    RowPlan pl;
-    if ((st = plan_mx((int)H, esz, (int)N, sm_margin, di, &pl)) != RN_OK) return st;
+    MxPlan pl;
+    if ((st = plan_mx(nk, (int)H, esz, (int)N, sm_margin, di, &pl)) != RN_OK) return st;
     MxParams p{};
     p.x = x;
     p.gamma = gamma;
@@ -333,7 +337,8 @@ rn_status fwd_common(int nk, const void* x, rn_dtype dt, const float* gamma, con
     p.apply_warps = pl.apply_warps;
     p.stats_warps = pl.stats_warps;
     p.n_tiles = (int)(N / 32);
-    return launch_mx(nk, bf16, pl.ng, p, pl.l, stream);
+    p.n_tbar = pl.n_tbar;
+    return launch_mx(nk, bf16, 1, p, pl.l, stream);
   }
 
   FwdPlan pl;

@@ -155,49 +155,59 @@ __global__ void __launch_bounds__(WIDE ? kMaxThreadsWide : kMaxThreads, WIDE ? 1
     // c1 = mean(dy) and c2 = mean(dy * xhat) = rsigma * mean(dy * (x - mu))
     const int j = warp - A;
     const float inv_h = 1.0f / (float)H;
+    // stats warp j takes rows j, j + S, j + 2S, ... of the CTA's sequence:
+    // row `within` of chunk c (c = blockIdx.x, blockIdx.x + grid, ...);
+    // only the last chunk of all may be short, and it is the CTA's last
+    int c = blockIdx.x, within = j;
+    while (within >= R) {
+      within -= R;
+      c += G;
+    }
     RingPos pos{0u, 0u};
-    int q = 0;
-    for (int c = blockIdx.x; c < p.n_chunks; c += G) {
-      const int r1 = min((c + 1) * R, p.N);
-      for (int r = c * R; r < r1; ++r, ++q) {
-        if (q % S == j) {
-          const uint32_t s = pos.slot;
-          // not paced by the apply warps: wait for the previous use of the
-          // slot to be released first, so that the parity wait below cannot
-          // match a phase one lap old (alias-free as stats warps < slots)
-          if (q >= (int)Q) mbar_wait(smem_u32(&empty[s]), pos.phase ^ 1u, &g_err_bwd, kErrStatsWait);
-          mbar_wait(smem_u32(&full[s]), pos.phase, &g_err_bwd, kErrStatsWait);
-          const unsigned char* xr = ring + (size_t)s * slot_bytes;
-          const unsigned char* dr = xr + row_bytes;
-          const float2 m = meta[s];
-          const float mu = LN ? m.x : 0.f;
-          float2 s1 = make_float2(0.f, 0.f), s2 = make_float2(0.f, 0.f);
-          for (int cc = lane; cc < nchunks; cc += 32) {
-            const typename V::Raw xw = V::load(xr, cc);
-            const typename V::Raw dw = V::load(dr, cc);
-            float2 gp[PAIRS];
+    pos.advance((uint32_t)j, Q);
+    for (int q = j; c < p.n_chunks; q += S) {
+      const int r = c * R + within;
+      if (r >= p.N) break;
+      const uint32_t s = pos.slot;
+      // not paced by the apply warps: wait for the previous use of the
+      // slot to be released first, so that the parity wait below cannot
+      // match a phase one lap old (alias-free as stats warps < slots)
+      if (q >= (int)Q) mbar_wait(smem_u32(&empty[s]), pos.phase ^ 1u, &g_err_bwd, kErrStatsWait);
+      mbar_wait(smem_u32(&full[s]), pos.phase, &g_err_bwd, kErrStatsWait);
+      const unsigned char* xr = ring + (size_t)s * slot_bytes;
+      const unsigned char* dr = xr + row_bytes;
+      const float2 m = meta[s];
+      const float mu = LN ? m.x : 0.f;
+      float2 s1 = make_float2(0.f, 0.f), s2 = make_float2(0.f, 0.f);
+      for (int cc = lane; cc < nchunks; cc += 32) {
+        const typename V::Raw xw = V::load(xr, cc);
+        const typename V::Raw dw = V::load(dr, cc);
+        float2 gp[PAIRS];
 #pragma unroll
-            for (int i = 0; i < PAIRS; i += 2) {
-              const float4 g4 = gsv[(i / 2) * nchunks + cc];
-              gp[i] = make_float2(g4.x, g4.y);
-              gp[i + 1] = make_float2(g4.z, g4.w);
-            }
-#pragma unroll
-            for (int i = 0; i < PAIRS; ++i) {
-              const float2 d = LN ? V::sub(xw, i, mu) : V::f32(xw, i);
-              const float2 dy = mul2(V::f32(dw, i), gp[i]);
-              s1 = add2(s1, dy);
-              s2 = fma2(dy, d, s2);
-            }
-          }
-          const float a1 = warp_sum(s1.x + s1.y);
-          const float a2 = warp_sum(s2.x + s2.y);
-          if (lane == 0) {
-            rstat[s] = make_float4(mu, m.y, LN ? a1 * inv_h : 0.f, m.y * (a2 * inv_h));
-            mbar_arrive(smem_u32(&ready[s]));
-          }
+        for (int i = 0; i < PAIRS; i += 2) {
+          const float4 g4 = gsv[(i / 2) * nchunks + cc];
+          gp[i] = make_float2(g4.x, g4.y);
+          gp[i + 1] = make_float2(g4.z, g4.w);
         }
-        pos.advance(1, Q);
+#pragma unroll
+        for (int i = 0; i < PAIRS; ++i) {
+          const float2 d = LN ? V::sub(xw, i, mu) : V::f32(xw, i);
+          const float2 dy = mul2(V::f32(dw, i), gp[i]);
+          s1 = add2(s1, dy);
+          s2 = fma2(dy, d, s2);
+        }
+      }
+      const float a1 = warp_sum(s1.x + s1.y);
+      const float a2 = warp_sum(s2.x + s2.y);
+      if (lane == 0) {
+        rstat[s] = make_float4(mu, m.y, LN ? a1 * inv_h : 0.f, m.y * (a2 * inv_h));
+        mbar_arrive(smem_u32(&ready[s]));
+      }
+      pos.advance((uint32_t)S, Q);
+      within += S;
+      while (within >= R) {
+        within -= R;
+        c += G;
       }
     }
     return;

@@ -59,6 +59,7 @@ struct MxParams {
   int stats_warps;
   int Q;
   int n_tiles;          // N / 32
+  int n_tbar;           // tile "ready" barriers (> Q / 32 + 1)
 };
 
 struct BwdParams {

@@ -8,23 +8,26 @@
 //   producer     one lane streams rows of x into a shared-memory ring with
 //                cp.async.bulk ("full" mbarrier per slot);
 //   stats warps  take rows in turn: mean / rsigma from shared memory
-//                (LayerNorm: two passes), published on the slot's "ready"
-//                mbarrier and written to mu / rsigma;
+//                (LayerNorm: two passes), written to mu / rsigma and to the
+//                slot, and counted on the tile's "ready" mbarrier (32
+//                arrivals: one per row of the 32-row tile);
 //   apply warps  work on tiles of 32 rows (the height of a column block),
 //                each warp on 64-column sub-tiles: every thread holds y for
 //                an 8-row x 8-column block in registers, computed once
-//                (gamma / beta for its columns from the L1-cached global
-//                copies).  From those registers it forms
-//       rowwise  the 1x32 row-block maxima (4 lanes, 2 shuffle steps), their
+//                (gamma / beta from a shared-memory copy staged at start).
+//                One sweep over |y| gives the thread's 8 row maxima and 8
+//                column maxima; from those
+//       rowwise  the 1x32 block maxima (4 lanes, 2 shuffle steps), their
 //                E8M0 codes and the rowwise E4M3 codes;
-//       colwise  the 32x1 column-block maxima (4 row groups, 2 shuffle
-//                steps), their codes, and the columnwise codes, 8 per column
-//                per thread, stored as 8 contiguous bytes of the transposed
-//                [H, N] array;
+//       colwise  the 32x1 block maxima (4 row groups, 2 shuffle steps), their
+//                codes, and the columnwise codes, 8 per column per thread,
+//                stored as 8 contiguous bytes of the transposed [H, N] array;
+//                output addresses advance from per-tile cursors;
 //   then the tile's 32 slots are released ("empty").
 // Both directions quantize the same y32 (one computation per element).
 // Arithmetic is on element pairs (f32x2); bf16 inputs enter through the
-// mixed-precision forms.
+// mixed-precision forms.  When H is a multiple of 64 every sub-tile is whole
+// and no lane needs a bounds test.
 #include <cuda_runtime.h>
 
 #include "rn_device.cuh"
@@ -39,49 +42,89 @@ __device__ unsigned g_err_mx;
 constexpr int kMaxThreads = 16 * 32;
 constexpr int kTile = 32;
 
-// y of the 8 columns (four pairs) of chunk v in one row
-template <typename TIn, int NK>
-__device__ __forceinline__ void y8(const unsigned char* rowp, int v, float mean, float rs,
-                                   const float2* g, const float2* b, float2* y) {
-  using V = Vec<TIn, 8>;
-  const typename V::Raw raw = V::load(rowp, v);
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    if constexpr (NK == kLn)
-      y[i] = fma2(mul2(V::sub(raw, i, mean), splat2(rs)), g[i], b[i]);
-    else if constexpr (NK == kRms)
-      y[i] = mul2(mul2(V::f32(raw, i), splat2(rs)), g[i]);
-    else
-      y[i] = V::f32(raw, i);
-  }
+// one chunk of 8 columns from shared memory (32-bit shared address)
+template <typename TIn>
+__device__ __forceinline__ typename Vec<TIn, 8>::Raw load8(uint32_t addr);
+
+template <>
+__device__ __forceinline__ Vec<uint16_t, 8>::Raw load8<uint16_t>(uint32_t addr) {
+  Vec<uint16_t, 8>::Raw r;
+  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r.w[0]), "=r"(r.w[1]), "=r"(r.w[2]), "=r"(r.w[3])
+               : "r"(addr));
+  return r;
 }
 
-template <typename TIn, int NK>
+template <>
+__device__ __forceinline__ Vec<float, 8>::Raw load8<float>(uint32_t addr) {
+  Vec<float, 8>::Raw r;
+  asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(r.p[0].x), "=f"(r.p[0].y), "=f"(r.p[1].x), "=f"(r.p[1].y)
+               : "r"(addr));
+  asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(r.p[2].x), "=f"(r.p[2].y), "=f"(r.p[3].x), "=f"(r.p[3].y)
+               : "r"(addr + 16));
+  return r;
+}
+
+// maxima with NaN winning
+__device__ __forceinline__ float max3n(float a, float b, float c) {
+  float r;
+  asm("max.NaN.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
+__device__ __forceinline__ float max2n(float a, float b) {
+  float r;
+  asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
+  return r;
+}
+
+template <typename TIn, int NK, bool FULL>
 __global__ void __launch_bounds__(kMaxThreads, 1) rn_mx_kernel(const MxParams p) {
   using V = Vec<TIn, 8>;
   constexpr bool STATS = (NK != kIdentity);
+  constexpr bool LN = (NK == kLn);
   extern __shared__ __align__(128) unsigned char smem[];
   const int A = p.apply_warps;
   const int S = STATS ? p.stats_warps : 0;
   const int H = p.H;
   const int N = p.N;
-  const int nchunks = H >> 3;
+  const int nchunks = H >> 3;  // chunks of 8 columns
   const uint32_t row_bytes = (uint32_t)H * sizeof(TIn);
+  constexpr uint32_t kChunkBytes = 8 * sizeof(TIn);
   const uint32_t Q = (uint32_t)p.Q;
+  const int NT = p.n_tbar;
+  const size_t gb_bytes = STATS ? (size_t)H * sizeof(float) * (LN ? 2 : 1) : 0;
 
-  unsigned char* ring = smem;
-  float2* rstat = reinterpret_cast<float2*>(smem + (size_t)Q * row_bytes);  // [Q]
+  float4* gsm = reinterpret_cast<float4*>(smem);  // [2][nchunks]: chunk c's g, part j
+  float4* bsm = gsm + 2 * (size_t)nchunks;        // same for beta (LayerNorm)
+  unsigned char* ring = smem + gb_bytes;
+  float2* rstat = reinterpret_cast<float2*>(ring + (size_t)Q * row_bytes);  // [Q]
   uint64_t* full = reinterpret_cast<uint64_t*>(rstat + Q);
-  uint64_t* ready = full + Q;
-  uint64_t* empty = ready + Q;
+  uint64_t* empty = full + Q;
+  uint64_t* tready = empty + Q;  // [NT]: statistics of a tile's 32 rows written
 
-  if (threadIdx.x == 0) {
-    for (uint32_t i = 0; i < Q; ++i) {
-      mbar_init(smem_u32(&full[i]), 1);
-      mbar_init(smem_u32(&ready[i]), 1);
-      mbar_init(smem_u32(&empty[i]), A);
-    }
+  for (uint32_t i = threadIdx.x; i < Q; i += blockDim.x) {
+    mbar_init(smem_u32(&full[i]), 1);
+    mbar_init(smem_u32(&empty[i]), A);
     fence_barrier_init();
+  }
+  for (int i = threadIdx.x; i < NT; i += blockDim.x) {
+    mbar_init(smem_u32(&tready[i]), kTile);
+    fence_barrier_init();
+  }
+  if constexpr (STATS) {
+    const int n4 = H / 4;
+    for (int u = threadIdx.x; u < n4; u += blockDim.x) {
+      const int c = u >> 1, j = u & 1;
+      const float4 gv = reinterpret_cast<const float4*>(p.gamma)[u];
+      gsm[j * nchunks + c] =
+          p.zcg ? make_float4(1.0f + gv.x, 1.0f + gv.y, 1.0f + gv.z, 1.0f + gv.w) : gv;
+      if (LN)
+        bsm[j * nchunks + c] = p.beta ? reinterpret_cast<const float4*>(p.beta)[u]
+                                      : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
   }
   __syncthreads();
 
@@ -118,57 +161,61 @@ __global__ void __launch_bounds__(kMaxThreads, 1) rn_mx_kernel(const MxParams p)
     if constexpr (STATS) {
       const int j = warp - A;
       const float inv_h = 1.0f / (float)H;
+      // stats warp j takes rows j, j + S, j + 2S, ... of the CTA's sequence
+      // (row q: tile blockIdx.x + (q / 32) * grid, row q % 32 of it)
+      const int my_tiles = p.n_tiles > (int)blockIdx.x ? (p.n_tiles - 1 - (int)blockIdx.x) / G + 1 : 0;
+      const int nq = my_tiles * kTile;
       RingPos pos{0u, 0u};
-      int q = 0;
-      for (int t = blockIdx.x; t < p.n_tiles; t += G) {
-        for (int k = 0; k < kTile; ++k, ++q) {
-          if (q % S == j) {
-            const uint32_t s = pos.slot;
-            // not paced by the apply warps: wait for the previous use of the
-            // slot to be released first, so that the parity wait below
-            // cannot match a phase one lap old (stats warps < slots)
-            if (q >= (int)Q) mbar_wait(smem_u32(&empty[s]), pos.phase ^ 1u, &g_err_mx, kErrStatsWait);
-            mbar_wait(smem_u32(&full[s]), pos.phase, &g_err_mx, kErrStatsWait);
-            const unsigned char* rowp = ring + (size_t)s * row_bytes;
-            float2 a[4];
-            float mean = 0.f;
-            if constexpr (NK == kLn) {
+      pos.advance((uint32_t)j, Q);
+      for (int q = j; q < nq; q += S, pos.advance((uint32_t)S, Q)) {
+        const int t = (int)blockIdx.x + (q / kTile) * G;
+        const int k = q % kTile;
+        const uint32_t s = pos.slot;
+        // not paced by the apply warps: wait for the previous use of the
+        // slot to be released first, so that the parity wait below
+        // cannot match a phase one lap old (stats warps < slots)
+        if (q >= (int)Q) mbar_wait(smem_u32(&empty[s]), pos.phase ^ 1u, &g_err_mx, kErrStatsWait);
+        mbar_wait(smem_u32(&full[s]), pos.phase, &g_err_mx, kErrStatsWait);
+        const unsigned char* rowp = ring + (size_t)s * row_bytes;
+        float2 a[4];
+        float mean = 0.f;
+        if constexpr (LN) {
 #pragma unroll
-              for (int i = 0; i < 4; ++i) a[i] = make_float2(0.f, 0.f);
-              for (int c = lane; c < nchunks; c += 32) {
-                const typename V::Raw raw = V::load(rowp, c);
+          for (int i = 0; i < 4; ++i) a[i] = make_float2(0.f, 0.f);
+          for (int c = lane; c < nchunks; c += 32) {
+            const typename V::Raw raw = V::load(rowp, c);
 #pragma unroll
-                for (int i = 0; i < 4; ++i) V::acc(a[i], raw, i);
-              }
-              mean = warp_sum((a[0].x + a[0].y) + (a[1].x + a[1].y) + (a[2].x + a[2].y) +
-                              (a[3].x + a[3].y)) * inv_h;
-            }
+            for (int i = 0; i < 4; ++i) V::acc(a[i], raw, i);
+          }
+          mean = warp_sum((a[0].x + a[0].y) + (a[1].x + a[1].y) + (a[2].x + a[2].y) +
+                          (a[3].x + a[3].y)) * inv_h;
+        }
 #pragma unroll
-            for (int i = 0; i < 4; ++i) a[i] = make_float2(0.f, 0.f);
-            for (int c = lane; c < nchunks; c += 32) {
-              const typename V::Raw raw = V::load(rowp, c);
+        for (int i = 0; i < 4; ++i) a[i] = make_float2(0.f, 0.f);
+        for (int c = lane; c < nchunks; c += 32) {
+          const typename V::Raw raw = V::load(rowp, c);
 #pragma unroll
-              for (int i = 0; i < 4; ++i) {
-                if constexpr (NK == kLn) {
-                  const float2 d = V::sub(raw, i, mean);
-                  a[i] = fma2(d, d, a[i]);
-                } else {
-                  V::sq_acc(a[i], raw, i);
-                }
-              }
-            }
-            const float m2 = warp_sum((a[0].x + a[0].y) + (a[1].x + a[1].y) + (a[2].x + a[2].y) +
-                                      (a[3].x + a[3].y));
-            const float rs = __frsqrt_rn(m2 * inv_h + p.eps);
-            if (lane == 0) {
-              const int r = t * kTile + k;
-              rstat[s] = make_float2(mean, rs);
-              if (NK == kLn) p.mu[r] = mean;
-              p.rsigma[r] = rs;
-              mbar_arrive(smem_u32(&ready[s]));
+          for (int i = 0; i < 4; ++i) {
+            if constexpr (LN) {
+              const float2 d = V::sub(raw, i, mean);
+              a[i] = fma2(d, d, a[i]);
+            } else {
+              V::sq_acc(a[i], raw, i);
             }
           }
-          pos.advance(1, Q);
+        }
+        const float m2 = warp_sum((a[0].x + a[0].y) + (a[1].x + a[1].y) + (a[2].x + a[2].y) +
+                                  (a[3].x + a[3].y));
+        const float rs = __frsqrt_rn(m2 * inv_h + p.eps);
+        if (lane == 0) {
+          const int r = t * kTile + k;
+          rstat[s] = make_float2(mean, rs);
+          if (LN) p.mu[r] = mean;
+          p.rsigma[r] = rs;
+          // the tile barrier's phases are alias-free: stats warps run at
+          // most a ring (Q rows) ahead of the apply warps and NT tile
+          // barriers cover more than Q / 32 + 1 tiles
+          mbar_arrive(smem_u32(&tready[(q / kTile) % NT]));
         }
       }
     }
@@ -178,130 +225,164 @@ __global__ void __launch_bounds__(kMaxThreads, 1) rn_mx_kernel(const MxParams p)
   // ---------------------------------------------------------- apply warps
   // Each apply warp takes 64-column sub-tiles of the 32-row tile (w, w + A,
   // ...).  Lane = hb*16 + rg*4 + cc: the thread holds y of rows 8rg..8rg+7
-  // and columns 64*sub + 32*hb + 8*cc .. +7 in registers.  A row block (32
-  // columns) spans the 4 lanes cc = 0..3 (shuffles xor 1, 2); a column block
-  // (32 rows) spans the 4 lanes rg = 0..3 (shuffles xor 4, 8).
+  // and of chunk cl = 4hb + cc of the sub-tile (columns 64 sub + 8 cl ..
+  // + 7).  A row block (32 columns) spans the 4 lanes cc = 0..3 (shuffles
+  // xor 1, 2); a column block (32 rows) spans the 4 lanes rg = 0..3
+  // (shuffles xor 4, 8).
   const int hb = lane >> 4, rg = (lane >> 2) & 3, cc = lane & 3;
+  const int cl = hb * 4 + cc;
   const int nsub = (nchunks + 7) >> 3;
-  const int hs = H >> 5;   // row scales per row
-  const int ns = N >> 5;   // column scales per column
+  const int hs = H >> 5;  // row scales per row
+  const int ns = N >> 5;  // column scales per column
+  const uint32_t ring_u32 = smem_u32(ring);
+  const bool rowwise = p.data != nullptr;
+  const bool colwise = p.col_data != nullptr;
 
   RingPos pos{0u, 0u};
-  for (int tile = blockIdx.x; tile < p.n_tiles; tile += G) {
+  int tl = 0;
+  for (int tile = blockIdx.x; tile < p.n_tiles; tile += G, ++tl) {
     const int r0 = tile * kTile;
-    // the whole warp waits for the tile's 32 rows (warp-uniform waits; "ready"
-    // implies the row has landed)
-    {
+    if constexpr (STATS) {
+      // the 32 rows' statistics are written (which implies they landed)
+      mbar_wait(smem_u32(&tready[tl % NT]), (uint32_t)(tl / NT) & 1u, &g_err_mx, kErrReadyWait);
+    } else {
       RingPos rp = pos;
       for (int k = 0; k < kTile; ++k) {
-        if constexpr (STATS)
-          mbar_wait(smem_u32(&ready[rp.slot]), rp.phase, &g_err_mx, kErrReadyWait);
-        else
-          mbar_wait(smem_u32(&full[rp.slot]), rp.phase, &g_err_mx, kErrFullWait);
+        mbar_wait(smem_u32(&full[rp.slot]), rp.phase, &g_err_mx, kErrFullWait);
         rp.advance(1, Q);
       }
     }
-    uint32_t slot[8];
+    uint32_t rowa[8];  // shared address of this thread's chunk in each of its 8 rows
     float2 st8[8];
     {
       RingPos rp = pos.ahead(8 * rg, Q);
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
-        slot[j] = rp.slot;
+        rowa[j] = ring_u32 + rp.slot * row_bytes + cl * kChunkBytes;
         st8[j] = STATS ? rstat[rp.slot] : make_float2(0.f, 1.f);
         rp.advance(1, Q);
       }
     }
+    // output cursors of the tile (offset by sub-tile below)
+    uint8_t* const dptr = rowwise ? p.data + ((size_t)(r0 + 8 * rg) * H + cl * 8) : nullptr;
+    uint8_t* const sptr = rowwise ? p.row_scales + ((size_t)(r0 + 8 * rg) * hs + hb) : nullptr;
+    uint8_t* const cptr = colwise ? p.col_data + ((size_t)cl * 8 * N + r0 + 8 * rg) : nullptr;
+    uint8_t* const csptr = colwise ? p.col_scales + ((size_t)cl * 8 * ns + tile) : nullptr;
+
     for (int sub = warp; sub < nsub; sub += A) {
-      const int v = sub * 8 + hb * 4 + cc;  // chunk of 8 columns
-      const bool valid = v < nchunks;
+      const int c = sub * 8 + cl;  // chunk of 8 columns
+      const bool valid = FULL || c < nchunks;
       float2 g2[4], b2[4];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        g2[i] = make_float2(0.f, 0.f);
-        b2[i] = make_float2(0.f, 0.f);
-        if (NK != kIdentity && valid) {
-          const int c = v * 8 + 2 * i;
-          const float ga = __ldg(p.gamma + c), gb = __ldg(p.gamma + c + 1);
-          g2[i] = p.zcg ? make_float2(1.0f + ga, 1.0f + gb) : make_float2(ga, gb);
-          if (NK == kLn && p.beta) b2[i] = make_float2(__ldg(p.beta + c), __ldg(p.beta + c + 1));
+      for (int jj = 0; jj < 2; ++jj) {
+        float4 gv = make_float4(0.f, 0.f, 0.f, 0.f), bv = gv;
+        if (STATS && valid) {
+          gv = gsm[jj * nchunks + c];
+          if (LN) bv = bsm[jj * nchunks + c];
         }
+        g2[2 * jj] = make_float2(gv.x, gv.y);
+        g2[2 * jj + 1] = make_float2(gv.z, gv.w);
+        b2[2 * jj] = make_float2(bv.x, bv.y);
+        b2[2 * jj + 1] = make_float2(bv.z, bv.w);
       }
+      const uint32_t soff = (uint32_t)sub * 8 * kChunkBytes;
       float2 y[8][4];
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
 #pragma unroll
         for (int i = 0; i < 4; ++i) y[j][i] = make_float2(0.f, 0.f);
-        if (valid) y8<TIn, NK>(ring + (size_t)slot[j] * row_bytes, v, st8[j].x, st8[j].y, g2, b2, y[j]);
+        if (valid) {
+          const typename V::Raw raw = load8<TIn>(rowa[j] + soff);
+          const float2 rs2 = splat2(st8[j].y);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            if constexpr (LN)
+              y[j][i] = fma2(mul2(V::sub(raw, i, st8[j].x), rs2), g2[i], b2[i]);
+            else if constexpr (NK == kRms)
+              y[j][i] = mul2(mul2(V::f32(raw, i), rs2), g2[i]);
+            else
+              y[j][i] = V::f32(raw, i);
+          }
+        }
+      }
+      // one sweep over |y|: row maxima (8 values each) and column maxima
+      // (8 values each), two rows at a time
+      float rmax[8], cmax[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        rmax[k] = 0.f;
+        cmax[k] = 0.f;
+      }
+#pragma unroll
+      for (int j = 0; j < 8; j += 2) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float a0 = fabsf(y[j][i].x), b0 = fabsf(y[j][i].y);
+          const float a1 = fabsf(y[j + 1][i].x), b1 = fabsf(y[j + 1][i].y);
+          rmax[j] = max3n(rmax[j], a0, b0);
+          rmax[j + 1] = max3n(rmax[j + 1], a1, b1);
+          cmax[2 * i] = max3n(cmax[2 * i], a0, a1);
+          cmax[2 * i + 1] = max3n(cmax[2 * i + 1], b0, b1);
+        }
       }
       // ------------------------------------------------- rowwise 1x32 blocks
-      if (p.data != nullptr) {
+      if (rowwise) {
+        uint8_t* dp = dptr + (size_t)sub * 64;
+        uint8_t* sp = sptr + 2 * sub;
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-          float m = amax_acc2(amax_acc2(0.f, y[j][0]), y[j][1]);
-          m = amax_acc2(amax_acc2(m, y[j][2]), y[j][3]);
-          uint32_t mb = abs_bits(m);
-          mb = max(mb, __shfl_xor_sync(0xFFFFFFFFu, mb, 1));
-          mb = max(mb, __shfl_xor_sync(0xFFFFFFFFu, mb, 2));
-          const uint32_t code = e8m0_code(__uint_as_float(mb));
+          float m = max2n(rmax[j], __shfl_xor_sync(0xFFFFFFFFu, rmax[j], 1));
+          m = max2n(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
+          const uint32_t code = e8m0_code(m);
           const float2 inv = splat2(e8m0_inv_scale(code));
           if (valid) {
-            const size_t row = (size_t)(r0 + 8 * rg + j);
-            uint32_t c[4];
+            uint32_t q[4];
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-              const float2 q = mul2(y[j][i], inv);
-              c[i] = pack_e4m3x2(q.x, q.y);
+              const float2 v = mul2(y[j][i], inv);
+              q[i] = pack_e4m3x2(v.x, v.y);
             }
-            *reinterpret_cast<uint2*>(p.data + row * H + (size_t)v * 8) =
-                make_uint2(c[0] | (c[1] << 16), c[2] | (c[3] << 16));
-            if (cc == 0) p.row_scales[row * hs + (v >> 2)] = (uint8_t)code;
+            *reinterpret_cast<uint2*>(dp) = make_uint2(q[0] | (q[1] << 16), q[2] | (q[3] << 16));
+            if (cc == 0) *sp = (uint8_t)code;
           }
+          dp += H;
+          sp += hs;
         }
       }
       // ---------------------------------------------- columnwise 32x1 blocks
-      if (p.col_data != nullptr) {
-        float cm[8];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          float a = 0.f, b = 0.f;
-#pragma unroll
-          for (int j = 0; j < 8; j += 2) {
-            a = amax_acc2(a, make_float2(y[j][i].x, y[j + 1][i].x));
-            b = amax_acc2(b, make_float2(y[j][i].y, y[j + 1][i].y));
-          }
-          cm[2 * i] = a;
-          cm[2 * i + 1] = b;
-        }
+      if (colwise) {
         float cinv[8];
         uint32_t ccode[8];
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          uint32_t mb = abs_bits(cm[c]);
-          mb = max(mb, __shfl_xor_sync(0xFFFFFFFFu, mb, 4));
-          mb = max(mb, __shfl_xor_sync(0xFFFFFFFFu, mb, 8));
-          ccode[c] = e8m0_code(__uint_as_float(mb));
-          cinv[c] = e8m0_inv_scale(ccode[c]);
+        for (int k = 0; k < 8; ++k) {
+          float m = max2n(cmax[k], __shfl_xor_sync(0xFFFFFFFFu, cmax[k], 4));
+          m = max2n(m, __shfl_xor_sync(0xFFFFFFFFu, m, 8));
+          ccode[k] = e8m0_code(m);
+          cinv[k] = e8m0_inv_scale(ccode[k]);
         }
         if (valid) {
+          uint8_t* cp = cptr + (size_t)sub * 64 * N;
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
             const float2 ci = make_float2(cinv[2 * i], cinv[2 * i + 1]);
-            float2 q[8];
+            float2 qv[8];
 #pragma unroll
-            for (int j = 0; j < 8; ++j) q[j] = mul2(y[j][i], ci);
-            const uint32_t lo0 = pack_e4m3x2(q[0].x, q[1].x) | (pack_e4m3x2(q[2].x, q[3].x) << 16);
-            const uint32_t hi0 = pack_e4m3x2(q[4].x, q[5].x) | (pack_e4m3x2(q[6].x, q[7].x) << 16);
-            const uint32_t lo1 = pack_e4m3x2(q[0].y, q[1].y) | (pack_e4m3x2(q[2].y, q[3].y) << 16);
-            const uint32_t hi1 = pack_e4m3x2(q[4].y, q[5].y) | (pack_e4m3x2(q[6].y, q[7].y) << 16);
-            const size_t col = (size_t)v * 8 + 2 * i;
-            *reinterpret_cast<uint2*>(p.col_data + col * N + (size_t)(r0 + 8 * rg)) = make_uint2(lo0, hi0);
-            *reinterpret_cast<uint2*>(p.col_data + (col + 1) * N + (size_t)(r0 + 8 * rg)) =
-                make_uint2(lo1, hi1);
+            for (int j = 0; j < 8; ++j) qv[j] = mul2(y[j][i], ci);
+            const uint32_t lo0 = pack_e4m3x2(qv[0].x, qv[1].x) | (pack_e4m3x2(qv[2].x, qv[3].x) << 16);
+            const uint32_t hi0 = pack_e4m3x2(qv[4].x, qv[5].x) | (pack_e4m3x2(qv[6].x, qv[7].x) << 16);
+            const uint32_t lo1 = pack_e4m3x2(qv[0].y, qv[1].y) | (pack_e4m3x2(qv[2].y, qv[3].y) << 16);
+            const uint32_t hi1 = pack_e4m3x2(qv[4].y, qv[5].y) | (pack_e4m3x2(qv[6].y, qv[7].y) << 16);
+            *reinterpret_cast<uint2*>(cp) = make_uint2(lo0, hi0);
+            *reinterpret_cast<uint2*>(cp + N) = make_uint2(lo1, hi1);
+            cp += 2 * (size_t)N;
           }
           if (rg == 0) {
+            uint8_t* csp = csptr + (size_t)sub * 64 * ns;
 #pragma unroll
-            for (int c = 0; c < 8; ++c) p.col_scales[((size_t)v * 8 + c) * ns + tile] = (uint8_t)ccode[c];
+            for (int k = 0; k < 8; ++k) {
+              *csp = (uint8_t)ccode[k];
+              csp += ns;
+            }
           }
         }
       }
@@ -319,10 +400,10 @@ __global__ void __launch_bounds__(kMaxThreads, 1) rn_mx_kernel(const MxParams p)
   }
 }
 
-template <typename TIn, int NK>
+template <typename TIn, int NK, bool FULL>
 rn_status launch_t(const MxParams& p, const Launch& l, cudaStream_t s) {
-  auto k = rn_mx_kernel<TIn, NK>;
-  if (l.threads > kMaxThreads) return RN_ERR_UNSUPPORTED;
+  auto k = rn_mx_kernel<TIn, NK, FULL>;
+  if (l.threads > kMaxThreads || p.n_tbar < 1) return RN_ERR_UNSUPPORTED;
   if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)l.smem) !=
       cudaSuccess)
     return RN_ERR_CUDA;
@@ -332,14 +413,19 @@ rn_status launch_t(const MxParams& p, const Launch& l, cudaStream_t s) {
   return cudaGetLastError() == cudaSuccess ? RN_OK : RN_ERR_CUDA;
 }
 
+template <typename TIn, int NK>
+rn_status launch_f(const MxParams& p, const Launch& l, cudaStream_t s) {
+  return (p.H % 64 == 0) ? launch_t<TIn, NK, true>(p, l, s) : launch_t<TIn, NK, false>(p, l, s);
+}
+
 }  // namespace
 
 rn_status launch_mx(int nk, bool bf16, int ng, const MxParams& p, const Launch& l,
                     cudaStream_t s) {
   (void)ng;
-  if (nk == kIdentity) return bf16 ? RN_ERR_UNSUPPORTED : launch_t<float, kIdentity>(p, l, s);
-  if (bf16) return nk == kLn ? launch_t<uint16_t, kLn>(p, l, s) : launch_t<uint16_t, kRms>(p, l, s);
-  return nk == kLn ? launch_t<float, kLn>(p, l, s) : launch_t<float, kRms>(p, l, s);
+  if (nk == kIdentity) return bf16 ? RN_ERR_UNSUPPORTED : launch_f<float, kIdentity>(p, l, s);
+  if (bf16) return nk == kLn ? launch_f<uint16_t, kLn>(p, l, s) : launch_f<uint16_t, kRms>(p, l, s);
+  return nk == kLn ? launch_f<float, kLn>(p, l, s) : launch_f<float, kRms>(p, l, s);
 }
 
 rn_status read_clear_error_mx(unsigned* code) {
