@@ -17,11 +17,13 @@
 //                (gamma / beta from a shared-memory copy staged at start).
 //                One sweep over |y| gives the thread's 8 row maxima and 8
 //                column maxima; from those
-//       rowwise  the 1x32 block maxima (4 lanes, 2 shuffle steps), their
-//                E8M0 codes and the rowwise E4M3 codes;
-//       colwise  the 32x1 block maxima (4 row groups, 2 shuffle steps), their
-//                codes, and the columnwise codes, 8 per column per thread,
-//                stored as 8 contiguous bytes of the transposed [H, N] array;
+//       rowwise  the 1x32 block maxima (the 4 lanes of a block reduce-scatter
+//                them, so that each lane encodes 2 of the 8 blocks it touches
+//                and the inverse scales are gathered back), the E8M0 codes
+//                and the rowwise E4M3 codes;
+//       colwise  the same for the 32x1 blocks (4 row groups), and the
+//                columnwise codes, 8 per column per thread, stored as 8
+//                contiguous bytes of the transposed [H, N] array;
 //                output addresses advance from per-tile cursors;
 //   then the tile's 32 slots are released ("empty").
 // Both directions quantize the same y32 (one computation per element).
@@ -78,6 +80,48 @@ __device__ __forceinline__ float max2n(float a, float b) {
   float r;
   asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
   return r;
+}
+
+// The 8 maxima a lane holds for items 0..7 (rows or columns of its 8 x 8
+// block) are reduced over the 4 lanes of a block group, which differ in the
+// lane bits s1 (high) and s0 (low).  The lane with group index gi = 2 b1 + b0
+// ends with the group maxima of items gi and gi + 4 (a two-step
+// reduce-scatter: 6 shuffles instead of 16 for a full all-reduce).
+__device__ __forceinline__ void block_max_scatter(const float (&v)[8], int b1, int b0, int s1,
+                                                  int s0, float& o0, float& o1) {
+  float r[4];
+#pragma unroll
+  for (int m = 0; m < 4; ++m) {
+    const int k = (m & 1) + 4 * (m >> 1);  // 0, 1, 4, 5
+    const float keep = b1 ? v[k + 2] : v[k];
+    const float send = b1 ? v[k] : v[k + 2];
+    r[m] = max2n(keep, __shfl_xor_sync(0xFFFFFFFFu, send, s1));
+  }
+  const float k0 = b0 ? r[1] : r[0], x0 = b0 ? r[0] : r[1];
+  const float k1 = b0 ? r[3] : r[2], x1 = b0 ? r[2] : r[3];
+  o0 = max2n(k0, __shfl_xor_sync(0xFFFFFFFFu, x0, s0));
+  o1 = max2n(k1, __shfl_xor_sync(0xFFFFFFFFu, x1, s0));
+}
+
+// The inverse of block_max_scatter's layout: from each lane's values for
+// items gi and gi + 4, every lane of the group gets all 8 (two steps, 6
+// shuffles).
+__device__ __forceinline__ void gather8(float i0, float i1, int b1, int b0, int s1, int s0,
+                                        float (&out)[8]) {
+  const float p0 = __shfl_xor_sync(0xFFFFFFFFu, i0, s0);
+  const float p1 = __shfl_xor_sync(0xFFFFFFFFu, i1, s0);
+  float a[4];  // items 2 b1 + {0, 1, 4, 5}
+  a[0] = b0 ? p0 : i0;
+  a[1] = b0 ? i0 : p0;
+  a[2] = b0 ? p1 : i1;
+  a[3] = b0 ? i1 : p1;
+#pragma unroll
+  for (int m = 0; m < 4; ++m) {
+    const int k = (m & 1) + 4 * (m >> 1);
+    const float q = __shfl_xor_sync(0xFFFFFFFFu, a[m], s1);
+    out[k] = b1 ? q : a[m];
+    out[k + 2] = b1 ? a[m] : q;
+  }
 }
 
 template <typename TIn, int NK, bool FULL>
@@ -326,40 +370,42 @@ __global__ void __launch_bounds__(kMaxThreads, 1) rn_mx_kernel(const MxParams p)
         }
       }
       // ------------------------------------------------- rowwise 1x32 blocks
+      // a row block spans the lanes cc = 0..3 (lane bits 2 and 1); lane cc
+      // encodes rows cc and cc + 4 and stores their scales
       if (rowwise) {
-        uint8_t* dp = dptr + (size_t)sub * 64;
-        uint8_t* sp = sptr + 2 * sub;
+        float m0, m1;
+        block_max_scatter(rmax, cc >> 1, cc & 1, 2, 1, m0, m1);
+        const uint32_t code0 = e8m0_code(m0), code1 = e8m0_code(m1);
+        float inv[8];
+        gather8(e8m0_inv_scale(code0), e8m0_inv_scale(code1), cc >> 1, cc & 1, 2, 1, inv);
+        if (valid) {
+          uint8_t* dp = dptr + (size_t)sub * 64;
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          float m = max2n(rmax[j], __shfl_xor_sync(0xFFFFFFFFu, rmax[j], 1));
-          m = max2n(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
-          const uint32_t code = e8m0_code(m);
-          const float2 inv = splat2(e8m0_inv_scale(code));
-          if (valid) {
+          for (int j = 0; j < 8; ++j) {
+            const float2 iv = splat2(inv[j]);
             uint32_t q[4];
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-              const float2 v = mul2(y[j][i], inv);
+              const float2 v = mul2(y[j][i], iv);
               q[i] = pack_e4m3x2(v.x, v.y);
             }
             *reinterpret_cast<uint2*>(dp) = make_uint2(q[0] | (q[1] << 16), q[2] | (q[3] << 16));
-            if (cc == 0) *sp = (uint8_t)code;
+            dp += H;
           }
-          dp += H;
-          sp += hs;
+          uint8_t* sp = sptr + 2 * sub + (size_t)cc * hs;
+          sp[0] = (uint8_t)code0;
+          sp[4 * (size_t)hs] = (uint8_t)code1;
         }
       }
       // ---------------------------------------------- columnwise 32x1 blocks
+      // a column block spans the lanes rg = 0..3 (lane bits 8 and 4); lane rg
+      // encodes columns rg and rg + 4 and stores their scales
       if (colwise) {
+        float m0, m1;
+        block_max_scatter(cmax, rg >> 1, rg & 1, 8, 4, m0, m1);
+        const uint32_t code0 = e8m0_code(m0), code1 = e8m0_code(m1);
         float cinv[8];
-        uint32_t ccode[8];
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          float m = max2n(cmax[k], __shfl_xor_sync(0xFFFFFFFFu, cmax[k], 4));
-          m = max2n(m, __shfl_xor_sync(0xFFFFFFFFu, m, 8));
-          ccode[k] = e8m0_code(m);
-          cinv[k] = e8m0_inv_scale(ccode[k]);
-        }
+        gather8(e8m0_inv_scale(code0), e8m0_inv_scale(code1), rg >> 1, rg & 1, 8, 4, cinv);
         if (valid) {
           uint8_t* cp = cptr + (size_t)sub * 64 * N;
 #pragma unroll
@@ -376,14 +422,9 @@ __global__ void __launch_bounds__(kMaxThreads, 1) rn_mx_kernel(const MxParams p)
             *reinterpret_cast<uint2*>(cp + N) = make_uint2(lo1, hi1);
             cp += 2 * (size_t)N;
           }
-          if (rg == 0) {
-            uint8_t* csp = csptr + (size_t)sub * 64 * ns;
-#pragma unroll
-            for (int k = 0; k < 8; ++k) {
-              *csp = (uint8_t)ccode[k];
-              csp += ns;
-            }
-          }
+          uint8_t* csp = csptr + ((size_t)sub * 64 + rg) * ns;
+          csp[0] = (uint8_t)code0;
+          csp[4 * (size_t)ns] = (uint8_t)code1;
         }
       }
     }
