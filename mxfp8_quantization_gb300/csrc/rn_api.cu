@@ -176,8 +176,8 @@ rn_status plan_fwd(int nk, int H, int esz, int N, int sm_margin, const DeviceInf
 }
 
 // MXFP8: apply warps take 64-column sub-tiles of each 32-row tile (A <= 10
-// warps, as few as give the same sub-tiles per warp), S = max(2, A/2) stats
-// warps (fewer when A + S would pass 15), a producer; one CTA per SM with a
+// warps, as few as give the same sub-tiles per warp), S = min(8, 15 - A)
+// stats warps, a producer; one CTA per SM with a
 // ring of at least 33 rows (a 32-row tile plus look-ahead) and gamma / beta
 // staged in shared memory.
 struct MxPlan {
@@ -191,9 +191,12 @@ rn_status plan_mx(int nk, int H, int esz, int N, int sm_margin, const DeviceInfo
   // the largest A <= 10 that spreads the sub-tiles evenly
   int A = nsub < 10 ? nsub : 10;
   while (A > 1 && (nsub % A) != 0 && (nsub + A - 1) / A == (nsub + A - 2) / (A - 1)) --A;
-  int S = A / 2 > 2 ? A / 2 : 2;
-  if (A + S > 15) S = 15 - A;
+  // stats warps: as many as fit beside the apply warps in 15 (a 32-row tile's
+  // statistics should keep up with its apply work)
+  int S = 15 - A;
+  if (S > 8) S = 8;
   const size_t row_bytes = (size_t)H * esz;
+  if (H / 8 > 32 * 16) return RN_ERR_UNSUPPORTED;  // a stats lane holds <= 16 chunks
   const size_t gb = nk == kIdentity ? 0 : (size_t)H * sizeof(float) * (nk == kLn ? 2 : 1);
   // per slot: the row, (mean, rsigma), two mbarriers; fixed: gamma / beta,
   // the tile barriers (at most 8), slack

@@ -124,7 +124,9 @@ __device__ __forceinline__ void gather8(float i0, float i1, int b1, int b0, int 
   }
 }
 
-template <typename TIn, int NK, bool FULL>
+// FULL: H % 64 == 0 (whole sub-tiles); SNC: 8-column chunks of a row a stats
+// lane holds (nchunks <= 32 SNC), SFULL: exactly SNC
+template <typename TIn, int NK, bool FULL, int SNC, bool SFULL>
 __global__ void __launch_bounds__(kMaxThreads, 1) rn_mx_kernel(const MxParams p) {
   using V = Vec<TIn, 8>;
   constexpr bool STATS = (NK != kIdentity);
@@ -220,34 +222,41 @@ __global__ void __launch_bounds__(kMaxThreads, 1) rn_mx_kernel(const MxParams p)
         // cannot match a phase one lap old (stats warps < slots)
         if (q >= (int)Q) mbar_wait(smem_u32(&empty[s]), pos.phase ^ 1u, &g_err_mx, kErrStatsWait);
         mbar_wait(smem_u32(&full[s]), pos.phase, &g_err_mx, kErrStatsWait);
+        // the row part of this lane (chunks lane, lane + 32, ...) in registers
         const unsigned char* rowp = ring + (size_t)s * row_bytes;
+        typename V::Raw raw[SNC];
+#pragma unroll
+        for (int k = 0; k < SNC; ++k)
+          if (SFULL || lane + 32 * k < nchunks) raw[k] = V::load(rowp, lane + 32 * k);
         float2 a[4];
         float mean = 0.f;
         if constexpr (LN) {
 #pragma unroll
           for (int i = 0; i < 4; ++i) a[i] = make_float2(0.f, 0.f);
-          for (int c = lane; c < nchunks; c += 32) {
-            const typename V::Raw raw = V::load(rowp, c);
 #pragma unroll
-            for (int i = 0; i < 4; ++i) V::acc(a[i], raw, i);
-          }
+          for (int k = 0; k < SNC; ++k)
+            if (SFULL || lane + 32 * k < nchunks) {
+#pragma unroll
+              for (int i = 0; i < 4; ++i) V::acc(a[i], raw[k], i);
+            }
           mean = warp_sum((a[0].x + a[0].y) + (a[1].x + a[1].y) + (a[2].x + a[2].y) +
                           (a[3].x + a[3].y)) * inv_h;
         }
 #pragma unroll
         for (int i = 0; i < 4; ++i) a[i] = make_float2(0.f, 0.f);
-        for (int c = lane; c < nchunks; c += 32) {
-          const typename V::Raw raw = V::load(rowp, c);
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            if constexpr (LN) {
-              const float2 d = V::sub(raw, i, mean);
-              a[i] = fma2(d, d, a[i]);
-            } else {
-              V::sq_acc(a[i], raw, i);
+        for (int k = 0; k < SNC; ++k)
+          if (SFULL || lane + 32 * k < nchunks) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              if constexpr (LN) {
+                const float2 d = V::sub(raw[k], i, mean);
+                a[i] = fma2(d, d, a[i]);
+              } else {
+                V::sq_acc(a[i], raw[k], i);
+              }
             }
           }
-        }
         const float m2 = warp_sum((a[0].x + a[0].y) + (a[1].x + a[1].y) + (a[2].x + a[2].y) +
                                   (a[3].x + a[3].y));
         const float rs = __frsqrt_rn(m2 * inv_h + p.eps);
@@ -441,10 +450,10 @@ __global__ void __launch_bounds__(kMaxThreads, 1) rn_mx_kernel(const MxParams p)
   }
 }
 
-template <typename TIn, int NK, bool FULL>
+template <typename TIn, int NK, bool FULL, int SNC, bool SFULL>
 rn_status launch_t(const MxParams& p, const Launch& l, cudaStream_t s) {
-  auto k = rn_mx_kernel<TIn, NK, FULL>;
-  if (l.threads > kMaxThreads || p.n_tbar < 1) return RN_ERR_UNSUPPORTED;
+  auto k = rn_mx_kernel<TIn, NK, FULL, SNC, SFULL>;
+  if (l.threads > kMaxThreads || p.n_tbar < 1 || p.H / 8 > 32 * SNC) return RN_ERR_UNSUPPORTED;
   if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)l.smem) !=
       cudaSuccess)
     return RN_ERR_CUDA;
@@ -454,9 +463,16 @@ rn_status launch_t(const MxParams& p, const Launch& l, cudaStream_t s) {
   return cudaGetLastError() == cudaSuccess ? RN_OK : RN_ERR_CUDA;
 }
 
+// bf16 H = 2048 takes the exact shape (whole sub-tiles, 8 chunks a stats
+// lane); other H multiples of 64 / of 32 the general ones, with stats lanes
+// of up to 16 chunks for bf16 (H <= 4096) and 8 for fp32 (H <= 2048, which
+// the ring of >= 33 fp32 rows does not reach anyway)
 template <typename TIn, int NK>
 rn_status launch_f(const MxParams& p, const Launch& l, cudaStream_t s) {
-  return (p.H % 64 == 0) ? launch_t<TIn, NK, true>(p, l, s) : launch_t<TIn, NK, false>(p, l, s);
+  constexpr int kSnc = sizeof(TIn) == 2 ? 16 : 8;
+  if (sizeof(TIn) == 2 && p.H == 2048) return launch_t<TIn, NK, true, 8, true>(p, l, s);
+  if (p.H % 64 == 0) return launch_t<TIn, NK, true, kSnc, false>(p, l, s);
+  return launch_t<TIn, NK, false, kSnc, false>(p, l, s);
 }
 
 }  // namespace
