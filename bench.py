@@ -417,7 +417,7 @@ def run_rn(args):
                          "algorithmic_bytes": b_fwd},
         "cpu_baseline": cpu,
         "e2e": e2e,
-        "gpu_launches": 3 * args.steps,
+        "gpu_launches": 4 * args.steps,  # init + forward, backward + column reduction
         "clocks": clocks,
         "workloads": extra,
     }
