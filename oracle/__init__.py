@@ -11,7 +11,9 @@ LayerNorm and RMSNorm forward returning the normalized, optionally quantized
 output together with mu (LayerNorm only) and rsigma; backward returning dx,
 dgamma and dbeta (LayerNorm only); zero-centered gamma; four output paths
 (unfused, fully fused delayed-scaling FP8 / MXFP8, norm+amax then quantize
-for current-scaling FP8).  The formats come from their public definitions:
+for current-scaling FP8).  The residual add + norm follows the fused
+reduce-scatter + residual add + RMSNorm + all-gather named on the page "NVIDIA
+Megatron-Core ... inference_layers" (its single-GPU core).  The formats come from their public definitions:
 FP8 E4M3 from the OCP 8-bit floating point specification, MXFP8 block
 scaling (E8M0 shared scale over 32 elements) from the OCP Microscaling
 Formats v1.0 specification.  The pages give no formula for any of this; the
@@ -19,7 +21,8 @@ readings taken where they are silent are listed in each function.
 
 Module map:
   formats  E4M3 decode/encode, E8M0 shared exponents, bf16 rounding.
-  norm     row statistics, affine apply, quantization stages, backward.
+  norm     row statistics, affine apply, quantization stages, backward,
+           residual add + norm.
 
 Parity status: every function here is pinned by CPU tests against closed
 forms, exact rational arithmetic, finite differences, brute force or
@@ -34,4 +37,5 @@ from .formats import (  # noqa: F401
 from .norm import (  # noqa: F401
     layernorm_stats, rmsnorm_stats, norm_apply, layernorm_fwd, rmsnorm_fwd,
     layernorm_bwd, rmsnorm_bwd, quantize, QUANT_MODES,
+    residual_add, rmsnorm_add_fwd, layernorm_add_fwd,
 )

@@ -44,7 +44,7 @@ from __future__ import annotations
 
 import numpy as np
 
-from .formats import E4M3_MAX, bf16_bits, e4m3_encode, e8m0_from_amax
+from .formats import E4M3_MAX, bf16_bits, e4m3_encode, e8m0_from_amax, round_to_bf16
 
 QUANT_MODES = ("none", "fp8_delayed", "fp8_current", "mxfp8")
 MX_BLOCK = 32
@@ -227,3 +227,52 @@ def layernorm_bwd(dz, x, mu, rsigma, gamma, zero_centered_gamma=False, dtype="bf
 def rmsnorm_bwd(dz, x, rsigma, gamma, zero_centered_gamma=False, dtype="bf16") -> dict:
     """RMSNorm backward -> dict(dx, dgamma, and fp64 forms); no dbeta."""
     return _bwd(dz, x, None, rsigma, gamma, zero_centered_gamma, dtype)
+
+
+# --------------------------------------------------- residual add + norm
+# Source: the page "NVIDIA Megatron-Core ... core.tensor_parallel.
+# inference_layers" names a fused reduce-scatter + residual add + RMSNorm +
+# all-gather; on one GPU its core is "add the residual, then normalize (and
+# quantize)".  The page gives no rounding.  Reading: the sum is the new
+# residual stream, kept in the stream's dtype (rounded once, to nearest even),
+# and the norm is applied to that stored value, so that the next layer's
+# residual input is exactly what was normalized.
+def residual_add(x, residual, dtype: str = "bf16") -> np.ndarray:
+    """h = x + residual rounded once to `dtype` ("bf16" or "f32"), as fp64.
+
+    The fp64 sum is exact for two bf16 values, and for two fp32 values it
+    rounds to fp32 like the exact sum (an addend too small to be exact in
+    fp64 is far below half an fp32 ulp of the other).
+    """
+    s = _f64(x) + _f64(residual)
+    if dtype == "bf16":
+        return round_to_bf16(s)
+    if dtype == "f32":
+        return s.astype(np.float32).astype(np.float64)
+    raise ValueError(dtype)
+
+
+def _stream(h, dtype: str):
+    return bf16_bits(h) if dtype == "bf16" else h.astype(np.float32)
+
+
+def rmsnorm_add_fwd(x, residual, gamma, eps, dtype="bf16", zero_centered_gamma=False,
+                    mode="none", out_dtype="bf16", scale=None, amax=None) -> dict:
+    """RMSNorm of h = residual_add(x, residual) -> rmsnorm_fwd's dict plus
+    residual_out (h in the stream dtype)."""
+    h = residual_add(x, residual, dtype)
+    res = rmsnorm_fwd(h, gamma, eps, zero_centered_gamma, mode, out_dtype, scale, amax)
+    res["residual_out"] = _stream(h, dtype)
+    res["h"] = h
+    return res
+
+
+def layernorm_add_fwd(x, residual, gamma, beta, eps, dtype="bf16", zero_centered_gamma=False,
+                      mode="none", out_dtype="bf16", scale=None, amax=None) -> dict:
+    """LayerNorm of h = residual_add(x, residual) -> layernorm_fwd's dict plus
+    residual_out."""
+    h = residual_add(x, residual, dtype)
+    res = layernorm_fwd(h, gamma, beta, eps, zero_centered_gamma, mode, out_dtype, scale, amax)
+    res["residual_out"] = _stream(h, dtype)
+    res["h"] = h
+    return res

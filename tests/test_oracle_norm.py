@@ -271,3 +271,81 @@ def test_fp8_pipeline_by_loops():
             p = float(np.float32(y32 * np.float32(w.scale)))
             assert res["data"][i, j] == _bf_e4m3(p)
     assert res["amax"] == np.float32(amax)
+
+
+# ------------------------------------------------- residual add + norm
+def _bf16_exact_rne(fr):
+    """Round a Fraction to the nearest bf16 (ties to even) by integer
+    arithmetic on the exponent and an 8-bit significand."""
+    from fractions import Fraction
+    import math
+    if fr == 0:
+        return 0.0
+    sign = -1 if fr < 0 else 1
+    a = abs(fr)
+    e = math.floor(math.log2(a.numerator) - math.log2(a.denominator))
+    while Fraction(2) ** e > a:
+        e -= 1
+    while Fraction(2) ** (e + 1) <= a:
+        e += 1
+    q = a / Fraction(2) ** (e - 7)          # in [128, 256)
+    n = q.numerator // q.denominator
+    rem = q - n
+    if rem > Fraction(1, 2) or (rem == Fraction(1, 2) and n % 2 == 1):
+        n += 1
+    return sign * float(Fraction(n) * Fraction(2) ** (e - 7))
+
+
+def test_residual_add_rounds_once_to_nearest_even():
+    # ties at the bf16 ulp of 1 (2**-7) and of 256 (2): even wins; just above
+    # a tie rounds up
+    x = np.array([1.0, 1.0, 256.0, 256.0, -3.0], dtype=np.float64)
+    r = np.array([2.0 ** -8, 2.0 ** -8 + 2.0 ** -16, 1.0, 3.0, 2.0 ** -8], dtype=np.float64)
+    h = oracle.residual_add(x, r, "bf16")
+    assert list(h) == [1.0, 1.0 + 2.0 ** -7, 256.0, 260.0, -3.0]
+    # fp32 stream: 1 + 2**-24 is a tie at fp32's ulp of 1 -> 1
+    h32 = oracle.residual_add(np.array([1.0]), np.array([2.0 ** -24]), "f32")
+    assert h32[0] == 1.0
+
+
+def test_residual_add_matches_exact_rational_rounding():
+    from fractions import Fraction
+    rng = np.random.default_rng(11)
+    x = oracle.round_to_bf16(rng.normal(0, 4, 400))
+    r = oracle.round_to_bf16(rng.normal(0, 1, 400) * np.exp2(rng.integers(-20, 8, 400)))
+    h = oracle.residual_add(x, r, "bf16")
+    want = [_bf16_exact_rne(Fraction(float(a)) + Fraction(float(b))) for a, b in zip(x, r)]
+    assert np.array_equal(h, np.array(want))
+
+
+def test_residual_add_norm_special_cases():
+    rng = np.random.default_rng(12)
+    x = oracle.round_to_bf16(rng.normal(0.3, 1.5, (5, 64)))
+    g = rng.normal(1.0, 0.1, 64)
+    b = rng.normal(0.0, 0.1, 64)
+    # residual 0: the plain norms of x, and residual_out = x
+    res = oracle.rmsnorm_add_fwd(x, np.zeros_like(x), g, 1e-5)
+    ref = oracle.rmsnorm_fwd(x, g, 1e-5)
+    assert np.array_equal(res["rsigma"], ref["rsigma"]) and np.array_equal(res["data"], ref["data"])
+    assert np.array_equal(res["residual_out"], oracle.bf16_bits(x))
+    res = oracle.layernorm_add_fwd(x, np.zeros_like(x), g, b, 1e-5)
+    ref = oracle.layernorm_fwd(x, g, b, 1e-5)
+    assert np.array_equal(res["mu"], ref["mu"]) and np.array_equal(res["data"], ref["data"])
+    # residual -x: h = 0, rsigma = 1/sqrt(eps) exactly (fp32 eps), y = 0 (LN: beta)
+    res = oracle.rmsnorm_add_fwd(x, -x, g, 1e-5)
+    assert np.all(res["h"] == 0) and np.all(res["y"] == 0)
+    assert np.allclose(res["rsigma"], np.float32(1.0 / np.sqrt(float(np.float32(1e-5)))), rtol=0, atol=0)
+    res = oracle.layernorm_add_fwd(x, -x, g, b, 1e-5)
+    assert np.all(res["mu"] == 0) and np.allclose(res["y"], np.broadcast_to(b, (5, 64)), rtol=0, atol=0)
+
+
+def test_residual_add_rmsnorm_closed_form():
+    # x = [1, 2, 3, 4], r = 1/2 -> h = [3/2, 5/2, 7/2, 9/2] (bf16-exact);
+    # mean(h^2) = (9 + 25 + 49 + 81) / 16 = 41/4; with eps 0, rsigma = 2/sqrt(41)
+    # and y_j = h_j * 2/sqrt(41) (gamma 1)
+    x = np.array([[1.0, 2.0, 3.0, 4.0]])
+    r = np.full((1, 4), 0.5)
+    res = oracle.rmsnorm_add_fwd(x, r, np.ones(4), 0.0, out_dtype="f32")
+    rs = 2.0 / np.sqrt(41.0)
+    assert abs(float(res["rsigma"][0]) - rs) <= 1e-7 * rs
+    assert np.allclose(res["y"], np.array([[1.5, 2.5, 3.5, 4.5]]) * rs, rtol=1e-15, atol=0)
