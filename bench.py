@@ -76,6 +76,8 @@ def algorithmic_bytes(kind, N, H, esz, ln, extra=None):
         return E * esz + 2 * E + 2 * (E // 32) + vec + stats
     if kind == "bwd":                        # dz, x in, dx out, dgamma (+dbeta) out
         return 3 * E * esz + stats + H * 4 + vec
+    if kind == "fwd_add_fp8":                # x, residual in; h and codes out
+        return 3 * E * esz + E * 1 + vec + stats
     raise ValueError(kind)
 
 
@@ -232,6 +234,24 @@ class Prepared:
                 [vp(self.x.data_ptr()), self.dtype_code, vp(self.gamma.data_ptr()), N, H,
                  ctypes.c_float(w.eps), int(w.zero_centered_gamma), 0, mcode, ctypes.byref(o),
                  vp(self.rs.data_ptr())])
+
+    def add_args(self, mode, scale=None):
+        """rn_rmsnorm_add_fwd / rn_layernorm_add_fwd: h = x + residual
+        (stored), then the norm of h with output `mode`."""
+        torch, w = self.torch, self.w
+        to = (lambda a: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to("cuda")) \
+            if w.dtype == "bf16" else (lambda a: torch.from_numpy(a).to("cuda"))
+        self.res = to(w.residual)
+        self.h = torch.empty_like(self.x)
+        fn, args = self.fwd_args(mode, scale)
+        vp = ctypes.c_void_p
+        if self.ln:
+            # (x, dtype, gamma, beta, N, H, eps, zcg, margin, mode, out, mu, rs)
+            return ("rn_layernorm_add_fwd",
+                    [args[0], vp(self.res.data_ptr())] + args[1:11] + [vp(self.h.data_ptr())] + args[11:])
+        # (x, dtype, gamma, N, H, eps, zcg, margin, mode, out, rs)
+        return ("rn_rmsnorm_add_fwd",
+                [args[0], vp(self.res.data_ptr())] + args[1:10] + [vp(self.h.data_ptr())] + args[10:])
 
     def bwd_args(self, sm_margin=0):
         rn, torch = self.rn, self.torch
@@ -469,7 +489,7 @@ def run_e2e(torch, lib, P, fwd, bwd, w, steps, step_bytes):
 
 def run_other_workloads(torch, rn, lib, rn_inputs, flush, peak, steps, warmup, only=None):
     """Full-size timing of the other workloads; ``only`` restricts the run to
-    one group ("rms_small", "rms_current", "mxfp8", "bwd_f32", "bwd_bf16")."""
+    one group ("rms_small", "rms_current", "mxfp8", "bwd_f32", "bwd_bf16", "rms_add")."""
     res = {}
 
     def want(name):
@@ -500,6 +520,14 @@ def run_other_workloads(torch, rn, lib, rn_inputs, flush, peak, steps, warmup, o
                    statistics.mean(t["mx"]), 1)
             del P
         del w
+    if want("rms_add"):
+        w = rn_inputs.make("rms_add")
+        P = Prepared(rn, torch, w, ln=False)
+        t = time_calls(torch, lib, [("add", P.add_args("fp8_delayed", scale=w.scale))], steps, warmup,
+                       flush)
+        report("rms_add_8192x4096_fwd_fp8_delayed", "fwd_add_fp8", w.N, w.H, 2, False,
+               statistics.mean(t["add"]), 2)
+        del P, w
     for name in ("bwd_f32", "bwd_bf16"):
         if not want(name):
             continue
@@ -597,7 +625,7 @@ def main():
     ap.add_argument("--quick", action="store_true", help="headline workload only")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--only", default=None,
-                    choices=["rms_small", "rms_current", "mxfp8", "bwd_f32", "bwd_bf16"],
+                    choices=["rms_small", "rms_current", "mxfp8", "bwd_f32", "bwd_bf16", "rms_add"],
                     help="time only this workload group (prints its results; for profiling)")
     args = ap.parse_args()
     if args.warmup < 3:

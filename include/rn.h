@@ -127,6 +127,33 @@ rn_status rn_rmsnorm_fwd(const void* x, rn_dtype x_dtype, const float* gamma,
                          float* rsigma, void* stream);
 
 /*
+ * Residual add + LayerNorm / RMSNorm forward: the single-GPU core of the
+ * fused "reduce-scatter + residual add + RMSNorm + all-gather" named on the
+ * page "NVIDIA Megatron-Core ... core.tensor_parallel.inference_layers"
+ * (the collectives are not part of this library).
+ *   h = x + residual, each element rounded once (to nearest even) to the
+ *       dtype of x — the new residual stream, written to residual_out;
+ *   then exactly rn_layernorm_fwd / rn_rmsnorm_fwd of h (mu, rsigma, output
+ *   per `mode`).
+ * x, residual, residual_out: [N, H] in `dtype`, 16-byte aligned;
+ * residual_out may not alias x or residual.  Modes NONE, FP8_DELAYED and
+ * FP8_CURRENT (its second pass reads residual_out); MXFP8 returns
+ * RN_ERR_UNSUPPORTED.  Other arguments, errors and conventions as in the
+ * plain forward.
+ */
+rn_status rn_layernorm_add_fwd(const void* x, const void* residual, rn_dtype dtype,
+                               const float* gamma, const float* beta, int64_t N, int64_t H,
+                               float eps, int zero_centered_gamma, int sm_margin,
+                               rn_quant_mode mode, const rn_output* out, void* residual_out,
+                               float* mu, float* rsigma, void* stream);
+
+rn_status rn_rmsnorm_add_fwd(const void* x, const void* residual, rn_dtype dtype,
+                             const float* gamma, int64_t N, int64_t H, float eps,
+                             int zero_centered_gamma, int sm_margin, rn_quant_mode mode,
+                             const rn_output* out, void* residual_out, float* rsigma,
+                             void* stream);
+
+/*
  * LayerNorm backward (page: layernorm_bwd(dz, x, mu, rsigma, gamma,
  * sm_margin, zero_centered_gamma) -> (dx, dgamma, dbeta)).
  *   dz, x, dx: [N, H] in `dtype`; mu, rsigma: the forward's fp32 [N];

@@ -31,7 +31,7 @@ import torch
 
 __all__ = [
     "layernorm_fwd", "rmsnorm_fwd", "layernorm_bwd", "rmsnorm_bwd", "quantize_only",
-    "layernorm_bwd_noalloc",
+    "layernorm_bwd_noalloc", "layernorm_add_fwd", "rmsnorm_add_fwd",
     "bwd_workspace_bytes", "device_error", "Fp8Output", "MXFP8Output", "lib_path", "RNError",
     "QUANT_MODES",
 ]
@@ -82,13 +82,18 @@ def _load():
     lib.rn_rmsnorm_fwd.argtypes = [vp, i32, vp, i64, i64, f32, i32, i32, i32, outp, vp, vp]
     lib.rn_layernorm_bwd.argtypes = [vp, vp, i32, vp, vp, vp, i64, i64, i32, i32, vp, vp, vp, vp, szp, vp]
     lib.rn_rmsnorm_bwd.argtypes = [vp, vp, i32, vp, vp, i64, i64, i32, i32, vp, vp, vp, szp, vp]
+    lib.rn_layernorm_add_fwd.argtypes = [vp, vp, i32, vp, vp, i64, i64, f32, i32, i32, i32, outp,
+                                         vp, vp, vp, vp]
+    lib.rn_rmsnorm_add_fwd.argtypes = [vp, vp, i32, vp, i64, i64, f32, i32, i32, i32, outp, vp, vp,
+                                       vp]
     lib.rn_quantize_only.argtypes = [vp, i64, i64, i32, outp, vp]
     lib.rn_layernorm_bwd_noalloc.argtypes = [vp, vp, i32, vp, vp, vp, i64, i64, i32, i32, vp, vp, vp, vp]
     lib.rn_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint)]
     lib.rn_status_str.argtypes = [i32]
     lib.rn_status_str.restype = ctypes.c_char_p
     for f in ("rn_layernorm_fwd", "rn_rmsnorm_fwd", "rn_layernorm_bwd", "rn_rmsnorm_bwd",
-              "rn_quantize_only", "rn_device_error", "rn_abi_version", "rn_layernorm_bwd_noalloc"):
+              "rn_quantize_only", "rn_device_error", "rn_abi_version", "rn_layernorm_bwd_noalloc",
+              "rn_layernorm_add_fwd", "rn_rmsnorm_add_fwd"):
         getattr(lib, f).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -223,6 +228,47 @@ def rmsnorm_fwd(x, gamma, eps, quant="none", sm_margin=0, zero_centered_gamma=Fa
                             ctypes.byref(o), _ptr(rsigma), _stream())
     _check(st, "rn_rmsnorm_fwd")
     return res, rsigma
+
+
+def layernorm_add_fwd(x, residual, gamma, beta, eps, quant="none", sm_margin=0,
+                      zero_centered_gamma=False, scale=None, out_dtype=None):
+    """h = x + residual (rounded to x's dtype), LayerNorm(h) -> (output, h, mu, rsigma)."""
+    lib = _load()
+    _need(x, "x")
+    N, H = x.shape
+    _need(residual, "residual", x.dtype, (N, H))
+    _need(gamma, "gamma", torch.float32, (H,))
+    if beta is not None:
+        _need(beta, "beta", torch.float32, (H,))
+    h = torch.empty_like(x)
+    mu = torch.empty(N, dtype=torch.float32, device=x.device)
+    rsigma = torch.empty(N, dtype=torch.float32, device=x.device)
+    o, res = _make_output(x, quant, out_dtype, scale)
+    st = lib.rn_layernorm_add_fwd(_ptr(x), _ptr(residual), _dtype_code(x), _ptr(gamma), _ptr(beta),
+                                  N, H, float(eps), int(bool(zero_centered_gamma)), int(sm_margin),
+                                  QUANT_MODES[quant], ctypes.byref(o), _ptr(h), _ptr(mu),
+                                  _ptr(rsigma), _stream())
+    _check(st, "rn_layernorm_add_fwd")
+    return res, h, mu, rsigma
+
+
+def rmsnorm_add_fwd(x, residual, gamma, eps, quant="none", sm_margin=0,
+                    zero_centered_gamma=False, scale=None, out_dtype=None):
+    """h = x + residual (rounded to x's dtype), RMSNorm(h) -> (output, h, rsigma)."""
+    lib = _load()
+    _need(x, "x")
+    N, H = x.shape
+    _need(residual, "residual", x.dtype, (N, H))
+    _need(gamma, "gamma", torch.float32, (H,))
+    h = torch.empty_like(x)
+    rsigma = torch.empty(N, dtype=torch.float32, device=x.device)
+    o, res = _make_output(x, quant, out_dtype, scale)
+    st = lib.rn_rmsnorm_add_fwd(_ptr(x), _ptr(residual), _dtype_code(x), _ptr(gamma), N, H,
+                                float(eps), int(bool(zero_centered_gamma)), int(sm_margin),
+                                QUANT_MODES[quant], ctypes.byref(o), _ptr(h), _ptr(rsigma),
+                                _stream())
+    _check(st, "rn_rmsnorm_add_fwd")
+    return res, h, rsigma
 
 
 def bwd_workspace_bytes(N, H, dtype, layernorm=True) -> int:

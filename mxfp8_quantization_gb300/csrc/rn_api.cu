@@ -136,7 +136,7 @@ struct FwdPlan {
 int fwd_max_threads(int nc) { return nc >= 16 ? 512 : (nc >= 8 ? 768 : 1024); }
 
 rn_status plan_fwd(int nk, int H, int esz, int N, int sm_margin, const DeviceInfo& di,
-                   FwdPlan* pl) {
+                   FwdPlan* pl, int rows_per_slot = 1) {
   const int nchunks = H * esz / 16;
   FwdShape sh{1, 16, false};
   while (sh.g <= 8 && nchunks > 32 * sh.g * 16) sh.g *= 2;
@@ -150,13 +150,15 @@ rn_status plan_fwd(int nk, int H, int esz, int N, int sm_margin, const DeviceInf
   // fixed: gamma/beta, group exchange (14 groups x 4 x 8 floats), amax words
   // (32), slack; per slot: the row, (mu, rsigma), two mbarriers
   const size_t fixed = gb + 14 * 4 * 8 * sizeof(float) + 32 * sizeof(uint32_t) + 64;
-  const size_t per_slot = (size_t)H * esz + sizeof(float2) + 16;
+  // (with a residual add a slot holds the x row and the residual row)
+  const size_t per_slot = (size_t)rows_per_slot * H * esz + sizeof(float2) + 16;
   const size_t budget = cta_smem_budget(di, 1);
   int Q = budget > fixed ? (int)((budget - fixed) / per_slot) : 0;
   if (Q > 64) Q = 64;
   if (g >= 4) {
-    // leave L1 room for gamma / beta
-    const int qmax = (int)((size_t(128) << 10) / per_slot);
+    // leave L1 room for gamma / beta (but keep two slots when they fit)
+    int qmax = (int)((size_t(128) << 10) / per_slot);
+    if (qmax < 2) qmax = 2;
     if (Q > qmax) Q = qmax;
   }
   int W = (fwd_max_threads(sh.nc) / 32 - 1) / g * g;
@@ -298,7 +300,16 @@ rn_status check_margin(int sm_margin, const DeviceInfo& di) {
 // ---------------------------------------------------------------- forward
 rn_status fwd_common(int nk, const void* x, rn_dtype dt, const float* gamma, const float* beta,
                      int64_t N, int64_t H, float eps, int zcg, int sm_margin, rn_quant_mode mode,
-                     const rn_output* out, float* mu, float* rsigma, cudaStream_t stream) {
+                     const rn_output* out, float* mu, float* rsigma, cudaStream_t stream,
+                     bool res = false, const void* residual = nullptr,
+                     void* residual_out = nullptr) {
+  // with a residual add (res): residual and residual_out are [N, H] in x's
+  // dtype; like the other row tensors they may be NULL when N == 0
+  if (res && ((N > 0 && (residual == nullptr || residual_out == nullptr)) || nk == kIdentity))
+    return RN_ERR_INVALID;
+  if (res && mode == RN_QUANT_MXFP8) return RN_ERR_UNSUPPORTED;
+  if (res && N > 0 && (!aligned(residual, 16) || !aligned(residual_out, 16)))
+    return RN_ERR_UNSUPPORTED;
   if ((x == nullptr && N > 0) || !dtype_ok(dt) || N < 0 || H < 1 || N > INT32_MAX ||
       H > INT32_MAX)
     return RN_ERR_INVALID;
@@ -345,7 +356,7 @@ rn_status fwd_common(int nk, const void* x, rn_dtype dt, const float* gamma, con
   }
 
   FwdPlan pl;
-  if ((st = plan_fwd(nk, (int)H, esz, (int)N, sm_margin, di, &pl)) != RN_OK) return st;
+  if ((st = plan_fwd(nk, (int)H, esz, (int)N, sm_margin, di, &pl, res ? 2 : 1)) != RN_OK) return st;
   FwdParams p{};
   p.x = x;
   p.gamma = gamma;
@@ -362,22 +373,38 @@ rn_status fwd_common(int nk, const void* x, rn_dtype dt, const float* gamma, con
   p.eps = eps;
   p.zcg = zcg ? 1 : 0;
   p.out_f32 = (mode == RN_QUANT_NONE && out->out_dtype == RN_F32) ? 1 : 0;
+  p.residual = residual;
+  p.residual_out = residual_out;
   p.workers = pl.workers;
   p.Q = pl.Q;
   p.reverse = 0;
+  // pass 1 (or the only pass): with a residual, the kernel that adds it
+  auto first = [&](int qmode, bool pdl) {
+    return res ? launch_fwd_res(nk, bf16, pl.sh, qmode, p, pl.l, pdl, stream)
+               : launch_fwd(nk, bf16, pl.sh, qmode, p, pl.l, pdl, stream);
+  };
 
   switch (mode) {
     case RN_QUANT_NONE:
-      return launch_fwd(nk, bf16, pl.sh, kQNone, p, pl.l, false, stream);
+      return first(kQNone, false);
     case RN_QUANT_FP8_DELAYED:
       if ((st = launch_fwd_init(out->amax, out->scale, out->scale_inv, stream)) != RN_OK) return st;
-      return launch_fwd(nk, bf16, pl.sh, kQDelayed, p, pl.l, true, stream);
-    case RN_QUANT_FP8_CURRENT:
+      return first(kQDelayed, true);
+    case RN_QUANT_FP8_CURRENT: {
       if ((st = launch_fwd_init(out->amax, nullptr, nullptr, stream)) != RN_OK) return st;
-      if ((st = launch_fwd(nk, bf16, pl.sh, kQCurAmax, p, pl.l, true, stream)) != RN_OK)
-        return st;
-      p.reverse = 1;
-      return launch_fwd(nk, bf16, pl.sh, kQCurQuant, p, pl.l, true, stream);
+      if ((st = first(kQCurAmax, true)) != RN_OK) return st;
+      // pass 2 normalizes the stored sum h (with a residual) or x again
+      FwdPlan p2 = pl;
+      if (res && (st = plan_fwd(nk, (int)H, esz, (int)N, sm_margin, di, &p2, 1)) != RN_OK) return st;
+      FwdParams q = p;
+      if (res) q.x = residual_out;
+      q.residual = nullptr;
+      q.residual_out = nullptr;
+      q.workers = p2.workers;
+      q.Q = p2.Q;
+      q.reverse = 1;
+      return launch_fwd(nk, bf16, p2.sh, kQCurQuant, q, p2.l, true, stream);
+    }
     default:
       return RN_ERR_INVALID;
   }
@@ -520,6 +547,26 @@ rn_status rn_rmsnorm_fwd(const void* x, rn_dtype x_dtype, const float* gamma, in
                     mode, out, nullptr, rsigma, static_cast<cudaStream_t>(stream));
 }
 
+rn_status rn_layernorm_add_fwd(const void* x, const void* residual, rn_dtype dtype,
+                               const float* gamma, const float* beta, int64_t N, int64_t H,
+                               float eps, int zero_centered_gamma, int sm_margin,
+                               rn_quant_mode mode, const rn_output* out, void* residual_out,
+                               float* mu, float* rsigma, void* stream) {
+  return fwd_common(kLn, x, dtype, gamma, beta, N, H, eps, zero_centered_gamma, sm_margin, mode,
+                    out, mu, rsigma, static_cast<cudaStream_t>(stream), true, residual,
+                    residual_out);
+}
+
+rn_status rn_rmsnorm_add_fwd(const void* x, const void* residual, rn_dtype dtype,
+                             const float* gamma, int64_t N, int64_t H, float eps,
+                             int zero_centered_gamma, int sm_margin, rn_quant_mode mode,
+                             const rn_output* out, void* residual_out, float* rsigma,
+                             void* stream) {
+  return fwd_common(kRms, x, dtype, gamma, nullptr, N, H, eps, zero_centered_gamma, sm_margin,
+                    mode, out, nullptr, rsigma, static_cast<cudaStream_t>(stream), true, residual,
+                    residual_out);
+}
+
 rn_status rn_layernorm_bwd(const void* dz, const void* x, rn_dtype dtype, const float* mu,
                            const float* rsigma, const float* gamma, int64_t N, int64_t H,
                            int zero_centered_gamma, int sm_margin, void* dx, float* dgamma,
@@ -561,7 +608,10 @@ rn_status rn_device_error(unsigned int* code) {
   if (cudaDeviceSynchronize() != cudaSuccess) return RN_ERR_CUDA;
   unsigned a = 0, b = 0, c = 0;
   rn_status st;
+  unsigned a2 = 0;
   if ((st = read_clear_error_fwd(&a)) != RN_OK) return st;
+  if ((st = read_clear_error_fwd_res(&a2)) != RN_OK) return st;
+  if (a == 0) a = a2;
   if ((st = read_clear_error_mx(&b)) != RN_OK) return st;
   if ((st = read_clear_error_bwd(&c)) != RN_OK) return st;
   *code = a ? a : (b ? b : c);

@@ -381,6 +381,16 @@ struct Vec<uint16_t, 8> {  // bf16, 16 bytes
     const uint4 v = *reinterpret_cast<const uint4*>(p + (size_t)c * 16);
     return Raw{{v.x, v.y, v.z, v.w}};
   }
+  __device__ __forceinline__ static void store(unsigned char* p, int c, const Raw& r) {
+    *reinterpret_cast<uint4*>(p + (size_t)c * 16) = make_uint4(r.w[0], r.w[1], r.w[2], r.w[3]);
+  }
+  // element-wise a + b, each rounded once to bf16 (nearest even)
+  __device__ __forceinline__ static Raw add_rn(const Raw& a, const Raw& b) {
+    Raw r;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) asm("add.rn.bf16x2 %0, %1, %2;" : "=r"(r.w[i]) : "r"(a.w[i]), "r"(b.w[i]));
+    return r;
+  }
   __device__ __forceinline__ static float2 f32(const Raw& r, int i) { return bf16x2_f32(r.w[i]); }
   __device__ __forceinline__ static float2 sub(const Raw& r, int i, float m) {
     return bf16x2_sub(r.w[i], m);
@@ -426,6 +436,12 @@ struct Vec<float, 4> {  // fp32, 16 bytes
   __device__ __forceinline__ static Raw load(const unsigned char* p, int c) {
     const float4 v = *reinterpret_cast<const float4*>(p + (size_t)c * 16);
     return Raw{{make_float2(v.x, v.y), make_float2(v.z, v.w)}};
+  }
+  __device__ __forceinline__ static void store(unsigned char* p, int c, const Raw& r) {
+    *reinterpret_cast<float4*>(p + (size_t)c * 16) = make_float4(r.p[0].x, r.p[0].y, r.p[1].x, r.p[1].y);
+  }
+  __device__ __forceinline__ static Raw add_rn(const Raw& a, const Raw& b) {
+    return Raw{{add2(a.p[0], b.p[0]), add2(a.p[1], b.p[1])}};
   }
   __device__ __forceinline__ static float2 f32(const Raw& r, int i) { return r.p[i]; }
   __device__ __forceinline__ static float2 sub(const Raw& r, int i, float m) {

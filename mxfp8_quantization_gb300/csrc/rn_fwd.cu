@@ -33,6 +33,11 @@
 //     just before zeroes amax; the forward is launched as its programmatic
 //     dependent and waits for it (griddepcontrol.wait) only before that
 //     atomicMax.
+// With a residual (RES), the producer brings the residual row along with
+// the x row, each lane forms h = x + residual rounded once to the stream
+// dtype, stores it (the new residual stream) and normalizes h.  This file is
+// compiled twice: as is (the plain instantiations) and with RN_FWD_RES_TU
+// set (the residual ones), so that the two halves build in parallel.
 // Current scaling runs the kernel twice: pass 1 (statistics + amax, no
 // output) and pass 2 (quantize with 448/amax from the saved mu / rsigma), the
 // second launched as a programmatic dependent of the first and walking the
@@ -41,6 +46,10 @@
 
 #include "rn_device.cuh"
 #include "rn_internal.h"
+
+#ifndef RN_FWD_RES_TU
+#define RN_FWD_RES_TU 0
+#endif
 
 // the (G, NC, FULL) row shapes compiled in
 #ifndef RN_FWD_SHAPES
@@ -140,7 +149,7 @@ __device__ __forceinline__ float group_sum(float v, float* red, int group, int w
 
 // FULL: every lane holds exactly NC chunks of every row (H = NC * 32 * G
 // chunks), so no chunk needs a bounds test
-template <typename TIn, int NK, int QM, int G, int NC, bool FULL>
+template <typename TIn, int NK, int QM, int G, int NC, bool FULL, bool RES>
 __global__ void __launch_bounds__(max_threads<NC>(), 1) rn_fwd_kernel(const FwdParams p) {
   constexpr int VEC = 16 / (int)sizeof(TIn);
   using V = Vec<TIn, VEC>;
@@ -160,13 +169,14 @@ __global__ void __launch_bounds__(max_threads<NC>(), 1) rn_fwd_kernel(const FwdP
   const int H = p.H;
   const int nchunks = H / VEC;
   const uint32_t row_bytes = (uint32_t)H * sizeof(TIn);
+  const uint32_t slot_bytes = RES ? 2 * row_bytes : row_bytes;  // x row (then the residual row)
   const uint32_t Q = (uint32_t)p.Q;
   const size_t gb_bytes = GB_SMEM ? (size_t)H * sizeof(float) * (LN ? 2 : 1) : 0;
 
   float4* gsm = reinterpret_cast<float4*>(smem);  // [F4][nchunks]: g of chunk c, part j
   float4* bsm = gsm + (size_t)F4 * nchunks;       // same for beta (LayerNorm)
   unsigned char* ring = smem + gb_bytes;
-  float2* rstat = reinterpret_cast<float2*>(ring + (size_t)Q * row_bytes);  // [Q] (mu, rsigma)
+  float2* rstat = reinterpret_cast<float2*>(ring + (size_t)Q * slot_bytes);  // [Q] (mu, rsigma)
   float* red = reinterpret_cast<float*>(rstat + Q);                   // [kMaxGroups][4][8]
   uint32_t* red2 = reinterpret_cast<uint32_t*>(red + kMaxGroups * 4 * 8);  // [32]
   uint64_t* full = reinterpret_cast<uint64_t*>(red2 + 32);                  // row landed
@@ -206,9 +216,13 @@ __global__ void __launch_bounds__(max_threads<NC>(), 1) rn_fwd_kernel(const FwdP
           cp_async4(smem_u32(&rstat[s].y), p.rsigma + r);
           cp_async_arrive(bar);
         }
-        mbar_arrive_expect_tx(bar, row_bytes);
-        bulk_g2s(smem_u32(ring + (size_t)s * row_bytes), xb + (size_t)r * row_bytes, row_bytes,
+        mbar_arrive_expect_tx(bar, slot_bytes);
+        bulk_g2s(smem_u32(ring + (size_t)s * slot_bytes), xb + (size_t)r * row_bytes, row_bytes,
                  bar);
+        if constexpr (RES)
+          bulk_g2s(smem_u32(ring + (size_t)s * slot_bytes + row_bytes),
+                   static_cast<const unsigned char*>(p.residual) + (size_t)r * row_bytes, row_bytes,
+                   bar);
         pos.advance(1, Q);
       }
       // every copy this CTA issued must have landed before it exits
@@ -274,11 +288,14 @@ __global__ void __launch_bounds__(max_threads<NC>(), 1) rn_fwd_kernel(const FwdP
     // match a phase one lap old (alias-free since NGR < Q)
     if (i >= (int)Q) mbar_wait(smem_u32(&empty[s]), pos.phase ^ 1u, &g_err_fwd, kErrStatsWait);
     mbar_wait(smem_u32(&full[s]), pos.phase, &g_err_fwd, kErrFullWait);
-    const unsigned char* rowp = ring + (size_t)s * row_bytes;
+    const unsigned char* rowp = ring + (size_t)s * slot_bytes;
     Raw raw[NC];
 #pragma unroll
     for (int k = 0; k < NC; ++k)
-      if (k < nvalid) raw[k] = V::load(rowp, cbase + k * CSTEP);
+      if (k < nvalid) {
+        raw[k] = V::load(rowp, cbase + k * CSTEP);
+        if constexpr (RES) raw[k] = V::add_rn(raw[k], V::load(rowp + row_bytes, cbase + k * CSTEP));
+      }
     float mean = 0.0f, rs = 1.0f;
     if constexpr (META) {
       const float2 m = rstat[s];
@@ -289,6 +306,13 @@ __global__ void __launch_bounds__(max_threads<NC>(), 1) rn_fwd_kernel(const FwdP
     if (lane == 0) mbar_arrive(smem_u32(&empty[s]));
     pos.advance((uint32_t)NGR, Q);
     const int r = seq.row(i);
+    if constexpr (RES) {
+      // the new residual stream: h in the input dtype
+      unsigned char* hrow = static_cast<unsigned char*>(p.residual_out) + (size_t)r * row_bytes;
+#pragma unroll
+      for (int k = 0; k < NC; ++k)
+        if (k < nvalid) V::store(hrow, cbase + k * CSTEP, raw[k]);
+    }
 
     if constexpr (STATS) {
       float2 a[PAIRS];
@@ -402,6 +426,7 @@ __global__ void __launch_bounds__(max_threads<NC>(), 1) rn_fwd_kernel(const FwdP
   }
 }
 
+#if !RN_FWD_RES_TU
 // zeroes amax (and forms scale_inv = 1/scale for delayed scaling) ahead of
 // the forward, which is launched as its programmatic dependent
 __global__ void rn_fwd_init_kernel(float* amax, const float* scale, float* scale_inv) {
@@ -409,10 +434,11 @@ __global__ void rn_fwd_init_kernel(float* amax, const float* scale, float* scale
   *amax = 0.0f;
   if (scale != nullptr) *scale_inv = __fdiv_rn(1.0f, *scale);
 }
+#endif
 
 template <typename TIn, int NK, int QM, int G, int NC, bool FULL>
 rn_status launch_t(const FwdParams& p, const Launch& l, bool pdl, cudaStream_t s) {
-  auto k = rn_fwd_kernel<TIn, NK, QM, G, NC, FULL>;
+  auto k = rn_fwd_kernel<TIn, NK, QM, G, NC, FULL, RN_FWD_RES_TU != 0>;
   // the shared-memory exchange buffers and named barriers exist for at most
   // kMaxGroups groups of G >= 2 warps and 31 worker warps
   const int workers = l.threads / 32 - 1;
@@ -458,12 +484,38 @@ rn_status launch_q(const FwdShape& sh, int qmode, const FwdParams& p, const Laun
       else return launch_shape<TIn, NK, kQNone>(sh, p, l, pdl, s);
     case kQDelayed: return launch_shape<TIn, NK, kQDelayed>(sh, p, l, pdl, s);
     case kQCurAmax: return launch_shape<TIn, NK, kQCurAmax>(sh, p, l, pdl, s);
+#if !RN_FWD_RES_TU
+    // (with a residual, current scaling's pass 2 reads the stored sum as
+    // its x: the plain kernel)
     case kQCurQuant: return launch_shape<TIn, NK, kQCurQuant>(sh, p, l, pdl, s);
+#endif
     default: return RN_ERR_INVALID;
   }
 }
 
 }  // namespace
+
+#if RN_FWD_RES_TU
+
+rn_status launch_fwd_res(int nk, bool bf16, const FwdShape& sh, int qmode, const FwdParams& p,
+                         const Launch& l, bool pdl, cudaStream_t s) {
+  if (nk == kIdentity || p.residual == nullptr || p.residual_out == nullptr) return RN_ERR_INVALID;
+  if (bf16)
+    return nk == kLn ? launch_q<uint16_t, kLn>(sh, qmode, p, l, pdl, s)
+                     : launch_q<uint16_t, kRms>(sh, qmode, p, l, pdl, s);
+  return nk == kLn ? launch_q<float, kLn>(sh, qmode, p, l, pdl, s)
+                   : launch_q<float, kRms>(sh, qmode, p, l, pdl, s);
+}
+
+rn_status read_clear_error_fwd_res(unsigned* code) {
+  unsigned v = 0, zero = 0;
+  if (cudaMemcpyFromSymbol(&v, g_err_fwd, sizeof(v)) != cudaSuccess) return RN_ERR_CUDA;
+  if (cudaMemcpyToSymbol(g_err_fwd, &zero, sizeof(zero)) != cudaSuccess) return RN_ERR_CUDA;
+  *code = v;
+  return RN_OK;
+}
+
+#else
 
 rn_status launch_fwd_init(float* amax, const float* scale, float* scale_inv, cudaStream_t s) {
   rn_fwd_init_kernel<<<1, 1, 0, s>>>(amax, scale, scale_inv);
@@ -488,5 +540,7 @@ rn_status read_clear_error_fwd(unsigned* code) {
   *code = v;
   return RN_OK;
 }
+
+#endif  // RN_FWD_RES_TU
 
 }  // namespace rn

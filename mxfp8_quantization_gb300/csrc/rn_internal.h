@@ -37,6 +37,8 @@ struct FwdParams {
   float eps;
   int zcg;              // zero-centered gamma
   int out_f32;          // kQNone: 1 = fp32 output, 0 = bf16
+  const void* residual; // residual add: the residual [N, H] (x's dtype), or NULL
+  void* residual_out;   // residual add: h = x + residual [N, H], or NULL
   int workers;          // worker warps (a multiple of the row group size)
   int Q;                // ring slots (rows); more than workers / group size
   int reverse;          // walk the rows from the last one
@@ -129,6 +131,10 @@ struct FwdShape {
 // pdl: launch as a programmatic dependent of the previous kernel
 rn_status launch_fwd(int nk, bool bf16, const FwdShape& sh, int qmode, const FwdParams& p,
                      const Launch& l, bool pdl, cudaStream_t s);
+// the same with a residual add (p.residual, p.residual_out set; no pass 2 of
+// current scaling, which reads the stored sum through launch_fwd)
+rn_status launch_fwd_res(int nk, bool bf16, const FwdShape& sh, int qmode, const FwdParams& p,
+                         const Launch& l, bool pdl, cudaStream_t s);
 // one-thread kernel: amax = 0 and, when scale != NULL, scale_inv = 1/scale
 rn_status launch_fwd_init(float* amax, const float* scale, float* scale_inv, cudaStream_t s);
 rn_status launch_mx(int nk, bool bf16, int ng, const MxParams& p, const Launch& l,
@@ -145,6 +151,7 @@ rn_status launch_colreduce(const ColReduceParams& p, cudaStream_t s);
 
 // device error words, one per translation unit
 rn_status read_clear_error_fwd(unsigned* code);
+rn_status read_clear_error_fwd_res(unsigned* code);
 rn_status read_clear_error_mx(unsigned* code);
 rn_status read_clear_error_bwd(unsigned* code);
 

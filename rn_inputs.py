@@ -27,6 +27,10 @@ Recipes (one per workload; every draw comes from
                     gamma = 1 + 0.1 N(0,1), beta ~ N(0, 0.1), eps 1e-5.
 * ``bwd_bf16``      backward, x bf16 [3000 x 5120] ~ N(0,1), dz bf16 ~ N(0,1),
                     gamma = 1 + 0.1 N(0,1), beta ~ N(0, 0.1), eps 1e-5.
+* ``rms_add``       residual add + RMSNorm (or LayerNorm) fwd, x bf16
+                    [8192 x 4096] ~ N(0,1) (a sublayer's output), residual
+                    bf16 ~ N(0, 3) (the residual stream), gamma = 1 + 0.1 N(0,1),
+                    beta ~ N(0, 0.1), eps 1e-5, FP8 E4M3 scale fixed at 448/8.
 
 Every recipe takes optional ``N``/``H`` overrides so that tests can draw the
 same distributions at sizes the oracle finishes in seconds.
@@ -84,6 +88,7 @@ class Workload:
     scale: float | None = None     # FP8 delayed scale (fp32), when fixed
     amax_history: np.ndarray | None = None  # float32 [16]
     extra: dict = field(default_factory=dict)
+    residual: np.ndarray | None = None      # same storage as x (residual add), or None
 
     def x_f64(self, rows=slice(None)) -> np.ndarray:
         return rows_view_f64(self.x, self.dtype, rows)
@@ -91,6 +96,10 @@ class Workload:
     def dz_f64(self, rows=slice(None)) -> np.ndarray:
         assert self.dz is not None
         return rows_view_f64(self.dz, self.dtype, rows)
+
+    def residual_f64(self, rows=slice(None)) -> np.ndarray:
+        assert self.residual is not None
+        return rows_view_f64(self.residual, self.dtype, rows)
 
 
 def rows_view_f64(a: np.ndarray, dtype: str, rows=slice(None)) -> np.ndarray:
@@ -173,6 +182,15 @@ def _bwd(rng, N, H, dtype, name):
     return Workload(name, N, H, dtype, x, gamma, beta, dz, 1e-5)
 
 
+def _rms_add(rng, N, H):
+    x = _store(rng.standard_normal((N, H)), "bf16")
+    residual = _store(rng.normal(0.0, 3.0, (N, H)), "bf16")
+    gamma = _f32(1.0 + 0.1 * rng.standard_normal(H))
+    beta = _f32(rng.normal(0.0, 0.1, H))
+    return Workload("rms_add", N, H, "bf16", x, gamma, beta, None, 1e-5,
+                    scale=float(np.float32(448.0) / np.float32(8.0)), residual=residual)
+
+
 WORKLOADS = {
     "rms_small": ((256, 1024), _rms_small),
     "ln_delayed": ((8192, 4096), _ln_delayed),
@@ -180,6 +198,7 @@ WORKLOADS = {
     "mxfp8": ((65536, 2048), _mxfp8),
     "bwd_f32": ((131072, 1024), lambda rng, N, H: _bwd(rng, N, H, "f32", "bwd_f32")),
     "bwd_bf16": ((3000, 5120), lambda rng, N, H: _bwd(rng, N, H, "bf16", "bwd_bf16")),
+    "rms_add": ((8192, 4096), _rms_add),
 }
 
 

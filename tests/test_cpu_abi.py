@@ -117,3 +117,19 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(rn, "_LIB_PATH", str(tmp_path / "missing.so"))
     with pytest.raises(rn.RNError, match="missing"):
         rn._load()
+
+
+def test_residual_add_forward_rejects_bad_arguments_on_host(lib):
+    x, r, h = ctypes.c_void_p(0x1000), ctypes.c_void_p(0x8000), ctypes.c_void_p(0x9000)
+    g, rs, mu = ctypes.c_void_p(0x2000), ctypes.c_void_p(0x3000), ctypes.c_void_p(0x4000)
+    o = _out(data=0x5000, out_dtype=0)
+    # the residual and the stored sum are required
+    assert lib.rn_rmsnorm_add_fwd(x, None, 0, g, 4, 1024, 1e-5, 0, 0, 0, ctypes.byref(o), h, rs, None) == 1
+    assert lib.rn_rmsnorm_add_fwd(x, r, 0, g, 4, 1024, 1e-5, 0, 0, 0, ctypes.byref(o), None, rs, None) == 1
+    # MXFP8 output is not offered with the residual add
+    om = _out(data=0x5000, row_scales=0x6000)
+    assert lib.rn_layernorm_add_fwd(x, r, 0, g, None, 64, 1024, 1e-5, 0, 0, 3, ctypes.byref(om), h, mu,
+                                    rs, None) == 2
+    # misaligned residual
+    assert lib.rn_rmsnorm_add_fwd(x, ctypes.c_void_p(0x8004), 0, g, 4, 1024, 1e-5, 0, 0, 0, ctypes.byref(o),
+                                  h, rs, None) == 2
