@@ -22,7 +22,7 @@ readings taken where they are silent are listed in each function.
 Module map:
   formats  E4M3 decode/encode, E8M0 shared exponents, bf16 rounding.
   norm     row statistics, affine apply, quantization stages, backward,
-           residual add + norm.
+           residual add + norm, the delayed-scaling history step.
 
 Parity status: every function here is pinned by CPU tests against closed
 forms, exact rational arithmetic, finite differences, brute force or
@@ -37,5 +37,5 @@ from .formats import (  # noqa: F401
 from .norm import (  # noqa: F401
     layernorm_stats, rmsnorm_stats, norm_apply, layernorm_fwd, rmsnorm_fwd,
     layernorm_bwd, rmsnorm_bwd, quantize, QUANT_MODES,
-    residual_add, rmsnorm_add_fwd, layernorm_add_fwd,
+    residual_add, rmsnorm_add_fwd, layernorm_add_fwd, amax_history_update,
 )

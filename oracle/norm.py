@@ -276,3 +276,27 @@ def layernorm_add_fwd(x, residual, gamma, beta, eps, dtype="bf16", zero_centered
     res["residual_out"] = _stream(h, dtype)
     res["h"] = h
     return res
+
+
+# ------------------------------------------- delayed-scaling recipe step
+# The page describes delayed scaling (FP8 with a scale chosen from earlier
+# steps' amax) without the bookkeeping.  Reading (the common recipe, margin
+# 0): the history keeps the most recent amax at index 0; a step shifts it by
+# one place and puts the new amax first; the next scale is
+# fp32(448 / max(history)) by one IEEE fp32 division, except that a maximum
+# that is 0 or not finite keeps the previous scale; scale_inv = fp32(1 / scale).
+def amax_history_update(history, amax, scale):
+    """-> (new history float32 [L], new scale float32, new scale_inv float32)."""
+    h = np.asarray(history, dtype=np.float32)
+    new = np.empty_like(h)
+    if h.size:
+        new[0] = np.float32(amax)
+        new[1:] = h[:-1]
+    m = np.float32(np.max(new)) if new.size else np.float32(0.0)
+    if np.isnan(new).any():
+        m = np.float32(np.nan)
+    if np.isfinite(m) and m > 0:
+        s = np.float32(np.float32(E4M3_MAX) / m)
+    else:
+        s = np.float32(scale)
+    return new, s, np.float32(np.float32(1.0) / s)

@@ -349,3 +349,35 @@ def test_residual_add_rmsnorm_closed_form():
     rs = 2.0 / np.sqrt(41.0)
     assert abs(float(res["rsigma"][0]) - rs) <= 1e-7 * rs
     assert np.allclose(res["y"], np.array([[1.5, 2.5, 3.5, 4.5]]) * rs, rtol=1e-15, atol=0)
+
+
+# ------------------------------------------- delayed-scaling history step
+def test_amax_history_update_by_hand():
+    h, s, si = oracle.amax_history_update([4.0, 5.0, 3.0, 6.0], 2.0, 10.0)
+    # shifted down, the new amax first; the oldest value (6) drops out
+    assert list(h) == [2.0, 4.0, 5.0, 3.0]
+    assert s == np.float32(448.0 / 5.0) and si == np.float32(1.0) / s
+    # the new amax is the largest
+    h, s, _ = oracle.amax_history_update([1.0, 1.0], 7.0, 3.0)
+    assert list(h) == [7.0, 1.0] and s == np.float32(64.0)
+    # length 1: the history is just the new amax
+    h, s, _ = oracle.amax_history_update([9.0], 0.5, 3.0)
+    assert list(h) == [0.5] and s == np.float32(896.0)
+
+
+def test_amax_history_update_keeps_scale_without_a_usable_maximum():
+    for hist, amax in (([0.0, 0.0, 0.0], 0.0), ([np.inf, 1.0], 2.0), ([1.0, 2.0], np.nan)):
+        h, s, si = oracle.amax_history_update(hist, amax, 12.5)
+        assert s == np.float32(12.5) and si == np.float32(0.08)
+    # an infinity that has just dropped out no longer matters
+    h, s, _ = oracle.amax_history_update([1.0, np.inf], 4.0, 12.5)
+    assert list(h) == [4.0, 1.0] and s == np.float32(112.0)
+
+
+def test_amax_history_update_matches_the_workload_scale():
+    # the ln_delayed workload's scale is 448 / max(history): one step with a
+    # new amax below that maximum leaves the maximum (unless it drops out)
+    w = rn_inputs.make("ln_delayed", N=8, H=64)
+    hist = w.amax_history
+    h, s, _ = oracle.amax_history_update(hist, 1.0, w.scale)
+    assert s == np.float32(np.float32(448.0) / np.max(hist[:-1]))
