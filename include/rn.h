@@ -218,6 +218,24 @@ rn_status rn_layernorm_bwd_noalloc(const void* dz, const void* x, rn_dtype dtype
                                    void* stream);
 
 /*
+ * Delayed-scaling recipe step (closes the loop around RN_QUANT_FP8_DELAYED;
+ * the page describes delayed scaling but not its bookkeeping, so this is the
+ * common recipe with margin 0):
+ *   amax_history: device fp32 [history_len], most recent first, updated in
+ *                 place: shifted down one place, *amax written at index 0;
+ *   amax:         device fp32 scalar, the new amax (e.g. a forward's output);
+ *   scale:        device fp32 scalar, in: the current scale, out: the next,
+ *                 fp32(448 / max(history)) by IEEE division, or unchanged
+ *                 when that maximum is 0, negative, infinite or NaN;
+ *   scale_inv:    device fp32 scalar, out: fp32(1 / scale).
+ * 1 <= history_len <= 1024 (else RN_ERR_INVALID / RN_ERR_UNSUPPORTED);
+ * one small kernel on `stream`.
+ */
+rn_status rn_delayed_scaling_update(float* amax_history, int64_t history_len,
+                                    const float* amax, float* scale,
+                                    float* scale_inv, void* stream);
+
+/*
  * Quantization stage alone on caller-given fp32 values y [N, H] (the
  * page's UNFUSED path: norm, then a separate quantize).  Same output
  * descriptor and arithmetic as the fused forward for `mode`

@@ -31,7 +31,7 @@ import torch
 
 __all__ = [
     "layernorm_fwd", "rmsnorm_fwd", "layernorm_bwd", "rmsnorm_bwd", "quantize_only",
-    "layernorm_bwd_noalloc", "layernorm_add_fwd", "rmsnorm_add_fwd",
+    "layernorm_bwd_noalloc", "layernorm_add_fwd", "rmsnorm_add_fwd", "delayed_scaling_update",
     "bwd_workspace_bytes", "device_error", "Fp8Output", "MXFP8Output", "lib_path", "RNError",
     "QUANT_MODES",
 ]
@@ -87,13 +87,14 @@ def _load():
     lib.rn_rmsnorm_add_fwd.argtypes = [vp, vp, i32, vp, i64, i64, f32, i32, i32, i32, outp, vp, vp,
                                        vp]
     lib.rn_quantize_only.argtypes = [vp, i64, i64, i32, outp, vp]
+    lib.rn_delayed_scaling_update.argtypes = [vp, i64, vp, vp, vp, vp]
     lib.rn_layernorm_bwd_noalloc.argtypes = [vp, vp, i32, vp, vp, vp, i64, i64, i32, i32, vp, vp, vp, vp]
     lib.rn_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint)]
     lib.rn_status_str.argtypes = [i32]
     lib.rn_status_str.restype = ctypes.c_char_p
     for f in ("rn_layernorm_fwd", "rn_rmsnorm_fwd", "rn_layernorm_bwd", "rn_rmsnorm_bwd",
               "rn_quantize_only", "rn_device_error", "rn_abi_version", "rn_layernorm_bwd_noalloc",
-              "rn_layernorm_add_fwd", "rn_rmsnorm_add_fwd"):
+              "rn_layernorm_add_fwd", "rn_rmsnorm_add_fwd", "rn_delayed_scaling_update"):
         getattr(lib, f).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -269,6 +270,21 @@ def rmsnorm_add_fwd(x, residual, gamma, eps, quant="none", sm_margin=0,
                                 _stream())
     _check(st, "rn_rmsnorm_add_fwd")
     return res, h, rsigma
+
+
+def delayed_scaling_update(amax_history, amax, scale):
+    """One delayed-scaling step on device tensors: shifts `amax` (fp32 [1])
+    into `amax_history` (fp32 [L], most recent first) and updates `scale`
+    (fp32 [1]) in place; returns scale_inv (fp32 [1])."""
+    lib = _load()
+    _need(amax_history, "amax_history", torch.float32)
+    _need(amax, "amax", torch.float32, (1,))
+    _need(scale, "scale", torch.float32, (1,))
+    scale_inv = torch.empty(1, dtype=torch.float32, device=scale.device)
+    st = lib.rn_delayed_scaling_update(_ptr(amax_history), amax_history.numel(), _ptr(amax),
+                                       _ptr(scale), _ptr(scale_inv), _stream())
+    _check(st, "rn_delayed_scaling_update")
+    return scale_inv
 
 
 def bwd_workspace_bytes(N, H, dtype, layernorm=True) -> int:

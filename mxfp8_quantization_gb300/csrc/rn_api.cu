@@ -584,6 +584,18 @@ rn_status rn_rmsnorm_bwd(const void* dz, const void* x, rn_dtype dtype, const fl
                     static_cast<cudaStream_t>(stream));
 }
 
+rn_status rn_delayed_scaling_update(float* amax_history, int64_t history_len, const float* amax,
+                                    float* scale, float* scale_inv, void* stream) {
+  if (amax_history == nullptr || amax == nullptr || scale == nullptr || scale_inv == nullptr ||
+      history_len < 1)
+    return RN_ERR_INVALID;
+  if (history_len > kMaxHistory) return RN_ERR_UNSUPPORTED;
+  if (!aligned(amax_history, 4) || !aligned(amax, 4) || !aligned(scale, 4) || !aligned(scale_inv, 4))
+    return RN_ERR_UNSUPPORTED;
+  return launch_amax_history(amax_history, (int)history_len, amax, scale, scale_inv,
+                             static_cast<cudaStream_t>(stream));
+}
+
 rn_status rn_quantize_only(const float* y, int64_t N, int64_t H, rn_quant_mode mode,
                            const rn_output* out, void* stream) {
   if (mode != RN_QUANT_FP8_DELAYED && mode != RN_QUANT_FP8_CURRENT && mode != RN_QUANT_MXFP8)

@@ -149,6 +149,11 @@ rn_status launch_bwd_fused(bool ln, bool big, const BwdParams& p, const Launch& 
                            cudaStream_t s);
 rn_status launch_colreduce(const ColReduceParams& p, cudaStream_t s);
 
+// delayed-scaling history step (one CTA; 1 <= L <= kMaxHistory)
+constexpr int kMaxHistory = 1024;
+rn_status launch_amax_history(float* hist, int L, const float* amax, float* scale,
+                              float* scale_inv, cudaStream_t s);
+
 // device error words, one per translation unit
 rn_status read_clear_error_fwd(unsigned* code);
 rn_status read_clear_error_fwd_res(unsigned* code);

@@ -133,3 +133,10 @@ def test_residual_add_forward_rejects_bad_arguments_on_host(lib):
     # misaligned residual
     assert lib.rn_rmsnorm_add_fwd(x, ctypes.c_void_p(0x8004), 0, g, 4, 1024, 1e-5, 0, 0, 0, ctypes.byref(o),
                                   h, rs, None) == 2
+
+
+def test_delayed_scaling_update_rejects_bad_arguments_on_host(lib):
+    p = ctypes.c_void_p(0x1000)
+    assert lib.rn_delayed_scaling_update(p, 0, p, p, p, None) == 1      # empty history
+    assert lib.rn_delayed_scaling_update(None, 4, p, p, p, None) == 1
+    assert lib.rn_delayed_scaling_update(p, 2048, p, p, p, None) == 2   # longer than 1024
