@@ -78,6 +78,8 @@ def algorithmic_bytes(kind, N, H, esz, ln, extra=None):
         return 3 * E * esz + stats + H * 4 + vec
     if kind == "fwd_add_fp8":                # x, residual in; h and codes out
         return 3 * E * esz + E * 1 + vec + stats
+    if kind == "history":                    # history read + written (H entries), 3 scalars
+        return 2 * H * 4 + 12
     raise ValueError(kind)
 
 
@@ -520,6 +522,18 @@ def run_other_workloads(torch, rn, lib, rn_inputs, flush, peak, steps, warmup, o
                    statistics.mean(t["mx"]), 1)
             del P
         del w
+    if want("rms_small"):
+        # the delayed-scaling history step (1024 entries): one tiny kernel,
+        # launch-latency bound
+        hist = torch.rand(1024, device="cuda")
+        amax = torch.ones(1, device="cuda")
+        scl = torch.ones(1, device="cuda")
+        sinv = torch.empty(1, device="cuda")
+        vp = ctypes.c_void_p
+        fa = ("rn_delayed_scaling_update", [vp(hist.data_ptr()), 1024, vp(amax.data_ptr()),
+                                            vp(scl.data_ptr()), vp(sinv.data_ptr())])
+        t = time_calls(torch, lib, [("h", fa)], steps, warmup, flush)
+        report("delayed_scaling_update_1024", "history", 1, 1024, 4, False, statistics.mean(t["h"]), 1)
     if want("rms_add"):
         w = rn_inputs.make("rms_add")
         P = Prepared(rn, torch, w, ln=False)
