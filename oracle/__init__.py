@@ -15,12 +15,15 @@ for current-scaling FP8).  The residual add + norm follows the fused
 reduce-scatter + residual add + RMSNorm + all-gather named on the page "NVIDIA
 Megatron-Core ... inference_layers" (its single-GPU core).  The formats come from their public definitions:
 FP8 E4M3 from the OCP 8-bit floating point specification, MXFP8 block
-scaling (E8M0 shared scale over 32 elements) from the OCP Microscaling
-Formats v1.0 specification.  The pages give no formula for any of this; the
+scaling (E8M0 shared scale over 32 elements) and the FP4 E2M1 element format
+from the OCP Microscaling Formats v1.0 specification; NVFP4 (E2M1 elements,
+an E4M3 scale per 16 elements, an fp32 tensor scale) from NVIDIA's published
+description of that format, the page naming only the FUSED_NORM_AMAX_NVFP4
+path.  The pages give no formula for any of this; the
 readings taken where they are silent are listed in each function.
 
 Module map:
-  formats  E4M3 decode/encode, E8M0 shared exponents, bf16 rounding.
+  formats  E4M3 and E2M1 decode/encode, E8M0 shared exponents, bf16 rounding.
   norm     row statistics, affine apply, quantization stages, backward,
            residual add + norm, the delayed-scaling history step.
 
@@ -32,7 +35,8 @@ so no pin comes from the pages themselves.
 from . import formats, norm  # noqa: F401
 from .formats import (  # noqa: F401
     E4M3_MAX, e4m3_decode, e4m3_encode, e4m3_magnitudes, e8m0_from_amax,
-    round_to_bf16, bf16_bits,
+    round_to_bf16, bf16_bits, E2M1_MAX, e2m1_decode, e2m1_encode, e2m1_magnitudes,
+    e2m1_pack, e2m1_unpack,
 )
 from .norm import (  # noqa: F401
     layernorm_stats, rmsnorm_stats, norm_apply, layernorm_fwd, rmsnorm_fwd,

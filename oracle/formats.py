@@ -8,6 +8,10 @@
   unsigned biased exponent (bias 127) encoding 2**(code-127) for codes 0..254
   and NaN for 0xFF.
 * bf16 — 1 sign, 8 exponent, 7 mantissa bits (the top half of an fp32).
+* FP4 E2M1 — OCP Microscaling Formats (MX) v1.0, element format "FP4 E2M1":
+  1 sign bit, 2 exponent bits with bias 1, 1 mantissa bit; exponent field 0
+  encodes the subnormal m * 0.5; no NaN or infinity; magnitudes 0, 0.5, 1,
+  1.5, 2, 3, 4, 6 for the codes 0..7, bit 3 the sign.
 
 Conversion rules the kernels must reproduce (the page on TransformerEngine's
 normalization extension names the formats only; these are the plainest
@@ -21,6 +25,10 @@ readings):
   [-127, 127] and stored as e + 127.  amax = 0 gives code 0; amax = NaN gives
   0xFF.  amax = +inf is read as the value its fp32 exponent field encodes,
   2**128, giving e = 120 (code 247).
+* to E2M1: round to nearest, ties to the even code (the one whose mantissa
+  bit is 0); magnitudes above 6 saturate to 6; the sign bit follows the
+  input's sign, so negative values that round to zero give 0x8.  Two codes
+  share a byte, the element with the lower index in the low nibble.
 """
 from __future__ import annotations
 
@@ -142,3 +150,73 @@ def bf16_bits(v) -> np.ndarray:
     bits = (r.view(np.uint32) >> 16).astype(np.uint16)
     bits = np.where(np.isnan(r), np.uint16(0x7FC0), bits)
     return bits.astype(np.uint16)
+
+
+# ------------------------------------------------------------- FP4 E2M1
+E2M1_MAX = 6.0
+
+
+def _e2m1_value(code: int) -> float:
+    """Value of one 4-bit E2M1 code, from the bit fields."""
+    s = -1.0 if code & 0x8 else 1.0
+    e = (code >> 1) & 0x3
+    m = code & 0x1
+    if e == 0:
+        return s * m * 0.5                 # subnormal: (m/2) * 2**(1-1)
+    return s * (1.0 + m / 2.0) * 2.0 ** (e - 1)
+
+
+_E2M1_DECODE = np.array([_e2m1_value(c) for c in range(16)], dtype=np.float64)
+
+
+def e2m1_decode(codes) -> np.ndarray:
+    """4-bit E2M1 codes (0..15, any integer dtype) -> fp64 values (exact)."""
+    return _E2M1_DECODE[np.asarray(codes, dtype=np.int64) & 0xF]
+
+
+def e2m1_magnitudes() -> np.ndarray:
+    """The 8 non-negative E2M1 magnitudes, codes 0..7 in order."""
+    return _E2M1_DECODE[:8].copy()
+
+
+_E2M1_MAGS = e2m1_magnitudes()
+
+
+def e2m1_encode(v) -> np.ndarray:
+    """Round values (taken exactly, as fp64) to 4-bit E2M1 codes (uint8 0..15).
+
+    Nearest magnitude, ties to the even code, saturating at 6; sign from the
+    input's sign bit.  The magnitudes increase with the code, so the two
+    neighbours of |v| come from a sorted search.  NaN has no E2M1 code: the
+    caller must not pass one.
+    """
+    v = np.asarray(v, dtype=np.float64)
+    if np.isnan(v).any():
+        raise ValueError("E2M1 has no NaN")
+    a = np.abs(v)
+    idx = np.clip(np.searchsorted(_E2M1_MAGS, a, side="left"), 1, 7)
+    lo = _E2M1_MAGS[idx - 1]
+    hi = _E2M1_MAGS[idx]
+    dlo = a - lo
+    dhi = hi - a
+    take_hi = np.where(dhi == dlo, (idx % 2) == 0, dhi < dlo)
+    code = np.where(take_hi, idx, idx - 1)
+    code = np.where(a >= E2M1_MAX, 7, code)
+    code = np.where(np.signbit(v), code | 0x8, code)
+    return code.astype(np.uint8)
+
+
+def e2m1_pack(codes) -> np.ndarray:
+    """[..., 2k] 4-bit codes -> [..., k] bytes: element 2j low, 2j+1 high."""
+    c = np.asarray(codes, dtype=np.uint8)
+    assert c.shape[-1] % 2 == 0
+    return (c[..., 0::2] | (c[..., 1::2] << 4)).astype(np.uint8)
+
+
+def e2m1_unpack(packed) -> np.ndarray:
+    """Inverse of e2m1_pack: [..., k] bytes -> [..., 2k] 4-bit codes."""
+    b = np.asarray(packed, dtype=np.uint8)
+    out = np.empty(b.shape[:-1] + (2 * b.shape[-1],), dtype=np.uint8)
+    out[..., 0::2] = b & 0xF
+    out[..., 1::2] = b >> 4
+    return out

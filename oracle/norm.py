@@ -33,6 +33,19 @@ The pages print no formula.  Readings taken (the plainest standard ones):
              A = max |y32|, code_e8m0(A), element code = E4M3(y32 * 2**-e)
              (a power-of-two scaling, exact); the columnwise data is stored
              transposed, [H, N], with scales [H, N/32].
+    NVFP4    (the page names this path, FUSED_NORM_AMAX_NVFP4, as the
+             current-scaling scheme applied to NVFP4, and defines no format;
+             the reading is NVIDIA's published NVFP4 layout: E2M1 elements,
+             one E4M3 scale per 16 consecutive elements of a row, and one fp32
+             scale for the tensor): amax as for current scaling,
+             S = fp32(448 * 6 / amax) (the largest E4M3 times the largest
+             E2M1; capped at the largest finite fp32; S = 1 when amax = 0),
+             k = fp32(S / 6); per block of 16 along a row A = max |y32|,
+             scale code sc = E4M3(fp32(A * k)), with v = its value
+             e = fp32(S / v) (e = 0 when v = 0), element code =
+             E2M1(fp32(y32 * e)); codes packed two to a byte (element 2j in
+             the low nibble); the value an element stands for is
+             E2M1 value * v / S.  Rowwise only.
 * the backward takes mu and rsigma as given (the saved fp32 values), forms
   xhat = (x - mu) * rsigma (RMSNorm: x * rsigma), dy = dz * g_eff and
     LayerNorm  dx = rsigma * (dy - mean(dy) - xhat * mean(dy * xhat))
@@ -44,10 +57,12 @@ from __future__ import annotations
 
 import numpy as np
 
-from .formats import E4M3_MAX, bf16_bits, e4m3_encode, e8m0_from_amax, round_to_bf16
+from .formats import (E2M1_MAX, E4M3_MAX, bf16_bits, e2m1_encode, e2m1_pack, e4m3_decode,
+                      e4m3_encode, e8m0_from_amax, round_to_bf16)
 
-QUANT_MODES = ("none", "fp8_delayed", "fp8_current", "mxfp8")
+QUANT_MODES = ("none", "fp8_delayed", "fp8_current", "mxfp8", "nvfp4")
 MX_BLOCK = 32
+NV_BLOCK = 16
 
 
 def _f64(a) -> np.ndarray:
@@ -138,10 +153,44 @@ def mx_blocks_1d(y32_rows) -> tuple[np.ndarray, np.ndarray]:
     return q.reshape(n, h), code
 
 
+def nvfp4_global_scale(amax) -> np.float32:
+    """S = fp32(448 * 6 / amax) by one IEEE fp32 division, capped at the
+    largest finite fp32; amax = 0 -> 1."""
+    a = np.float32(amax)
+    if a == 0:
+        return np.float32(1.0)
+    with np.errstate(over="ignore", divide="ignore"):
+        s = np.float32(np.float32(E4M3_MAX * E2M1_MAX) / a)
+    return np.minimum(s, np.float32(np.finfo(np.float32).max))
+
+
+def nvfp4_blocks_1d(y32_rows, S) -> tuple[np.ndarray, np.ndarray]:
+    """NVFP4-quantize along the last axis in blocks of 16 with tensor scale S
+    -> (packed E2M1 codes [n, h/2], E4M3 block-scale codes [n, h/16])."""
+    y = np.asarray(y32_rows, dtype=np.float32)
+    n, h = y.shape
+    assert h % NV_BLOCK == 0
+    if np.isnan(y).any():
+        raise ValueError("NVFP4 has no code for NaN")
+    S = np.float32(S)
+    k = np.float32(S / np.float32(E2M1_MAX))
+    yb = y.reshape(n, h // NV_BLOCK, NV_BLOCK)
+    A = np.max(np.abs(yb), axis=-1)                      # fp32, exact
+    with np.errstate(over="ignore"):
+        sc = e4m3_encode((A * k).astype(np.float64))     # fp32 product, then E4M3
+    v = e4m3_decode(sc).astype(np.float32)               # exact
+    with np.errstate(divide="ignore"):
+        e = np.where(v == 0, np.float32(0.0), S / np.where(v == 0, np.float32(1.0), v))
+    e = e.astype(np.float32)
+    p = yb * e[..., None]                                # fp32 products
+    codes = e2m1_encode(p.astype(np.float64)).reshape(n, h)
+    return e2m1_pack(codes), sc
+
+
 def quantize(y32, mode: str, scale=None, amax=None) -> dict:
     """Quantization stage for a block of fp32 pre-quantization rows.
 
-    ``y32`` [n, H] fp32.  For fp8_current the tensor-wide ``amax`` may be
+    ``y32`` [n, H] fp32.  For fp8_current and nvfp4 the tensor-wide ``amax`` may be
     given (when y32 is only a sample of the rows); otherwise it is taken from
     y32.  Returns the fields the entry points return for that mode.
     """
@@ -155,6 +204,12 @@ def quantize(y32, mode: str, scale=None, amax=None) -> dict:
         s = current_scale(am)
         return {"data": fp8_codes(y32, s), "amax": am, "scale": s,
                 "scale_inv": scale_inverse(s)}
+    if mode == "nvfp4":
+        am = tensor_amax(y32) if amax is None else np.float32(amax)
+        S = nvfp4_global_scale(am)
+        q, sc = nvfp4_blocks_1d(y32, S)
+        return {"data": q, "row_scales": sc, "amax": am, "scale": S,
+                "scale_inv": scale_inverse(S)}
     if mode == "mxfp8":
         rq, rs = mx_blocks_1d(y32)
         cq, cs = mx_blocks_1d(np.ascontiguousarray(y32.T))

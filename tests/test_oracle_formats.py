@@ -184,3 +184,53 @@ def test_fp8_stage_small_by_hand(mode):
 def test_fp8_current_zero_tensor():
     r = oracle.quantize(np.zeros((2, 32), np.float32), "fp8_current")
     assert r["amax"] == 0 and r["scale"] == 1.0 and np.all(r["data"] == 0)
+
+
+# ------------------------------------------------------------- FP4 E2M1
+def test_e2m1_decode_golden():
+    for code, val in _read_sections("e2m1_codes.txt")["decode"]:
+        got = float(oracle.e2m1_decode(int(code, 16)))
+        want = _val(val)
+        assert got == want and math.copysign(1, got) == math.copysign(1, want), (code, got, want)
+
+
+def test_e2m1_encode_golden():
+    for val, code in _read_sections("e2m1_codes.txt")["encode"]:
+        got = int(oracle.e2m1_encode(np.float64(_val(val))))
+        assert got == int(code, 16), (val, hex(got), code)
+
+
+def _brute_force_e2m1(x):
+    """Nearest of the 8 magnitudes by exhaustive distance (ties -> the code
+    with mantissa bit 0), saturating at 6, sign from the sign bit."""
+    mags = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+    a = min(abs(x), 6.0)
+    best = min(range(8), key=lambda c: (abs(a - mags[c]), c % 2))
+    return best | (0x8 if math.copysign(1.0, x) < 0 else 0)
+
+
+def test_e2m1_encode_vs_brute_force():
+    rng = np.random.default_rng(3)
+    mags = oracle.e2m1_magnitudes()
+    mids = (mags[:-1] + mags[1:]) / 2
+    pts = [mags, mids, np.nextafter(mids, 0), np.nextafter(mids, 1e9), np.nextafter(mags, 1e9),
+           rng.uniform(0, 8, 3000), np.exp2(rng.uniform(-10, 5, 1000)), np.array([1e30, np.inf])]
+    v = np.concatenate(pts)
+    v = np.concatenate([v, -v])
+    want = np.array([_brute_force_e2m1(float(t)) for t in v], dtype=np.uint8)
+    assert np.array_equal(oracle.e2m1_encode(v), want)
+
+
+def test_e2m1_roundtrip_and_packing():
+    codes = np.arange(16, dtype=np.uint8)
+    dec = oracle.e2m1_decode(codes)
+    assert np.array_equal(oracle.e2m1_encode(dec), codes)    # -0 keeps 0x8
+    # element 2j in the low nibble: codes (1, 2) -> 0x21
+    assert oracle.e2m1_pack(np.array([1, 2], np.uint8))[0] == 0x21
+    rng = np.random.default_rng(4)
+    c = rng.integers(0, 16, (5, 64)).astype(np.uint8)
+    p = oracle.e2m1_pack(c)
+    assert p.shape == (5, 32)
+    assert np.array_equal(oracle.e2m1_unpack(p), c)
+    # byte j of a row is 16 * code[2j+1] + code[2j], by integer arithmetic
+    assert np.array_equal(p.astype(int), 16 * c[:, 1::2].astype(int) + c[:, 0::2].astype(int))

@@ -8,7 +8,13 @@ Pins (none of them re-runs the oracle's own formula):
 * central finite differences of L = sum(dz * y) for dx, dgamma, dbeta,
   plus sum_j dx_ij = 0 (LayerNorm) and sum_j dx_ij x_ij = 0 (RMSNorm, eps=0);
 * pure-Python loop re-derivations of the MXFP8 blocks (rowwise and the
-  transposed columnwise layout) on tiny inputs, with a brute-force E4M3.
+  transposed columnwise layout) on tiny inputs, with a brute-force E4M3;
+* NVFP4: a 4 x 16 tensor worked by hand (tests/golden/nvfp4_blocks.txt),
+  properties the scale construction forces (the block holding the tensor
+  amax gets the largest E4M3 scale, the largest element of a block with a
+  normal scale the largest E2M1 code, the dequantization error bound, exact
+  invariance under power-of-two scaling of the input, correct rounding of
+  the tensor scale) and a loop re-derivation with brute-force E2M1.
 """
 import math
 import os
@@ -381,3 +387,150 @@ def test_amax_history_update_matches_the_workload_scale():
     hist = w.amax_history
     h, s, _ = oracle.amax_history_update(hist, 1.0, w.scale)
     assert s == np.float32(np.float32(448.0) / np.max(hist[:-1]))
+
+
+# -------------------------------------------------------------- NVFP4 pins
+def _sections(name):
+    sec, out = None, {}
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            if line.startswith("["):
+                sec = line.strip("[]")
+                out[sec] = []
+            else:
+                out[sec].append(line.split())
+    return out
+
+
+def test_nvfp4_golden_by_hand():
+    g = _sections("nvfp4_blocks.txt")
+    y = np.array([[float(t) for t in r] for r in g["input"]], dtype=np.float32)
+    r = oracle.quantize(y, "nvfp4")
+    assert float(r["amax"]) == float(g["amax"][0][0])
+    assert float(r["scale"]) == float(g["scale"][0][0])
+    # scale_inv: 1/1536 correctly rounded to fp32 (within half an fp32 ulp)
+    assert abs(float(r["scale_inv"]) - 1.0 / 1536.0) <= 2.0 ** -24 * (1.0 / 1536.0)
+    assert [int(c) for c in r["row_scales"][:, 0]] == [int(t, 16) for t in g["row_scales"][0]]
+    want = np.array([[int(t, 16) for t in row] for row in g["data"]], dtype=np.uint8)
+    assert np.array_equal(r["data"], want)
+
+
+def _nvfp4_case(seed, N=48, H=128):
+    rng = np.random.default_rng(seed)
+    # blocks of very different magnitudes, some zero blocks, some outliers
+    y = rng.standard_normal((N, H)) * np.exp2(rng.integers(-12, 4, (N, H // 16)))[..., None].repeat(16, -1).reshape(N, H)
+    y[rng.random((N, H)) < 0.02] *= 40.0
+    y[:3, :16] = 0.0
+    return y.astype(np.float32)
+
+
+def test_nvfp4_scale_construction_properties():
+    y = _nvfp4_case(30)
+    N, H = y.shape
+    r = oracle.quantize(y, "nvfp4")
+    amax = float(np.max(np.abs(y)))
+    assert float(r["amax"]) == amax
+    S = float(r["scale"])
+    assert abs(S - 2688.0 / amax) <= 2.0 ** -24 * (2688.0 / amax)        # one correct rounding
+    sc = r["row_scales"]
+    assert sc.shape == (N, H // 16) and r["data"].shape == (N, H // 2)
+    codes = oracle.e2m1_unpack(r["data"]).reshape(N, H // 16, 16)
+    yb = y.astype(np.float64).reshape(N, H // 16, 16)
+    A = np.abs(yb).max(axis=-1)
+    # the block that holds the tensor amax: A * S / 6 = 448 -> the top scale
+    i, j = np.unravel_index(np.argmax(A), A.shape)
+    assert sc[i, j] == 0x7E
+    # scale codes are non-negative; zero blocks get scale 0 and codes 0
+    assert np.all(sc < 0x80)
+    zero = A == 0
+    assert np.all(sc[zero] == 0) and np.all(codes[zero] == 0)
+    v = oracle.e4m3_decode(sc)
+    # blocks with a normal E4M3 scale: the largest element maps to +-6
+    normal = v >= 2.0 ** -6
+    top = np.take_along_axis(codes, np.abs(yb).argmax(axis=-1)[..., None], -1)[..., 0]
+    assert np.all((top[normal] & 0x7) == 7)
+    # dequantization: value = E2M1 * v / S; the E2M1 grid's largest half-step
+    # is 1 (between 4 and 6), and v <= (A * S / 6) * (1 + 2**-4) for normal v
+    deq = oracle.e2m1_decode(codes) * (v / S)[..., None]
+    err = np.abs(deq - yb)
+    bound = (A * 1.0625 / 6.0)[..., None] * (1 + 1e-6) + 1e-30
+    assert np.all(err[normal] <= bound[normal])
+    # signs: a nonzero code carries the sign of its element
+    nz = (codes & 0x7) != 0
+    assert np.all(((codes & 0x8) != 0)[nz] == (yb < 0)[nz])
+
+
+def test_nvfp4_power_of_two_invariance():
+    """Scaling the tensor by 2**j scales S by 2**-j exactly and leaves every
+    code unchanged (all products shift exponent only), barring underflow."""
+    y = _nvfp4_case(31)
+    r0 = oracle.quantize(y, "nvfp4")
+    for j in (-20, -3, 5, 30):
+        r = oracle.quantize((y * np.float32(2.0 ** j)).astype(np.float32), "nvfp4")
+        assert float(r["scale"]) == float(r0["scale"]) * 2.0 ** -j
+        assert np.array_equal(r["row_scales"], r0["row_scales"])
+        assert np.array_equal(r["data"], r0["data"])
+
+
+def test_nvfp4_zero_and_tiny_tensors():
+    r = oracle.quantize(np.zeros((2, 32), np.float32), "nvfp4")
+    assert float(r["amax"]) == 0 and float(r["scale"]) == 1.0 and float(r["scale_inv"]) == 1.0
+    assert not r["data"].any() and not r["row_scales"].any()
+    # amax = 2**-140 (fp32 subnormal): 2688 / amax overflows fp32 -> capped
+    y = np.zeros((1, 16), np.float32)
+    y[0, 3] = np.float32(2.0 ** -140)
+    r = oracle.quantize(y, "nvfp4")
+    assert float(r["scale"]) == float(np.finfo(np.float32).max)
+
+
+def _loop_nvfp4(y):
+    """Row by row, block by block, element by element with fp32 scalars, a
+    brute-force E4M3 for the scale and a brute-force E2M1 for the elements."""
+    mags = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+    amax = np.float32(max(abs(float(t)) for t in y.ravel()))
+    S = np.float32(1.0) if amax == 0 else np.float32(np.float32(2688.0) / amax)
+    k = np.float32(S / np.float32(6.0))
+    N, H = y.shape
+    scales = np.zeros((N, H // 16), np.uint8)
+    codes = np.zeros((N, H), np.uint8)
+    for i in range(N):
+        for b in range(H // 16):
+            blk = y[i, 16 * b:16 * b + 16]
+            A = np.float32(max(abs(float(t)) for t in blk))
+            c = _bf_e4m3(float(np.float32(A * k)))
+            scales[i, b] = c
+            vv = np.float32(oracle.e4m3_decode(np.uint8(c)))
+            e = np.float32(0.0) if vv == 0 else np.float32(S / vv)
+            for t in range(16):
+                p = float(np.float32(blk[t] * e))
+                a = min(abs(p), 6.0)
+                m = min(range(8), key=lambda q: (abs(a - mags[q]), q % 2))
+                codes[i, 16 * b + t] = m | (8 if math.copysign(1.0, p) < 0 else 0)
+    packed = np.zeros((N, H // 2), np.uint8)
+    for i in range(N):
+        for jj in range(H // 2):
+            packed[i, jj] = codes[i, 2 * jj] + 16 * codes[i, 2 * jj + 1]
+    return packed, scales
+
+
+def test_nvfp4_by_loops():
+    y = _nvfp4_case(32, N=6, H=64)
+    r = oracle.quantize(y, "nvfp4")
+    packed, scales = _loop_nvfp4(y)
+    assert np.array_equal(r["row_scales"], scales)
+    assert np.array_equal(r["data"], packed)
+
+
+def test_nvfp4_fused_forward_is_norm_then_quantize():
+    """The NVFP4 forward quantizes fp32(y) of the same norm with the tensor
+    amax of that y (the norm+amax then quantize path)."""
+    w = rn_inputs.make("rms_current", N=8, H=256)
+    x = w.x_f64()
+    res = oracle.rmsnorm_fwd(x, w.gamma, w.eps, False, "nvfp4")
+    y32 = res["y"].astype(np.float32)
+    assert float(res["amax"]) == float(np.max(np.abs(y32)))
+    packed, scales = _loop_nvfp4(y32)
+    assert np.array_equal(res["data"], packed) and np.array_equal(res["row_scales"], scales)
