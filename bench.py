@@ -72,6 +72,8 @@ def algorithmic_bytes(kind, N, H, esz, ln, extra=None):
         return E * esz + E * 1 + vec + stats
     if kind == "fwd_fp8_current":            # x read twice (amax pass, quantize pass)
         return 2 * E * esz + E * 1 + vec + 2 * stats
+    if kind == "fwd_nvfp4":                  # x read twice; E2M1 codes (half a byte) and scales out
+        return 2 * E * esz + E // 2 + E // 16 + vec + 2 * stats
     if kind == "fwd_mxfp8":                  # x in, row + col codes and scales out
         return E * esz + 2 * E + 2 * (E // 32) + vec + stats
     if kind == "bwd":                        # dz, x in, dx out, dgamma (+dbeta) out
@@ -209,6 +211,13 @@ class Prepared:
             o.data, o.scale_out, o.scale_inv, o.amax = (data.data_ptr(), sc.data_ptr(),
                                                         sinv.data_ptr(), amax.data_ptr())
             keep = [data, sc, sinv, amax]
+        elif mode == "nvfp4":
+            d = torch.empty((N, H // 2), dtype=torch.uint8, device="cuda")
+            rsc = torch.empty((N, H // 16), dtype=torch.uint8, device="cuda")
+            sc, sinv, amax = (torch.empty(1, dtype=torch.float32, device="cuda") for _ in range(3))
+            o.data, o.row_scales, o.scale_out, o.scale_inv, o.amax = (
+                d.data_ptr(), rsc.data_ptr(), sc.data_ptr(), sinv.data_ptr(), amax.data_ptr())
+            keep = [d, rsc, sc, sinv, amax]
         elif mode == "mxfp8":
             d = torch.empty((N, H), dtype=torch.uint8, device="cuda")
             rsc = torch.empty((N, H // 32), dtype=torch.uint8, device="cuda")
@@ -511,7 +520,10 @@ def run_other_workloads(torch, rn, lib, rn_inputs, flush, peak, steps, warmup, o
         P = Prepared(rn, torch, w, ln=False)
         t = time_calls(torch, lib, [("cur", P.fwd_args("fp8_current"))], steps, warmup, flush)
         report("rms_16384x8192_fwd_fp8_current", "fwd_fp8_current", w.N, w.H, 2, False,
-               statistics.mean(t["cur"]), 2)
+               statistics.mean(t["cur"]), 3)
+        t = time_calls(torch, lib, [("nv", P.fwd_args("nvfp4"))], steps, warmup, flush)
+        report("rms_16384x8192_fwd_nvfp4", "fwd_nvfp4", w.N, w.H, 2, False,
+               statistics.mean(t["nv"]), 3)
         del P, w
     if want("mxfp8"):
         w = rn_inputs.make("mxfp8")

@@ -1,12 +1,13 @@
 /*
  * rn.h — C ABI of a GB300 (sm_103a) library of fused LayerNorm / RMSNorm
- * kernels with FP8 (E4M3) and MXFP8 output quantization.
+ * kernels with FP8 (E4M3), MXFP8 and NVFP4 output quantization.
  *
  * What is computed follows the page "Implementation:NVIDIA TransformerEngine
  * PyTorch Ext Normalization": forward functions normalize each row of x and
  * optionally quantize the output, choosing between an unfused path, a fully
  * fused kernel (delayed-scaling FP8, MXFP8) and a norm+amax-then-quantize
- * path (current-scaling FP8) (section "Description"); they return the output,
+ * path (current-scaling FP8, and the same for NVFP4) (section "Description");
+ * they return the output,
  * mu (LayerNorm only) and rsigma (section "I/O Contract"); backward functions
  * return dx, dgamma and dbeta; gamma may be zero-centered; sm_margin leaves
  * SMs free; calls that need scratch memory follow a two-step protocol (query
@@ -24,7 +25,18 @@
  *   MXFP8        per block of 32 (1x32 along rows and 32x1 down columns):
  *                e = floor(log2(max|y32|)) - 8 clamped to [-127,127], stored
  *                as the E8M0 byte e+127; code = E4M3(y32 * 2^-e)
+ *   NVFP4        (the page names the path only; NVIDIA's published NVFP4
+ *                layout is taken): amax = max|y32|, S = 448*6/amax (fp32
+ *                division, capped at the largest finite fp32; 1 if amax ==
+ *                0); per block of 16 along a row A = max|y32|, scale code
+ *                sc = E4M3(fp32(A * fp32(S/6))), element code
+ *                E2M1(fp32(y32 * fp32(S / value(sc)))) (0 when value(sc)
+ *                == 0); x is read twice as for FP8_CURRENT.  The value an
+ *                element stands for is E2M1 value * value(sc) / S.
  *   E4M3 conversion: round to nearest even, saturate to +-448, NaN -> 0x7F.
+ *   E2M1 conversion: round to nearest even, saturate to +-6; the sign bit
+ *                follows the input (negative values that round to 0 give
+ *                0x8).  NVFP4 output of non-finite inputs is unspecified.
  *
  * Conventions for every entry point:
  *   - All tensor arguments are DEVICE pointers, row-major, owned by the
@@ -35,9 +47,9 @@
  *   - x is [N, H]; gamma, beta are fp32 [H]; mu, rsigma are fp32 [N].
  *   - Pointers must be 16-byte aligned; H must be a multiple of 8 for bf16
  *     and of 4 for fp32.  MXFP8 additionally needs H % 32 == 0 and
- *     N % 32 == 0.  Violations return RN_ERR_UNSUPPORTED (shape/alignment)
- *     or RN_ERR_INVALID (missing pointer, bad enum, negative size) before
- *     anything is launched.
+ *     N % 32 == 0; NVFP4 needs H % 16 == 0.  Violations return
+ *     RN_ERR_UNSUPPORTED (shape/alignment) or RN_ERR_INVALID (missing
+ *     pointer, bad enum, negative size) before anything is launched.
  *   - 0 <= sm_margin < number of SMs; the persistent grid uses
  *     (SMs - sm_margin) CTAs.  No result depends on sm_margin.
  *   - N == 0 is valid and launches nothing (the backward then writes zeros
@@ -59,7 +71,9 @@ typedef enum {
   RN_QUANT_NONE = 0,        /* unquantized output in out_dtype */
   RN_QUANT_FP8_DELAYED = 1, /* E4M3 with a caller-given scale */
   RN_QUANT_FP8_CURRENT = 2, /* E4M3 with scale = 448 / amax of this tensor */
-  RN_QUANT_MXFP8 = 3        /* E4M3 with E8M0 scales per 1x32 and 32x1 block */
+  RN_QUANT_MXFP8 = 3,       /* E4M3 with E8M0 scales per 1x32 and 32x1 block */
+  RN_QUANT_NVFP4 = 4        /* E2M1 with an E4M3 scale per 1x16 block and an
+                               fp32 tensor scale 448*6/amax */
 } rn_quant_mode;
 
 typedef enum { RN_BF16 = 0, RN_F32 = 1 } rn_dtype;
@@ -81,10 +95,15 @@ typedef enum {
  *   col_data    MXFP8: columnwise codes stored TRANSPOSED, uint8 [H, N]:
  *               col_data[j, i] is the code of y[i, j] in its 32x1 block.
  *   col_scales  MXFP8: E8M0 bytes [H, N/32] (scale of col_data[j, 32b:32b+32]).
+ *   NVFP4:      data = E2M1 codes packed two per byte, uint8 [N, H/2]
+ *               (byte j of row i: element 2j in bits 0-3, 2j+1 in bits
+ *               4-7); row_scales = E4M3 scale codes [N, H/16] (scale of
+ *               elements 16b .. 16b+15 of a row); scale_out = S;
+ *               scale_inv = fp32(1/S); amax as for FP8_CURRENT.
  *   scale       FP8_DELAYED: input, device fp32 scalar.
  *   scale_out   FP8_CURRENT: output, device fp32 scalar (448 / amax).
- *   scale_inv   FP8_*: output, device fp32 scalar 1/scale (IEEE division).
- *   amax        FP8_*: output, device fp32 scalar max|y32|; the library
+ *   scale_inv   FP8_*, NVFP4: output, device fp32 scalar 1/scale (IEEE division).
+ *   amax        FP8_*, NVFP4: output, device fp32 scalar max|y32|; the library
  *               zeroes it on `stream` before reducing into it.
  *   out_dtype   NONE only: RN_BF16 or RN_F32 (fp32 returns y32 itself).
  * MXFP8 may skip either direction: data == NULL skips the rowwise output
@@ -136,8 +155,8 @@ rn_status rn_rmsnorm_fwd(const void* x, rn_dtype x_dtype, const float* gamma,
  *   then exactly rn_layernorm_fwd / rn_rmsnorm_fwd of h (mu, rsigma, output
  *   per `mode`).
  * x, residual, residual_out: [N, H] in `dtype`, 16-byte aligned;
- * residual_out may not alias x or residual.  Modes NONE, FP8_DELAYED and
- * FP8_CURRENT (its second pass reads residual_out); MXFP8 returns
+ * residual_out may not alias x or residual.  Modes NONE, FP8_DELAYED,
+ * FP8_CURRENT and NVFP4 (their second pass reads residual_out); MXFP8 returns
  * RN_ERR_UNSUPPORTED.  Other arguments, errors and conventions as in the
  * plain forward.
  */
@@ -239,7 +258,7 @@ rn_status rn_delayed_scaling_update(float* amax_history, int64_t history_len,
  * Quantization stage alone on caller-given fp32 values y [N, H] (the
  * page's UNFUSED path: norm, then a separate quantize).  Same output
  * descriptor and arithmetic as the fused forward for `mode`
- * (FP8_DELAYED, FP8_CURRENT or MXFP8); lets the quantizer be checked bit
+ * (FP8_DELAYED, FP8_CURRENT, MXFP8 or NVFP4); lets the quantizer be checked bit
  * for bit on arbitrary fp32 inputs.
  */
 rn_status rn_quantize_only(const float* y, int64_t N, int64_t H,

@@ -1,4 +1,4 @@
-"""GB300 fused LayerNorm / RMSNorm with FP8 and MXFP8 output.
+"""GB300 fused LayerNorm / RMSNorm with FP8, MXFP8 and NVFP4 output.
 
 Thin Python binding over the C ABI in ``include/rn.h`` (``librn.so``, built
 in-tree by ``_build.build()``).  This module only marshals arguments: it
@@ -19,7 +19,8 @@ PyTorch Ext Normalization" (section "Signature"):
         -> (dx, dgamma)
 
 ``quant`` is one of "none", "fp8_delayed" (needs ``scale``), "fp8_current",
-"mxfp8"; the page's quantizer object becomes this string plus the scale.
+"mxfp8", "nvfp4"; the page's quantizer object becomes this string plus the
+scale.
 """
 from __future__ import annotations
 
@@ -32,13 +33,14 @@ import torch
 __all__ = [
     "layernorm_fwd", "rmsnorm_fwd", "layernorm_bwd", "rmsnorm_bwd", "quantize_only",
     "layernorm_bwd_noalloc", "layernorm_add_fwd", "rmsnorm_add_fwd", "delayed_scaling_update",
-    "bwd_workspace_bytes", "device_error", "Fp8Output", "MXFP8Output", "lib_path", "RNError",
+    "bwd_workspace_bytes", "device_error", "Fp8Output", "MXFP8Output", "NVFP4Output", "lib_path",
+    "RNError",
     "QUANT_MODES",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_HERE, "librn.so")
-QUANT_MODES = {"none": 0, "fp8_delayed": 1, "fp8_current": 2, "mxfp8": 3}
+QUANT_MODES = {"none": 0, "fp8_delayed": 1, "fp8_current": 2, "mxfp8": 3, "nvfp4": 4}
 _BF16, _F32 = 0, 1
 
 
@@ -152,6 +154,16 @@ class MXFP8Output:
     col_scales: torch.Tensor | None  # uint8 [H, N/32]
 
 
+@dataclass
+class NVFP4Output:
+    """NVFP4: E2M1 codes with an E4M3 scale per 1x16 block and a tensor scale."""
+    data: torch.Tensor        # uint8 [N, H/2], two codes per byte (even element low)
+    row_scales: torch.Tensor  # uint8 [N, H/16] E4M3 block-scale codes
+    scale: torch.Tensor       # fp32 [1] S = 448 * 6 / amax
+    scale_inv: torch.Tensor   # fp32 [1] 1 / S
+    amax: torch.Tensor        # fp32 [1]
+
+
 def _make_output(x, quant, out_dtype, scale, rowwise=True, colwise=True):
     N, H = x.shape
     dev = x.device
@@ -192,6 +204,17 @@ def _make_output(x, quant, out_dtype, scale, rowwise=True, colwise=True):
             res.col_scales = torch.empty((H, N // 32), dtype=torch.uint8, device=dev)
             o.col_data = res.col_data.data_ptr()
             o.col_scales = res.col_scales.data_ptr()
+        return o, res
+    if quant == "nvfp4":
+        f32 = dict(dtype=torch.float32, device=dev)
+        res = NVFP4Output(torch.empty((N, H // 2), dtype=torch.uint8, device=dev),
+                          torch.empty((N, H // 16), dtype=torch.uint8, device=dev),
+                          torch.empty(1, **f32), torch.empty(1, **f32), torch.empty(1, **f32))
+        o.data = res.data.data_ptr()
+        o.row_scales = res.row_scales.data_ptr()
+        o.scale_out = res.scale.data_ptr()
+        o.scale_inv = res.scale_inv.data_ptr()
+        o.amax = res.amax.data_ptr()
         return o, res
     raise RNError(f"unknown quant mode {quant!r}")
 

@@ -136,7 +136,7 @@ struct FwdPlan {
 int fwd_max_threads(int nc) { return nc >= 16 ? 512 : (nc >= 8 ? 768 : 1024); }
 
 rn_status plan_fwd(int nk, int H, int esz, int N, int sm_margin, const DeviceInfo& di,
-                   FwdPlan* pl, int rows_per_slot = 1) {
+                   FwdPlan* pl, int rows_per_slot = 1, size_t extra_bytes = 0) {
   const int nchunks = H * esz / 16;
   FwdShape sh{1, 16, false};
   while (sh.g <= 8 && nchunks > 32 * sh.g * 16) sh.g *= 2;
@@ -149,7 +149,8 @@ rn_status plan_fwd(int nk, int H, int esz, int N, int sm_margin, const DeviceInf
       (nk != kIdentity && g <= 2) ? (size_t)H * sizeof(float) * (nk == kLn ? 2 : 1) : 0;
   // fixed: gamma/beta, group exchange (14 groups x 4 x 8 floats), amax words
   // (32), slack; per slot: the row, (mu, rsigma), two mbarriers
-  const size_t fixed = gb + 14 * 4 * 8 * sizeof(float) + 32 * sizeof(uint32_t) + 64;
+  // (+ extra_bytes after the barriers: the NVFP4 factor table)
+  const size_t fixed = gb + 14 * 4 * 8 * sizeof(float) + 32 * sizeof(uint32_t) + 64 + extra_bytes;
   // (with a residual add a slot holds the x row and the residual row)
   const size_t per_slot = (size_t)rows_per_slot * H * esz + sizeof(float2) + 16;
   const size_t budget = cta_smem_budget(di, 1);
@@ -260,6 +261,10 @@ rn_status check_out(rn_quant_mode mode, const rn_output* o, int64_t N, int64_t H
     if (mode == RN_QUANT_NONE)
       return (o->out_dtype == RN_BF16 || o->out_dtype == RN_F32) ? RN_OK : RN_ERR_INVALID;
     if (mode == RN_QUANT_MXFP8) return (H % 32 == 0) ? RN_OK : RN_ERR_UNSUPPORTED;
+    if (mode == RN_QUANT_NVFP4) {
+      if (!(o->scale_out && o->scale_inv && o->amax)) return RN_ERR_INVALID;
+      return (H % 16 == 0) ? RN_OK : RN_ERR_UNSUPPORTED;
+    }
     return RN_ERR_INVALID;
   }
   switch (mode) {
@@ -285,6 +290,11 @@ rn_status check_out(rn_quant_mode mode, const rn_output* o, int64_t N, int64_t H
       if (colwise && !aligned(o->col_data, 16)) return RN_ERR_UNSUPPORTED;
       break;
     }
+    case RN_QUANT_NVFP4:
+      if (!out_fields_only(o, true, true, false, false, false, true, true, true))
+        return RN_ERR_INVALID;
+      if (H % 16 != 0) return RN_ERR_UNSUPPORTED;
+      break;
     default:
       return RN_ERR_INVALID;
   }
@@ -404,6 +414,23 @@ rn_status fwd_common(int nk, const void* x, rn_dtype dt, const float* gamma, con
       q.Q = p2.Q;
       q.reverse = 1;
       return launch_fwd(nk, bf16, p2.sh, kQCurQuant, q, p2.l, true, stream);
+    }
+    case RN_QUANT_NVFP4: {
+      // the same two passes; pass 2 needs room for its factor table
+      if ((st = launch_fwd_init(out->amax, nullptr, nullptr, stream)) != RN_OK) return st;
+      if ((st = first(kQCurAmax, true)) != RN_OK) return st;
+      FwdPlan p2;
+      if ((st = plan_fwd(nk, (int)H, esz, (int)N, sm_margin, di, &p2, 1, kNvTableBytes)) != RN_OK)
+        return st;
+      FwdParams q = p;
+      if (res) q.x = residual_out;
+      q.residual = nullptr;
+      q.residual_out = nullptr;
+      q.scales = out->row_scales;
+      q.workers = p2.workers;
+      q.Q = p2.Q;
+      q.reverse = 1;
+      return launch_fwd(nk, bf16, p2.sh, kQNvfp4, q, p2.l, true, stream);
     }
     default:
       return RN_ERR_INVALID;
@@ -598,7 +625,8 @@ rn_status rn_delayed_scaling_update(float* amax_history, int64_t history_len, co
 
 rn_status rn_quantize_only(const float* y, int64_t N, int64_t H, rn_quant_mode mode,
                            const rn_output* out, void* stream) {
-  if (mode != RN_QUANT_FP8_DELAYED && mode != RN_QUANT_FP8_CURRENT && mode != RN_QUANT_MXFP8)
+  if (mode != RN_QUANT_FP8_DELAYED && mode != RN_QUANT_FP8_CURRENT && mode != RN_QUANT_MXFP8 &&
+      mode != RN_QUANT_NVFP4)
     return RN_ERR_INVALID;
   return fwd_common(kIdentity, y, RN_F32, nullptr, nullptr, N, H, 0.0f, 0, 0, mode, out, nullptr,
                     nullptr, static_cast<cudaStream_t>(stream));

@@ -42,6 +42,12 @@
 // output) and pass 2 (quantize with 448/amax from the saved mu / rsigma), the
 // second launched as a programmatic dependent of the first and walking the
 // rows backwards so that it starts on the rows pass 1 left in L2.
+// NVFP4 output takes the same two passes; its pass 2 quantizes each run of 16
+// elements of a row (the chunks of two adjacent lanes for bf16, four for
+// fp32) with one E4M3 scale: the lanes of a block exchange their maxima with
+// shuffles, convert A * S/6 to E4M3, look the element factor S / value(code)
+// up in a 128-entry shared-memory table built once per CTA, and convert
+// y * factor to E2M1 codes, two per byte.
 #include <cuda_runtime.h>
 
 #include "rn_device.cuh"
@@ -114,6 +120,44 @@ __device__ __forceinline__ void store_chunk(unsigned char* o, int out_f32, const
   }
 }
 
+// value of a non-negative E4M3 code (0..0x7F), exact (through f16)
+__device__ __forceinline__ float e4m3_code_value(uint32_t code) {
+  uint32_t h2;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"((unsigned short)code));
+  float f;
+  asm("cvt.f32.f16 %0, %1;" : "=f"(f) : "h"((unsigned short)(h2 & 0xFFFFu)));
+  return f;
+}
+
+// E2M1 codes of 2 * PAIRS values (round to nearest even, saturating at 6),
+// element 0 in the low nibble; PAIRS = 4 fills a word, PAIRS = 2 its low half
+template <int PAIRS>
+__device__ __forceinline__ uint32_t pack_e2m1(const float2* q) {
+  uint32_t r;
+  if constexpr (PAIRS == 4) {
+    // (the first source of the conversion lands in the high nibble)
+    asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b1, %4, %3;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b2, %6, %5;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b3, %8, %7;\n\t"
+        "mov.b32 %0, {b0, b1, b2, b3};\n\t}"
+        : "=r"(r)
+        : "f"(q[0].x), "f"(q[0].y), "f"(q[1].x), "f"(q[1].y), "f"(q[2].x), "f"(q[2].y),
+          "f"(q[3].x), "f"(q[3].y));
+  } else {
+    unsigned short h;
+    asm("{\n\t.reg .b8 b0, b1;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b1, %4, %3;\n\t"
+        "mov.b16 %0, {b0, b1};\n\t}"
+        : "=h"(h)
+        : "f"(q[0].x), "f"(q[0].y), "f"(q[1].x), "f"(q[1].y));
+    r = h;
+  }
+  return r;
+}
+
 // The rows of this CTA: b, b + g, b + 2g, ... (b = blockIdx.x, g = gridDim.x),
 // from the last one when reverse.
 struct RowSeq {
@@ -158,9 +202,11 @@ __global__ void __launch_bounds__(max_threads<NC>(), 1) rn_fwd_kernel(const FwdP
   constexpr int F4 = VEC / 4;  // float4 of gamma per chunk
   constexpr bool LN = (NK == kLn);
   constexpr bool NORM = (NK != kIdentity);
-  // pass 2 of current scaling gets mu / rsigma with each row
-  constexpr bool META = (QM == kQCurQuant && NORM);
-  constexpr bool STATS = (QM != kQCurQuant && NORM);
+  constexpr bool NV = (QM == kQNvfp4);
+  // pass 2 of current scaling / NVFP4 gets mu / rsigma with each row
+  constexpr bool PASS2 = (QM == kQCurQuant || NV);
+  constexpr bool META = (PASS2 && NORM);
+  constexpr bool STATS = (!PASS2 && NORM);
   constexpr bool AMAX = (QM == kQDelayed || QM == kQCurAmax);
   constexpr bool GB_SMEM = NORM && G <= 2;
   extern __shared__ __align__(128) unsigned char smem[];
@@ -181,6 +227,7 @@ __global__ void __launch_bounds__(max_threads<NC>(), 1) rn_fwd_kernel(const FwdP
   uint32_t* red2 = reinterpret_cast<uint32_t*>(red + kMaxGroups * 4 * 8);  // [32]
   uint64_t* full = reinterpret_cast<uint64_t*>(red2 + 32);                  // row landed
   uint64_t* empty = full + Q;                                               // row read out
+  float* nv_tbl = reinterpret_cast<float*>(empty + Q);  // NVFP4: [128] S / value(code)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -264,7 +311,8 @@ __global__ void __launch_bounds__(max_threads<NC>(), 1) rn_fwd_kernel(const FwdP
   asm volatile("mov.b32 %0, %1;" : "=r"(nvalid_apply) : "r"(nvalid));
   const float inv_h = 1.0f / (float)H;
   const int oesz = (QM == kQNone) ? (p.out_f32 ? 4 : 2) : 1;  // output bytes per element
-  const size_t ostep = (size_t)CSTEP * VEC * oesz;              // output bytes from k to k + 1
+  // output bytes from k to k + 1 (NVFP4: half a byte per element)
+  const size_t ostep = NV ? (size_t)CSTEP * VEC / 2 : (size_t)CSTEP * VEC * oesz;
 
   float scale = 1.0f;
   if constexpr (QM == kQDelayed) scale = *p.scale;
@@ -276,6 +324,21 @@ __global__ void __launch_bounds__(max_threads<NC>(), 1) rn_fwd_kernel(const FwdP
       *p.scale_out = scale;
       *p.scale_inv = __fdiv_rn(1.0f, scale);
     }
+  }
+  float kq = 0.0f;  // NVFP4: S / 6
+  if constexpr (NV) {
+    pdl_wait();  // amax comes from pass 1
+    const float am = *p.amax;
+    float S = (am == 0.0f) ? 1.0f : __fdiv_rn(2688.0f, am);  // 448 * 6 / amax
+    if (S > 3.402823466e38f) S = 3.402823466e38f;             // (NaN passes through)
+    kq = __fdiv_rn(S, 6.0f);
+    for (int c = threadIdx.x; c < 128; c += 32 * W)
+      nv_tbl[c] = (c == 0) ? 0.0f : __fdiv_rn(S, e4m3_code_value((uint32_t)c));
+    if (blockIdx.x == 0 && threadIdx.x == 0) {
+      *p.scale_out = S;
+      *p.scale_inv = __fdiv_rn(1.0f, S);
+    }
+    named_sync(kBarWorkers, 32 * W);
   }
   float ymax = 0.0f, ymin = 0.0f;  // amax = max(ymax, -ymin)
 
@@ -358,10 +421,16 @@ __global__ void __launch_bounds__(max_threads<NC>(), 1) rn_fwd_kernel(const FwdP
     }
 
     unsigned char* orow =
-        static_cast<unsigned char*>(p.out) + ((size_t)r * H + (size_t)cbase * VEC) * oesz;
+        NV ? static_cast<unsigned char*>(p.out) + ((size_t)r * H + (size_t)cbase * VEC) / 2
+           : static_cast<unsigned char*>(p.out) + ((size_t)r * H + (size_t)cbase * VEC) * oesz;
+    // NVFP4 block scales: one byte per 16 elements, written by the block's
+    // first lane
+    uint8_t* srow = NV ? p.scales + ((size_t)r * H + (size_t)cbase * VEC) / 16 : nullptr;
     const float2 rs2 = splat2(rs);
 #pragma unroll
     for (int k = 0; k < NC; ++k) {
+      float2 y[PAIRS];
+      float bm = 0.0f;  // NVFP4: max |y| of this lane's chunk
       if (k < nvalid_apply) {
         const int c = cbase + k * CSTEP;
         float4 gv[F4], bv[F4];
@@ -381,7 +450,6 @@ __global__ void __launch_bounds__(max_threads<NC>(), 1) rn_fwd_kernel(const FwdP
             }
           }
         }
-        float2 y[PAIRS];
 #pragma unroll
         for (int j = 0; j < PAIRS; ++j) {
           if constexpr (NORM) {
@@ -404,9 +472,31 @@ __global__ void __launch_bounds__(max_threads<NC>(), 1) rn_fwd_kernel(const FwdP
             ymax = max3(ymax, y[j]);
             ymin = min3(ymin, y[j]);
           }
+          if constexpr (NV) bm = fmaxf(bm, fmaxf(fabsf(y[j].x), fabsf(y[j].y)));
         }
-        if constexpr (QM != kQCurAmax)
+        if constexpr (QM != kQCurAmax && !NV)
           store_chunk<PAIRS, QM>(orow + (size_t)k * ostep, p.out_f32, y, scale);
+      }
+      if constexpr (NV) {
+        // a block of 16 elements spans 16 / VEC adjacent lanes (all of them
+        // valid or none, since H % 16 == 0); every lane takes part in the
+        // exchange
+        bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 1));
+        if constexpr (VEC == 4) bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 2));
+        if (k < nvalid_apply) {
+          const uint32_t sc = pack_e4m3x2(__fmul_rn(bm, kq), 0.0f) & 0x7Fu;
+          const float2 e2 = splat2(nv_tbl[sc]);
+          float2 q[PAIRS];
+#pragma unroll
+          for (int j = 0; j < PAIRS; ++j) q[j] = mul2(y[j], e2);
+          const uint32_t codes = pack_e2m1<PAIRS>(q);
+          unsigned char* o = orow + (size_t)k * ostep;
+          if constexpr (PAIRS == 4)
+            *reinterpret_cast<uint32_t*>(o) = codes;
+          else
+            *reinterpret_cast<unsigned short*>(o) = (unsigned short)codes;
+          if ((lane & (16 / VEC - 1)) == 0) srow[(size_t)k * (CSTEP * VEC / 16)] = (uint8_t)sc;
+        }
       }
     }
   }
@@ -488,6 +578,7 @@ rn_status launch_q(const FwdShape& sh, int qmode, const FwdParams& p, const Laun
     // (with a residual, current scaling's pass 2 reads the stored sum as
     // its x: the plain kernel)
     case kQCurQuant: return launch_shape<TIn, NK, kQCurQuant>(sh, p, l, pdl, s);
+    case kQNvfp4: return launch_shape<TIn, NK, kQNvfp4>(sh, p, l, pdl, s);
 #endif
     default: return RN_ERR_INVALID;
   }

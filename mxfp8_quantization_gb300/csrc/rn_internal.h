@@ -20,19 +20,26 @@ enum FwdQuant : int {
   kQDelayed = 1,    // E4M3 with a given scale, + amax
   kQCurAmax = 2,    // current scaling, pass 1: statistics + amax, no output
   kQCurQuant = 3,   // current scaling, pass 2: quantize with 448/amax
+  kQNvfp4 = 4,      // NVFP4, pass 2 (pass 1 is kQCurAmax): E2M1 codes with an
+                    // E4M3 scale per 16 elements and S = 448*6/amax
 };
+
+// NVFP4 pass 2 keeps a table of the 128 element factors S / value(scale
+// code) in shared memory
+constexpr int kNvTableBytes = 128 * 4;
 
 struct FwdParams {
   const void* x;
   const float* gamma;   // 16-byte aligned
   const float* beta;
-  void* out;            // [N, H] (bf16/fp32 or E4M3 codes)
+  void* out;            // [N, H] (bf16/fp32 or E4M3 codes); NVFP4: [N, H/2]
+  uint8_t* scales;      // NVFP4: E4M3 block-scale codes [N, H/16]
   float* mu;            // LayerNorm: written (pass 1) or read (kQCurQuant)
   float* rsigma;
   const float* scale;   // kQDelayed
   float* amax;          // kQDelayed, kQCurAmax: reduced into; kQCurQuant: read
-  float* scale_inv;     // kQCurQuant (kQDelayed: written by the init kernel)
-  float* scale_out;     // kQCurQuant
+  float* scale_inv;     // kQCurQuant, kQNvfp4 (kQDelayed: written by the init kernel)
+  float* scale_out;     // kQCurQuant, kQNvfp4
   int N, H;
   float eps;
   int zcg;              // zero-centered gamma

@@ -19,6 +19,10 @@ the reading is given here and in the design notes):
 * MXFP8 E8M0 codes: equal, except where the oracle's block maximum lies
   within 1e-6 * (block max of w) of a power of two; such blocks are checked
   only for their exponent being one of the two neighbours.
+* NVFP4: the tensor scale within 1e-5 relative; E4M3 block-scale codes and
+  E2M1 element codes equal except one-step misses at rounding boundaries,
+  with the FP8 windows carried through the block and element factors (see
+  ``check_nvfp4``); bit-exact in the stand-alone quantizer.
 * amax (fused): |amax_gpu - amax_ref| <= 1e-6 * max(w); bit-exact in the
   stand-alone quantizer (identical inputs).
 * dx: fp32 |dx - ref| <= 2e-3 * max(|ref|, rms_row(ref)); bf16 within one bf16
@@ -135,3 +139,66 @@ def check_mx(gpu_q, gpu_s, y32_ref, w, what):
     p = y32_ref.astype(np.float64) * inv
     win = 1e-6 * w * inv
     return check_fp8_codes(gpu_q[same], ref_q[same], p[same], win[same], what)
+
+
+# ------------------------------------------------------------------ NVFP4
+# E2M1 rounding boundaries in |p|: 0 (sign) and the midpoints of 0, .5, 1,
+# 1.5, 2, 3, 4, 6
+_E2M1_BOUNDS = np.array([0.0, 0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0])
+
+
+def _ord4(codes):
+    c = codes.astype(np.int64)
+    mag = c & 0x7
+    return np.where(c & 0x8, -mag, mag)
+
+
+def _near_e2m1_boundary(p_abs, window):
+    d = np.min(np.abs(p_abs[..., None] - _E2M1_BOUNDS), axis=-1)
+    return d <= window
+
+
+def check_nvfp4(gpu_data, gpu_scales, y32_ref, w, S_ref, S_gpu, what, max_frac=1e-3):
+    """NVFP4 rowwise output ([n, H/2] packed codes, [n, H/16] scale codes)
+    against the oracle's quantization of its own y32 with its own tensor
+    scale S_ref.
+
+    * |S_gpu / S_ref - 1| <= 1e-5 (the amax tolerance, read through S);
+    * block-scale codes equal, except one E4M3 step where the oracle's
+      A * S/6 lies within 1e-6 * (block max of w) * S/6, widened by the
+      relative difference of the two tensor scales, of a rounding boundary;
+    * in blocks whose scales agree, element codes equal, except one E2M1
+      step (or the sign of a zero) where p = y32 * S / v lies within
+      1e-6 * w * S / v (same widening) of an E2M1 rounding boundary;
+    * at most max_frac of the blocks / elements use an exemption.
+    """
+    y = np.asarray(y32_ref, np.float32)
+    n, h = y.shape
+    nb = h // 16
+    S_ref, S_gpu = float(S_ref), float(S_gpu)
+    rel = abs(S_gpu / S_ref - 1.0)
+    assert rel <= 1e-5, f"{what}: tensor scale {S_gpu} vs {S_ref}"
+    ref_q, ref_s = oracle.norm.nvfp4_blocks_1d(y, np.float32(S_ref))
+    k = float(np.float32(np.float32(S_ref) / np.float32(6.0)))
+    A = np.abs(y.astype(np.float64)).reshape(n, nb, 16).max(axis=2)
+    wb = np.asarray(w, np.float64).reshape(n, nb, 16).max(axis=2)
+    ps = A * k
+    check_fp8_codes(np.asarray(gpu_scales), ref_s, ps, 1e-6 * wb * k + 2.0 * rel * ps,
+                    what + " scales", max_frac)
+    same = np.asarray(gpu_scales) == ref_s
+    v = oracle.e4m3_decode(ref_s)
+    e = np.where(v == 0, 0.0, S_ref / np.where(v == 0, 1.0, v))
+    cg = oracle.e2m1_unpack(np.asarray(gpu_data, np.uint8)).reshape(n, nb, 16)[same]
+    cr = oracle.e2m1_unpack(ref_q).reshape(n, nb, 16)[same]
+    p = (y.astype(np.float64).reshape(n, nb, 16) * e[..., None])[same]
+    win = (1e-6 * np.asarray(w, np.float64).reshape(n, nb, 16) * e[..., None])[same] + 2.0 * rel * np.abs(p)
+    diff = cg != cr
+    nd = int(diff.sum())
+    if nd == 0:
+        return 0
+    step = np.abs(_ord4(cg[diff]) - _ord4(cr[diff]))
+    ok = (step <= 1) & _near_e2m1_boundary(np.abs(p[diff]), win[diff])
+    assert ok.all(), (f"{what}: {int((~ok).sum())} E2M1 mismatches not at a rounding boundary; "
+                      f"e.g. gpu={cg[diff][~ok][:5]} ref={cr[diff][~ok][:5]} p={p[diff][~ok][:5]}")
+    assert nd <= max_frac * cg.size, f"{what}: {nd} boundary mismatches"
+    return nd

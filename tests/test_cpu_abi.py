@@ -87,6 +87,27 @@ def test_forward_rejects_bad_arguments_on_host(lib):
     assert lib.rn_quantize_only(x, 4, 1024, 0, ctypes.byref(o), None) == 1
 
 
+def test_nvfp4_forward_rejects_bad_arguments_on_host(lib):
+    x = ctypes.c_void_p(0x1000)
+    g = ctypes.c_void_p(0x2000)
+    rs = ctypes.c_void_p(0x3000)
+    full = dict(data=0x5000, row_scales=0x6000, scale_out=0x7000, scale_inv=0x7010, amax=0x7020)
+    # every NVFP4 output is required; the FP8 / MX-only fields must be NULL
+    for drop in full:
+        o = _out(**{k: v for k, v in full.items() if k != drop})
+        assert lib.rn_rmsnorm_fwd(x, 0, g, 4, 1024, 1e-5, 0, 0, 4, ctypes.byref(o), rs, None) == 1, drop
+    for extra in ("col_data", "col_scales", "scale"):
+        o = _out(**full, **{extra: 0x8000})
+        assert lib.rn_rmsnorm_fwd(x, 0, g, 4, 1024, 1e-5, 0, 0, 4, ctypes.byref(o), rs, None) == 1, extra
+    # rows must hold whole 16-element blocks (H = 1032 is a valid bf16 row)
+    o = _out(**full)
+    assert lib.rn_rmsnorm_fwd(x, 0, g, 4, 1032, 1e-5, 0, 0, 4, ctypes.byref(o), rs, None) == 2
+    assert lib.rn_quantize_only(x, 4, 1028, 4, ctypes.byref(o), None) == 2
+    # misaligned packed output
+    o = _out(**dict(full, data=0x5008))
+    assert lib.rn_rmsnorm_fwd(x, 0, g, 4, 1024, 1e-5, 0, 0, 4, ctypes.byref(o), rs, None) == 2
+
+
 def test_backward_workspace_query_needs_no_device(lib):
     n = ctypes.c_size_t(0)
     # bf16 8192 x 4096: chunks of 8 rows -> 1024 partial rows of dgamma, dbeta
