@@ -12,7 +12,8 @@ import torch
 import mxfp8_quantization_gb300 as rn
 import oracle
 import rn_inputs
-from parity import (bf16_ulp, check_fp8_codes, check_mx, check_stats, term_magnitude)
+from parity import (bf16_ulp, check_fp8_codes, check_mx, check_nvfp4, check_stats,
+                    term_magnitude)
 from test_gpu_parity import bf16_bits, to_dev
 
 pytestmark = pytest.mark.gpu
@@ -95,6 +96,35 @@ def test_rms_current_16384x8192():
     p = (ref["y"].astype(np.float32) * np.float32(s_ref)).astype(np.float64)
     win = 1e-6 * s_ref * wt + np.abs(p) * abs(float(s_gpu) / s_ref - 1.0)
     check_fp8_codes(out.data.cpu().numpy()[rows], ref["data"], p, win, "rms fp8 current")
+
+
+def test_rms_nvfp4_16384x8192():
+    """The NVFP4 path on the current-scaling workload (the bench's NVFP4
+    line): tensor amax over every row, codes and block scales on sampled
+    rows."""
+    w = rn_inputs.make("rms_current")
+    x = to_dev(w.x, "bf16")
+    g = to_dev(w.gamma, "f32")
+    out, rs = rn.rmsnorm_fwd(x, g, w.eps, quant="nvfp4")
+    amax = np.float32(0.0)
+    wmax = 0.0
+    for r0 in range(0, w.N, 2048):
+        xb = w.x_f64(slice(r0, r0 + 2048))
+        f = oracle.rmsnorm_fwd(xb, w.gamma, w.eps, False, "none", "f32")
+        amax = max(amax, oracle.norm.tensor_amax(f["y"].astype(np.float32)))
+        wmax = max(wmax, float(term_magnitude(xb, None, f["rsigma"], w.gamma, None, False).max()))
+    am_gpu = np.float32(out.amax.item())
+    assert abs(float(am_gpu) - float(amax)) <= 1e-6 * wmax
+    S = np.float32(out.scale.item())
+    assert S == np.float32(2688.0) / am_gpu
+    assert np.float32(out.scale_inv.item()) == np.float32(1.0) / S
+    rows = _sample_rows(w.N, 400, seed=3)
+    xr = w.x_f64(rows)
+    ref = oracle.rmsnorm_fwd(xr, w.gamma, w.eps, False, "nvfp4", amax=amax)
+    check_stats(None, rs.cpu().numpy()[rows], xr, None, ref["rsigma"])
+    wt = term_magnitude(xr, None, ref["rsigma"], w.gamma, None, False)
+    check_nvfp4(out.data.cpu().numpy()[rows], out.row_scales.cpu().numpy()[rows],
+                ref["y"].astype(np.float32), wt, ref["scale"], S, "rms nvfp4 full")
 
 
 @pytest.mark.parametrize("ln", [True, False], ids=["ln", "rms"])
