@@ -167,6 +167,14 @@ FWD_CASES = [
     ("mxfp8", 96, None, True, "mxfp8"),
     ("mxfp8", 96, None, False, "mxfp8"),
     ("mxfp8", 64, 512, True, "mxfp8"),
+    # bf16 rows of 256 .. 2048 columns take the kernel that holds a 32-row
+    # tile in registers (every shape it has); other widths the ring kernel
+    ("mxfp8", 160, 256, False, "mxfp8"),
+    ("mxfp8", 96, 1024, True, "mxfp8"),
+    ("mxfp8", 96, 1024, False, "mxfp8"),
+    ("mxfp8", 64, 768, True, "mxfp8"),
+    ("mxfp8", 64, 800, False, "mxfp8"),
+    ("mxfp8", 32, 3072, True, "mxfp8"),
     ("bwd_f32", 67, 1024, True, "none"),
     ("bwd_f32", 67, 1024, False, "fp8_delayed"),
     ("bwd_f32", 64, 1024, True, "mxfp8"),
@@ -230,6 +238,22 @@ def test_forward_sm_margin_and_repeat_bit_identical():
     for o in (b, c):
         assert torch.equal(a[0].data, o[0].data) and torch.equal(a[0].amax, o[0].amax)
         assert np.array_equal(a[1], o[1]) and np.array_equal(a[2], o[2])
+
+
+@pytest.mark.parametrize("H", [256, 2048])
+def test_mxfp8_single_direction_and_margin(H):
+    """Rowwise-only and columnwise-only MXFP8 outputs equal the matching
+    halves of the two-direction call, for any sm_margin."""
+    w = rn_inputs.make("mxfp8", N=192, H=H)
+    both = _run_fwd(w, True, "mxfp8")
+    row = _run_fwd(w, True, "mxfp8", sm_margin=5, colwise=False)
+    col = _run_fwd(w, True, "mxfp8", sm_margin=100, rowwise=False)
+    assert row[0].col_data is None and col[0].data is None
+    assert torch.equal(both[0].data, row[0].data) and torch.equal(both[0].row_scales, row[0].row_scales)
+    assert torch.equal(both[0].col_data, col[0].col_data)
+    assert torch.equal(both[0].col_scales, col[0].col_scales)
+    for o in (row, col):
+        assert np.array_equal(both[1], o[1]) and np.array_equal(both[2], o[2])
 
 
 def test_forward_empty():
