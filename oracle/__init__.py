@@ -26,13 +26,15 @@ Module map:
   formats  E4M3 and E2M1 decode/encode, E8M0 shared exponents, bf16 rounding.
   norm     row statistics, affine apply, quantization stages, backward,
            residual add + norm, the delayed-scaling history step.
+  act      scaled SReLU / SwiGLU / clamped SwiGLU forward and backward (the
+           page "Activation + GroupedLinear Fusion for MOE ...").
 
 Parity status: every function here is pinned by CPU tests against closed
 forms, exact rational arithmetic, finite differences, brute force or
 hand-checked format values.  The pages print no worked example for any norm,
 so no pin comes from the pages themselves.
 """
-from . import formats, norm  # noqa: F401
+from . import act, formats, norm  # noqa: F401
 from .formats import (  # noqa: F401
     E4M3_MAX, e4m3_decode, e4m3_encode, e4m3_magnitudes, e8m0_from_amax,
     round_to_bf16, bf16_bits, E2M1_MAX, e2m1_decode, e2m1_encode, e2m1_magnitudes,

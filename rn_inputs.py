@@ -1,4 +1,4 @@
-"""Seeded synthetic inputs for the normalization workloads.
+"""Seeded synthetic inputs for the normalization and activation workloads.
 
 This module only draws random numbers and stores them in the dtypes the
 workloads name.  It holds none of the normalization or quantization
@@ -31,6 +31,12 @@ Recipes (one per workload; every draw comes from
                     [8192 x 4096] ~ N(0,1) (a sublayer's output), residual
                     bf16 ~ N(0, 3) (the residual stream), gamma = 1 + 0.1 N(0,1),
                     beta ~ N(0, 0.1), eps 1e-5, FP8 E4M3 scale fixed at 448/8.
+* ``moe_act``       scaled activations of a mixture-of-experts MLP (65536
+                    tokens, hidden 2048, as in the grouped-MLP measurements
+                    the activation page quotes): x bf16 [N x 2H] ~ N(0, 2)
+                    (the first fc layer's output: gate half, then linear
+                    half), row scales fp32 ~ U[0, 1) (routing weights), dy
+                    bf16 [N x H] ~ N(0,1); H = 2048 is the output width.
 
 Every recipe takes optional ``N``/``H`` overrides so that tests can draw the
 same distributions at sizes the oracle finishes in seconds.
@@ -89,6 +95,7 @@ class Workload:
     amax_history: np.ndarray | None = None  # float32 [16]
     extra: dict = field(default_factory=dict)
     residual: np.ndarray | None = None      # same storage as x (residual add), or None
+    scales: np.ndarray | None = None        # float32 [N] row scales (activations), or None
 
     def x_f64(self, rows=slice(None)) -> np.ndarray:
         return rows_view_f64(self.x, self.dtype, rows)
@@ -191,6 +198,21 @@ def _rms_add(rng, N, H):
                     scale=float(np.float32(448.0) / np.float32(8.0)), residual=residual)
 
 
+def _moe_act(rng, N, H):
+    x = np.empty((N, 2 * H), dtype=np.uint16)
+    step = 8192
+    for r0 in range(0, N, step):
+        n = min(step, N - r0)
+        x[r0:r0 + n] = to_bf16_bits(rng.normal(0.0, 2.0, (n, 2 * H)))
+    scales = _f32(rng.uniform(0.0, 1.0, N))
+    dy = np.empty((N, H), dtype=np.uint16)
+    for r0 in range(0, N, step):
+        n = min(step, N - r0)
+        dy[r0:r0 + n] = to_bf16_bits(rng.standard_normal((n, H)))
+    return Workload("moe_act", N, H, "bf16", x, np.ones(0, np.float32), None, dy, 0.0,
+                    scales=scales)
+
+
 WORKLOADS = {
     "rms_small": ((256, 1024), _rms_small),
     "ln_delayed": ((8192, 4096), _ln_delayed),
@@ -199,6 +221,7 @@ WORKLOADS = {
     "bwd_f32": ((131072, 1024), lambda rng, N, H: _bwd(rng, N, H, "f32", "bwd_f32")),
     "bwd_bf16": ((3000, 5120), lambda rng, N, H: _bwd(rng, N, H, "bf16", "bwd_bf16")),
     "rms_add": ((8192, 4096), _rms_add),
+    "moe_act": ((65536, 2048), _moe_act),
 }
 
 
