@@ -80,6 +80,15 @@ def algorithmic_bytes(kind, N, H, esz, ln, extra=None):
         return 3 * E * esz + stats + H * 4 + vec
     if kind == "fwd_add_fp8":                # x, residual in; h and codes out
         return 3 * E * esz + E * 1 + vec + stats
+    # scaled SwiGLU, E = N x H outputs from N x 2H inputs, row scales fp32
+    if kind == "act_fwd_none":               # x in (2E), y out
+        return 2 * E * esz + E * esz + 4 * N
+    if kind == "act_fwd_fp8_current":        # x read twice, E4M3 codes out
+        return 2 * (2 * E * esz + 4 * N) + E
+    if kind == "act_fwd_mxfp8":              # x in, rowwise codes + E8M0 scales out
+        return 2 * E * esz + E + E // 32 + 4 * N
+    if kind == "act_bwd":                    # dy, x in; dx out (2E); scales in, dscales out
+        return E * esz + 2 * E * esz + 2 * E * esz + 8 * N
     if kind == "history":                    # history read + written (H entries), 3 scalars
         return 2 * H * 4 + 12
     raise ValueError(kind)
@@ -500,7 +509,8 @@ def run_e2e(torch, lib, P, fwd, bwd, w, steps, step_bytes):
 
 def run_other_workloads(torch, rn, lib, rn_inputs, flush, peak, steps, warmup, only=None):
     """Full-size timing of the other workloads; ``only`` restricts the run to
-    one group ("rms_small", "rms_current", "mxfp8", "bwd_f32", "bwd_bf16", "rms_add")."""
+    one group ("rms_small", "rms_current", "mxfp8", "bwd_f32", "bwd_bf16", "rms_add",
+    "moe_act")."""
     res = {}
 
     def want(name):
@@ -554,6 +564,50 @@ def run_other_workloads(torch, rn, lib, rn_inputs, flush, peak, steps, warmup, o
         report("rms_add_8192x4096_fwd_fp8_delayed", "fwd_add_fp8", w.N, w.H, 2, False,
                statistics.mean(t["add"]), 2)
         del P, w
+    if want("moe_act"):
+        # scaled SwiGLU of a mixture-of-experts MLP: 65536 tokens x 2048
+        w = rn_inputs.make("moe_act")
+        to = lambda a: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to("cuda")
+        x, dy = to(w.x), to(w.dz)
+        sc = torch.from_numpy(w.scales).to("cuda")
+        N, H = w.N, w.H
+        vp, f32 = ctypes.c_void_p, ctypes.c_float
+        keep = []
+
+        def fwd_args(mode):
+            o = rn._Output()
+            if mode == "none":
+                d = torch.empty((N, H), dtype=torch.bfloat16, device="cuda")
+                o.data, o.out_dtype = d.data_ptr(), 0
+                keep.append(d)
+            elif mode == "fp8_current":
+                d = torch.empty((N, H), dtype=torch.uint8, device="cuda")
+                t3 = [torch.empty(1, dtype=torch.float32, device="cuda") for _ in range(3)]
+                o.data, o.scale_out, o.scale_inv, o.amax = (d.data_ptr(), t3[0].data_ptr(),
+                                                            t3[1].data_ptr(), t3[2].data_ptr())
+                keep.extend([d] + t3)
+            else:
+                d = torch.empty((N, H), dtype=torch.uint8, device="cuda")
+                r = torch.empty((N, H // 32), dtype=torch.uint8, device="cuda")
+                o.data, o.row_scales = d.data_ptr(), r.data_ptr()
+                keep.extend([d, r])
+            keep.append(o)
+            return ("rn_scaled_act_fwd", [1, vp(x.data_ptr()), 0, vp(sc.data_ptr()), N, H, f32(7.0),
+                                          f32(1.702), rn.QUANT_MODES[mode], ctypes.byref(o)])
+
+        dx = torch.empty_like(x)
+        ds = torch.empty(N, dtype=torch.float32, device="cuda")
+        bwd = ("rn_scaled_act_bwd", [1, vp(dy.data_ptr()), vp(x.data_ptr()), 0, vp(sc.data_ptr()), N, H,
+                                     f32(7.0), f32(1.702), vp(dx.data_ptr()), vp(ds.data_ptr())])
+        t = time_calls(torch, lib, [("none", fwd_args("none")), ("cur", fwd_args("fp8_current")),
+                                    ("mx", fwd_args("mxfp8")), ("bwd", bwd)], steps, warmup, flush)
+        report("swiglu_65536x2048_fwd_bf16", "act_fwd_none", N, H, 2, False, statistics.mean(t["none"]), 1)
+        report("swiglu_65536x2048_fwd_fp8_current", "act_fwd_fp8_current", N, H, 2, False,
+               statistics.mean(t["cur"]), 3)
+        report("swiglu_65536x2048_fwd_mxfp8_rowwise", "act_fwd_mxfp8", N, H, 2, False,
+               statistics.mean(t["mx"]), 1)
+        report("swiglu_65536x2048_bwd", "act_bwd", N, H, 2, False, statistics.mean(t["bwd"]), 1)
+        del x, dy, dx, keep, w
     for name in ("bwd_f32", "bwd_bf16"):
         if not want(name):
             continue
@@ -651,7 +705,8 @@ def main():
     ap.add_argument("--quick", action="store_true", help="headline workload only")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--only", default=None,
-                    choices=["rms_small", "rms_current", "mxfp8", "bwd_f32", "bwd_bf16", "rms_add"],
+                    choices=["rms_small", "rms_current", "mxfp8", "bwd_f32", "bwd_bf16", "rms_add",
+                             "moe_act"],
                     help="time only this workload group (prints its results; for profiling)")
     args = ap.parse_args()
     if args.warmup < 3:

@@ -1,6 +1,8 @@
 /*
  * rn.h — C ABI of a GB300 (sm_103a) library of fused LayerNorm / RMSNorm
- * kernels with FP8 (E4M3), MXFP8 and NVFP4 output quantization.
+ * kernels with FP8 (E4M3), MXFP8 and NVFP4 output quantization, and of the
+ * scaled activations (SReLU, SwiGLU, clamped SwiGLU) with the same
+ * quantized outputs.
  *
  * What is computed follows the page "Implementation:NVIDIA TransformerEngine
  * PyTorch Ext Normalization": forward functions normalize each row of x and
@@ -253,6 +255,57 @@ rn_status rn_layernorm_bwd_noalloc(const void* dz, const void* x, rn_dtype dtype
 rn_status rn_delayed_scaling_update(float* amax_history, int64_t history_len,
                                     const float* amax, float* scale,
                                     float* scale_inv, void* stream);
+
+/*
+ * Scaled activations (page "Activation + GroupedLinear Fusion for MOE and
+ * other MOE optimizations", section "Better Kernels for Scaled Activations":
+ * scaled SReLU, SwiGLU and clamped SwiGLU as fused kernels whose backward
+ * also returns the gradient of the scales).  The page gives no formula;
+ * standard readings:
+ *   y[i, j] = s_i * act(x)[i, j], one fp32 scale per row (NULL: all 1);
+ *   RN_ACT_SRELU           x [N, H]:  act = max(x, 0)^2
+ *   RN_ACT_SWIGLU          x [N, 2H] = [a | b]: act = a * sigmoid(a) * b
+ *   RN_ACT_CLAMPED_SWIGLU  x [N, 2H] = [a | b]: ac = min(a, limit),
+ *                          bc = clamp(b, -limit, limit),
+ *                          act = ac * sigmoid(alpha * ac) * (bc + 1)
+ *                          (limit >= 0; e.g. limit 7, alpha 1.702)
+ * sigmoid(z) = 1 / (1 + exp(-z)); y is formed in fp32.  limit and alpha are
+ * ignored by the other forms.  Outputs of non-finite inputs are unspecified.
+ */
+typedef enum {
+  RN_ACT_SRELU = 0,
+  RN_ACT_SWIGLU = 1,
+  RN_ACT_CLAMPED_SWIGLU = 2
+} rn_act;
+
+/*
+ * Forward: H is the OUTPUT width; x is [N, H] (SReLU) or [N, 2H] in `dtype`
+ * (16-byte aligned; H * element size a multiple of 16), scales fp32 [N] or
+ * NULL.  `mode` and *out as for rn_layernorm_fwd, with MXFP8 giving the
+ * rowwise 1x32 blocks only (data [N, H], row_scales [N, H/32]; col_data and
+ * col_scales must be NULL, else RN_ERR_UNSUPPORTED; H % 32 == 0) and NVFP4
+ * not offered (RN_ERR_UNSUPPORTED).  FP8_CURRENT reads x twice (amax pass,
+ * then quantize).  Asynchronous on `stream`; no workspace.
+ */
+rn_status rn_scaled_act_fwd(rn_act act, const void* x, rn_dtype dtype,
+                            const float* scales, int64_t N, int64_t H,
+                            float limit, float alpha, rn_quant_mode mode,
+                            const rn_output* out, void* stream);
+
+/*
+ * Backward: dy [N, H] and x (the forward's input) in `dtype`; writes
+ *   dx [N, H] or [N, 2H] (the shape of x, `dtype`):
+ *       dx = s_i * dy * d act / d x   (the a half, then the b half);
+ *       the clamps pass the gradient where the input lies within the
+ *       bounds, bounds included;
+ *   dscales fp32 [N] (may be NULL to skip): sum_j dy[i, j] * act(x)[i, j].
+ * dx is rounded once to `dtype`; dscales is an fp32 sum in an unspecified
+ * but fixed order.  Pointers 16-byte aligned (dscales 4).
+ */
+rn_status rn_scaled_act_bwd(rn_act act, const void* dy, const void* x, rn_dtype dtype,
+                            const float* scales, int64_t N, int64_t H,
+                            float limit, float alpha, void* dx, float* dscales,
+                            void* stream);
 
 /*
  * Quantization stage alone on caller-given fp32 values y [N, H] (the

@@ -20,7 +20,9 @@ PyTorch Ext Normalization" (section "Signature"):
 
 ``quant`` is one of "none", "fp8_delayed" (needs ``scale``), "fp8_current",
 "mxfp8", "nvfp4"; the page's quantizer object becomes this string plus the
-scale.
+scale.  ``scaled_act_fwd`` / ``scaled_act_bwd`` are the scaled SReLU, SwiGLU
+and clamped SwiGLU of the page "Activation + GroupedLinear Fusion for MOE
+and other MOE optimizations".
 """
 from __future__ import annotations
 
@@ -35,13 +37,14 @@ __all__ = [
     "layernorm_bwd_noalloc", "layernorm_add_fwd", "rmsnorm_add_fwd", "delayed_scaling_update",
     "bwd_workspace_bytes", "device_error", "Fp8Output", "MXFP8Output", "NVFP4Output", "lib_path",
     "RNError",
-    "QUANT_MODES",
+    "QUANT_MODES", "ACTS", "scaled_act_fwd", "scaled_act_bwd",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_HERE, "librn.so")
 QUANT_MODES = {"none": 0, "fp8_delayed": 1, "fp8_current": 2, "mxfp8": 3, "nvfp4": 4}
 _BF16, _F32 = 0, 1
+ACTS = {"srelu": 0, "swiglu": 1, "clamped_swiglu": 2}
 
 
 class RNError(RuntimeError):
@@ -90,13 +93,16 @@ def _load():
                                        vp]
     lib.rn_quantize_only.argtypes = [vp, i64, i64, i32, outp, vp]
     lib.rn_delayed_scaling_update.argtypes = [vp, i64, vp, vp, vp, vp]
+    lib.rn_scaled_act_fwd.argtypes = [i32, vp, i32, vp, i64, i64, f32, f32, i32, outp, vp]
+    lib.rn_scaled_act_bwd.argtypes = [i32, vp, vp, i32, vp, i64, i64, f32, f32, vp, vp, vp]
     lib.rn_layernorm_bwd_noalloc.argtypes = [vp, vp, i32, vp, vp, vp, i64, i64, i32, i32, vp, vp, vp, vp]
     lib.rn_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint)]
     lib.rn_status_str.argtypes = [i32]
     lib.rn_status_str.restype = ctypes.c_char_p
     for f in ("rn_layernorm_fwd", "rn_rmsnorm_fwd", "rn_layernorm_bwd", "rn_rmsnorm_bwd",
               "rn_quantize_only", "rn_device_error", "rn_abi_version", "rn_layernorm_bwd_noalloc",
-              "rn_layernorm_add_fwd", "rn_rmsnorm_add_fwd", "rn_delayed_scaling_update"):
+              "rn_layernorm_add_fwd", "rn_rmsnorm_add_fwd", "rn_delayed_scaling_update",
+              "rn_scaled_act_fwd", "rn_scaled_act_bwd"):
         getattr(lib, f).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -308,6 +314,46 @@ def delayed_scaling_update(amax_history, amax, scale):
                                        _ptr(scale), _ptr(scale_inv), _stream())
     _check(st, "rn_delayed_scaling_update")
     return scale_inv
+
+
+def _act_width(x, act):
+    if act not in ACTS:
+        raise RNError(f"unknown activation {act!r}")
+    return x.shape[1] if act == "srelu" else x.shape[1] // 2
+
+
+def scaled_act_fwd(x, act, scales=None, quant="none", limit=7.0, alpha=1.702, scale=None,
+                   out_dtype=None):
+    """y = scales[:, None] * act(x): x [N, H] (srelu) or [N, 2H] (swiglu,
+    clamped_swiglu: gate half, then linear half); returns the output in the
+    form of the forward norm calls (MXFP8: rowwise blocks only)."""
+    lib = _load()
+    _need(x, "x")
+    N, H = x.shape[0], _act_width(x, act)
+    if scales is not None:
+        _need(scales, "scales", torch.float32, (N,))
+    o, res = _make_output(x[:, :H], quant, out_dtype, scale, True, False)
+    st = lib.rn_scaled_act_fwd(ACTS[act], _ptr(x), _dtype_code(x), _ptr(scales), N, H,
+                               float(limit), float(alpha), QUANT_MODES[quant], ctypes.byref(o),
+                               _stream())
+    _check(st, "rn_scaled_act_fwd")
+    return res
+
+
+def scaled_act_bwd(dy, x, act, scales=None, limit=7.0, alpha=1.702, dscales=True):
+    """-> (dx shaped like x, dscales fp32 [N] or None)."""
+    lib = _load()
+    _need(x, "x")
+    N, H = x.shape[0], _act_width(x, act)
+    _need(dy, "dy", x.dtype, (N, H))
+    if scales is not None:
+        _need(scales, "scales", torch.float32, (N,))
+    dx = torch.empty_like(x)
+    ds = torch.empty(N, dtype=torch.float32, device=x.device) if dscales else None
+    st = lib.rn_scaled_act_bwd(ACTS[act], _ptr(dy), _ptr(x), _dtype_code(x), _ptr(scales), N, H,
+                               float(limit), float(alpha), _ptr(dx), _ptr(ds), _stream())
+    _check(st, "rn_scaled_act_bwd")
+    return dx, ds
 
 
 def bwd_workspace_bytes(N, H, dtype, layernorm=True) -> int:

@@ -14,7 +14,7 @@ from concurrent.futures import ThreadPoolExecutor
 HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 LIB = os.path.join(HERE, "librn.so")
-SOURCES = ["rn_api.cu", "rn_fwd.cu", "rn_fwd_res.cu", "rn_mx.cu", "rn_bwd.cu", "rn_scaling.cu"]
+SOURCES = ["rn_api.cu", "rn_fwd.cu", "rn_fwd_res.cu", "rn_mx.cu", "rn_bwd.cu", "rn_scaling.cu", "rn_act.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2"]
 

@@ -632,6 +632,99 @@ rn_status rn_quantize_only(const float* y, int64_t N, int64_t H, rn_quant_mode m
                     nullptr, static_cast<cudaStream_t>(stream));
 }
 
+// ------------------------------------------------------ scaled activations
+static rn_status act_common_checks(rn_act act, const void* x, rn_dtype dt, const float* scales,
+                                   int64_t N, int64_t H, float limit, float alpha) {
+  if (act != RN_ACT_SRELU && act != RN_ACT_SWIGLU && act != RN_ACT_CLAMPED_SWIGLU)
+    return RN_ERR_INVALID;
+  if ((x == nullptr && N > 0) || !dtype_ok(dt) || N < 0 || H < 1 || N > INT32_MAX ||
+      H > INT32_MAX / 2)
+    return RN_ERR_INVALID;
+  if (act == RN_ACT_CLAMPED_SWIGLU && (!(limit >= 0.0f) || !(alpha == alpha) ||
+                                       alpha > 3.4e38f || alpha < -3.4e38f))
+    return RN_ERR_INVALID;
+  if (!row_ok(H, dt) || !aligned(x, 16) || (scales && !aligned(scales, 4)))
+    return RN_ERR_UNSUPPORTED;
+  return RN_OK;
+}
+
+rn_status rn_scaled_act_fwd(rn_act act, const void* x, rn_dtype dtype, const float* scales,
+                            int64_t N, int64_t H, float limit, float alpha, rn_quant_mode mode,
+                            const rn_output* out, void* stream) {
+  rn_status st = act_common_checks(act, x, dtype, scales, N, H, limit, alpha);
+  if (st != RN_OK) return st;
+  if (mode == RN_QUANT_NVFP4) return RN_ERR_UNSUPPORTED;
+  if (mode == RN_QUANT_MXFP8 && out != nullptr &&
+      (out->col_data != nullptr || out->col_scales != nullptr))
+    return RN_ERR_UNSUPPORTED;  // rowwise blocks only
+  if (mode == RN_QUANT_MXFP8) {
+    if (out == nullptr) return RN_ERR_INVALID;
+    if (N > 0 && !out_fields_only(out, true, true, false, false, false, false, false, false))
+      return RN_ERR_INVALID;
+    if (H % 32 != 0) return RN_ERR_UNSUPPORTED;
+    if (N > 0 && !aligned(out->data, 16)) return RN_ERR_UNSUPPORTED;
+  } else if ((st = check_out(mode, out, N, H)) != RN_OK) {
+    return st;
+  }
+  DeviceInfo di;
+  if ((st = device_info(&di)) != RN_OK) return st;
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (N == 0 && (mode == RN_QUANT_NONE || mode == RN_QUANT_MXFP8)) return RN_OK;
+  ActParams p{};
+  p.x = x;
+  p.out = out->data;
+  p.row_scales = mode == RN_QUANT_MXFP8 ? out->row_scales : nullptr;
+  p.scales = scales;
+  p.scale = out->scale;
+  p.amax = out->amax;
+  p.scale_inv = out->scale_inv;
+  p.scale_out = out->scale_out;
+  p.N = (int)N;
+  p.H = (int)H;
+  p.limit = limit;
+  p.alpha = alpha;
+  p.out_f32 = (mode == RN_QUANT_NONE && out->out_dtype == RN_F32) ? 1 : 0;
+  const bool bf16 = dtype == RN_BF16;
+  switch (mode) {
+    case RN_QUANT_NONE:
+    case RN_QUANT_MXFP8:
+      return launch_act_fwd(act, bf16, kQNone, p, di.sms, false, s);
+    case RN_QUANT_FP8_DELAYED:
+      if ((st = launch_fwd_init(out->amax, out->scale, out->scale_inv, s)) != RN_OK) return st;
+      return launch_act_fwd(act, bf16, kQDelayed, p, di.sms, true, s);
+    case RN_QUANT_FP8_CURRENT:
+      if ((st = launch_fwd_init(out->amax, nullptr, nullptr, s)) != RN_OK) return st;
+      if ((st = launch_act_fwd(act, bf16, kQCurAmax, p, di.sms, true, s)) != RN_OK) return st;
+      return launch_act_fwd(act, bf16, kQCurQuant, p, di.sms, true, s);
+    default:
+      return RN_ERR_INVALID;
+  }
+}
+
+rn_status rn_scaled_act_bwd(rn_act act, const void* dy, const void* x, rn_dtype dtype,
+                            const float* scales, int64_t N, int64_t H, float limit, float alpha,
+                            void* dx, float* dscales, void* stream) {
+  rn_status st = act_common_checks(act, x, dtype, scales, N, H, limit, alpha);
+  if (st != RN_OK) return st;
+  if (N > 0 && (dy == nullptr || dx == nullptr)) return RN_ERR_INVALID;
+  if ((dy && !aligned(dy, 16)) || (dx && !aligned(dx, 16)) || (dscales && !aligned(dscales, 4)))
+    return RN_ERR_UNSUPPORTED;
+  DeviceInfo di;
+  if ((st = device_info(&di)) != RN_OK) return st;
+  if (N == 0) return RN_OK;
+  ActParams p{};
+  p.x = x;
+  p.dy = dy;
+  p.out = dx;
+  p.scales = scales;
+  p.dscales = dscales;
+  p.N = (int)N;
+  p.H = (int)H;
+  p.limit = limit;
+  p.alpha = alpha;
+  return launch_act_bwd(act, dtype == RN_BF16, p, di.sms, static_cast<cudaStream_t>(stream));
+}
+
 const char* rn_status_str(rn_status s) {
   switch (s) {
     case RN_OK: return "ok";

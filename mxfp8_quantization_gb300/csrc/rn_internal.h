@@ -97,6 +97,26 @@ struct ColReduceParams {
   int nacc;
 };
 
+// scaled activations (forward with a quantize epilogue, backward)
+enum ActKind : int { kActSrelu = 0, kActSwiglu = 1, kActClampedSwiglu = 2 };
+
+struct ActParams {
+  const void* x;          // [N, H] (SReLU) or [N, 2H] (gate half, linear half)
+  const void* dy;         // backward: [N, H]
+  void* out;              // forward: y (bf16 / fp32) or E4M3 codes [N, H];
+                          // backward: dx, the shape of x
+  uint8_t* row_scales;    // forward MXFP8 (rowwise): E8M0 [N, H/32], else NULL
+  const float* scales;    // [N] row scales, or NULL (all 1)
+  const float* scale;     // FP8 delayed
+  float* amax;            // FP8 modes
+  float* scale_inv;       // FP8 current (pass 2)
+  float* scale_out;       // FP8 current (pass 2)
+  float* dscales;         // backward: [N] or NULL
+  int N, H;               // H: output width
+  float limit, alpha;     // clamped SwiGLU
+  int out_f32;            // forward NONE: fp32 output
+};
+
 // launch shape shared by the persistent kernels
 struct Launch {
   int work;             // independent work items (tiles / chunks): grid upper bound
@@ -155,6 +175,12 @@ rn_status launch_bwd(bool ln, bool bf16, int ng, const BwdParams& p, const Launc
 rn_status launch_bwd_fused(bool ln, bool big, const BwdParams& p, const Launch& l,
                            cudaStream_t s);
 rn_status launch_colreduce(const ColReduceParams& p, cudaStream_t s);
+
+// scaled activations; qmode kQNone with p.row_scales set = MXFP8 rowwise;
+// sms: SMs the grid may use; pdl: programmatic dependent of the previous kernel
+rn_status launch_act_fwd(int act, bool bf16, int qmode, const ActParams& p, int sms, bool pdl,
+                         cudaStream_t s);
+rn_status launch_act_bwd(int act, bool bf16, const ActParams& p, int sms, cudaStream_t s);
 
 // delayed-scaling history step (one CTA; 1 <= L <= kMaxHistory)
 constexpr int kMaxHistory = 1024;

@@ -34,7 +34,7 @@ from __future__ import annotations
 import numpy as np
 
 from .formats import bf16_bits, round_to_bf16
-from .norm import quantize
+from .norm import mx_blocks_1d, quantize
 
 ACTS = ("srelu", "swiglu", "clamped_swiglu")
 
@@ -112,9 +112,9 @@ def scaled_act_fwd(x, scales, act, mode="none", out_dtype="bf16", limit=7.0, alp
     res = {"y": y}
     if mode == "none":
         res["data"] = _out(y, out_dtype)
-    elif mode == "mxfp8":
-        q = quantize(y.astype(np.float32), "mxfp8")
-        res.update(data=q["data"], row_scales=q["row_scales"])
+    elif mode == "mxfp8":   # rowwise 1x32 blocks only: N need not be a multiple of 32
+        q, sc = mx_blocks_1d(y.astype(np.float32))
+        res.update(data=q, row_scales=sc)
     else:
         res.update(quantize(y.astype(np.float32), mode, scale=scale, amax=amax))
     return res

@@ -161,3 +161,32 @@ def test_delayed_scaling_update_rejects_bad_arguments_on_host(lib):
     assert lib.rn_delayed_scaling_update(p, 0, p, p, p, None) == 1      # empty history
     assert lib.rn_delayed_scaling_update(None, 4, p, p, p, None) == 1
     assert lib.rn_delayed_scaling_update(p, 2048, p, p, p, None) == 2   # longer than 1024
+
+
+def test_scaled_activation_rejects_bad_arguments_on_host(lib):
+    x = ctypes.c_void_p(0x1000)
+    o = _out(data=0x5000, out_dtype=0)
+    f32 = ctypes.c_float
+    # bad activation, NULL x, bad dtype, negative N
+    assert lib.rn_scaled_act_fwd(7, x, 0, None, 4, 1024, f32(7), f32(1.702), 0, ctypes.byref(o), None) == 1
+    assert lib.rn_scaled_act_fwd(1, None, 0, None, 4, 1024, f32(7), f32(1.702), 0, ctypes.byref(o), None) == 1
+    assert lib.rn_scaled_act_fwd(1, x, 5, None, 4, 1024, f32(7), f32(1.702), 0, ctypes.byref(o), None) == 1
+    assert lib.rn_scaled_act_fwd(1, x, 0, None, -1, 1024, f32(7), f32(1.702), 0, ctypes.byref(o), None) == 1
+    # clamped SwiGLU needs a limit >= 0 and a finite alpha
+    assert lib.rn_scaled_act_fwd(2, x, 0, None, 4, 1024, f32(-1), f32(1.702), 0, ctypes.byref(o), None) == 1
+    assert lib.rn_scaled_act_fwd(2, x, 0, None, 4, 1024, f32(float("nan")), f32(1.702), 0, ctypes.byref(o), None) == 1
+    assert lib.rn_scaled_act_fwd(2, x, 0, None, 4, 1024, f32(7), f32(float("inf")), 0, ctypes.byref(o), None) == 1
+    # rows of whole 16-byte chunks, aligned x
+    assert lib.rn_scaled_act_fwd(1, x, 0, None, 4, 1020, f32(7), f32(1.702), 0, ctypes.byref(o), None) == 2
+    assert lib.rn_scaled_act_fwd(1, ctypes.c_void_p(0x1008), 0, None, 4, 1024, f32(7), f32(1.702), 0, ctypes.byref(o), None) == 2
+    # MXFP8 rowwise only; no NVFP4
+    om = _out(data=0x5000, row_scales=0x6000, col_data=0x7000, col_scales=0x8000)
+    assert lib.rn_scaled_act_fwd(1, x, 0, None, 4, 1024, f32(7), f32(1.702), 3, ctypes.byref(om), None) == 2
+    om = _out(data=0x5000, row_scales=0x6000)
+    assert lib.rn_scaled_act_fwd(1, x, 0, None, 4, 1040, f32(7), f32(1.702), 3, ctypes.byref(om), None) == 2
+    on = _out(data=0x5000, row_scales=0x6000, scale_out=0x7000, scale_inv=0x7010, amax=0x7020)
+    assert lib.rn_scaled_act_fwd(1, x, 0, None, 4, 1024, f32(7), f32(1.702), 4, ctypes.byref(on), None) == 2
+    # backward: NULL dy / dx, misaligned dx
+    assert lib.rn_scaled_act_bwd(1, None, x, 0, None, 4, 1024, f32(7), f32(1.702), x, None, None) == 1
+    assert lib.rn_scaled_act_bwd(1, x, x, 0, None, 4, 1024, f32(7), f32(1.702), None, None, None) == 1
+    assert lib.rn_scaled_act_bwd(1, x, x, 0, None, 4, 1024, f32(7), f32(1.702), ctypes.c_void_p(0x2004), None, None) == 2
