@@ -77,11 +77,11 @@ size_t cta_smem_budget(const DeviceInfo& di, int per_sm) {
 }
 
 // Warp roles of the row kernels: A apply warps (each thread owning NG
-// 16-byte chunks of every row), S = max(2, A/2) stats warps (fewer than the
-// ring's slots, which their pacing on slot releases relies on), one producer.
-// Compact shape: NG <= 2, A <= 8, two CTAs per SM when each still holds a
-// ring of >= 6 slots.  Otherwise the wide shape: one CTA per SM, NG in
-// {2, 4, 8}, A <= 16.
+// 16-byte chunks of every row), S = max(2, A/2) stats warps (at most 3 in
+// the compact shape; fewer than the ring's slots, which their pacing on slot
+// releases relies on), one producer.  Compact shape: NG <= 2, A <= 8, two
+// CTAs per SM when each still holds a ring of >= 6 slots.  Otherwise the
+// wide shape: one CTA per SM, NG in {2, 4, 8}, A <= 16.
 struct Roles {
   int ng, A, S, per_sm, Q;
 };
@@ -97,6 +97,7 @@ rn_status plan_roles(int nchunks, size_t per_slot, size_t fixed, const DeviceInf
       r->ng = ng;
       r->A = round_up((nchunks + ng - 1) / ng, 32) / 32;
       r->S = r->A / 2 > 2 ? r->A / 2 : 2;
+      if (r->S > 3) r->S = 3;          // 12 warps a CTA: 80 registers a thread
       if (r->S > Q - 1) r->S = Q - 1;  // stats warps must be fewer than slots
       r->per_sm = 2;
       r->Q = Q;

@@ -36,9 +36,11 @@ namespace {
 
 __device__ unsigned g_err_bwd;
 
-// compact shape: at most 8 apply + 4 stats warps + the producer, two CTAs
-// per SM; wide shape: up to 16 apply + 8 stats warps + the producer, one CTA
-constexpr int kMaxThreads = 416;
+// compact shape: at most 8 apply + 3 stats warps + the producer, two CTAs
+// per SM (24 warps an SM leave 80 registers a thread: a fourth stats warp
+// cut that to 72 and made the apply warps spill); wide shape: up to 16
+// apply + 8 stats warps + the producer, one CTA
+constexpr int kMaxThreads = 384;
 constexpr int kMaxThreadsWide = 800;
 // rows the producer issues before waiting for the first one to land
 constexpr uint32_t kStartRows = 2;
