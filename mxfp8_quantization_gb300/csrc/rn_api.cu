@@ -187,6 +187,7 @@ rn_status plan_fwd(int nk, int H, int esz, int N, int sm_margin, const DeviceInf
 struct MxPlan {
   int Q, n_tbar, apply_warps, stats_warps;
   Launch l;
+  int Qs = 0;  // slab kernel: row-ring slots
 };
 
 rn_status plan_mx(int nk, int H, int esz, int N, int sm_margin, const DeviceInfo& di,
@@ -219,6 +220,47 @@ rn_status plan_mx(int nk, int H, int esz, int N, int sm_margin, const DeviceInfo
   pl->l.work = N / 32;
   pl->l.sms = di.sms - sm_margin;
   pl->l.per_sm = 1;
+  return RN_OK;
+}
+
+// MXFP8 slab kernel (bf16, H a multiple of kMxSlabCols, H <= 4096): A apply
+// warps, the largest divisor of the slabs per row up to 8; S = 6 stats
+// warps; two producer warps (16 warps in all); a row ring of about 80 KB (a multiple of S
+// rows) and a slab ring of 3 A slabs, both shrunk to fit; NT = 3 tiles of
+// statistics in flight.
+rn_status plan_mx_slab(int nk, int H, int N, int sm_margin, const DeviceInfo& di, MxPlan* pl) {
+  if (nk == kIdentity || H % kMxSlabCols != 0 || H > 4096) return RN_ERR_UNSUPPORTED;
+  const int nslab = H / kMxSlabCols;
+  int A = nslab < 8 ? nslab : 8;
+  while (nslab % A != 0) --A;
+  const int S = 6;  // LayerNorm's two statistics passes need 6 (4: 170 us, 6: 146 us)
+  const int NT = 3;
+  const size_t row_bytes = (size_t)H * 2;
+  const size_t slab_bytes = (size_t)32 * kMxSlabCols * 2;
+  const size_t gb = (size_t)H * sizeof(float) * (nk == kLn ? 2 : 1);
+  const size_t budget = cta_smem_budget(di, 1);
+  auto need = [&](int qs, int qa) {
+    return gb + (size_t)qs * row_bytes + (size_t)qa * slab_bytes + (size_t)NT * 32 * 8 +
+           8 * (2 * (size_t)qs + 2 * (size_t)qa + 2 * NT) + 64;
+  };
+  // rows in flight: about 80 KB an SM sustains the HBM stream; slabs: one in
+  // work and two in flight per apply warp
+  int Qs = S * (int)(((size_t)80 << 10) / (row_bytes * S));
+  if (Qs < S) Qs = S;
+  int Qa = 3 * A;
+  while (need(Qs, Qa) > budget && Qs > S) Qs -= S;
+  while (need(Qs, Qa) > budget && Qa > A) Qa -= A;
+  if (need(Qs, Qa) > budget) return RN_ERR_UNSUPPORTED;
+  pl->Q = Qa;
+  pl->n_tbar = NT;
+  pl->apply_warps = A;
+  pl->stats_warps = S;
+  pl->l.threads = 32 * (A + S + 2);
+  pl->l.smem = need(Qs, Qa);
+  pl->l.work = N / 32;
+  pl->l.sms = di.sms - sm_margin;
+  pl->l.per_sm = 1;
+  pl->Qs = Qs;
   return RN_OK;
 }
 
@@ -343,7 +385,9 @@ rn_status fwd_common(int nk, const void* x, rn_dtype dt, const float* gamma, con
 
   if (mode == RN_QUANT_MXFP8) {
     MxPlan pl;
-    if ((st = plan_mx(nk, (int)H, esz, (int)N, sm_margin, di, &pl)) != RN_OK) return st;
+    // bf16 rows of whole slabs: the kernel with separate row and slab rings
+    const bool slab = bf16 && plan_mx_slab(nk, (int)H, (int)N, sm_margin, di, &pl) == RN_OK;
+    if (!slab && (st = plan_mx(nk, (int)H, esz, (int)N, sm_margin, di, &pl)) != RN_OK) return st;
     MxParams p{};
     p.x = x;
     p.gamma = gamma;
@@ -363,6 +407,8 @@ rn_status fwd_common(int nk, const void* x, rn_dtype dt, const float* gamma, con
     p.stats_warps = pl.stats_warps;
     p.n_tiles = (int)(N / 32);
     p.n_tbar = pl.n_tbar;
+    p.Qs = pl.Qs;
+    if (slab) return launch_mx_slab(nk, p, pl.l, stream);
     return launch_mx(nk, bf16, 1, p, pl.l, stream);
   }
 

@@ -340,7 +340,7 @@ __global__ void __launch_bounds__(max_threads<NC>(), 1) rn_fwd_kernel(const FwdP
     }
     named_sync(kBarWorkers, 32 * W);
   }
-  float ymax = 0.0f, ymin = 0.0f;  // amax = max(ymax, -ymin)
+  float ymax = 0.0f;  // running max |y| (NaN wins)
 
   RingPos pos{(uint32_t)group, 0u};
   int par = 0;
@@ -469,8 +469,7 @@ __global__ void __launch_bounds__(max_threads<NC>(), 1) rn_fwd_kernel(const FwdP
             y[j] = V::f32(raw[k], j);
           }
           if constexpr (AMAX) {
-            ymax = max3(ymax, y[j]);
-            ymin = min3(ymin, y[j]);
+            ymax = amax_acc2(ymax, y[j]);  // one 3-input max on magnitudes a pair
           }
           if constexpr (NV) bm = fmaxf(bm, fmaxf(fabsf(y[j].x), fabsf(y[j].y)));
         }
@@ -502,9 +501,7 @@ __global__ void __launch_bounds__(max_threads<NC>(), 1) rn_fwd_kernel(const FwdP
   }
 
   if constexpr (AMAX) {
-    float amax_t;
-    asm("max.NaN.f32 %0, %1, %2;" : "=f"(amax_t) : "f"(ymax), "f"(-ymin));
-    const uint32_t b = warp_umax(abs_bits(amax_t));
+    const uint32_t b = warp_umax(abs_bits(ymax));
     if (lane == 0) red2[warp] = b;
     named_sync(kBarWorkers, 32 * W);
     if (threadIdx.x == 0) {

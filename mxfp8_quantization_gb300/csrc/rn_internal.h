@@ -68,7 +68,8 @@ struct MxParams {
   int stats_warps;
   int Q;
   int n_tiles;          // N / 32
-  int n_tbar;           // tile "ready" barriers (> Q / 32 + 1)
+  int n_tbar;           // tile "ready" barriers (> Q / 32 + 1); slab kernel: tiles in flight
+  int Qs;               // slab kernel: row-ring slots (a multiple of stats_warps)
 };
 
 struct BwdParams {
@@ -166,6 +167,11 @@ rn_status launch_fwd_res(int nk, bool bf16, const FwdShape& sh, int qmode, const
 rn_status launch_fwd_init(float* amax, const float* scale, float* scale_inv, cudaStream_t s);
 rn_status launch_mx(int nk, bool bf16, int ng, const MxParams& p, const Launch& l,
                     cudaStream_t s);
+// MXFP8 with separate row (statistics) and slab (quantization) rings: bf16,
+// H a multiple of kMxSlabCols; Q = slab slots, Qs = row slots, n_tbar =
+// tiles in flight
+constexpr int kMxSlabCols = 64;
+rn_status launch_mx_slab(int nk, const MxParams& p, const Launch& l, cudaStream_t s);
 // backward with stats warps (rows of any length)
 rn_status launch_bwd(bool ln, bool bf16, int ng, const BwdParams& p, const Launch& l,
                      cudaStream_t s);
