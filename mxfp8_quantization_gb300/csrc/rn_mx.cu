@@ -3,8 +3,12 @@
 // "Implementation:NVIDIA TransformerEngine PyTorch Ext Normalization",
 // section "Description": the fully fused MXFP8 path).
 //
-// Design (one persistent CTA per SM, warp-specialized, no CTA-wide barrier
-// on the row path):
+// Two kernels: rn_mx_slab_kernel (further below) for bf16 rows of whole
+// 64-column slabs, and the ring kernel described here for the other rows
+// (fp32, other widths, the stand-alone quantizer).
+//
+// Ring-kernel design (one persistent CTA per SM, warp-specialized, no
+// CTA-wide barrier on the row path):
 //   producer     one lane streams rows of x into a shared-memory ring with
 //                cp.async.bulk ("full" mbarrier per slot);
 //   stats warps  take rows in turn: mean / rsigma from shared memory
