@@ -60,8 +60,8 @@
 // the (G, NC, FULL) row shapes compiled in
 #ifndef RN_FWD_SHAPES
 #define RN_FWD_SHAPES                                                            \
-  RN_FWD_SHAPE(1, 4, false) RN_FWD_SHAPE(1, 16, false) RN_FWD_SHAPE(2, 16, false) \
-  RN_FWD_SHAPE(4, 16, false) RN_FWD_SHAPE(8, 16, false)
+  RN_FWD_SHAPE(1, 4, false) RN_FWD_SHAPE(1, 16, false) RN_FWD_SHAPE(2, 8, false)  \
+  RN_FWD_SHAPE(2, 16, false) RN_FWD_SHAPE(4, 16, false) RN_FWD_SHAPE(8, 16, false)
 #endif
 
 namespace rn {
