@@ -175,6 +175,8 @@ FWD_CASES = [
     ("mxfp8", 64, 768, True, "mxfp8"),
     ("mxfp8", 64, 800, False, "mxfp8"),
     ("mxfp8", 32, 3072, True, "mxfp8"),
+    ("mxfp8", 64, 4096, True, "mxfp8"),     # the widest slab rows (16 chunks a stats lane)
+    ("mxfp8", 32, 4096, False, "mxfp8"),
     ("bwd_f32", 67, 1024, True, "none"),
     ("bwd_f32", 67, 1024, False, "fp8_delayed"),
     ("bwd_f32", 64, 1024, True, "mxfp8"),
