@@ -42,6 +42,10 @@ __device__ unsigned g_err_bwd;
 // apply + 8 stats warps + the producer, one CTA
 constexpr int kMaxThreads = 384;
 constexpr int kMaxThreadsWide = 800;
+// compact shape with 4 chunks a thread: 4 apply + 3 stats warps + the
+// producer (256 threads, 128 registers: the 4 chunks' gamma and dgamma /
+// dbeta sums stay in registers)
+constexpr int kMaxThreadsNg4 = 256;
 // rows the producer issues before waiting for the first one to land
 constexpr uint32_t kStartRows = 2;
 
@@ -65,7 +69,8 @@ __device__ __forceinline__ void store_dx<float>(void* base, size_t elem, const f
 }
 
 template <typename TIn, int NG, bool LN, bool WIDE>
-__global__ void __launch_bounds__(WIDE ? kMaxThreadsWide : kMaxThreads, WIDE ? 1 : 2)
+__global__ void __launch_bounds__(WIDE ? kMaxThreadsWide : (NG >= 4 ? kMaxThreadsNg4 : kMaxThreads),
+                                  WIDE ? 1 : 2)
     rn_bwd_kernel(const BwdParams p) {
   constexpr int VEC = 16 / (int)sizeof(TIn);
   using V = Vec<TIn, VEC>;
@@ -586,7 +591,7 @@ rn_status launch_t(const BwdParams& p, const Launch& l, cudaStream_t s) {
   return cudaGetLastError() == cudaSuccess ? RN_OK : RN_ERR_CUDA;
 }
 
-// compact shape for NG 1 and 2; wide shape for NG 2, 4 and 8
+// compact shape for NG 1, 2 and 4; wide shape for NG 2, 4 and 8
 template <typename TIn, bool LN>
 rn_status launch_ng(int ng, const BwdParams& p, const Launch& l, cudaStream_t s) {
   const bool wide = l.threads > kMaxThreads || l.per_sm == 1;
@@ -594,6 +599,9 @@ rn_status launch_ng(int ng, const BwdParams& p, const Launch& l, cudaStream_t s)
     switch (ng) {
       case 1: return launch_t<TIn, 1, LN, false>(p, l, s);
       case 2: return launch_t<TIn, 2, LN, false>(p, l, s);
+      case 4:
+        if (l.threads > kMaxThreadsNg4) return RN_ERR_UNSUPPORTED;
+        return launch_t<TIn, 4, LN, false>(p, l, s);
       default: return RN_ERR_UNSUPPORTED;
     }
   }
