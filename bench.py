@@ -74,6 +74,8 @@ def algorithmic_bytes(kind, N, H, esz, ln, extra=None):
         return 2 * E * esz + E * 1 + vec + 2 * stats
     if kind == "fwd_nvfp4":                  # x read twice; E2M1 codes (half a byte) and scales out
         return 2 * E * esz + E // 2 + E // 16 + vec + 2 * stats
+    if kind == "fwd_mxfp8_row":              # x in, rowwise codes and scales out
+        return E * esz + E + E // 32 + vec + stats
     if kind == "fwd_mxfp8":                  # x in, row + col codes and scales out
         return E * esz + 2 * E + 2 * (E // 32) + vec + stats
     if kind == "bwd":                        # dz, x in, dx out, dgamma (+dbeta) out
@@ -227,6 +229,11 @@ class Prepared:
             o.data, o.row_scales, o.scale_out, o.scale_inv, o.amax = (
                 d.data_ptr(), rsc.data_ptr(), sc.data_ptr(), sinv.data_ptr(), amax.data_ptr())
             keep = [d, rsc, sc, sinv, amax]
+        elif mode == "mxfp8_row":
+            d = torch.empty((N, H), dtype=torch.uint8, device="cuda")
+            rsc = torch.empty((N, H // 32), dtype=torch.uint8, device="cuda")
+            o.data, o.row_scales = d.data_ptr(), rsc.data_ptr()
+            keep = [d, rsc]
         elif mode == "mxfp8":
             d = torch.empty((N, H), dtype=torch.uint8, device="cuda")
             rsc = torch.empty((N, H // 32), dtype=torch.uint8, device="cuda")
@@ -241,7 +248,7 @@ class Prepared:
             keep = [data]
         self.fwd_keep = keep
         self.fwd_out = o
-        mcode = rn.QUANT_MODES[mode]
+        mcode = rn.QUANT_MODES["mxfp8" if mode == "mxfp8_row" else mode]
         w = self.w
         vp = ctypes.c_void_p
         if self.ln:
@@ -562,6 +569,11 @@ def run_other_workloads(torch, rn, lib, rn_inputs, flush, peak, steps, warmup, o
             t = time_calls(torch, lib, [("mx", P.fwd_args("mxfp8"))], steps, warmup, flush)
             report(f"{'ln' if ln else 'rms'}_65536x2048_fwd_mxfp8", "fwd_mxfp8", w.N, w.H, 2, ln,
                    statistics.mean(t["mx"]), 1)
+            if ln:
+                # the rowwise blocks alone (one pass of the row kernel)
+                t = time_calls(torch, lib, [("mr", P.fwd_args("mxfp8_row"))], steps, warmup, flush)
+                report("ln_65536x2048_fwd_mxfp8_rowwise_only", "fwd_mxfp8_row", w.N, w.H, 2, ln,
+                       statistics.mean(t["mr"]), 1)
             del P
         del w
     if want("rms_small"):

@@ -42,6 +42,9 @@
 // output) and pass 2 (quantize with 448/amax from the saved mu / rsigma), the
 // second launched as a programmatic dependent of the first and walking the
 // rows backwards so that it starts on the rows pass 1 left in L2.
+// MXFP8 calls that want the rowwise blocks only take this kernel too, in one
+// pass: the 1x32 block maximum over the 4 (bf16) or 8 (fp32) lanes of a
+// block, its E8M0 code, and E4M3 codes of y * 2^-e.
 // NVFP4 output takes the same two passes; its pass 2 quantizes each run of 16
 // elements of a row (the chunks of two adjacent lanes for bf16, four for
 // fp32) with one E4M3 scale: the lanes of a block exchange their maxima with
@@ -59,9 +62,10 @@
 
 // the (G, NC, FULL) row shapes compiled in
 #ifndef RN_FWD_SHAPES
-#define RN_FWD_SHAPES                                                            \
-  RN_FWD_SHAPE(1, 4, false) RN_FWD_SHAPE(1, 16, false) RN_FWD_SHAPE(2, 8, false)  \
-  RN_FWD_SHAPE(2, 16, false) RN_FWD_SHAPE(4, 16, false) RN_FWD_SHAPE(8, 16, false)
+#define RN_FWD_SHAPES                                                              \
+  RN_FWD_SHAPE(1, 4, false) RN_FWD_SHAPE(1, 8, false) RN_FWD_SHAPE(1, 16, false)    \
+  RN_FWD_SHAPE(2, 8, false) RN_FWD_SHAPE(2, 16, false) RN_FWD_SHAPE(4, 16, false)   \
+  RN_FWD_SHAPE(8, 16, false)
 #endif
 
 namespace rn {
@@ -203,6 +207,7 @@ __global__ void __launch_bounds__(max_threads<NC>(), 1) rn_fwd_kernel(const FwdP
   constexpr bool LN = (NK == kLn);
   constexpr bool NORM = (NK != kIdentity);
   constexpr bool NV = (QM == kQNvfp4);
+  constexpr bool MXR = (QM == kQMxRow);
   // pass 2 of current scaling / NVFP4 gets mu / rsigma with each row
   constexpr bool PASS2 = (QM == kQCurQuant || NV);
   constexpr bool META = (PASS2 && NORM);
@@ -423,14 +428,16 @@ __global__ void __launch_bounds__(max_threads<NC>(), 1) rn_fwd_kernel(const FwdP
     unsigned char* orow =
         NV ? static_cast<unsigned char*>(p.out) + ((size_t)r * H + (size_t)cbase * VEC) / 2
            : static_cast<unsigned char*>(p.out) + ((size_t)r * H + (size_t)cbase * VEC) * oesz;
-    // NVFP4 block scales: one byte per 16 elements, written by the block's
-    // first lane
-    uint8_t* srow = NV ? p.scales + ((size_t)r * H + (size_t)cbase * VEC) / 16 : nullptr;
+    // NVFP4 / MXFP8 block scales: one byte per 16 / 32 elements, written by
+    // the block's first lane
+    uint8_t* srow = NV    ? p.scales + ((size_t)r * H + (size_t)cbase * VEC) / 16
+                    : MXR ? p.scales + ((size_t)r * H + (size_t)cbase * VEC) / 32
+                          : nullptr;
     const float2 rs2 = splat2(rs);
 #pragma unroll
     for (int k = 0; k < NC; ++k) {
       float2 y[PAIRS];
-      float bm = 0.0f;  // NVFP4: max |y| of this lane's chunk
+      float bm = 0.0f;  // NVFP4 / MXFP8 rowwise: max |y| of this lane's chunk
       if (k < nvalid_apply) {
         const int c = cbase + k * CSTEP;
         float4 gv[F4], bv[F4];
@@ -472,8 +479,9 @@ __global__ void __launch_bounds__(max_threads<NC>(), 1) rn_fwd_kernel(const FwdP
             ymax = amax_acc2(ymax, y[j]);  // one 3-input max on magnitudes a pair
           }
           if constexpr (NV) bm = fmaxf(bm, fmaxf(fabsf(y[j].x), fabsf(y[j].y)));
+          if constexpr (MXR) bm = amax_acc2(bm, y[j]);  // NaN wins
         }
-        if constexpr (QM != kQCurAmax && !NV)
+        if constexpr (QM != kQCurAmax && !NV && !MXR)
           store_chunk<PAIRS, QM>(orow + (size_t)k * ostep, p.out_f32, y, scale);
       }
       if constexpr (NV) {
@@ -495,6 +503,20 @@ __global__ void __launch_bounds__(max_threads<NC>(), 1) rn_fwd_kernel(const FwdP
           else
             *reinterpret_cast<unsigned short*>(o) = (unsigned short)codes;
           if ((lane & (16 / VEC - 1)) == 0) srow[(size_t)k * (CSTEP * VEC / 16)] = (uint8_t)sc;
+        }
+      }
+      if constexpr (MXR) {
+        // a 1x32 block spans 32 / VEC adjacent lanes (all valid or none:
+        // H % 32 == 0); E8M0 code of the block maximum, codes E4M3(y * 2^-e)
+#pragma unroll
+        for (int o = 1; o < 32 / VEC; o <<= 1) {
+          const float w = __shfl_xor_sync(0xffffffffu, bm, o);
+          asm("max.NaN.f32 %0, %0, %1;" : "+f"(bm) : "f"(w));
+        }
+        if (k < nvalid_apply) {
+          const uint32_t code = e8m0_code(bm);
+          store_chunk<PAIRS, QM>(orow + (size_t)k * ostep, 0, y, e8m0_inv_scale(code));
+          if ((lane & (32 / VEC - 1)) == 0) srow[(size_t)k * (CSTEP * VEC / 32)] = (uint8_t)code;
         }
       }
     }
@@ -576,6 +598,7 @@ rn_status launch_q(const FwdShape& sh, int qmode, const FwdParams& p, const Laun
     // its x: the plain kernel)
     case kQCurQuant: return launch_shape<TIn, NK, kQCurQuant>(sh, p, l, pdl, s);
     case kQNvfp4: return launch_shape<TIn, NK, kQNvfp4>(sh, p, l, pdl, s);
+    case kQMxRow: return launch_shape<TIn, NK, kQMxRow>(sh, p, l, pdl, s);
 #endif
     default: return RN_ERR_INVALID;
   }

@@ -22,6 +22,7 @@ enum FwdQuant : int {
   kQCurQuant = 3,   // current scaling, pass 2: quantize with 448/amax
   kQNvfp4 = 4,      // NVFP4, pass 2 (pass 1 is kQCurAmax): E2M1 codes with an
                     // E4M3 scale per 16 elements and S = 448*6/amax
+  kQMxRow = 5,      // MXFP8 rowwise blocks only (1x32, E8M0 scales), one pass
 };
 
 // NVFP4 pass 2 keeps a table of the 128 element factors S / value(scale
@@ -33,7 +34,7 @@ struct FwdParams {
   const float* gamma;   // 16-byte aligned
   const float* beta;
   void* out;            // [N, H] (bf16/fp32 or E4M3 codes); NVFP4: [N, H/2]
-  uint8_t* scales;      // NVFP4: E4M3 block-scale codes [N, H/16]
+  uint8_t* scales;      // NVFP4: E4M3 block-scale codes [N, H/16]; kQMxRow: E8M0 [N, H/32]
   float* mu;            // LayerNorm: written (pass 1) or read (kQCurQuant)
   float* rsigma;
   const float* scale;   // kQDelayed

@@ -243,19 +243,41 @@ def test_forward_sm_margin_and_repeat_bit_identical():
 
 
 @pytest.mark.parametrize("H", [256, 2048])
-def test_mxfp8_single_direction_and_margin(H):
-    """Rowwise-only and columnwise-only MXFP8 outputs equal the matching
-    halves of the two-direction call, for any sm_margin."""
+def test_mxfp8_columnwise_only_and_margin(H):
+    """Columnwise-only MXFP8 equals the columnwise half of the two-direction
+    call (the same kernel) for any sm_margin."""
     w = rn_inputs.make("mxfp8", N=192, H=H)
     both = _run_fwd(w, True, "mxfp8")
-    row = _run_fwd(w, True, "mxfp8", sm_margin=5, colwise=False)
     col = _run_fwd(w, True, "mxfp8", sm_margin=100, rowwise=False)
-    assert row[0].col_data is None and col[0].data is None
-    assert torch.equal(both[0].data, row[0].data) and torch.equal(both[0].row_scales, row[0].row_scales)
+    assert col[0].data is None
     assert torch.equal(both[0].col_data, col[0].col_data)
     assert torch.equal(both[0].col_scales, col[0].col_scales)
-    for o in (row, col):
-        assert np.array_equal(both[1], o[1]) and np.array_equal(both[2], o[2])
+    assert np.array_equal(both[1], col[1]) and np.array_equal(both[2], col[2])
+
+
+ROW_ONLY = [
+    # (workload, N, H, ln, sm_margin): rowwise-only MXFP8 takes the one-pass row kernel
+    ("mxfp8", 192, 2048, True, 0),
+    ("mxfp8", 96, 256, False, 5),
+    ("mxfp8", 64, 800, True, 0),       # lanes with a ragged share of the row
+    ("mxfp8", 32, 8192, True, 0),      # four warps a row
+    ("bwd_f32", 64, 1024, True, 0),    # fp32: a block spans 8 lanes
+    ("bwd_f32", 32, 96, False, 0),
+]
+
+
+@pytest.mark.parametrize("case", ROW_ONLY, ids=lambda c: f"{c[0]}-{c[1]}x{c[2]}-{'ln' if c[3] else 'rms'}-m{c[4]}")
+def test_mxfp8_rowwise_only(case):
+    name, N, H, ln, margin = case
+    w = rn_inputs.make(name, N=N, H=H)
+    if ln and w.beta is None:
+        w.beta = (np.random.default_rng(1).normal(0, 0.1, w.H)).astype(np.float32)
+    out, mu, rs = _run_fwd(w, ln, "mxfp8", sm_margin=margin, colwise=False)
+    assert out.col_data is None and out.col_scales is None
+    ref = _oracle_fwd(w, ln, "none")
+    check_stats(mu, rs, w.x_f64(), ref.get("mu"), ref["rsigma"])
+    check_mx(out.data.cpu().numpy(), out.row_scales.cpu().numpy(), ref["y"].astype(np.float32),
+             _terms(w, ref, ln), "mx-row-only")
 
 
 def test_forward_empty():
