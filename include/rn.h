@@ -158,8 +158,9 @@ rn_status rn_rmsnorm_fwd(const void* x, rn_dtype x_dtype, const float* gamma,
  *   per `mode`).
  * x, residual, residual_out: [N, H] in `dtype`, 16-byte aligned;
  * residual_out may not alias x or residual.  Modes NONE, FP8_DELAYED,
- * FP8_CURRENT and NVFP4 (their second pass reads residual_out); MXFP8 returns
- * RN_ERR_UNSUPPORTED.  Other arguments, errors and conventions as in the
+ * FP8_CURRENT and NVFP4 (their second pass reads residual_out), and MXFP8
+ * with the rowwise blocks only (col_data NULL; asking for the columnwise
+ * copy returns RN_ERR_UNSUPPORTED).  Other arguments, errors and conventions as in the
  * plain forward.
  */
 rn_status rn_layernorm_add_fwd(const void* x, const void* residual, rn_dtype dtype,

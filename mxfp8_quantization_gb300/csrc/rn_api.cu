@@ -377,7 +377,10 @@ rn_status fwd_common(int nk, const void* x, rn_dtype dt, const float* gamma, con
   // dtype; like the other row tensors they may be NULL when N == 0
   if (res && ((N > 0 && (residual == nullptr || residual_out == nullptr)) || nk == kIdentity))
     return RN_ERR_INVALID;
-  if (res && mode == RN_QUANT_MXFP8) return RN_ERR_UNSUPPORTED;
+  // with a residual add, MXFP8 gives the rowwise blocks only (one pass of
+  // the row kernel); the columnwise copy needs the 32-row tile kernels
+  if (res && mode == RN_QUANT_MXFP8 && (out == nullptr || out->col_data != nullptr))
+    return RN_ERR_UNSUPPORTED;
   if (res && N > 0 && (!aligned(residual, 16) || !aligned(residual_out, 16)))
     return RN_ERR_UNSUPPORTED;
   if ((x == nullptr && N > 0) || !dtype_ok(dt) || N < 0 || H < 1 || N > INT32_MAX ||
@@ -418,6 +421,15 @@ rn_status fwd_common(int nk, const void* x, rn_dtype dt, const float* gamma, con
     p.zcg = zcg ? 1 : 0;
     p.workers = pl.workers;
     p.Q = pl.Q;
+    if (res) {
+      FwdPlan pr;
+      if ((st = plan_fwd(nk, (int)H, esz, (int)N, sm_margin, di, &pr, 2)) != RN_OK) return st;
+      p.residual = residual;
+      p.residual_out = residual_out;
+      p.workers = pr.workers;
+      p.Q = pr.Q;
+      return launch_fwd_res(nk, bf16, pr.sh, kQMxRow, p, pr.l, false, stream);
+    }
     return launch_fwd(nk, bf16, pl.sh, kQMxRow, p, pl.l, false, stream);
   }
   if (mode == RN_QUANT_MXFP8) {

@@ -593,12 +593,12 @@ rn_status launch_q(const FwdShape& sh, int qmode, const FwdParams& p, const Laun
       else return launch_shape<TIn, NK, kQNone>(sh, p, l, pdl, s);
     case kQDelayed: return launch_shape<TIn, NK, kQDelayed>(sh, p, l, pdl, s);
     case kQCurAmax: return launch_shape<TIn, NK, kQCurAmax>(sh, p, l, pdl, s);
+    case kQMxRow: return launch_shape<TIn, NK, kQMxRow>(sh, p, l, pdl, s);
 #if !RN_FWD_RES_TU
-    // (with a residual, current scaling's pass 2 reads the stored sum as
-    // its x: the plain kernel)
+    // (with a residual, the second passes read the stored sum as their x:
+    // the plain kernel)
     case kQCurQuant: return launch_shape<TIn, NK, kQCurQuant>(sh, p, l, pdl, s);
     case kQNvfp4: return launch_shape<TIn, NK, kQNvfp4>(sh, p, l, pdl, s);
-    case kQMxRow: return launch_shape<TIn, NK, kQMxRow>(sh, p, l, pdl, s);
 #endif
     default: return RN_ERR_INVALID;
   }

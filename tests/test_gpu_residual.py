@@ -9,7 +9,7 @@ import torch
 import mxfp8_quantization_gb300 as rn
 import oracle
 import rn_inputs
-from parity import check_bf16, check_fp8_codes, check_stats, term_magnitude
+from parity import check_bf16, check_fp8_codes, check_mx, check_stats, term_magnitude
 
 pytestmark = pytest.mark.gpu
 
@@ -67,6 +67,9 @@ CASES = [
     ("rms_add", 3, 8, True, "none"),
     ("bwd_f32", 67, 1024, False, "none"),
     ("bwd_f32", 67, 1024, True, "fp8_delayed"),
+    ("rms_add", 96, 4096, True, "mxfp8"),
+    ("rms_add", 64, 2048, False, "mxfp8"),
+    ("bwd_f32", 64, 1024, True, "mxfp8"),
 ]
 
 
@@ -80,6 +83,11 @@ def _check(w, ln, mode, got, ref):
     check_stats(mu, rs, hf, ref.get("mu"), ref["rsigma"])
     wt = term_magnitude(hf, ref.get("mu") if ln else None, ref["rsigma"], w.gamma,
                         w.beta if ln else None, False)
+    if mode == "mxfp8":   # rowwise blocks only with the residual add
+        assert out.col_data is None and out.col_scales is None
+        check_mx(out.data.cpu().numpy(), out.row_scales.cpu().numpy(), ref["y"].astype(np.float32),
+                 wt, "residual mx-row")
+        return
     if mode == "none":
         if w.dtype == "bf16":
             check_bf16(bits(out), ref["y"], wt)
@@ -111,8 +119,10 @@ def test_residual_add_full_size_and_margin():
     assert np.array_equal(a[3], b[3]) and torch.equal(a[0].amax, b[0].amax)
 
 
-def test_residual_add_mxfp8_unsupported():
+def test_residual_add_mxfp8_is_rowwise_only():
+    """With the residual add, MXFP8 gives the rowwise blocks (a columnwise
+    request is refused on the host: tests/test_cpu_abi.py)."""
     w = _workload("rms_add", 64, 256)
-    with pytest.raises(rn.RNError):
-        rn.rmsnorm_add_fwd(to_dev(w.x, "bf16"), to_dev(w.residual, "bf16"), to_dev(w.gamma, "f32"),
-                           w.eps, quant="mxfp8")
+    out, h, rs = rn.rmsnorm_add_fwd(to_dev(w.x, "bf16"), to_dev(w.residual, "bf16"),
+                                    to_dev(w.gamma, "f32"), w.eps, quant="mxfp8")
+    assert out.col_data is None and out.data.shape == (64, 256) and out.row_scales.shape == (64, 8)
