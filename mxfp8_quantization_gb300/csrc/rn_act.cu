@@ -104,6 +104,19 @@ __device__ __forceinline__ void act_grad(float a, float b, float lim, float alph
   }
 }
 
+// E4M3 codes of s * y for one chunk (VEC values), element 0 in the low byte
+template <int VEC>
+__device__ __forceinline__ void store_e4m3(uint8_t* o, const float* y, float s) {
+  float2 z[VEC / 2];
+#pragma unroll
+  for (int i = 0; i < VEC / 2; ++i) z[i] = mul2(make_float2(y[2 * i], y[2 * i + 1]), splat2(s));
+  if constexpr (VEC == 8)
+    *reinterpret_cast<uint2*>(o) = make_uint2(pack_e4m3x4(z[0].x, z[0].y, z[1].x, z[1].y),
+                                              pack_e4m3x4(z[2].x, z[2].y, z[3].x, z[3].y));
+  else
+    *reinterpret_cast<uint32_t*>(o) = pack_e4m3x4(z[0].x, z[0].y, z[1].x, z[1].y);
+}
+
 __device__ __forceinline__ float warp_max_nan(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
@@ -166,10 +179,12 @@ __global__ void __launch_bounds__(kActThreads, 3) rn_act_fwd_kernel(const ActPar
           chunk_f32<TIn>(va[k], a);
           if constexpr (GLU) chunk_f32<TIn>(vb[k], b);
 #pragma unroll
-          for (int e = 0; e < VEC; ++e) {
-            y[e] = act_value<ACT>(a[e], GLU ? b[e] : 0.0f, p.limit, p.alpha) * s;
-            if constexpr (AMAX) asm("max.NaN.f32 %0, %0, %1;" : "+f"(amax) : "f"(fabsf(y[e])));
-            if (QM == kQNone && mx) asm("max.NaN.f32 %0, %0, %1;" : "+f"(bm) : "f"(fabsf(y[e])));
+          for (int e = 0; e < VEC; ++e) y[e] = act_value<ACT>(a[e], GLU ? b[e] : 0.0f, p.limit, p.alpha) * s;
+          // magnitudes two at a time (3-input max; NaN wins)
+#pragma unroll
+          for (int e = 0; e < VEC; e += 2) {
+            if constexpr (AMAX) amax = amax_acc2(amax, make_float2(y[e], y[e + 1]));
+            if (QM == kQNone && mx) bm = amax_acc2(bm, make_float2(y[e], y[e + 1]));
           }
         }
         if (QM == kQNone && mx) {
@@ -183,14 +198,7 @@ __global__ void __launch_bounds__(kActThreads, 3) rn_act_fwd_kernel(const ActPar
           if (valid) {
             const uint32_t code = e8m0_code(bm);
             const float inv = e8m0_inv_scale(code);
-            uint8_t* o = static_cast<uint8_t*>(p.out) + (size_t)row * H + (size_t)c * VEC;
-            if constexpr (VEC == 8)
-              *reinterpret_cast<uint2*>(o) =
-                  make_uint2(pack_e4m3x4(y[0] * inv, y[1] * inv, y[2] * inv, y[3] * inv),
-                             pack_e4m3x4(y[4] * inv, y[5] * inv, y[6] * inv, y[7] * inv));
-            else
-              *reinterpret_cast<uint32_t*>(o) =
-                  pack_e4m3x4(y[0] * inv, y[1] * inv, y[2] * inv, y[3] * inv);
+            store_e4m3<VEC>(static_cast<uint8_t*>(p.out) + (size_t)row * H + (size_t)c * VEC, y, inv);
             if ((lane & (32 / VEC - 1)) == 0)
               p.row_scales[(size_t)row * (H / 32) + (size_t)c * VEC / 32] = (uint8_t)code;
           }
@@ -216,14 +224,7 @@ __global__ void __launch_bounds__(kActThreads, 3) rn_act_fwd_kernel(const ActPar
                   make_uint2(pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3]));
           }
         } else {  // E4M3 codes with the tensor scale
-          uint8_t* o = static_cast<uint8_t*>(p.out) + (size_t)row * H + (size_t)c * VEC;
-          if constexpr (VEC == 8)
-            *reinterpret_cast<uint2*>(o) =
-                make_uint2(pack_e4m3x4(y[0] * scale, y[1] * scale, y[2] * scale, y[3] * scale),
-                           pack_e4m3x4(y[4] * scale, y[5] * scale, y[6] * scale, y[7] * scale));
-          else
-            *reinterpret_cast<uint32_t*>(o) =
-                pack_e4m3x4(y[0] * scale, y[1] * scale, y[2] * scale, y[3] * scale);
+          store_e4m3<VEC>(static_cast<uint8_t*>(p.out) + (size_t)row * H + (size_t)c * VEC, y, scale);
         }
       }
     }
