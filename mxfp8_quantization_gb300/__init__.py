@@ -135,6 +135,12 @@ def _need(t, name, dtype=None, shape=None):
         raise RNError(f"{name} is required")
     if not t.is_cuda or not t.is_contiguous():
         raise RNError(f"{name} must be a contiguous CUDA tensor")
+    # the library launches on the current device (and picks its per-device
+    # state by it): a tensor on another device would be read through the
+    # wrong device's pointers
+    if t.device.index != torch.cuda.current_device():
+        raise RNError(f"{name} is on {t.device}, but the current device is "
+                      f"cuda:{torch.cuda.current_device()}")
     if dtype is not None and t.dtype != dtype:
         raise RNError(f"{name} must be {dtype}, got {t.dtype}")
     if shape is not None and tuple(t.shape) != tuple(shape):

@@ -131,18 +131,18 @@ rn_status plan_roles(int nchunks, size_t per_slot, size_t fixed, const DeviceInf
 // without them, need more than the 128 registers a thread of a 512-thread
 // CTA has).  Threads a CTA follow from NC (512 for NC = 16, 768 for 8, 1024
 // for 4: the registers of the row part); W = every warp but the producer, in whole
-// groups, at most 14 groups of G >= 2; one CTA per SM; a ring of Q > W / G
-// rows.
+// groups, at most 14 groups of G >= 2; one CTA per SM; a ring of Q slots of
+// 2^rps_log2 adjacent rows each, W / G <= (Q - 1) 2^rps_log2.
 struct FwdPlan {
   FwdShape sh;
-  int workers, Q;
+  int workers, Q, rps_log2;
   Launch l;
 };
 
 int fwd_max_threads(int nc) { return nc >= 16 ? 512 : (nc >= 8 ? 768 : 1024); }
 
 rn_status plan_fwd(int nk, int H, int esz, int N, int sm_margin, const DeviceInfo& di,
-                   FwdPlan* pl, int rows_per_slot = 1, size_t extra_bytes = 0) {
+                   FwdPlan* pl, int streams = 1, size_t extra_bytes = 0) {
   const int nchunks = H * esz / 16;
   FwdShape sh{1, 16, false};
   while (sh.g <= 8 && nchunks > 32 * sh.g * 16) sh.g *= 2;
@@ -165,12 +165,21 @@ rn_status plan_fwd(int nk, int H, int esz, int N, int sm_margin, const DeviceInf
   // for longer rows
   const size_t gb =
       (nk != kIdentity && g <= 2) ? (size_t)H * sizeof(float) * (nk == kLn ? 2 : 1) : 0;
+  // a slot holds 2^lg adjacent rows, moved by one copy (each copy request
+  // costs the copy engine time of its own: 4 KB rows one a copy kept the
+  // stream at two thirds of the HBM rate): copies of at least 8 KB, as long
+  // as every SM still gets 4 groups or more
+  const size_t row_bytes = (size_t)H * esz;
+  const long long sms = di.sms - sm_margin;
+  int lg = 0;
+  while (lg < 3 && (row_bytes << lg) < 8192 && (long long)(N >> (lg + 1)) >= 4 * sms) ++lg;
+  const int rps = 1 << lg;
   // fixed: gamma/beta, group exchange (14 groups x 4 x 8 floats), amax words
-  // (32), slack; per slot: the row, (mu, rsigma), two mbarriers
+  // (32), slack; per slot: the rows, their (mu, rsigma), two mbarriers
   // (+ extra_bytes after the barriers: the NVFP4 factor table)
   const size_t fixed = gb + 14 * 4 * 8 * sizeof(float) + 32 * sizeof(uint32_t) + 64 + extra_bytes;
-  // (with a residual add a slot holds the x row and the residual row)
-  const size_t per_slot = (size_t)rows_per_slot * H * esz + sizeof(float2) + 16;
+  // (with a residual add a slot holds the x rows and the residual rows)
+  const size_t per_slot = (size_t)rps * ((size_t)streams * row_bytes + sizeof(float2)) + 16;
   const size_t budget = cta_smem_budget(di, 1);
   int Q = budget > fixed ? (int)((budget - fixed) / per_slot) : 0;
   if (Q > 64) Q = 64;
@@ -180,17 +189,21 @@ rn_status plan_fwd(int nk, int H, int esz, int N, int sm_margin, const DeviceInf
     if (qmax < 2) qmax = 2;
     if (Q > qmax) Q = qmax;
   }
+  if (Q < 2) return RN_ERR_UNSUPPORTED;
   int W = (fwd_max_threads(sh.nc) / 32 - 1) / g * g;
   // groups of several warps: at most 14 (their named barriers are 1 .. 14)
   if (g > 1 && W / g > 14) W = 14 * g;
-  while (W > g && W / g >= Q) W -= g;
-  if (W / g >= Q) return RN_ERR_UNSUPPORTED;
+  // rows in work at once (one a group) stay within Q - 1 slots, which keeps
+  // the slot barriers' parity waits alias-free
+  while (W > g && W / g > (Q - 1) * rps) W -= g;
+  if (W / g > (Q - 1) * rps) return RN_ERR_UNSUPPORTED;
   pl->sh = sh;
   pl->workers = W;
   pl->Q = Q;
+  pl->rps_log2 = lg;
   pl->l.threads = 32 * (W + 1);
   pl->l.smem = (size_t)Q * per_slot + fixed;
-  pl->l.work = N;
+  pl->l.work = (N + rps - 1) / rps;
   pl->l.sms = di.sms - sm_margin;
   pl->l.per_sm = 1;
   return RN_OK;
@@ -421,6 +434,7 @@ rn_status fwd_common(int nk, const void* x, rn_dtype dt, const float* gamma, con
     p.zcg = zcg ? 1 : 0;
     p.workers = pl.workers;
     p.Q = pl.Q;
+    p.rps_log2 = pl.rps_log2;
     if (res) {
       FwdPlan pr;
       if ((st = plan_fwd(nk, (int)H, esz, (int)N, sm_margin, di, &pr, 2)) != RN_OK) return st;
@@ -428,6 +442,7 @@ rn_status fwd_common(int nk, const void* x, rn_dtype dt, const float* gamma, con
       p.residual_out = residual_out;
       p.workers = pr.workers;
       p.Q = pr.Q;
+      p.rps_log2 = pr.rps_log2;
       return launch_fwd_res(nk, bf16, pr.sh, kQMxRow, p, pr.l, false, stream);
     }
     return launch_fwd(nk, bf16, pl.sh, kQMxRow, p, pl.l, false, stream);
@@ -483,6 +498,7 @@ rn_status fwd_common(int nk, const void* x, rn_dtype dt, const float* gamma, con
   p.residual_out = residual_out;
   p.workers = pl.workers;
   p.Q = pl.Q;
+  p.rps_log2 = pl.rps_log2;
   p.reverse = 0;
   // pass 1 (or the only pass): with a residual, the kernel that adds it
   auto first = [&](int qmode, bool pdl) {
@@ -508,6 +524,7 @@ rn_status fwd_common(int nk, const void* x, rn_dtype dt, const float* gamma, con
       q.residual_out = nullptr;
       q.workers = p2.workers;
       q.Q = p2.Q;
+      q.rps_log2 = p2.rps_log2;
       q.reverse = 1;
       return launch_fwd(nk, bf16, p2.sh, kQCurQuant, q, p2.l, true, stream);
     }
@@ -525,6 +542,7 @@ rn_status fwd_common(int nk, const void* x, rn_dtype dt, const float* gamma, con
       q.scales = out->row_scales;
       q.workers = p2.workers;
       q.Q = p2.Q;
+      q.rps_log2 = p2.rps_log2;
       q.reverse = 1;
       return launch_fwd(nk, bf16, p2.sh, kQNvfp4, q, p2.l, true, stream);
     }

@@ -5,10 +5,15 @@
 //
 // Design (one persistent CTA per SM, rows b, b + grid, b + 2 grid, ... for
 // CTA b):
-//   * producer warp: one lane streams whole rows of x into a ring of Q
+//   * producer warp: one lane streams rows of x into a ring of Q
 //     shared-memory slots with the bulk-copy engine (cp.async.bulk,
 //     completion on the slot's "full" mbarrier) and refills a slot as soon as
-//     its row has been read out ("empty"); when a pass needs the saved
+//     its rows have been read out ("empty").  A slot holds rps adjacent rows
+//     (rps = 2^rps_log2), moved by one copy: a copy engine request has a cost
+//     of its own, and rows of 4 KB one copy each left the stream at about
+//     two thirds of the HBM rate (65536 x 2048 bf16, FP8 delayed: 93 us with
+//     one row a copy, 59 us with two); so CTA b takes the row groups b,
+//     b + grid, ... of rps rows each.  When a pass needs the saved
 //     mu / rsigma of a row, the same lane fetches them into the slot with
 //     4-byte cp.async tracked by the same barrier;
 //   * worker warps, in groups of G warps (G = 1 up to H = 4096 bf16 /
@@ -162,17 +167,19 @@ __device__ __forceinline__ uint32_t pack_e2m1(const float2* q) {
   return r;
 }
 
-// The rows of this CTA: b, b + g, b + 2g, ... (b = blockIdx.x, g = gridDim.x),
-// from the last one when reverse.
+// The row groups of this CTA: b, b + g, b + 2g, ... (b = blockIdx.x,
+// g = gridDim.x), from the last one when reverse; group k holds rows
+// k rps .. k rps + rps - 1 (the last group of all may be short).
 struct RowSeq {
   int first, step, count;
   __device__ __forceinline__ explicit RowSeq(const FwdParams& p) {
     const int b = blockIdx.x, g = gridDim.x;
-    count = b < p.N ? (p.N - b + g - 1) / g : 0;
+    const int ng = (p.N + (1 << p.rps_log2) - 1) >> p.rps_log2;
+    count = b < ng ? (ng - b + g - 1) / g : 0;
     first = p.reverse ? b + (count - 1) * g : b;
     step = p.reverse ? -g : g;
   }
-  __device__ __forceinline__ int row(int i) const { return first + i * step; }
+  __device__ __forceinline__ int group(int i) const { return first + i * step; }
 };
 
 // sum of one value per warp over the G warps of a group, added in warp
@@ -220,15 +227,18 @@ __global__ void __launch_bounds__(max_threads<NC>(), 1) rn_fwd_kernel(const FwdP
   const int H = p.H;
   const int nchunks = H / VEC;
   const uint32_t row_bytes = (uint32_t)H * sizeof(TIn);
-  const uint32_t slot_bytes = RES ? 2 * row_bytes : row_bytes;  // x row (then the residual row)
+  const int lg = p.rps_log2;
+  const int rps = 1 << lg;                             // rows a slot holds
+  const uint32_t grp_bytes = (uint32_t)rps * row_bytes;
+  const uint32_t slot_bytes = RES ? 2 * grp_bytes : grp_bytes;  // x rows (then the residual rows)
   const uint32_t Q = (uint32_t)p.Q;
   const size_t gb_bytes = GB_SMEM ? (size_t)H * sizeof(float) * (LN ? 2 : 1) : 0;
 
   float4* gsm = reinterpret_cast<float4*>(smem);  // [F4][nchunks]: g of chunk c, part j
   float4* bsm = gsm + (size_t)F4 * nchunks;       // same for beta (LayerNorm)
   unsigned char* ring = smem + gb_bytes;
-  float2* rstat = reinterpret_cast<float2*>(ring + (size_t)Q * slot_bytes);  // [Q] (mu, rsigma)
-  float* red = reinterpret_cast<float*>(rstat + Q);                   // [kMaxGroups][4][8]
+  float2* rstat = reinterpret_cast<float2*>(ring + (size_t)Q * slot_bytes);  // [Q][rps] (mu, rsigma)
+  float* red = reinterpret_cast<float*>(rstat + (size_t)Q * rps);     // [kMaxGroups][4][8]
   uint32_t* red2 = reinterpret_cast<uint32_t*>(red + kMaxGroups * 4 * 8);  // [32]
   uint64_t* full = reinterpret_cast<uint64_t*>(red2 + 32);                  // row landed
   uint64_t* empty = full + Q;                                               // row read out
@@ -240,7 +250,7 @@ __global__ void __launch_bounds__(max_threads<NC>(), 1) rn_fwd_kernel(const FwdP
 
   for (uint32_t i = threadIdx.x; i < Q; i += blockDim.x) {
     mbar_init(smem_u32(&full[i]), META ? 2 : 1);
-    mbar_init(smem_u32(&empty[i]), G);
+    mbar_init(smem_u32(&empty[i]), G * rps);
     fence_barrier_init();
   }
   __syncthreads();
@@ -255,25 +265,28 @@ __global__ void __launch_bounds__(max_threads<NC>(), 1) rn_fwd_kernel(const FwdP
       const unsigned char* xb = static_cast<const unsigned char*>(p.x);
       RingPos pos{0u, 0u};
       for (int i = 0; i < seq.count; ++i) {
-        const int r = seq.row(i);
+        const int r0 = seq.group(i) << lg;
+        const int nr = min(rps, p.N - r0);  // rows of this group
+        const uint32_t bytes = (uint32_t)nr * row_bytes;
         const uint32_t s = pos.slot;
         // a start-up burst of whole rings from every SM lands all at once,
-        // late; instead the first kStartRows rows go out alone and the rest
-        // of the ring once row 0 is in, so that the workers start early
+        // late; instead the first kStartRows slots go out alone and the rest
+        // of the ring once slot 0 is in, so that the workers start early
         if (i == kStartRows) mbar_wait(smem_u32(&full[0]), 0u, &g_err_fwd, kErrFullWait);
         if (i >= (int)Q) mbar_wait(smem_u32(&empty[s]), pos.phase ^ 1u, &g_err_fwd, kErrEmptyWait);
         const uint32_t bar = smem_u32(&full[s]);
         if constexpr (META) {
-          if (LN) cp_async4(smem_u32(&rstat[s].x), p.mu + r);
-          cp_async4(smem_u32(&rstat[s].y), p.rsigma + r);
+          for (int j = 0; j < nr; ++j) {
+            if (LN) cp_async4(smem_u32(&rstat[s * rps + j].x), p.mu + r0 + j);
+            cp_async4(smem_u32(&rstat[s * rps + j].y), p.rsigma + r0 + j);
+          }
           cp_async_arrive(bar);
         }
-        mbar_arrive_expect_tx(bar, slot_bytes);
-        bulk_g2s(smem_u32(ring + (size_t)s * slot_bytes), xb + (size_t)r * row_bytes, row_bytes,
-                 bar);
+        mbar_arrive_expect_tx(bar, RES ? 2 * bytes : bytes);
+        bulk_g2s(smem_u32(ring + (size_t)s * slot_bytes), xb + (size_t)r0 * row_bytes, bytes, bar);
         if constexpr (RES)
-          bulk_g2s(smem_u32(ring + (size_t)s * slot_bytes + row_bytes),
-                   static_cast<const unsigned char*>(p.residual) + (size_t)r * row_bytes, row_bytes,
+          bulk_g2s(smem_u32(ring + (size_t)s * slot_bytes + grp_bytes),
+                   static_cast<const unsigned char*>(p.residual) + (size_t)r0 * row_bytes, bytes,
                    bar);
         pos.advance(1, Q);
       }
@@ -347,33 +360,44 @@ __global__ void __launch_bounds__(max_threads<NC>(), 1) rn_fwd_kernel(const FwdP
   }
   float ymax = 0.0f;  // running max |y| (NaN wins)
 
-  RingPos pos{(uint32_t)group, 0u};
+  // position i of the CTA's rows: row i & (rps - 1) of its group i >> lg,
+  // whose slot and phase `pos` tracks (groups advance by less than Q per
+  // step: NGR <= (Q - 1) rps)
+  RingPos pos{0u, 0u};
+  int kg = group >> lg;
+  pos.advance((uint32_t)kg, Q);
   int par = 0;
-  for (int i = group; i < seq.count; i += NGR) {
+  for (int i = group; i < (seq.count << lg); i += NGR) {
+    pos.advance((uint32_t)((i >> lg) - kg), Q);
+    kg = i >> lg;
+    const int jr = i & (rps - 1);
+    const int r = (seq.group(kg) << lg) + jr;
+    // the short last group of all: its missing rows are skipped by every
+    // warp of the group (that slot is never used again)
+    if (r >= p.N) continue;
     const uint32_t s = pos.slot;
     // before waiting for this use of the slot, wait for the previous use to
     // be released: that use has then landed, so the parity wait below cannot
-    // match a phase one lap old (alias-free since NGR < Q)
-    if (i >= (int)Q) mbar_wait(smem_u32(&empty[s]), pos.phase ^ 1u, &g_err_fwd, kErrStatsWait);
+    // match a phase one lap old (alias-free since NGR <= (Q - 1) rps: a group
+    // reaching this slot has already seen every earlier use of it issued)
+    if (kg >= (int)Q) mbar_wait(smem_u32(&empty[s]), pos.phase ^ 1u, &g_err_fwd, kErrStatsWait);
     mbar_wait(smem_u32(&full[s]), pos.phase, &g_err_fwd, kErrFullWait);
-    const unsigned char* rowp = ring + (size_t)s * slot_bytes;
+    const unsigned char* rowp = ring + (size_t)s * slot_bytes + (size_t)jr * row_bytes;
     Raw raw[NC];
 #pragma unroll
     for (int k = 0; k < NC; ++k)
       if (k < nvalid) {
         raw[k] = V::load(rowp, cbase + k * CSTEP);
-        if constexpr (RES) raw[k] = V::add_rn(raw[k], V::load(rowp + row_bytes, cbase + k * CSTEP));
+        if constexpr (RES) raw[k] = V::add_rn(raw[k], V::load(rowp + grp_bytes, cbase + k * CSTEP));
       }
     float mean = 0.0f, rs = 1.0f;
     if constexpr (META) {
-      const float2 m = rstat[s];
+      const float2 m = rstat[s * rps + jr];
       mean = LN ? m.x : 0.0f;
       rs = m.y;
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(smem_u32(&empty[s]));
-    pos.advance((uint32_t)NGR, Q);
-    const int r = seq.row(i);
     if constexpr (RES) {
       // the new residual stream: h in the input dtype
       unsigned char* hrow = static_cast<unsigned char*>(p.residual_out) + (size_t)r * row_bytes;

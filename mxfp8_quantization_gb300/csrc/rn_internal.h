@@ -48,7 +48,8 @@ struct FwdParams {
   const void* residual; // residual add: the residual [N, H] (x's dtype), or NULL
   void* residual_out;   // residual add: h = x + residual [N, H], or NULL
   int workers;          // worker warps (a multiple of the row group size)
-  int Q;                // ring slots (rows); more than workers / group size
+  int Q;                // ring slots; workers / group size <= (Q - 1) rows a slot
+  int rps_log2;         // a slot holds 2^rps_log2 adjacent rows (one copy)
   int reverse;          // walk the rows from the last one
 };
 

@@ -10,8 +10,8 @@ def test_norm_forward_and_backward_bytes():
     # LayerNorm fwd FP8 delayed, bf16: x in (2E), codes out (E), gamma + beta
     # (8H), mu + rsigma (8N)
     assert bench.algorithmic_bytes("fwd_fp8", N, H, 2, True) == 2 * E + E + 8 * H + 8 * N
-    # backward: dz, x in and dx out (3 x 2E), mu + rsigma in (8N), dgamma out
-    # (4H) and gamma + beta (8H)
+    # backward: dz, x in and dx out (3 x 2E), mu + rsigma in (8N), gamma in
+    # (4H), dgamma + dbeta out (8H)
     assert bench.algorithmic_bytes("bwd", N, H, 2, True) == 6 * E + 8 * N + 12 * H
     # the headline step is their sum
     assert (bench.algorithmic_bytes("fwd_fp8", N, H, 2, True) + bench.algorithmic_bytes("bwd", N, H, 2, True)

@@ -190,3 +190,20 @@ def test_scaled_activation_rejects_bad_arguments_on_host(lib):
     assert lib.rn_scaled_act_bwd(1, None, x, 0, None, 4, 1024, f32(7), f32(1.702), x, None, None) == 1
     assert lib.rn_scaled_act_bwd(1, x, x, 0, None, 4, 1024, f32(7), f32(1.702), None, None, None) == 1
     assert lib.rn_scaled_act_bwd(1, x, x, 0, None, 4, 1024, f32(7), f32(1.702), ctypes.c_void_p(0x2004), None, None) == 2
+
+
+def test_binding_rejects_a_tensor_on_another_device(monkeypatch):
+    import torch
+
+    class OnDevice1:
+        is_cuda = True
+        device = torch.device("cuda", 1)
+        dtype = torch.float32
+        shape = (4,)
+
+        def is_contiguous(self):
+            return True
+
+    monkeypatch.setattr(torch.cuda, "current_device", lambda: 0)
+    with pytest.raises(rn.RNError, match="current device"):
+        rn._need(OnDevice1(), "x")

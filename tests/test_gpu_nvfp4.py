@@ -142,6 +142,8 @@ FWD = [
     ("bwd_f32", 67, 1024, True, 0),          # fp32 input: a block spans four lanes
     ("bwd_f32", 33, 8192, False, 0),
     ("rms_small", 3, 16, False, 0),          # one block a row
+    ("rms_current", 2437, 1024, False, 0),   # four rows a ring slot, short last group
+    ("ln_delayed", 1301, 2048, True, 0),     # two rows a ring slot
 ]
 
 

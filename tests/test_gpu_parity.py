@@ -183,6 +183,14 @@ FWD_CASES = [
     ("ln_delayed", 9, 16384, True, "fp8_delayed"),
     ("rms_small", 1, 8, False, "none"),
     ("rms_small", 3, 8, True, "fp8_current"),
+    # rows of < 8 KB with many rows go several to a ring slot (one copy):
+    # 4 KB rows two a slot, 2 KB four, 1 KB eight; N leaves a short last group
+    ("ln_delayed", 1301, 2048, True, "fp8_delayed"),
+    ("ln_delayed", 1301, 2048, True, "none"),
+    ("rms_current", 2437, 1024, False, "fp8_current"),
+    ("rms_current", 2437, 1024, True, "fp8_current"),
+    ("bwd_f32", 4900, 256, True, "fp8_delayed"),
+    ("bwd_f32", 4900, 256, False, "none"),
 ]
 
 
@@ -263,6 +271,8 @@ ROW_ONLY = [
     ("mxfp8", 32, 8192, True, 0),      # four warps a row
     ("bwd_f32", 64, 1024, True, 0),    # fp32: a block spans 8 lanes
     ("bwd_f32", 32, 96, False, 0),
+    ("mxfp8", 1312, 2048, True, 0),    # two rows a ring slot
+    ("mxfp8", 4896, 512, False, 0),    # eight rows a ring slot
 ]
 
 

@@ -70,6 +70,11 @@ CASES = [
     ("rms_add", 96, 4096, True, "mxfp8"),
     ("rms_add", 64, 2048, False, "mxfp8"),
     ("bwd_f32", 64, 1024, True, "mxfp8"),
+    # rows of 4 / 2 KB go two / four to a ring slot (x and residual rows);
+    # N leaves a short last group
+    ("rms_add", 1301, 2048, False, "fp8_delayed"),
+    ("rms_add", 2437, 1024, True, "fp8_current"),
+    ("rms_add", 1312, 2048, True, "mxfp8"),
 ]
 
 

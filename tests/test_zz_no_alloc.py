@@ -3,9 +3,12 @@ allocate device memory where they run it.  It keeps its dgamma/dbeta partial
 sums in the library's fixed per-device scratch array instead of a workspace.
 
 Called here through the C ABI (ctypes, raw device pointers) and compared with
-the regular rn_layernorm_bwd on the same inputs, on two calls in a row with
-different shapes, so that whatever the first call left in the shared array
-cannot leak into the second.  This file is collected last on purpose.
+the regular rn_layernorm_bwd on the same inputs: both run the same kernels
+with the same chunking, so the results must be bit-identical.  Each call is
+also checked against the fp64 oracle.  The calls run back to back on the
+shared array, the largest problem first, so that a smaller call that read
+partials past its own chunk count would pick up the larger call's leftovers
+and fail.  This file is collected last on purpose.
 """
 import ctypes
 
@@ -16,6 +19,7 @@ import torch
 import mxfp8_quantization_gb300 as rn
 import oracle
 import rn_inputs
+from parity import bf16_ulp
 
 pytestmark = pytest.mark.gpu
 
@@ -24,21 +28,28 @@ def _dev_bf16(a):
     return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).cuda()
 
 
-def _case(N, H, seed):
+def _case(N, H, seed, zcg):
     w = rn_inputs.make("bwd_bf16", N=N, H=H, seed=seed)
-    m, r = oracle.layernorm_stats(w.x_f64(), w.eps)
-    return (_dev_bf16(w.x), _dev_bf16(w.dz), torch.from_numpy(w.gamma).cuda(),
-            torch.from_numpy(m.astype(np.float32)).cuda(), torch.from_numpy(r.astype(np.float32)).cuda())
+    x64, dz64 = w.x_f64(), w.dz_f64()
+    m, r = oracle.layernorm_stats(x64, w.eps)
+    mu, rs = m.astype(np.float32), r.astype(np.float32)
+    ref = oracle.layernorm_bwd(dz64, x64, mu, rs, w.gamma, zcg, "bf16")
+    xhat = (x64 - mu[:, None].astype(np.float64)) * rs[:, None].astype(np.float64)
+    den = (np.sum(np.abs(dz64 * xhat), axis=0), np.sum(np.abs(dz64), axis=0))
+    dev = (_dev_bf16(w.x), _dev_bf16(w.dz), torch.from_numpy(w.gamma).cuda(),
+           torch.from_numpy(mu).cuda(), torch.from_numpy(rs).cuda())
+    return dev, ref, den
 
 
-def _noalloc(lib, x, dz, g, mu, rs):
+def _noalloc(lib, x, dz, g, mu, rs, zcg, margin):
     N, H = x.shape
     dx = torch.empty_like(x)
     dg = torch.empty(H, dtype=torch.float32, device="cuda")
     db = torch.empty(H, dtype=torch.float32, device="cuda")
     p = lambda t: ctypes.c_void_p(t.data_ptr())
-    st = lib.rn_layernorm_bwd_noalloc(p(dz), p(x), 0, p(mu), p(rs), p(g), N, H, 0, 0, p(dx), p(dg),
-                                      p(db), ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    st = lib.rn_layernorm_bwd_noalloc(p(dz), p(x), 0, p(mu), p(rs), p(g), N, H, zcg, margin, p(dx),
+                                      p(dg), p(db),
+                                      ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
     assert st == 0, lib.rn_status_str(st)
     return dx, dg, db
 
@@ -48,23 +59,32 @@ def _bf16_to_f64(t):
             ).view(np.float32).astype(np.float64)
 
 
-def test_noalloc_backward_matches_regular_on_two_calls():
+def _check_oracle(got, ref, den):
+    # the parity tolerances: dx within one bf16 ulp of the oracle's rounded
+    # value (or 2e-3 of the row's rms), dgamma / dbeta within 1e-3 of the
+    # summed magnitudes of their terms
+    dx64 = ref["dx64"]
+    r = oracle.round_to_bf16(dx64)
+    rms = np.sqrt(np.mean(dx64 ** 2, axis=1, keepdims=True))
+    err = np.abs(_bf16_to_f64(got[0]) - r)
+    assert np.all((err <= bf16_ulp(r)) | (err <= 2e-3 * rms))
+    assert np.all(np.abs(got[1].cpu().numpy() - ref["dgamma64"]) <= 1e-3 * den[0])
+    assert np.all(np.abs(got[2].cpu().numpy() - ref["dbeta64"]) <= 1e-3 * den[1])
+
+
+def test_noalloc_backward_matches_regular_on_calls_in_a_row():
     lib = rn._load()
-    for N, H, seed in ((1000, 2048, 5), (3000, 5120, 6)):
-        x, dz, g, mu, rs = _case(N, H, seed)
-        ref = rn.layernorm_bwd(dz, x, mu, rs, g)
-        got = _noalloc(lib, x, dz, g, mu, rs)
+    # largest first: 375 chunks of partials (15 MB of the 16 MiB), then 125,
+    # then a zero-centered call with 16 SMs left free
+    for N, H, seed, zcg, margin in ((3000, 5120, 6, 0, 0), (1000, 2048, 5, 0, 0),
+                                    (1000, 2048, 7, 1, 16)):
+        (x, dz, g, mu, rs), ref, den = _case(N, H, seed, bool(zcg))
+        want = rn.layernorm_bwd(dz, x, mu, rs, g, margin, bool(zcg))
+        got = _noalloc(lib, x, dz, g, mu, rs, zcg, margin)
         torch.cuda.synchronize()
-        # the parity tests' tolerances: dx within one bf16 ulp, dgamma and
-        # dbeta within 1e-3 of the summed magnitudes of their terms
-        a, b = _bf16_to_f64(got[0]), _bf16_to_f64(ref[0])
-        ulp = np.exp2(np.floor(np.log2(np.maximum(np.abs(b), 2.0 ** -126))) - 7)
-        assert np.all(np.abs(a - b) <= ulp)
-        xh = (x.float() - mu[:, None]) * rs[:, None]
-        den_g = (dz.float() * xh).abs().sum(0).cpu().numpy().astype(np.float64)
-        den_b = dz.float().abs().sum(0).cpu().numpy().astype(np.float64)
-        assert np.all(np.abs(got[1].cpu().numpy() - ref[1].cpu().numpy()) <= 1e-3 * den_g)
-        assert np.all(np.abs(got[2].cpu().numpy() - ref[2].cpu().numpy()) <= 1e-3 * den_b)
+        for a, b in zip(got, want):
+            assert torch.equal(a, b)
+        _check_oracle(got, ref, den)
     assert rn.device_error() == 0
 
 
