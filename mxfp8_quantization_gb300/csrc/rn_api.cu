@@ -217,7 +217,6 @@ rn_status plan_fwd(int nk, int H, int esz, int N, int sm_margin, const DeviceInf
 struct MxPlan {
   int Q, n_tbar, apply_warps, stats_warps;
   Launch l;
-  int Qs = 0;  // slab kernel: row-ring slots
 };
 
 rn_status plan_mx(int nk, int H, int esz, int N, int sm_margin, const DeviceInfo& di,
@@ -253,44 +252,33 @@ rn_status plan_mx(int nk, int H, int esz, int N, int sm_margin, const DeviceInfo
   return RN_OK;
 }
 
-// MXFP8 slab kernel (bf16, H a multiple of kMxSlabCols, H <= 4096): A apply
-// warps, the largest divisor of the slabs per row up to 8; S = 6 stats
-// warps; two producer warps (16 warps in all); a row ring of about 80 KB (a multiple of S
-// rows) and a slab ring of 3 A slabs, both shrunk to fit; NT = 3 tiles of
-// statistics in flight.
-rn_status plan_mx_slab(int nk, int H, int N, int sm_margin, const DeviceInfo& di, MxPlan* pl) {
-  if (nk == kIdentity || H % kMxSlabCols != 0 || H > 4096) return RN_ERR_UNSUPPORTED;
-  const int nslab = H / kMxSlabCols;
-  int A = nslab < 8 ? nslab : 8;
-  while (nslab % A != 0) --A;
-  const int S = 6;  // LayerNorm's two statistics passes need 6 (4: 170 us, 6: 146 us)
-  const int NT = 3;
-  const size_t row_bytes = (size_t)H * 2;
-  const size_t slab_bytes = (size_t)32 * kMxSlabCols * 2;
-  const size_t gb = (size_t)H * sizeof(float) * (nk == kLn ? 2 : 1);
+// MXFP8 box kernel (bf16 H a multiple of 64, fp32 H of 32; N of 32): 16
+// worker warps, one CTA per SM; fixed: 1 KB for aligning the box ring to
+// 1024 bytes, the statistics partials of two tiles (2 x 2 nbox x 32
+// float2), two tiles' (mean, rsigma), two barriers; per slot: a 16 KB box,
+// an mbarrier, a ticket and a pending-read count.  At least 4 slots.
+rn_status plan_mx_box(int nk, int H, int esz, int N, int sm_margin, const DeviceInfo& di,
+                      MxPlan* pl) {
+  const int c0 = 128 / esz;
+  if (H % c0 != 0 || N % 32 != 0) return RN_ERR_UNSUPPORTED;
+  const int nbox = (H / c0 + 3) / 4;
+  const int nus = nk == kIdentity ? 0 : 2 * nbox;
+  const size_t fixed = 1024 + 2 * (size_t)nus * 32 * sizeof(float2) + 2 * 32 * sizeof(float2) +
+                       4 * sizeof(uint64_t) + 64;
+  const size_t per_slot = kMxBoxBytes + sizeof(uint64_t) + 2 * sizeof(uint32_t);
   const size_t budget = cta_smem_budget(di, 1);
-  auto need = [&](int qs, int qa) {
-    return gb + (size_t)qs * row_bytes + (size_t)qa * slab_bytes + (size_t)NT * 32 * 8 +
-           8 * (2 * (size_t)qs + 2 * (size_t)qa + 2 * NT) + 64;
-  };
-  // rows in flight: about 80 KB an SM sustains the HBM stream; slabs: one in
-  // work and two in flight per apply warp
-  int Qs = S * (int)(((size_t)80 << 10) / (row_bytes * S));
-  if (Qs < S) Qs = S;
-  int Qa = 3 * A;
-  while (need(Qs, Qa) > budget && Qs > S) Qs -= S;
-  while (need(Qs, Qa) > budget && Qa > A) Qa -= A;
-  if (need(Qs, Qa) > budget) return RN_ERR_UNSUPPORTED;
-  pl->Q = Qa;
-  pl->n_tbar = NT;
-  pl->apply_warps = A;
-  pl->stats_warps = S;
-  pl->l.threads = 32 * (A + S + 2);
-  pl->l.smem = need(Qs, Qa);
+  int Q = budget > fixed ? (int)((budget - fixed) / per_slot) : 0;
+  if (Q > 64) Q = 64;
+  if (Q < 4) return RN_ERR_UNSUPPORTED;
+  pl->Q = Q;
+  pl->n_tbar = 2;
+  pl->apply_warps = 16;
+  pl->stats_warps = 0;
+  pl->l.threads = kMxBoxThreads;
+  pl->l.smem = fixed + (size_t)Q * per_slot;
   pl->l.work = N / 32;
   pl->l.sms = di.sms - sm_margin;
   pl->l.per_sm = 1;
-  pl->Qs = Qs;
   return RN_OK;
 }
 
@@ -449,9 +437,10 @@ rn_status fwd_common(int nk, const void* x, rn_dtype dt, const float* gamma, con
   }
   if (mode == RN_QUANT_MXFP8) {
     MxPlan pl;
-    // bf16 rows of whole slabs: the kernel with separate row and slab rings
-    const bool slab = bf16 && plan_mx_slab(nk, (int)H, (int)N, sm_margin, di, &pl) == RN_OK;
-    if (!slab && (st = plan_mx(nk, (int)H, esz, (int)N, sm_margin, di, &pl)) != RN_OK) return st;
+    // rows of whole 128-byte column blocks: the box kernel; other bf16 rows
+    // (H of 32 mod 64 columns) the ring kernel, which holds a 32-row tile
+    const bool box = plan_mx_box(nk, (int)H, esz, (int)N, sm_margin, di, &pl) == RN_OK;
+    if (!box && (st = plan_mx(nk, (int)H, esz, (int)N, sm_margin, di, &pl)) != RN_OK) return st;
     MxParams p{};
     p.x = x;
     p.gamma = gamma;
@@ -471,8 +460,7 @@ rn_status fwd_common(int nk, const void* x, rn_dtype dt, const float* gamma, con
     p.stats_warps = pl.stats_warps;
     p.n_tiles = (int)(N / 32);
     p.n_tbar = pl.n_tbar;
-    p.Qs = pl.Qs;
-    if (slab) return launch_mx_slab(nk, p, pl.l, stream);
+    if (box) return launch_mx_box(nk, bf16, p, pl.l, stream);
     return launch_mx(nk, bf16, 1, p, pl.l, stream);
   }
 

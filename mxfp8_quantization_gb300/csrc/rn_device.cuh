@@ -46,6 +46,11 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
+// `count` arrivals at once
+__device__ __forceinline__ void mbar_arrive_cnt(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
                : "memory");
@@ -81,6 +86,39 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigne
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   while (!mbar_try_wait(bar, parity)) {
+    const long long dt = clock64() - t0;
+    if (dt > kErrorCheckCycles &&
+        (dt > kWaitLimitCycles || *reinterpret_cast<volatile unsigned*>(err) != 0u)) {
+      atomicCAS(err, 0u, code);
+      return false;
+    }
+  }
+  return true;
+}
+
+// A slot ticket: a shared-memory word the producer of a ring sets to the
+// use number of a slot (st.release) just before it refills the slot, which it
+// does only once the slot's previous use was released.  A consumer that finds
+// ticket == its use (ld.acquire) knows every earlier use of the slot has
+// completed, so the parity wait on the slot's "full" barrier that follows
+// cannot match an older phase, however far ahead of the slot the consumer
+// is.  Bounded like mbar_wait.
+__device__ __forceinline__ void ticket_set(uint32_t addr, uint32_t v) {
+  asm volatile("st.release.cta.shared::cta.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ uint32_t ticket_get(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.acquire.cta.shared::cta.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ bool ticket_wait(uint32_t addr, uint32_t want, unsigned* err,
+                                            unsigned code) {
+  if (ticket_get(addr) == want) return true;
+  const long long t0 = clock64();
+  while (ticket_get(addr) != want) {
+    __nanosleep(32);
     const long long dt = clock64() - t0;
     if (dt > kErrorCheckCycles &&
         (dt > kWaitLimitCycles || *reinterpret_cast<volatile unsigned*>(err) != 0u)) {
@@ -217,9 +255,17 @@ __device__ __forceinline__ uint32_t pack_e4m3x2(float lo, float hi) {
   return r;
 }
 
-// four fp32 -> four E4M3 codes in one word, element 0 in the low byte
+// four fp32 -> four E4M3 codes in one word, element 0 in the low byte (the
+// two halves joined by the register move)
 __device__ __forceinline__ uint32_t pack_e4m3x4(float a, float b, float c, float d) {
-  return pack_e4m3x2(a, b) | (pack_e4m3x2(c, d) << 16);
+  uint32_t r;
+  asm("{\n\t.reg .b16 lo, hi;\n\t"
+      "cvt.rn.satfinite.e4m3x2.f32 lo, %2, %1;\n\t"
+      "cvt.rn.satfinite.e4m3x2.f32 hi, %4, %3;\n\t"
+      "mov.b32 %0, {lo, hi};\n\t}"
+      : "=r"(r)
+      : "f"(a), "f"(b), "f"(c), "f"(d));
+  return r;
 }
 
 // |v| as ordered bits: for non-negative floats and NaN the unsigned order of

@@ -70,8 +70,7 @@ struct MxParams {
   int stats_warps;
   int Q;
   int n_tiles;          // N / 32
-  int n_tbar;           // tile "ready" barriers (> Q / 32 + 1); slab kernel: tiles in flight
-  int Qs;               // slab kernel: row-ring slots (a multiple of stats_warps)
+  int n_tbar;           // ring kernel: tile "ready" barriers (> Q / 32 + 1)
 };
 
 struct BwdParams {
@@ -169,11 +168,12 @@ rn_status launch_fwd_res(int nk, bool bf16, const FwdShape& sh, int qmode, const
 rn_status launch_fwd_init(float* amax, const float* scale, float* scale_inv, cudaStream_t s);
 rn_status launch_mx(int nk, bool bf16, int ng, const MxParams& p, const Launch& l,
                     cudaStream_t s);
-// MXFP8 with separate row (statistics) and slab (quantization) rings: bf16,
-// H a multiple of kMxSlabCols; Q = slab slots, Qs = row slots, n_tbar =
-// tiles in flight
-constexpr int kMxSlabCols = 64;
-rn_status launch_mx_slab(int nk, const MxParams& p, const Launch& l, cudaStream_t s);
+// MXFP8 both directions from boxes of 32 rows x 4 column blocks of 128
+// bytes, read twice (statistics, then quantization): 16 worker warps; H a
+// multiple of 128 / element size, N of 32; Q = box slots
+constexpr int kMxBoxThreads = 32 * 16;
+constexpr size_t kMxBoxBytes = 16384;
+rn_status launch_mx_box(int nk, bool bf16, const MxParams& p, const Launch& l, cudaStream_t s);
 // backward with stats warps (rows of any length)
 rn_status launch_bwd(bool ln, bool bf16, int ng, const BwdParams& p, const Launch& l,
                      cudaStream_t s);

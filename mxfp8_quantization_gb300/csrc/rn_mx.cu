@@ -3,9 +3,10 @@
 // "Implementation:NVIDIA TransformerEngine PyTorch Ext Normalization",
 // section "Description": the fully fused MXFP8 path).
 //
-// Two kernels: rn_mx_slab_kernel (further below) for bf16 rows of whole
-// 64-column slabs, and the ring kernel described here for the other rows
-// (fp32, other widths, the stand-alone quantizer).
+// Two kernels: rn_mx_box_kernel (further below) for rows of whole 128-byte
+// column blocks (bf16 H a multiple of 64, every fp32 row, the stand-alone
+// quantizer), and the ring kernel described here for the other bf16 rows (H
+// of 32 mod 64 columns).
 //
 // Ring-kernel design (one persistent CTA per SM, warp-specialized, no
 // CTA-wide barrier on the row path):
@@ -456,344 +457,519 @@ __global__ void __launch_bounds__(kMaxThreads, 1) rn_mx_kernel(const MxParams p)
 }
 
 // ---------------------------------------------------------------------------
-// Slab kernel (bf16, H a multiple of kMxSlabCols).  The ring kernel above
-// must hold a whole 32-row tile (the height of a column block) in shared
-// memory until every sub-tile of it is quantized; at H = 2048 its ring holds
-// about 52 rows, so the next tile's loads overlap only part of the current
-// tile's work.  Here the two uses of x are split:
-//   row producer  one lane streams whole rows (HBM -> shared, through L2)
-//                 into a row ring of about 80 KB (enough in flight for the
-//                 SM's share of HBM bandwidth);
-//   stats warps   take a row into registers, free its slot at once, and
-//                 write mean / rsigma into the tile's statistics buffer
-//                 (NT buffers, so statistics run up to NT tiles ahead; the
-//                 tile's "ready" barrier counts its 32 rows);
-//   slab producer one lane copies, once a tile's statistics are ready, each
-//                 32-row x kMxSlabCols slab of it again, now from L2, into a
-//                 ring of slabs with one 2-D tensor copy (TMA) a slab;
-//   apply warps   warp w takes slabs w, w + A, ... of every tile: the same
-//                 8 x 8 register blocks, maxima and codes as the ring kernel,
-//                 for the 64-column sub-tile(s) of a slab; then it frees
-//                 the slab and, after its last slab of the tile, arrives on
-//                 the tile's "done" barrier, which the stats warps wait on
-//                 before reusing the tile's statistics buffer.
-// HBM reads x about once; the slab copies mostly hit L2 (the rows were read
-// moments before).  Six stats warps keep up with LayerNorm's two passes
-// (with four the kernel waited on them: 170 vs 146 us at 65536 x 2048).
-// Slot reuse is alias-free: the row ring has a multiple of S
-// slots and the slab ring a multiple of A, so every slot is always consumed
-// by the same warp, which released its previous use itself.
-// one 32-row x kMxSlabCols box of x (tensor map `tm`: columns, then rows)
-// into shared memory, completion on `bar`
-__device__ __forceinline__ void tma_load_box(uint32_t dst, const CUtensorMap* tm, int col, int row,
-                                             uint32_t bar, uint64_t pol) {
+// Box kernel (bf16 rows of whole 64-column blocks, fp32 rows, the stand-alone
+// quantizer).  The ring kernel above must hold a whole 32-row tile (the
+// height of a column block) in shared memory until every sub-tile of it is
+// quantized, and its statistics warps and apply warps, fixed in number, leave
+// one of the two sides idle.  Here:
+//   * x moves in boxes of 32 rows x 4 column blocks of 128 bytes (16 KB, 256
+//     bf16 / 128 fp32 columns), one 3-D tensor copy each (dimensions: the
+//     128-byte column block, rows, column blocks) with the 128-byte swizzle
+//     (chunk c of row r of a column block sits at chunk c ^ (r & 7)), so a
+//     warp reading 8 rows' same chunk, or one row's 8 chunks, touches every
+//     bank once;
+//   * a tile is read twice: its boxes come from HBM for the row statistics
+//     (partial sums of each row over half a box, a lane per row, no cross-lane
+//     reduction) and again, from L2 moments later, for the quantization (the
+//     8 x 8 register blocks, both directions); no buffer holds a whole tile,
+//     so any row length fits;
+//   * 16 worker warps each do both kinds of work, in rounds: round k merges
+//     the partials of tile k - 1 into mu / rsigma (two rows a warp: the mean
+//     from the partial sums, then the sum of squared deviations as the
+//     partials' own plus n (m_u - mean)^2, both added in a fixed order), takes
+//     its share of tile k's statistics half-units and then of tile k - 1's
+//     64-column sub-tiles; a named barrier closes the round;
+//   * there is no producer warp (a 17th warp would leave 96 registers a
+//     thread: the register file of an SM quarter serves its 5 warps): the
+//     copies form one sequence in the order the rounds consume them (tile
+//     k's statistics boxes, then tile k - 1's quantization boxes), load i
+//     going to ring slot i mod Q; thread 0 issues the first Q, and the unit
+//     whose release brings a slot's pending-read count to zero issues the
+//     slot's next load at once (acquire-release count, then a proxy fence
+//     before the copy overwrites what was read); the slot's ticket, set
+//     before each refill, makes every consumer's wait alias-free.
+// bf16 enters the arithmetic through explicit unpacking (shift / mask) and
+// the packed f32x2 instructions.
+constexpr int kBoxRows = 32;                                      // a tile
+constexpr int kBoxCb = 4;                                         // 128-byte column blocks a box
+constexpr uint32_t kBoxBytes = (uint32_t)kBoxRows * 128 * kBoxCb;  // 16 KB
+constexpr int kBoxWorkers = 16;
+constexpr int kBoxThreads = 32 * kBoxWorkers;
+
+// Lanes of a quantization sub-tile: lane = hb*16 + rg*4 + cc (a quarter warp
+// reads two rows' half chunks), or with kLaneRowMajor lane = rg*8 + hb*4 + cc
+// (a quarter warp reads one row's 8 chunks, which the swizzle spreads over
+// all banks).  Row blocks span the lanes cc (shuffles xor 1, 2), column
+// blocks the lanes rg (xor kColS0, kColS1).
+constexpr bool kLaneRowMajor = false;
+constexpr int kColS0 = kLaneRowMajor ? 8 : 4;
+constexpr int kColS1 = kLaneRowMajor ? 16 : 8;
+
+// one box (32 rows x kBoxCb column blocks from column block `cb`, rows from
+// `row`) into shared memory, completion on `bar`
+__device__ __forceinline__ void tma_load_box3(uint32_t dst, const CUtensorMap* tm, int row, int cb,
+                                              uint32_t bar, uint64_t pol) {
   asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
-      " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(tm)), "r"(col), "r"(row), "r"(bar), "l"(pol)
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(tm)), "r"(0), "r"(row), "r"(cb), "r"(bar), "l"(pol)
       : "memory");
 }
 
-template <int NK, int SNC>
-__global__ void __launch_bounds__(kMaxThreads, 1)
-    rn_mx_slab_kernel(const MxParams p, const __grid_constant__ CUtensorMap tmx) {
-  using V = Vec<uint16_t, 8>;
-  constexpr bool LN = (NK == kLn);
-  constexpr uint32_t kPieceBytes = kMxSlabCols * 2;  // one row of a slab
-  constexpr uint32_t kSlabBytes = kTile * kPieceBytes;
-  extern __shared__ __align__(128) unsigned char smem[];
-  const int A = p.apply_warps;
-  const int S = p.stats_warps;
-  const int H = p.H;
-  const int N = p.N;
-  const int nchunks = H >> 3;
-  const uint32_t row_bytes = (uint32_t)H * 2;
-  const int nslab = H / kMxSlabCols;
-  const uint32_t Qs = (uint32_t)p.Qs, Qa = (uint32_t)p.Q;
-  const int NT = p.n_tbar;
-  const size_t gb_bytes = (size_t)H * sizeof(float) * (LN ? 2 : 1);
-
-  float4* gsm = reinterpret_cast<float4*>(smem);  // [2][nchunks]
-  float4* bsm = gsm + 2 * (size_t)nchunks;
-  unsigned char* sring = smem + gb_bytes;                        // [Qs] rows
-  unsigned char* aring = sring + (size_t)Qs * row_bytes;         // [Qa] slabs
-  float2* tstat = reinterpret_cast<float2*>(aring + (size_t)Qa * kSlabBytes);  // [NT][32]
-  uint64_t* sfull = reinterpret_cast<uint64_t*>(tstat + (size_t)NT * kTile);
-  uint64_t* sempty = sfull + Qs;
-  uint64_t* afull = sempty + Qs;
-  uint64_t* aempty = afull + Qa;
-  uint64_t* tready = aempty + Qa;  // [NT] 32 rows' statistics written
-  uint64_t* tdone = tready + NT;   // [NT] every apply warp finished the tile
-
-  for (uint32_t i = threadIdx.x; i < Qs; i += blockDim.x) {
-    mbar_init(smem_u32(&sfull[i]), 1);
-    mbar_init(smem_u32(&sempty[i]), 1);
-    fence_barrier_init();
-  }
-  for (uint32_t i = threadIdx.x; i < Qa; i += blockDim.x) {
-    mbar_init(smem_u32(&afull[i]), 1);
-    mbar_init(smem_u32(&aempty[i]), 1);
-    fence_barrier_init();
-  }
-  for (int i = threadIdx.x; i < NT; i += blockDim.x) {
-    mbar_init(smem_u32(&tready[i]), kTile);
-    mbar_init(smem_u32(&tdone[i]), A);
-    fence_barrier_init();
-  }
-  {
-    const int n4 = H / 4;
-    for (int u = threadIdx.x; u < n4; u += blockDim.x) {
-      const int c = u >> 1, j = u & 1;
-      const float4 gv = reinterpret_cast<const float4*>(p.gamma)[u];
-      gsm[j * nchunks + c] =
-          p.zcg ? make_float4(1.0f + gv.x, 1.0f + gv.y, 1.0f + gv.z, 1.0f + gv.w) : gv;
-      if (LN)
-        bsm[j * nchunks + c] = p.beta ? reinterpret_cast<const float4*>(p.beta)[u]
-                                      : make_float4(0.f, 0.f, 0.f, 0.f);
+// slot (index mod Q) and use (index / Q) of a ring load index, moved forward
+struct LoadPos {
+  uint32_t idx, slot, use;
+  __device__ __forceinline__ void to(uint32_t target, uint32_t q) {
+    uint32_t d = target - idx;
+    idx = target;
+    while (d >= q) {
+      d -= q;
+      ++use;
+    }
+    slot += d;
+    if (slot >= q) {
+      slot -= q;
+      ++use;
     }
   }
-  __syncthreads();
+};
+
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(addr));
+  return v;
+}
+
+// the four element pairs of a 16-byte chunk as fp32 pairs (bf16: 8 elements,
+// pairs 0..3; fp32: 4 elements, pairs 0..1)
+template <typename TIn>
+__device__ __forceinline__ float2 chunk_pair(const uint4& v, int i);
+template <>
+__device__ __forceinline__ float2 chunk_pair<uint16_t>(const uint4& v, int i) {
+  const uint32_t w = i == 0 ? v.x : (i == 1 ? v.y : (i == 2 ? v.z : v.w));
+  return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+}
+template <>
+__device__ __forceinline__ float2 chunk_pair<float>(const uint4& v, int i) {
+  return i == 0 ? make_float2(__uint_as_float(v.x), __uint_as_float(v.y))
+                : make_float2(__uint_as_float(v.z), __uint_as_float(v.w));
+}
+
+template <typename TIn, int NK>
+__global__ void __launch_bounds__(kBoxThreads, 1)
+    rn_mx_box_kernel(const MxParams p, const __grid_constant__ CUtensorMap tmx) {
+  constexpr int ESZ = (int)sizeof(TIn);
+  constexpr int C0 = 128 / ESZ;          // columns a column block holds
+  constexpr int SPB = C0 * kBoxCb / 64;  // 64-column sub-tiles a box holds (4 bf16, 2 fp32)
+  constexpr int PPC = 8 / ESZ;           // element pairs a 16-byte chunk holds (4 bf16, 2 fp32)
+  constexpr bool STATS = (NK != kIdentity);
+  constexpr bool LN = (NK == kLn);
+  // arrivals that release one use of a box slot: one from each of its SPB
+  // sub-tiles, or EMPTY / 2 from each of its two statistics half-units
+  constexpr uint32_t EMPTY = SPB > 2 ? SPB : 2;
+  extern __shared__ __align__(128) unsigned char smem_raw[];
+  // the 128-byte swizzle wants boxes at 1024-byte boundaries
+  unsigned char* smem = reinterpret_cast<unsigned char*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const int H = p.H;
+  const int N = p.N;
+  const uint32_t Q = (uint32_t)p.Q;
+  const int ncb = H / C0;                      // column blocks of a row
+  const int nbox = (ncb + kBoxCb - 1) / kBoxCb;
+  const int nus = STATS ? 2 * nbox : 0;        // statistics half-units a tile
+  const int nua = nbox * SPB;                  // sub-tiles a tile (some may lie past H)
+  unsigned char* ring = smem;
+  float2* pbuf = reinterpret_cast<float2*>(ring + (size_t)Q * kBoxBytes);  // [2][nus][32]
+  float2* tstat = pbuf + 2 * (size_t)nus * kBoxRows;                       // [2][32] (mean, rsigma)
+  uint64_t* full = reinterpret_cast<uint64_t*>(tstat + 2 * kBoxRows);
+  uint64_t* tready = full + Q;                                             // [2]
+  uint64_t* sdone = tready + 2;                                            // [2]
+  uint32_t* ticket = reinterpret_cast<uint32_t*>(sdone + 2);               // [Q]
+  uint32_t* pending = ticket + Q;                                          // [Q] reads left
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int G = gridDim.x;
   const int ntl = p.n_tiles > (int)blockIdx.x ? (p.n_tiles - 1 - (int)blockIdx.x) / G + 1 : 0;
-  const int nq = ntl * kTile;
-  const unsigned char* xb = static_cast<const unsigned char*>(p.x);
+  // round k: statistics of tile k, quantization of tile k - 1 (the
+  // stand-alone quantizer: quantization of tile k only)
+  const int nrounds = STATS ? ntl + 1 : ntl;
+  const uint32_t nload = (uint32_t)(STATS ? 2 : 1) * (uint32_t)ntl * (uint32_t)nbox;
+  const uint32_t ring_u32 = smem_u32(ring);
+  const uint64_t keep = l2_evict_last();   // statistics read: read again soon
+  const uint64_t once = l2_evict_first();  // quantization read: the last
 
-  if (warp == A + S) {
-    // -------------------------------------------------------- row producer
-    if (lane == 0) {
-      for (int q = 0; q < nq; ++q) {
-        const int r = ((int)blockIdx.x + (q / kTile) * G) * kTile + (q % kTile);
-        const uint32_t s = (uint32_t)q % Qs;
-        if (q >= (int)Qs)
-          mbar_wait(smem_u32(&sempty[s]), ((uint32_t)q / Qs - 1u) & 1u, &g_err_mx, kErrEmptyWait);
-        mbar_arrive_expect_tx(smem_u32(&sfull[s]), row_bytes);
-        bulk_g2s(smem_u32(sring + (size_t)s * row_bytes), xb + (size_t)r * row_bytes, row_bytes,
-                 smem_u32(&sfull[s]));
-      }
-      for (int q = nq > (int)Qs ? nq - (int)Qs : 0; q < nq; ++q)
-        mbar_wait(smem_u32(&sfull[q % Qs]), ((uint32_t)q / Qs) & 1u, &g_err_mx, kErrDrainWait);
+  // load i of the sequence into slot i mod Q (its ticket set first)
+  auto issue = [&](uint32_t i) {
+    const uint32_t s = i % Q, u = i / Q;
+    int t, b;
+    bool first;
+    if (!STATS) {
+      t = (int)(i / (uint32_t)nbox);
+      b = (int)(i - (uint32_t)t * nbox);
+      first = false;
+    } else if (i < (uint32_t)nbox) {
+      t = 0;
+      b = (int)i;
+      first = true;
+    } else {
+      // rounds 1 .. ntl: tile k's statistics boxes (while k < ntl), then tile
+      // k - 1's quantization boxes
+      const uint32_t j = i - (uint32_t)nbox;
+      const int k = 1 + (int)(j / (uint32_t)(2 * nbox));
+      const int r = (int)(j - (uint32_t)(k - 1) * 2 * nbox);
+      first = (k < ntl) && r < nbox;
+      t = first ? k : k - 1;
+      b = first ? r : (k < ntl ? r - nbox : r);
     }
-    return;
-  }
-
-  if (warp == A + S + 1) {
-    // ------------------------------------------------------- slab producer
-    // one tensor copy a slab (a copy per row piece would cost ~36 ns each
-    // in the copy engine, 32 times a slab)
+    ticket_set(smem_u32(&ticket[s]), u);
+    mbar_arrive_expect_tx(smem_u32(&full[s]), kBoxBytes);
+    tma_load_box3(ring_u32 + s * kBoxBytes, &tmx, ((int)blockIdx.x + t * G) * kBoxRows, b * kBoxCb,
+                  smem_u32(&full[s]), first ? keep : once);
+  };
+  // a unit done with slot s (use u) gives back its `cnt` reads; the last
+  // one refills the slot with load u Q + Q + s
+  auto release = [&](uint32_t s, uint32_t u, uint32_t cnt) {
+    __syncwarp();
     if (lane == 0) {
-      const uint64_t pol = l2_evict_first();  // the second and last read
-      for (int tl = 0; tl < ntl; ++tl) {
-        const int t = (int)blockIdx.x + tl * G;
-        mbar_wait(smem_u32(&tready[tl % NT]), (uint32_t)(tl / NT) & 1u, &g_err_mx, kErrReadyWait);
-        for (int j = 0; j < nslab; ++j) {
-          const uint32_t i = (uint32_t)(tl * nslab + j);
-          const uint32_t s = i % Qa;
-          if (i >= Qa)
-            mbar_wait(smem_u32(&aempty[s]), (i / Qa - 1u) & 1u, &g_err_mx, kErrEmptyWait);
-          mbar_arrive_expect_tx(smem_u32(&afull[s]), kSlabBytes);
-          tma_load_box(smem_u32(aring + (size_t)s * kSlabBytes), &tmx, j * kMxSlabCols, t * kTile,
-                       smem_u32(&afull[s]), pol);
+      uint32_t old;
+      asm volatile("atom.acq_rel.cta.shared::cta.add.u32 %0, [%1], %2;"
+                   : "=r"(old)
+                   : "r"(smem_u32(&pending[s])), "r"(0u - cnt)
+                   : "memory");
+      if (old == cnt) {
+        const uint32_t nxt = (u + 1) * Q + s;
+        pending[s] = EMPTY;
+        if (nxt < nload) {
+          fence_proxy_async();  // the reads of the slot before the copy that overwrites it
+          issue(nxt);
         }
       }
-      const uint32_t ni = (uint32_t)(ntl * nslab);
-      for (uint32_t i = ni > Qa ? ni - Qa : 0; i < ni; ++i)
-        mbar_wait(smem_u32(&afull[i % Qa]), (i / Qa) & 1u, &g_err_mx, kErrDrainWait);
     }
-    return;
-  }
+  };
 
-  if (warp >= A) {
-    // --------------------------------------------------------- stats warps
-    const int j = warp - A;
-    const float inv_h = 1.0f / (float)H;
-    for (int q = j; q < nq; q += S) {
-      const int tl = q / kTile, k = q % kTile;
-      // the statistics buffer of tile tl was last used by tile tl - NT
-      if (tl >= NT)
-        mbar_wait(smem_u32(&tdone[tl % NT]), (uint32_t)(tl / NT - 1) & 1u, &g_err_mx, kErrStatsWait);
-      const uint32_t s = (uint32_t)q % Qs;
-      mbar_wait(smem_u32(&sfull[s]), ((uint32_t)q / Qs) & 1u, &g_err_mx, kErrStatsWait);
-      const unsigned char* rowp = sring + (size_t)s * row_bytes;
-      typename V::Raw raw[SNC];
-#pragma unroll
-      for (int c = 0; c < SNC; ++c)
-        if (lane + 32 * c < nchunks) raw[c] = V::load(rowp, lane + 32 * c);
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&sempty[s]));
-      float2 a[4];
-      float mean = 0.f;
-      if constexpr (LN) {
-#pragma unroll
-        for (int i = 0; i < 4; ++i) a[i] = make_float2(0.f, 0.f);
-#pragma unroll
-        for (int c = 0; c < SNC; ++c)
-          if (lane + 32 * c < nchunks) {
-#pragma unroll
-            for (int i = 0; i < 4; ++i) V::acc(a[i], raw[c], i);
-          }
-        mean = warp_sum((a[0].x + a[0].y) + (a[1].x + a[1].y) + (a[2].x + a[2].y) +
-                        (a[3].x + a[3].y)) * inv_h;
-      }
-#pragma unroll
-      for (int i = 0; i < 4; ++i) a[i] = make_float2(0.f, 0.f);
-#pragma unroll
-      for (int c = 0; c < SNC; ++c)
-        if (lane + 32 * c < nchunks) {
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            if constexpr (LN) {
-              const float2 d = V::sub(raw[c], i, mean);
-              a[i] = fma2(d, d, a[i]);
-            } else {
-              V::sq_acc(a[i], raw[c], i);
-            }
-          }
-        }
-      const float m2 = warp_sum((a[0].x + a[0].y) + (a[1].x + a[1].y) + (a[2].x + a[2].y) +
-                                (a[3].x + a[3].y));
-      const float rs = __frsqrt_rn(m2 * inv_h + p.eps);
-      if (lane == 0) {
-        const int r = ((int)blockIdx.x + tl * G) * kTile + k;
-        tstat[(tl % NT) * kTile + k] = make_float2(mean, rs);
-        if (LN) p.mu[r] = mean;
-        p.rsigma[r] = rs;
-        mbar_arrive(smem_u32(&tready[tl % NT]));
-      }
-    }
-    return;
+  for (uint32_t i = threadIdx.x; i < Q; i += blockDim.x) {
+    mbar_init(smem_u32(&full[i]), 1);
+    ticket[i] = 0xFFFFFFFFu;
+    pending[i] = EMPTY;
   }
+  if (threadIdx.x < 2) {
+    mbar_init(smem_u32(&tready[threadIdx.x]), 1);
+    mbar_init(smem_u32(&sdone[threadIdx.x]), kBoxWorkers);
+  }
+  fence_barrier_init();
+  __syncthreads();
+  if (threadIdx.x == 0)
+    for (uint32_t i = 0; i < Q && i < nload; ++i) issue(i);
 
-  // ---------------------------------------------------------- apply warps
-  // lane = hb*16 + rg*4 + cc as in the ring kernel: rows 8rg..8rg+7, chunk
-  // cl = 4hb + cc of a 64-column sub-tile
-  const int hb = lane >> 4, rg = (lane >> 2) & 3, cc = lane & 3;
+  // ------------------------------------------------------------- workers
+  const int w = warp;
+  const float inv_h = 1.0f / (float)H;
+  // quantization lanes: rows 8rg..8rg+7 and chunk cl = 4hb + cc (columns
+  // 8cl..8cl+7) of a 64-column sub-tile (the lane layout: kLaneRowMajor)
+  const int hb = kLaneRowMajor ? (lane >> 2) & 1 : lane >> 4;
+  const int rg = kLaneRowMajor ? lane >> 3 : (lane >> 2) & 3;
+  const int cc = lane & 3;
   const int cl = hb * 4 + cc;
   const int hs = H >> 5;
   const int ns = N >> 5;
   const bool rowwise = p.data != nullptr;
   const bool colwise = p.col_data != nullptr;
-  const uint32_t aring_u32 = smem_u32(aring);
+  LoadPos pos{0u, 0u, 0u};
+  uint32_t li = 0;  // ring load index of the first box of the current pass
 
-  for (int tl = 0; tl < ntl; ++tl) {
-    const int tile = (int)blockIdx.x + tl * G;
-    const int r0 = tile * kTile;
-    mbar_wait(smem_u32(&tready[tl % NT]), (uint32_t)(tl / NT) & 1u, &g_err_mx, kErrReadyWait);
-    float2 st8[8];
+  for (int k = 0; k < nrounds; ++k) {
+    const int ta = STATS ? k - 1 : k;  // the tile quantized in this round
+    if constexpr (STATS) {
+      // Tile t's statistics units are done once every worker arrived on
+      // sdone[t & 1]; worker t mod 16 then merges the tile (a lane per row,
+      // its partials added in unit order) and arrives on tready[t & 1], which
+      // every worker waits on before quantizing the tile.  Each worker's
+      // units of tile t come after its quantization of tile t - 2, and the
+      // merge of tile t after every worker's units of tile t, so the partial
+      // and (mean, rsigma) buffers are free again when rewritten and no
+      // barrier phase can alias (every wait or arrival for tile t follows the
+      // completion of tile t - 2's phase of the same barrier).
+      if (ta >= 0 && w == (ta & (kBoxWorkers - 1))) {
+        mbar_wait(smem_u32(&sdone[ta & 1]), (uint32_t)(ta >> 1) & 1u, &g_err_mx, kErrReadyWait);
+        // ---------------------------------------------------------- merge
+        const float2* pb = pbuf + (size_t)(ta & 1) * nus * kBoxRows + lane;
+        float mean = 0.0f, m2 = 0.0f;
+        if constexpr (LN) {
+          float sx = 0.0f;
+          for (int u = 0; u < nus; ++u) sx += pb[u * kBoxRows].x;
+          mean = sx * inv_h;
+          for (int u = 0; u < nus; ++u) {
+            const int cb0 = (u >> 1) * kBoxCb + 2 * (u & 1);
+            const int nv = (cb0 < ncb) + (cb0 + 1 < ncb);
+            if (nv > 0) {
+              const float2 v = pb[u * kBoxRows];
+              const float nf = (float)(nv * C0);  // a power of two
+              const float d = v.x * (nv == 2 ? 1.0f / (2 * C0) : 1.0f / C0) - mean;
+              m2 += v.y + nf * d * d;
+            }
+          }
+        } else {
+          for (int u = 0; u < nus; ++u) m2 += pb[u * kBoxRows].x;
+        }
+        const float rs = __frsqrt_rn(m2 * inv_h + p.eps);
+        const int row = ((int)blockIdx.x + ta * G) * kBoxRows + lane;
+        tstat[(ta & 1) * kBoxRows + lane] = make_float2(mean, rs);
+        if (LN) p.mu[row] = mean;
+        p.rsigma[row] = rs;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&tready[ta & 1]));
+      }
+      if (k < ntl) {
+        // ----------------------------------------------- statistics units
+        // half-unit u: rows 0..31 (lane = row) x column blocks
+        // 2 (u & 1), +1 of box u >> 1; LayerNorm: (sum, sum of squared
+        // deviations from the unit's own mean), RMSNorm: (sum of squares, 0)
+        float2* pw = pbuf + (size_t)(k & 1) * nus * kBoxRows;
+        for (int u = w; u < nus; u += kBoxWorkers) {
+          pos.to(li + (uint32_t)(u >> 1), Q);
+          const uint32_t s = pos.slot;
+          ticket_wait(smem_u32(&ticket[s]), pos.use, &g_err_mx, kErrStatsWait);
+          mbar_wait(smem_u32(&full[s]), pos.use & 1u, &g_err_mx, kErrStatsWait);
+          const int cb0 = (u >> 1) * kBoxCb + 2 * (u & 1);
+          const int nv = min(2, ncb - cb0);  // valid column blocks (0..2), the same on every lane
+          const uint32_t base = ring_u32 + s * kBoxBytes + (uint32_t)(u & 1) * 2 * 4096 +
+                                (uint32_t)lane * 128;
+          // chunk c of column block h of this lane's row
+          auto chunk = [&](int h, int c) { return lds128(base + h * 4096 + ((c ^ (lane & 7)) << 4)); };
+          float2 a[4];
 #pragma unroll
-    for (int jr = 0; jr < 8; ++jr) st8[jr] = tstat[(tl % NT) * kTile + 8 * rg + jr];
-    uint8_t* const dptr = rowwise ? p.data + ((size_t)(r0 + 8 * rg) * H + cl * 8) : nullptr;
-    uint8_t* const sptr = rowwise ? p.row_scales + ((size_t)(r0 + 8 * rg) * hs + hb) : nullptr;
-    uint8_t* const cptr = colwise ? p.col_data + ((size_t)cl * 8 * N + r0 + 8 * rg) : nullptr;
-    uint8_t* const csptr = colwise ? p.col_scales + ((size_t)cl * 8 * ns + tile) : nullptr;
-
-    for (int js = warp; js < nslab; js += A) {
-      const uint32_t i = (uint32_t)(tl * nslab + js);
-      const uint32_t s = i % Qa;
-      mbar_wait(smem_u32(&afull[s]), (i / Qa) & 1u, &g_err_mx, kErrFullWait);
-      const uint32_t slab = aring_u32 + s * kSlabBytes + 8 * rg * kPieceBytes;
+          for (int i = 0; i < 4; ++i) a[i] = make_float2(0.f, 0.f);
+          float sx = 0.0f, q2 = 0.0f;
+          if constexpr (LN) {
+            // two passes over the unit: the sum, then the squared deviations
+            // from the unit's mean (read again from shared memory)
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+              if (h < nv) {
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                  const uint4 v = chunk(h, c);
+#pragma unroll
+                  for (int i = 0; i < PPC; ++i)
+                    a[(c * PPC + i) & 3] = add2(a[(c * PPC + i) & 3], chunk_pair<TIn>(v, i));
+                }
+              }
+            sx = (a[0].x + a[0].y) + (a[1].x + a[1].y) + (a[2].x + a[2].y) + (a[3].x + a[3].y);
+            // (nv == 0: an empty unit, which the merge skips)
+            const float um = nv > 0 ? sx * (nv == 2 ? 1.0f / (2 * C0) : 1.0f / C0) : 0.0f;
+            const float2 um2 = splat2(um);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) a[i] = make_float2(0.f, 0.f);
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+              if (h < nv) {
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                  const uint4 v = chunk(h, c);
+#pragma unroll
+                  for (int i = 0; i < PPC; ++i) {
+                    const float2 d = sub2(chunk_pair<TIn>(v, i), um2);
+                    a[(c * PPC + i) & 3] = fma2(d, d, a[(c * PPC + i) & 3]);
+                  }
+                }
+              }
+            q2 = (a[0].x + a[0].y) + (a[1].x + a[1].y) + (a[2].x + a[2].y) + (a[3].x + a[3].y);
+          } else {
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+              if (h < nv) {
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                  const uint4 v = chunk(h, c);
+#pragma unroll
+                  for (int i = 0; i < PPC; ++i) {
+                    const float2 x = chunk_pair<TIn>(v, i);
+                    a[(c * PPC + i) & 3] = fma2(x, x, a[(c * PPC + i) & 3]);
+                  }
+                }
+              }
+            sx = (a[0].x + a[0].y) + (a[1].x + a[1].y) + (a[2].x + a[2].y) + (a[3].x + a[3].y);
+          }
+          release(s, pos.use, EMPTY / 2);
+          pw[u * kBoxRows + lane] = make_float2(sx, q2);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&sdone[k & 1]));
+        li += (uint32_t)nbox;
+      }
+    }
+    if (ta < 0) continue;
+    // ------------------------------------------------ quantization units
+    const int tile = (int)blockIdx.x + ta * G;
+    const int r0 = tile * kBoxRows;
+    if constexpr (STATS)
+      mbar_wait(smem_u32(&tready[ta & 1]), (uint32_t)(ta >> 1) & 1u, &g_err_mx, kErrReadyWait);
+    // this thread's 8 rows' (mean, rsigma)
+    const float2* st8 = tstat + (ta & 1) * kBoxRows + 8 * rg;
+    // sub-tiles go two at a time (the same box: one wait, one release)
+    for (int a2 = w; 2 * a2 < nua; a2 += kBoxWorkers) {
+      const int b = (2 * a2) / SPB;
+      pos.to(li + (uint32_t)b, Q);
+      const uint32_t s = pos.slot;
+      ticket_wait(smem_u32(&ticket[s]), pos.use, &g_err_mx, kErrFullWait);
+      mbar_wait(smem_u32(&full[s]), pos.use & 1u, &g_err_mx, kErrFullWait);
 #pragma unroll 1
-      for (int u = 0; u < kMxSlabCols / 64; ++u) {
-        const int sub = js * (kMxSlabCols / 64) + u;  // 64-column sub-tile of the row
-        const int c = sub * 8 + cl;
-        float2 g2[4], b2[4];
+      for (int a = 2 * a2; a < 2 * a2 + 2; ++a) {
+        const int q = a - b * SPB;
+        const int sub = a;  // 64-column sub-tile of the row
+        if (64 * sub < H) {
+          // (fp32 rows of 32 mod 64 columns end in half a sub-tile; bf16 rows
+          // here are whole sub-tiles)
+          const bool valid = ESZ == 2 || 64 * sub + 8 * cl < H;
+          float2 g2[4], b2[4];
+          {
+            float4 gv[2] = {make_float4(0.f, 0.f, 0.f, 0.f), make_float4(0.f, 0.f, 0.f, 0.f)};
+            float4 bv[2] = {gv[0], gv[0]};
+            if (STATS && valid) {
+              const float4* gp = reinterpret_cast<const float4*>(p.gamma + 64 * sub + 8 * cl);
+              gv[0] = __ldg(gp);
+              gv[1] = __ldg(gp + 1);
+              if (p.zcg) {
 #pragma unroll
-        for (int jj = 0; jj < 2; ++jj) {
-          const float4 gv = gsm[jj * nchunks + c];
-          const float4 bv = LN ? bsm[jj * nchunks + c] : make_float4(0.f, 0.f, 0.f, 0.f);
-          g2[2 * jj] = make_float2(gv.x, gv.y);
-          g2[2 * jj + 1] = make_float2(gv.z, gv.w);
-          b2[2 * jj] = make_float2(bv.x, bv.y);
-          b2[2 * jj + 1] = make_float2(bv.z, bv.w);
-        }
-        const uint32_t coff = (uint32_t)(u * 64 + cl * 8) * 2;
-        float2 y[8][4];
+                for (int jj = 0; jj < 2; ++jj)
+                  gv[jj] = make_float4(1.0f + gv[jj].x, 1.0f + gv[jj].y, 1.0f + gv[jj].z, 1.0f + gv[jj].w);
+              }
+              if (LN && p.beta) {
+                const float4* bp = reinterpret_cast<const float4*>(p.beta + 64 * sub + 8 * cl);
+                bv[0] = __ldg(bp);
+                bv[1] = __ldg(bp + 1);
+              }
+            }
 #pragma unroll
-        for (int jr = 0; jr < 8; ++jr) {
-          const typename V::Raw raw = load8<uint16_t>(slab + jr * kPieceBytes + coff);
-          const float2 rs2 = splat2(st8[jr].y);
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            if constexpr (LN)
-              y[jr][q] = fma2(mul2(V::sub(raw, q, st8[jr].x), rs2), g2[q], b2[q]);
-            else
-              y[jr][q] = mul2(mul2(V::f32(raw, q), rs2), g2[q]);
+            for (int jj = 0; jj < 2; ++jj) {
+              g2[2 * jj] = make_float2(gv[jj].x, gv[jj].y);
+              g2[2 * jj + 1] = make_float2(gv[jj].z, gv[jj].w);
+              b2[2 * jj] = make_float2(bv[jj].x, bv[jj].y);
+              b2[2 * jj + 1] = make_float2(bv[jj].z, bv[jj].w);
+            }
           }
-        }
-        float rmax[8], cmax[8];
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          rmax[k] = 0.f;
-          cmax[k] = 0.f;
-        }
-#pragma unroll
-        for (int jr = 0; jr < 8; jr += 2) {
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const float a0 = fabsf(y[jr][q].x), b0 = fabsf(y[jr][q].y);
-            const float a1 = fabsf(y[jr + 1][q].x), b1 = fabsf(y[jr + 1][q].y);
-            rmax[jr] = max3n(rmax[jr], a0, b0);
-            rmax[jr + 1] = max3n(rmax[jr + 1], a1, b1);
-            cmax[2 * q] = max3n(cmax[2 * q], a0, a1);
-            cmax[2 * q + 1] = max3n(cmax[2 * q + 1], b0, b1);
-          }
-        }
-        if (rowwise) {
-          float m0, m1;
-          block_max_scatter(rmax, cc >> 1, cc & 1, 2, 1, m0, m1);
-          const uint32_t code0 = e8m0_code(m0), code1 = e8m0_code(m1);
-          float inv[8];
-          gather8(e8m0_inv_scale(code0), e8m0_inv_scale(code1), cc >> 1, cc & 1, 2, 1, inv);
-          uint8_t* dp = dptr + (size_t)sub * 64;
+          // this thread's 8 columns in the box: bf16, chunk cl of column block
+          // q; fp32, chunks 2 (cl & 3), +1 of column block 2q + (cl >> 2)
+          // row 8 rg + jr of the thread's column block starts at cbb + jr * 128;
+          // its chunk k sits at chunk k ^ jr (the 128-byte swizzle)
+          const uint32_t cbb = ring_u32 + s * kBoxBytes +
+                               (uint32_t)(ESZ == 2 ? q : 2 * q + (cl >> 2)) * 4096 + (uint32_t)rg * 1024;
+          const uint32_t ck = ESZ == 2 ? (uint32_t)cl << 4 : (uint32_t)(2 * (cl & 3)) << 4;
+          float2 y[8][4];
 #pragma unroll
           for (int jr = 0; jr < 8; ++jr) {
-            const float2 iv = splat2(inv[jr]);
-            uint32_t q4[4];
+            const uint32_t rowa = cbb + jr * 128;
+            float2 x2[4];
+            if constexpr (ESZ == 2) {
+              const uint4 v = lds128(rowa + (ck ^ (jr << 4)));
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              const float2 v = mul2(y[jr][q], iv);
-              q4[q] = pack_e4m3x2(v.x, v.y);
+              for (int i = 0; i < 4; ++i) x2[i] = chunk_pair<TIn>(v, i);
+            } else {
+              const uint4 v0 = lds128(rowa + (ck ^ (jr << 4)));
+              const uint4 v1 = lds128(rowa + ((ck + 16) ^ (jr << 4)));
+              x2[0] = chunk_pair<TIn>(v0, 0);
+              x2[1] = chunk_pair<TIn>(v0, 1);
+              x2[2] = chunk_pair<TIn>(v1, 0);
+              x2[3] = chunk_pair<TIn>(v1, 1);
             }
-            *reinterpret_cast<uint2*>(dp) = make_uint2(q4[0] | (q4[1] << 16), q4[2] | (q4[3] << 16));
-            dp += H;
-          }
-          uint8_t* sp = sptr + 2 * sub + (size_t)cc * hs;
-          sp[0] = (uint8_t)code0;
-          sp[4 * (size_t)hs] = (uint8_t)code1;
-        }
-        if (colwise) {
-          float m0, m1;
-          block_max_scatter(cmax, rg >> 1, rg & 1, 8, 4, m0, m1);
-          const uint32_t code0 = e8m0_code(m0), code1 = e8m0_code(m1);
-          float cinv[8];
-          gather8(e8m0_inv_scale(code0), e8m0_inv_scale(code1), rg >> 1, rg & 1, 8, 4, cinv);
-          uint8_t* cp = cptr + (size_t)sub * 64 * N;
+            const float2 ms = STATS ? st8[jr] : make_float2(0.f, 1.f);
+            const float2 rs2 = splat2(ms.y);
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const float2 ci = make_float2(cinv[2 * q], cinv[2 * q + 1]);
-            float2 qv[8];
-#pragma unroll
-            for (int jr = 0; jr < 8; ++jr) qv[jr] = mul2(y[jr][q], ci);
-            const uint32_t lo0 = pack_e4m3x2(qv[0].x, qv[1].x) | (pack_e4m3x2(qv[2].x, qv[3].x) << 16);
-            const uint32_t hi0 = pack_e4m3x2(qv[4].x, qv[5].x) | (pack_e4m3x2(qv[6].x, qv[7].x) << 16);
-            const uint32_t lo1 = pack_e4m3x2(qv[0].y, qv[1].y) | (pack_e4m3x2(qv[2].y, qv[3].y) << 16);
-            const uint32_t hi1 = pack_e4m3x2(qv[4].y, qv[5].y) | (pack_e4m3x2(qv[6].y, qv[7].y) << 16);
-            *reinterpret_cast<uint2*>(cp) = make_uint2(lo0, hi0);
-            *reinterpret_cast<uint2*>(cp + N) = make_uint2(lo1, hi1);
-            cp += 2 * (size_t)N;
+            for (int i = 0; i < 4; ++i) {
+              if constexpr (LN)
+                y[jr][i] = fma2(mul2(sub2(x2[i], splat2(ms.x)), rs2), g2[i], b2[i]);
+              else if constexpr (NK == kRms)
+                y[jr][i] = mul2(mul2(x2[i], rs2), g2[i]);
+              else
+                y[jr][i] = x2[i];
+              if (ESZ == 4 && !valid) y[jr][i] = make_float2(0.f, 0.f);
+            }
           }
-          uint8_t* csp = csptr + ((size_t)sub * 64 + rg) * ns;
-          csp[0] = (uint8_t)code0;
-          csp[4 * (size_t)ns] = (uint8_t)code1;
+          // one sweep over |y|: row maxima (8 values each) and column maxima
+          // (8 values each), two rows at a time
+          float rmax[8], cmax[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            rmax[i] = 0.f;
+            cmax[i] = 0.f;
+          }
+#pragma unroll
+          for (int jr = 0; jr < 8; jr += 2) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const float a0 = fabsf(y[jr][i].x), b0 = fabsf(y[jr][i].y);
+              const float a1 = fabsf(y[jr + 1][i].x), b1 = fabsf(y[jr + 1][i].y);
+              rmax[jr] = max3n(rmax[jr], a0, b0);
+              rmax[jr + 1] = max3n(rmax[jr + 1], a1, b1);
+              cmax[2 * i] = max3n(cmax[2 * i], a0, a1);
+              cmax[2 * i + 1] = max3n(cmax[2 * i + 1], b0, b1);
+            }
+          }
+          // the row blocks' and column blocks' maxima, scales and inverse
+          // scales, the two independent shuffle chains side by side
+          float rm0, rm1, cm0, cm1;
+          block_max_scatter(rmax, cc >> 1, cc & 1, 2, 1, rm0, rm1);
+          block_max_scatter(cmax, rg >> 1, rg & 1, kColS1, kColS0, cm0, cm1);
+          const uint32_t rcode0 = e8m0_code(rm0), rcode1 = e8m0_code(rm1);
+          const uint32_t ccode0 = e8m0_code(cm0), ccode1 = e8m0_code(cm1);
+          float inv[8], cinv[8];
+          gather8(e8m0_inv_scale(rcode0), e8m0_inv_scale(rcode1), cc >> 1, cc & 1, 2, 1, inv);
+          gather8(e8m0_inv_scale(ccode0), e8m0_inv_scale(ccode1), rg >> 1, rg & 1, kColS1, kColS0,
+                  cinv);
+          if (rowwise && valid) {
+            uint8_t* dp = p.data + ((size_t)(r0 + 8 * rg) * H + 64 * sub + 8 * cl);
+#pragma unroll
+            for (int jr = 0; jr < 8; ++jr) {
+              const float2 iv = splat2(inv[jr]);
+              float2 v[4];
+#pragma unroll
+              for (int i = 0; i < 4; ++i) v[i] = mul2(y[jr][i], iv);
+              *reinterpret_cast<uint2*>(dp) = make_uint2(pack_e4m3x4(v[0].x, v[0].y, v[1].x, v[1].y),
+                                                         pack_e4m3x4(v[2].x, v[2].y, v[3].x, v[3].y));
+              dp += H;
+            }
+            uint8_t* sp = p.row_scales + ((size_t)(r0 + 8 * rg + cc) * hs + 2 * sub + hb);
+            sp[0] = (uint8_t)rcode0;
+            sp[4 * (size_t)hs] = (uint8_t)rcode1;
+          }
+          if (colwise && valid) {
+            uint8_t* cp = p.col_data + ((size_t)(64 * sub + 8 * cl) * N + r0 + 8 * rg);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const float2 ci = make_float2(cinv[2 * i], cinv[2 * i + 1]);
+              float2 qv[8];
+#pragma unroll
+              for (int jr = 0; jr < 8; ++jr) qv[jr] = mul2(y[jr][i], ci);
+              *reinterpret_cast<uint2*>(cp) =
+                  make_uint2(pack_e4m3x4(qv[0].x, qv[1].x, qv[2].x, qv[3].x),
+                             pack_e4m3x4(qv[4].x, qv[5].x, qv[6].x, qv[7].x));
+              *reinterpret_cast<uint2*>(cp + N) =
+                  make_uint2(pack_e4m3x4(qv[0].y, qv[1].y, qv[2].y, qv[3].y),
+                             pack_e4m3x4(qv[4].y, qv[5].y, qv[6].y, qv[7].y));
+              cp += 2 * (size_t)N;
+            }
+            uint8_t* csp = p.col_scales + ((size_t)(64 * sub + 8 * cl + rg) * ns + tile);
+            csp[0] = (uint8_t)ccode0;
+            csp[4 * (size_t)ns] = (uint8_t)ccode1;
+          }
         }
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&aempty[s]));
+      release(s, pos.use, 2 * (EMPTY / SPB));
     }
-    if (lane == 0) mbar_arrive(smem_u32(&tdone[tl % NT]));
+    li += (uint32_t)nbox;
   }
+  // every copy issued has been waited on by its readers; after a wait that
+  // gave up (an error is recorded) one may still be in flight: wait for each
+  // slot's last load before the CTA leaves
+  __syncthreads();
+  if (threadIdx.x == 0)
+    for (uint32_t sl = 0; sl < Q && sl < nload; ++sl) {
+      const uint32_t last = sl + Q * ((nload - 1 - sl) / Q);
+      mbar_wait(smem_u32(&full[sl]), (last / Q) & 1u, &g_err_mx, kErrDrainWait);
+    }
 }
 
 // cuTensorMapEncodeTiled, fetched once through the runtime (no link against
@@ -816,25 +992,28 @@ EncodeTiledFn encode_tiled() {
   return fn;
 }
 
-template <int NK, int SNC>
-rn_status launch_slab_t(const MxParams& p, const Launch& l, cudaStream_t s) {
-  auto k = rn_mx_slab_kernel<NK, SNC>;
-  if (l.threads > kMaxThreads || p.H % kMxSlabCols != 0 || p.H / 8 > 32 * SNC || p.n_tbar < 2 ||
-      p.Qs < p.stats_warps || p.Qs % p.stats_warps != 0 || p.Q % p.apply_warps != 0 ||
-      (p.H / kMxSlabCols) % p.apply_warps != 0 || l.threads != 32 * (p.apply_warps + p.stats_warps + 2))
+template <typename TIn, int NK>
+rn_status launch_box_t(const MxParams& p, const Launch& l, cudaStream_t s) {
+  auto k = rn_mx_box_kernel<TIn, NK>;
+  constexpr int C0 = 128 / (int)sizeof(TIn);
+  if (l.threads != kBoxThreads || p.H % C0 != 0 || p.N % kBoxRows != 0 || p.Q < 2)
     return RN_ERR_UNSUPPORTED;
   EncodeTiledFn enc = encode_tiled();
   if (enc == nullptr) return RN_ERR_CUDA;
-  // x as a 2-D bf16 tensor [N rows][H columns]; boxes of 32 rows x kMxSlabCols
-  // columns (128 bytes a row: the inner extent is a multiple of 16 bytes)
+  // x [N][H] seen as 3-D: the 128-byte column block (C0 elements,
+  // contiguous), rows (stride H elements), column blocks (stride C0
+  // elements); a box is 32 rows x kBoxCb column blocks, 128-byte swizzled.
+  // Column blocks past H / C0 (the last box of a row) read as zeros.
   CUtensorMap tm;
-  const cuuint64_t dims[2] = {(cuuint64_t)p.H, (cuuint64_t)p.N};
-  const cuuint64_t strides[1] = {(cuuint64_t)p.H * 2};
-  const cuuint32_t box[2] = {(cuuint32_t)kMxSlabCols, (cuuint32_t)kTile};
-  const cuuint32_t estr[2] = {1, 1};
-  if (enc(&tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(p.x), dims, strides, box, estr,
-          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-          CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+  const cuuint64_t dims[3] = {(cuuint64_t)C0, (cuuint64_t)p.N, (cuuint64_t)(p.H / C0)};
+  const cuuint64_t strides[2] = {(cuuint64_t)p.H * sizeof(TIn), (cuuint64_t)128};
+  const cuuint32_t box[3] = {(cuuint32_t)C0, (cuuint32_t)kBoxRows, (cuuint32_t)kBoxCb};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUtensorMapDataType dt =
+      sizeof(TIn) == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+  if (enc(&tm, dt, 3, const_cast<void*>(p.x), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return RN_ERR_CUDA;
   if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)l.smem) !=
       cudaSuccess)
@@ -880,10 +1059,10 @@ rn_status launch_mx(int nk, bool bf16, int ng, const MxParams& p, const Launch& 
   return nk == kLn ? launch_f<float, kLn>(p, l, s) : launch_f<float, kRms>(p, l, s);
 }
 
-rn_status launch_mx_slab(int nk, const MxParams& p, const Launch& l, cudaStream_t s) {
-  if (nk == kLn) return p.H <= 2048 ? launch_slab_t<kLn, 8>(p, l, s) : launch_slab_t<kLn, 16>(p, l, s);
-  if (nk == kRms) return p.H <= 2048 ? launch_slab_t<kRms, 8>(p, l, s) : launch_slab_t<kRms, 16>(p, l, s);
-  return RN_ERR_UNSUPPORTED;
+rn_status launch_mx_box(int nk, bool bf16, const MxParams& p, const Launch& l, cudaStream_t s) {
+  if (nk == kIdentity) return bf16 ? RN_ERR_UNSUPPORTED : launch_box_t<float, kIdentity>(p, l, s);
+  if (bf16) return nk == kLn ? launch_box_t<uint16_t, kLn>(p, l, s) : launch_box_t<uint16_t, kRms>(p, l, s);
+  return nk == kLn ? launch_box_t<float, kLn>(p, l, s) : launch_box_t<float, kRms>(p, l, s);
 }
 
 rn_status read_clear_error_mx(unsigned* code) {

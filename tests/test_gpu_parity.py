@@ -167,16 +167,25 @@ FWD_CASES = [
     ("mxfp8", 96, None, True, "mxfp8"),
     ("mxfp8", 96, None, False, "mxfp8"),
     ("mxfp8", 64, 512, True, "mxfp8"),
-    # bf16 rows of 256 .. 2048 columns take the kernel that holds a 32-row
-    # tile in registers (every shape it has); other widths the ring kernel
+    # rows of whole 128-byte column blocks take the box kernel (bf16 H a
+    # multiple of 64, every fp32 row); other bf16 widths the ring kernel
     ("mxfp8", 160, 256, False, "mxfp8"),
     ("mxfp8", 96, 1024, True, "mxfp8"),
     ("mxfp8", 96, 1024, False, "mxfp8"),
     ("mxfp8", 64, 768, True, "mxfp8"),
     ("mxfp8", 64, 800, False, "mxfp8"),
     ("mxfp8", 32, 3072, True, "mxfp8"),
-    ("mxfp8", 64, 4096, True, "mxfp8"),     # the widest slab rows (16 chunks a stats lane)
+    ("mxfp8", 64, 4096, True, "mxfp8"),
     ("mxfp8", 32, 4096, False, "mxfp8"),
+    # wide rows, both directions (the box kernel holds no whole tile)
+    ("mxfp8", 32, 8192, True, "mxfp8"),
+    ("mxfp8", 64, 8192, True, "mxfp8"),
+    ("mxfp8", 32, 8192, False, "mxfp8"),
+    ("mxfp8", 32, 16384, True, "mxfp8"),
+    ("mxfp8", 96, 2112, True, "mxfp8"),     # a last box of one column block
+    ("bwd_f32", 64, 2048, True, "mxfp8"),
+    ("bwd_f32", 32, 4096, False, "mxfp8"),
+    ("bwd_f32", 64, 1056, True, "mxfp8"),   # fp32: a last sub-tile of 32 columns
     ("bwd_f32", 67, 1024, True, "none"),
     ("bwd_f32", 67, 1024, False, "fp8_delayed"),
     ("bwd_f32", 64, 1024, True, "mxfp8"),
@@ -408,3 +417,24 @@ def test_backward_workspace_too_small():
     ws = torch.empty(16, dtype=torch.uint8, device="cuda")
     with pytest.raises(rn.RNError, match="status 3"):
         rn.rmsnorm_bwd(x, x, rs, g, workspace=ws)
+
+
+@pytest.mark.parametrize("dtype,H,ln,ok", [
+    (torch.bfloat16, 41216, True, True), (torch.bfloat16, 41280, True, False),
+    (torch.float32, 20608, False, True), (torch.float32, 20640, False, False),
+    (torch.bfloat16, 3104, True, True), (torch.bfloat16, 3168, True, False),
+    (torch.bfloat16, 3296, False, True), (torch.bfloat16, 3360, False, False),
+])
+def test_mxfp8_two_direction_width_limits(dtype, H, ln, ok):
+    """The two-direction MXFP8 width limits the header states: the widest
+    accepted row runs, the next width is refused on the host."""
+    x = torch.randn((32, H), device="cuda").to(dtype)
+    g = torch.ones(H, device="cuda")
+    run = (lambda: rn.layernorm_fwd(x, g, None, 1e-5, quant="mxfp8")) if ln else \
+        (lambda: rn.rmsnorm_fwd(x, g, 1e-5, quant="mxfp8"))
+    if ok:
+        out = run()[0]
+        assert out.col_data.shape == (H, 32)
+    else:
+        with pytest.raises(rn.RNError, match="status 2"):
+            run()
