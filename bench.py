@@ -117,6 +117,63 @@ def profile_traffic(name, files):
     return float(m.group(1))
 
 
+# Roofline entries for the largest shape of every forward mode and of the
+# backward: (entry, workload result, kernels of the call, ncu summaries in
+# profiles/ whose traffic adds up to the call's, kernel source files).
+FWD_SRC = ["rn_fwd.cu", "rn_device.cuh"]
+ROOFLINES = [
+    ("rms_fwd_fp8_current_16384x8192", "rms_16384x8192_fwd_fp8_current",
+     "rn_rmsnorm_fwd FP8_CURRENT: rn_fwd_init_kernel + rn_fwd_kernel (amax pass) + rn_fwd_kernel (quantize pass)",
+     ["rn_fwd_rms_fp8_current_pass1_bf16_16384x8192.md", "rn_fwd_rms_fp8_current_pass2_bf16_16384x8192.md"],
+     FWD_SRC),
+    ("ln_fwd_mxfp8_65536x2048", "ln_65536x2048_fwd_mxfp8",
+     "rn_layernorm_fwd MXFP8 rowwise + columnwise: rn_mx_box_kernel",
+     ["rn_mx_ln_bf16_65536x2048.md"], ["rn_mx.cu", "rn_device.cuh"]),
+    ("rms_fwd_mxfp8_65536x2048", "rms_65536x2048_fwd_mxfp8",
+     "rn_rmsnorm_fwd MXFP8 rowwise + columnwise: rn_mx_box_kernel",
+     ["rn_mx_rms_bf16_65536x2048.md"], ["rn_mx.cu", "rn_device.cuh"]),
+    ("ln_fwd_mxfp8_rowwise_65536x2048", "ln_65536x2048_fwd_mxfp8_rowwise_only",
+     "rn_layernorm_fwd MXFP8 rowwise only: rn_fwd_kernel",
+     ["rn_fwd_ln_mxfp8_row_bf16_65536x2048.md"], FWD_SRC),
+    ("ln_fwd_none_65536x2048", "ln_65536x2048_fwd_none", "rn_layernorm_fwd NONE: rn_fwd_kernel",
+     ["rn_fwd_ln_none_bf16_65536x2048.md"], FWD_SRC),
+    ("rms_fwd_none_65536x2048", "rms_65536x2048_fwd_none", "rn_rmsnorm_fwd NONE: rn_fwd_kernel",
+     ["rn_fwd_rms_none_bf16_65536x2048.md"], FWD_SRC),
+    ("rms_fwd_none_16384x8192", "rms_16384x8192_fwd_none", "rn_rmsnorm_fwd NONE: rn_fwd_kernel",
+     ["rn_fwd_rms_none_bf16_16384x8192.md"], FWD_SRC),
+    ("ln_fwd_fp8_delayed_65536x2048", "ln_65536x2048_fwd_fp8_delayed",
+     "rn_layernorm_fwd FP8_DELAYED: rn_fwd_init_kernel + rn_fwd_kernel",
+     ["rn_fwd_ln_fp8_delayed_bf16_65536x2048.md"], FWD_SRC),
+    ("rms_fwd_fp8_delayed_65536x2048", "rms_65536x2048_fwd_fp8_delayed",
+     "rn_rmsnorm_fwd FP8_DELAYED: rn_fwd_init_kernel + rn_fwd_kernel",
+     ["rn_fwd_rms_fp8_delayed_bf16_65536x2048.md"], FWD_SRC),
+    ("rms_fwd_fp8_delayed_16384x8192", "rms_16384x8192_fwd_fp8_delayed",
+     "rn_rmsnorm_fwd FP8_DELAYED: rn_fwd_init_kernel + rn_fwd_kernel",
+     ["rn_fwd_rms_fp8_delayed_bf16_16384x8192.md"], FWD_SRC),
+    ("ln_bwd_f32_131072x1024", "ln_131072x1024_f32_bwd_margin0",
+     "rn_layernorm_bwd fp32: rn_bwd_fused_kernel + rn_colreduce_kernel",
+     ["rn_bwd_fused_ln_f32_131072x1024.md"], ["rn_bwd.cu", "rn_device.cuh"]),
+    ("rms_bwd_f32_131072x1024", "rms_131072x1024_f32_bwd_margin0",
+     "rn_rmsnorm_bwd fp32: rn_bwd_fused_kernel + rn_colreduce_kernel",
+     ["rn_bwd_fused_rms_f32_131072x1024.md"], ["rn_bwd.cu", "rn_device.cuh"]),
+    ("ln_bwd_bf16_3000x5120", "ln_3000x5120_bf16_bwd_margin0",
+     "rn_layernorm_bwd bf16: rn_bwd_kernel + rn_colreduce_kernel",
+     ["rn_bwd_ln_bf16_3000x5120.md"], ["rn_bwd.cu", "rn_device.cuh"]),
+]
+
+
+def roofline_entry(kernel, ms, algo_bytes, peak, peak_kind, profiles, files):
+    """achieved = algorithmic bytes / mean call time (CUDA events); traffic =
+    the sum of the committed ncu summaries' DRAM bytes per launch, or None
+    when one is missing or older than the kernel source."""
+    gbs = algo_bytes / (ms * 1e-3) / 1e9
+    tr = [profile_traffic(f, files) for f in profiles]
+    return {"kernel": kernel, "bound": "hbm", "achieved": round(gbs, 1), "peak": peak,
+            "peak_kind": peak_kind, "unit": "GB/s", "frac": round(gbs / peak, 4),
+            "traffic": None if any(t is None for t in tr) else int(sum(tr)),
+            "algorithmic_bytes": algo_bytes, "ms": round(ms, 5), "profiles": profiles}
+
+
 class ClockSampler:
     """nvidia-smi clock / throttle sampling in the background."""
     Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -335,6 +392,32 @@ def time_calls(torch, lib, calls, steps, warmup, flush):
             for i, (name, _) in enumerate(calls)}
 
 
+def l2_writeback_ms(torch, lib, fa, flush, reps=10):
+    """Estimate of the write-back a call leaves for later: at 8192 x 4096 part
+    of the call's output is still dirty in L2 (129 MB) when its end event
+    fires, and the next flush writes it to HBM outside the timed region.
+    Returns the mean flush time right after the call minus right after
+    another flush (ms, >= 0)."""
+    s = torch.cuda.current_stream()
+    stream = ctypes.c_void_p(s.cuda_stream)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+    def timed_flush():
+        a.record(s)
+        flush()
+        b.record(s)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b)
+    after_call, after_flush = [], []
+    for _ in range(reps):
+        flush()
+        call(lib, fa, stream)
+        after_call.append(timed_flush())
+        flush()
+        after_flush.append(timed_flush())
+    return max(0.0, statistics.mean(after_call) - statistics.mean(after_flush))
+
+
 def run_rn(args):
     import torch
     import torch.distributed as dist
@@ -408,6 +491,9 @@ def run_rn(args):
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         fwd_ms, bwd_ms = (float(v) for v in t.tolist())
 
+    wb_fwd = l2_writeback_ms(torch, lib, fwd, flush)
+    wb_bwd = l2_writeback_ms(torch, lib, bwd, flush)
+
     # ------------------------------------------------ end to end, host data
     e2e = None
     if rank == 0:
@@ -425,6 +511,19 @@ def run_rn(args):
             dist.destroy_process_group()
         return
     cpu = cpu_baseline(w, step_bytes) if not args.no_cpu else None
+    pk = f"{peak_kind}" + (f" ({peak_key})" if peak_key else "")
+    rooflines = {
+        "ln_fwd_fp8_delayed_8192x4096": roofline_entry(
+            "rn_layernorm_fwd FP8_DELAYED: rn_fwd_init_kernel + rn_fwd_kernel", fwd_ms, b_fwd, peak, pk,
+            ["rn_fwd_ln_fp8_delayed_bf16_8192x4096.md"], FWD_SRC),
+        "ln_bwd_bf16_8192x4096": roofline_entry(
+            "rn_layernorm_bwd bf16: rn_bwd_kernel + rn_colreduce_kernel", bwd_ms, b_bwd, peak, pk,
+            ["rn_bwd_ln_bf16_8192x4096.md"], ["rn_bwd.cu", "rn_device.cuh"]),
+    }
+    for name, key, kernel, profs, files in ROOFLINES:
+        if key in extra:
+            r = extra[key]
+            rooflines[name] = roofline_entry(kernel, r["ms"], r["algorithmic_bytes"], peak, pk, profs, files)
     bwd_gbs = b_bwd / (bwd_ms * 1e-3) / 1e9
     fwd_gbs = b_fwd / (fwd_ms * 1e-3) / 1e9
     traffic = profile_traffic("rn_bwd_ln_bf16_8192x4096.md", ["rn_bwd.cu", "rn_device.cuh"])
@@ -450,7 +549,10 @@ def run_rn(args):
                    "fwd_GBps": round(fwd_gbs, 1), "bwd_GBps": round(bwd_gbs, 1),
                    "algorithmic_bytes_per_step": step_bytes,
                    "pct_of_8TBps": round(100 * value / world / 8000.0, 2),
-                   "wall_s_timed_loop": round(t_wall, 3)},
+                   "wall_s_timed_loop": round(t_wall, 3),
+                   "l2_writeback_ms_est": {"fwd": round(wb_fwd, 5), "bwd": round(wb_bwd, 5)},
+                   "GBps_if_writeback_timed": round(world * step_bytes / ((ms_step + wb_fwd + wb_bwd) * 1e-3)
+                                                    / 1e9, 1)},
         "roofline": {"kernel": "rn_layernorm_bwd call (rn_bwd_kernel + rn_colreduce_kernel)",
                      "bound": "hbm", "achieved": round(bwd_gbs, 1), "peak": peak,
                      "peak_kind": f"{peak_kind}" + (f" ({peak_key})" if peak_key else ""),
@@ -462,6 +564,7 @@ def run_rn(args):
                          "traffic": profile_traffic("rn_fwd_ln_fp8_delayed_bf16_8192x4096.md",
                                                     ["rn_fwd.cu", "rn_device.cuh"]),
                          "algorithmic_bytes": b_fwd},
+        "rooflines": rooflines,
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": 4 * args.steps,  # init + forward, backward + column reduction
@@ -536,8 +639,8 @@ def run_e2e(torch, lib, P, fwd, bwd, w, steps, step_bytes):
 
 def run_other_workloads(torch, rn, lib, rn_inputs, flush, peak, steps, warmup, only=None):
     """Full-size timing of the other workloads; ``only`` restricts the run to
-    one group ("rms_small", "rms_current", "mxfp8", "bwd_f32", "bwd_bf16", "rms_add",
-    "moe_act")."""
+    one group ("rms_small", "rms_current", "mxfp8", "large_fwd", "bwd_f32", "bwd_bf16",
+    "rms_add", "moe_act")."""
     res = {}
 
     def want(name):
@@ -576,6 +679,23 @@ def run_other_workloads(torch, rn, lib, rn_inputs, flush, peak, steps, warmup, o
                        statistics.mean(t["mr"]), 1)
             del P
         del w
+    if want("large_fwd"):
+        # forward NONE and FP8 delayed at the largest shapes: the MXFP8
+        # workload's rows (65536 x 2048, LayerNorm and RMSNorm) and the
+        # current-scaling workload's (16384 x 8192, RMSNorm); the delayed
+        # scale is a fixed 1.0 (the kernels' work does not depend on it)
+        for wl, lns in (("mxfp8", (True, False)), ("rms_current", (False,))):
+            w = rn_inputs.make(wl)
+            for ln in lns:
+                P = Prepared(rn, torch, w, ln=ln)
+                tag = f"{'ln' if ln else 'rms'}_{w.N}x{w.H}"
+                t = time_calls(torch, lib, [("n", P.fwd_args("none"))], steps, warmup, flush)
+                report(f"{tag}_fwd_none", "fwd_none", w.N, w.H, 2, ln, statistics.mean(t["n"]), 1)
+                t = time_calls(torch, lib, [("d", P.fwd_args("fp8_delayed", scale=1.0))], steps, warmup,
+                               flush)
+                report(f"{tag}_fwd_fp8_delayed", "fwd_fp8", w.N, w.H, 2, ln, statistics.mean(t["d"]), 2)
+                del P
+            del w
     if want("rms_small"):
         # the delayed-scaling history step (1024 entries): one tiny kernel,
         # launch-latency bound
@@ -671,58 +791,138 @@ def _small(torch, rn, lib, rn_inputs, flush, steps, warmup, report):
     del P
 
 
-def cpu_baseline(w, step_bytes):
-    """The oracle as it stands, on this host, over the whole headline
-    workload once (fwd + FP8 delayed quantization + bwd)."""
+# ------------------------------------------------------- CPU oracle team
+# The oracle on every host core: one spawned worker process per core (spawn,
+# not fork: the parent may already hold a CUDA context), each regenerating
+# the seeded workload once, untimed; a timed call deals row blocks to them.
+_TEAM = {}
+
+
+def _team_init(barrier, workload):
     import oracle
-    x = w.x_f64()
-    dz = w.dz_f64()
-    t0 = time.time()
+    import rn_inputs
+    _TEAM["barrier"] = barrier
+    _TEAM["w"] = rn_inputs.make(workload)
+    _TEAM["oracle"] = oracle
+
+
+def _team_sync(_):
+    # every worker takes exactly one of these (each waits for all the others)
+    _TEAM["barrier"].wait(timeout=900)
+    return os.getpid()
+
+
+def _team_block(rows):
+    """LayerNorm fwd with FP8 delayed scaling + LayerNorm bwd of rows r0..r1
+    of the ln_delayed workload, by the oracle as it stands."""
+    r0, r1 = rows
+    w, oracle = _TEAM["w"], _TEAM["oracle"]
+    x = w.x_f64(slice(r0, r1))
+    dz = w.dz_f64(slice(r0, r1))
     f = oracle.layernorm_fwd(x, w.gamma, w.beta, w.eps, True, "fp8_delayed", scale=w.scale)
     oracle.layernorm_bwd(dz, x, f["mu"], f["rsigma"], w.gamma, True, "bf16")
-    dt = time.time() - t0
-    return {"value": round(step_bytes / dt / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "sample": f"the full workload, {w.N} rows x {w.H}, one fwd+bwd pass ({dt:.1f} s, "
-                      "numpy fp64, one thread)"}
+    return r1 - r0
+
+
+class OracleTeam:
+    """A pool of one oracle process per host core (numpy single-threaded in
+    each: one worker per core is the parallelism)."""
+
+    def __init__(self, workload="ln_delayed"):
+        import multiprocessing as mp
+        try:
+            self.cores = len(os.sched_getaffinity(0))
+        except AttributeError:
+            self.cores = os.cpu_count() or 1
+        ctx = mp.get_context("spawn")
+        keys = ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS")
+        saved = {k: os.environ.get(k) for k in keys}
+        for k in keys:
+            os.environ[k] = "1"
+        try:
+            barrier = ctx.Barrier(self.cores)
+            self.pool = ctx.Pool(self.cores, initializer=_team_init, initargs=(barrier, workload))
+        finally:
+            for k, v in saved.items():
+                if v is None:
+                    os.environ.pop(k, None)
+                else:
+                    os.environ[k] = v
+        pids = self.pool.map(_team_sync, range(self.cores), chunksize=1)
+        self.workers = len(set(pids))
+
+    def run(self, r0, r1):
+        """Rows r0..r1 in one block per worker; returns the wall seconds."""
+        n = r1 - r0
+        edges = [r0 + (n * i) // self.cores for i in range(self.cores + 1)]
+        blocks = [(edges[i], edges[i + 1]) for i in range(self.cores) if edges[i + 1] > edges[i]]
+        t0 = time.perf_counter()
+        done = sum(self.pool.map(_team_block, blocks, chunksize=1))
+        dt = time.perf_counter() - t0
+        assert done == n
+        return dt
+
+    def close(self):
+        self.pool.close()
+        self.pool.join()
+
+
+def cpu_baseline(w, step_bytes):
+    """The oracle as it stands, on all host cores, over the whole headline
+    workload once (fwd + FP8 delayed quantization + bwd), after a warm-up
+    over one small block a core."""
+    team = OracleTeam("ln_delayed")
+    try:
+        team.run(0, min(w.N, 8 * team.cores))
+        dt = team.run(0, w.N)
+    finally:
+        team.close()
+    return {"value": round(step_bytes / dt / 1e9, 4), "unit": "GB/s", "cores": team.cores,
+            "workers": team.workers, "kind": "oracle",
+            "rows_per_s": round(w.N / dt, 1),
+            "sample": f"the full workload, {w.N} rows x {w.H}, one fwd+bwd pass ({dt:.2f} s wall on "
+                      f"{team.cores} cores; numpy fp64, one process a core, row blocks)"}
 
 
 # ---------------------------------------------------------- reference arm
 def run_reference(args):
-    """The oracle (the only reference this method has here) on host cores;
-    each step is a bounded 32-row sample of the headline workload."""
+    """The oracle (the only reference this method has here) on all host
+    cores; each step is a bounded sample of the headline workload: 64 rows
+    a core, the next rows each step."""
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
-    import oracle
     import rn_inputs
     w = rn_inputs.make("ln_delayed")
-    rows = 32
+    team = OracleTeam("ln_delayed")
+    rows = min(w.N, 64 * team.cores)
     per_sample = algorithmic_bytes("fwd_fp8", rows, w.H, 2, True) + algorithmic_bytes("bwd", rows, w.H, 2, True)
 
     def step(k):
         r0 = (k * rows) % w.N
-        sl = slice(r0, r0 + rows)
-        x = w.x_f64(sl)
-        dz = w.dz_f64(sl)
-        f = oracle.layernorm_fwd(x, w.gamma, w.beta, w.eps, True, "fp8_delayed", scale=w.scale)
-        oracle.layernorm_bwd(dz, x, f["mu"], f["rsigma"], w.gamma, True, "bf16")
+        r0 = min(r0, w.N - rows)
+        return team.run(r0, r0 + rows)
 
-    for k in range(args.warmup):
-        step(k)
-    t0 = time.time()
-    for k in range(args.steps):
-        step(k)
-    dt = (time.time() - t0) / args.steps
+    try:
+        for k in range(args.warmup):
+            step(k)
+        times = [step(args.warmup + k) for k in range(args.steps)]
+    finally:
+        team.close()
+    dt = sum(times) / len(times)
     v = per_sample / dt / 1e9
     line = {"impl": "reference", "metric": METRIC, "value": round(v, 4), "unit": "GB/s",
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(dt * 1e3, 4), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded rn_inputs workload ln_delayed)",
             "config": {"workload": "LayerNorm fwd (FP8 delayed) + bwd, bf16 [8192 x 4096], "
-                                   f"each step a {rows}-row sample"},
-            "cpu_baseline": {"value": round(v, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-                             "sample": f"{rows} rows of 8192 per step"},
+                                   f"each step a {rows}-row sample",
+                       "rows_per_s": round(rows / dt, 1)},
+            "cpu_baseline": {"value": round(v, 4), "unit": "GB/s", "cores": team.cores,
+                             "workers": team.workers, "kind": "oracle",
+                             "sample": f"{rows} consecutive rows of 8192 per step ({rows // team.cores} "
+                                       "a core), one process a core"},
             "e2e": {"value": round(v, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line))
@@ -737,8 +937,8 @@ def main():
     ap.add_argument("--quick", action="store_true", help="headline workload only")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--only", default=None,
-                    choices=["rms_small", "rms_current", "mxfp8", "bwd_f32", "bwd_bf16", "rms_add",
-                             "moe_act"],
+                    choices=["rms_small", "rms_current", "mxfp8", "large_fwd", "bwd_f32", "bwd_bf16",
+                             "rms_add", "moe_act"],
                     help="time only this workload group (prints its results; for profiling)")
     args = ap.parse_args()
     if args.warmup < 3:
