@@ -582,7 +582,7 @@ __global__ void __launch_bounds__(kBoxThreads, 1)
   const int nua = nbox * SPB;                  // sub-tiles a tile (some may lie past H)
   unsigned char* ring = smem;
   float2* pbuf = reinterpret_cast<float2*>(ring + (size_t)Q * kBoxBytes);  // [2][nus][32]
-  float2* tstat = pbuf + 2 * (size_t)nus * kBoxRows;                       // [2][32] (mean, rsigma)
+  float2* tstat = pbuf + 2 * (size_t)nus * kBoxRows;                       // [2][32] (-mean rsigma, rsigma)
   uint64_t* full = reinterpret_cast<uint64_t*>(tstat + 2 * kBoxRows);
   uint64_t* tready = full + Q;                                             // [2]
   uint64_t* sdone = tready + 2;                                            // [2]
@@ -716,7 +716,9 @@ __global__ void __launch_bounds__(kBoxThreads, 1)
         }
         const float rs = __frsqrt_rn(m2 * inv_h + p.eps);
         const int row = ((int)blockIdx.x + ta * G) * kBoxRows + lane;
-        tstat[(ta & 1) * kBoxRows + lane] = make_float2(mean, rs);
+        // (-mean rsigma, rsigma): the apply forms x rsigma - mean rsigma with
+        // one fma
+        tstat[(ta & 1) * kBoxRows + lane] = make_float2(-mean * rs, rs);
         if (LN) p.mu[row] = mean;
         p.rsigma[row] = rs;
         __syncwarp();
@@ -744,39 +746,44 @@ __global__ void __launch_bounds__(kBoxThreads, 1)
           for (int i = 0; i < 4; ++i) a[i] = make_float2(0.f, 0.f);
           float sx = 0.0f, q2 = 0.0f;
           if constexpr (LN) {
-            // two passes over the unit: the sum, then the squared deviations
-            // from the unit's mean (read again from shared memory)
+            // per column block (C0 values of the lane's row, converted once
+            // into registers): the sum, then the squared deviations from the
+            // block's mean; the unit's two blocks are then joined by the
+            // pairwise formula M2 = M2_0 + M2_1 + (C0 / 2) (m_0 - m_1)^2
+            // (equal counts).  (nv == 0: an empty unit, which the merge skips.)
+            float sb[2] = {0.0f, 0.0f}, qb[2] = {0.0f, 0.0f};
 #pragma unroll
             for (int h = 0; h < 2; ++h)
               if (h < nv) {
+                float2 f[8 * PPC];
 #pragma unroll
                 for (int c = 0; c < 8; ++c) {
                   const uint4 v = chunk(h, c);
 #pragma unroll
-                  for (int i = 0; i < PPC; ++i)
-                    a[(c * PPC + i) & 3] = add2(a[(c * PPC + i) & 3], chunk_pair<TIn>(v, i));
+                  for (int i = 0; i < PPC; ++i) f[c * PPC + i] = chunk_pair<TIn>(v, i);
                 }
-              }
-            sx = (a[0].x + a[0].y) + (a[1].x + a[1].y) + (a[2].x + a[2].y) + (a[3].x + a[3].y);
-            // (nv == 0: an empty unit, which the merge skips)
-            const float um = nv > 0 ? sx * (nv == 2 ? 1.0f / (2 * C0) : 1.0f / C0) : 0.0f;
-            const float2 um2 = splat2(um);
 #pragma unroll
-            for (int i = 0; i < 4; ++i) a[i] = make_float2(0.f, 0.f);
+                for (int i = 0; i < 4; ++i) a[i] = f[i];
 #pragma unroll
-            for (int h = 0; h < 2; ++h)
-              if (h < nv) {
+                for (int k = 4; k < 8 * PPC; ++k) a[k & 3] = add2(a[k & 3], f[k]);
+                const float s = (a[0].x + a[0].y) + (a[1].x + a[1].y) + (a[2].x + a[2].y) + (a[3].x + a[3].y);
+                const float2 bm = splat2(s * (1.0f / C0));
 #pragma unroll
-                for (int c = 0; c < 8; ++c) {
-                  const uint4 v = chunk(h, c);
-#pragma unroll
-                  for (int i = 0; i < PPC; ++i) {
-                    const float2 d = sub2(chunk_pair<TIn>(v, i), um2);
-                    a[(c * PPC + i) & 3] = fma2(d, d, a[(c * PPC + i) & 3]);
-                  }
+                for (int i = 0; i < 4; ++i) {
+                  const float2 d = sub2(f[i], bm);
+                  a[i] = mul2(d, d);
                 }
+#pragma unroll
+                for (int k = 4; k < 8 * PPC; ++k) {
+                  const float2 d = sub2(f[k], bm);
+                  a[k & 3] = fma2(d, d, a[k & 3]);
+                }
+                sb[h] = s;
+                qb[h] = (a[0].x + a[0].y) + (a[1].x + a[1].y) + (a[2].x + a[2].y) + (a[3].x + a[3].y);
               }
-            q2 = (a[0].x + a[0].y) + (a[1].x + a[1].y) + (a[2].x + a[2].y) + (a[3].x + a[3].y);
+            sx = sb[0] + sb[1];
+            const float dm = (sb[0] - sb[1]) * (1.0f / C0);
+            q2 = nv == 2 ? (qb[0] + qb[1]) + (0.5f * C0) * dm * dm : qb[0];
           } else {
 #pragma unroll
             for (int h = 0; h < 2; ++h)
@@ -880,7 +887,7 @@ __global__ void __launch_bounds__(kBoxThreads, 1)
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
               if constexpr (LN)
-                y[jr][i] = fma2(mul2(sub2(x2[i], splat2(ms.x)), rs2), g2[i], b2[i]);
+                y[jr][i] = fma2(fma2(x2[i], rs2, splat2(ms.x)), g2[i], b2[i]);
               else if constexpr (NK == kRms)
                 y[jr][i] = mul2(mul2(x2[i], rs2), g2[i]);
               else
