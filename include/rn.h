@@ -166,11 +166,14 @@ rn_status rn_rmsnorm_fwd(const void* x, rn_dtype x_dtype, const float* gamma,
  *   then exactly rn_layernorm_fwd / rn_rmsnorm_fwd of h (mu, rsigma, output
  *   per `mode`).
  * x, residual, residual_out: [N, H] in `dtype`, 16-byte aligned;
- * residual_out may not alias x or residual.  Modes NONE, FP8_DELAYED,
- * FP8_CURRENT and NVFP4 (their second pass reads residual_out), and MXFP8
- * with the rowwise blocks only (col_data NULL; asking for the columnwise
- * copy returns RN_ERR_UNSUPPORTED).  Other arguments, errors and conventions as in the
- * plain forward.
+ * residual_out may not alias x or residual.  Every mode: FP8_CURRENT and
+ * NVFP4 read residual_out in their second pass; MXFP8 with the rowwise
+ * blocks only is one pass, and with the columnwise copy two kernels (the
+ * first forms h, the rowwise blocks when asked for and mu / rsigma, the
+ * second reads residual_out back for the columnwise blocks and writes mu /
+ * rsigma again from the same h), both planned before either is launched,
+ * with the width limits of the plain forward's two-direction MXFP8.  Other
+ * arguments, errors and conventions as in the plain forward.
  */
 rn_status rn_layernorm_add_fwd(const void* x, const void* residual, rn_dtype dtype,
                                const float* gamma, const float* beta, int64_t N, int64_t H,

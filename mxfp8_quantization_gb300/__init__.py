@@ -267,9 +267,10 @@ def rmsnorm_fwd(x, gamma, eps, quant="none", sm_margin=0, zero_centered_gamma=Fa
 
 
 def layernorm_add_fwd(x, residual, gamma, beta, eps, quant="none", sm_margin=0,
-                      zero_centered_gamma=False, scale=None, out_dtype=None):
-    """h = x + residual (rounded to x's dtype), LayerNorm(h) -> (output, h, mu, rsigma).
-    With quant="mxfp8" only the rowwise blocks are produced."""
+                      zero_centered_gamma=False, scale=None, out_dtype=None, rowwise=True,
+                      colwise=True):
+    """h = x + residual (rounded to x's dtype), LayerNorm(h) -> (output, h, mu, rsigma);
+    output per ``quant`` (MXFP8: the blocks ``rowwise`` / ``colwise`` select)."""
     lib = _load()
     _need(x, "x")
     N, H = x.shape
@@ -280,7 +281,7 @@ def layernorm_add_fwd(x, residual, gamma, beta, eps, quant="none", sm_margin=0,
     h = torch.empty_like(x)
     mu = torch.empty(N, dtype=torch.float32, device=x.device)
     rsigma = torch.empty(N, dtype=torch.float32, device=x.device)
-    o, res = _make_output(x, quant, out_dtype, scale, True, False)
+    o, res = _make_output(x, quant, out_dtype, scale, rowwise, colwise)
     st = lib.rn_layernorm_add_fwd(_ptr(x), _ptr(residual), _dtype_code(x), _ptr(gamma), _ptr(beta),
                                   N, H, float(eps), int(bool(zero_centered_gamma)), int(sm_margin),
                                   QUANT_MODES[quant], ctypes.byref(o), _ptr(h), _ptr(mu),
@@ -290,9 +291,10 @@ def layernorm_add_fwd(x, residual, gamma, beta, eps, quant="none", sm_margin=0,
 
 
 def rmsnorm_add_fwd(x, residual, gamma, eps, quant="none", sm_margin=0,
-                    zero_centered_gamma=False, scale=None, out_dtype=None):
-    """h = x + residual (rounded to x's dtype), RMSNorm(h) -> (output, h, rsigma).
-    With quant="mxfp8" only the rowwise blocks are produced."""
+                    zero_centered_gamma=False, scale=None, out_dtype=None, rowwise=True,
+                    colwise=True):
+    """h = x + residual (rounded to x's dtype), RMSNorm(h) -> (output, h, rsigma); output per
+    ``quant`` (MXFP8: the blocks ``rowwise`` / ``colwise`` select)."""
     lib = _load()
     _need(x, "x")
     N, H = x.shape
@@ -300,7 +302,7 @@ def rmsnorm_add_fwd(x, residual, gamma, eps, quant="none", sm_margin=0,
     _need(gamma, "gamma", torch.float32, (H,))
     h = torch.empty_like(x)
     rsigma = torch.empty(N, dtype=torch.float32, device=x.device)
-    o, res = _make_output(x, quant, out_dtype, scale, True, False)
+    o, res = _make_output(x, quant, out_dtype, scale, rowwise, colwise)
     st = lib.rn_rmsnorm_add_fwd(_ptr(x), _ptr(residual), _dtype_code(x), _ptr(gamma), N, H,
                                 float(eps), int(bool(zero_centered_gamma)), int(sm_margin),
                                 QUANT_MODES[quant], ctypes.byref(o), _ptr(h), _ptr(rsigma),

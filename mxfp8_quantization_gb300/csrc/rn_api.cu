@@ -378,10 +378,6 @@ rn_status fwd_common(int nk, const void* x, rn_dtype dt, const float* gamma, con
   // dtype; like the other row tensors they may be NULL when N == 0
   if (res && ((N > 0 && (residual == nullptr || residual_out == nullptr)) || nk == kIdentity))
     return RN_ERR_INVALID;
-  // with a residual add, MXFP8 gives the rowwise blocks only (one pass of
-  // the row kernel); the columnwise copy needs the 32-row tile kernels
-  if (res && mode == RN_QUANT_MXFP8 && (out == nullptr || out->col_data != nullptr))
-    return RN_ERR_UNSUPPORTED;
   if (res && N > 0 && (!aligned(residual, 16) || !aligned(residual_out, 16)))
     return RN_ERR_UNSUPPORTED;
   if ((x == nullptr && N > 0) || !dtype_ok(dt) || N < 0 || H < 1 || N > INT32_MAX ||
@@ -404,7 +400,44 @@ rn_status fwd_common(int nk, const void* x, rn_dtype dt, const float* gamma, con
   const bool bf16 = dt == RN_BF16;
   const int esz = elem_size(dt);
 
-  if (mode == RN_QUANT_MXFP8 && out->col_data == nullptr) {
+  // the input of the two-direction MXFP8 kernels, and its rowwise outputs
+  const void* mx_x = x;
+  uint8_t* mx_data = mode == RN_QUANT_MXFP8 ? static_cast<uint8_t*>(out->data) : nullptr;
+  uint8_t* mx_row_scales = mode == RN_QUANT_MXFP8 ? out->row_scales : nullptr;
+  if (mode == RN_QUANT_MXFP8 && res && out->col_data != nullptr) {
+    // residual add with the columnwise copy: the row kernel forms and stores
+    // h = x + residual, the rowwise blocks (when asked for) and mu / rsigma in
+    // one pass; the two-direction kernel below then reads h back for the
+    // columnwise blocks (and writes mu / rsigma again, from the same h).
+    // Both kernels are planned before the first is launched.
+    MxPlan mp;
+    if (plan_mx_box(nk, (int)H, esz, (int)N, sm_margin, di, &mp) != RN_OK &&
+        (st = plan_mx(nk, (int)H, esz, (int)N, sm_margin, di, &mp)) != RN_OK)
+      return st;
+    FwdPlan pr;
+    if ((st = plan_fwd(nk, (int)H, esz, (int)N, sm_margin, di, &pr, 2)) != RN_OK) return st;
+    FwdParams p{};
+    p.x = x;
+    p.gamma = gamma;
+    p.beta = beta;
+    p.out = out->data;
+    p.scales = out->data ? out->row_scales : nullptr;
+    p.mu = mu;
+    p.rsigma = rsigma;
+    p.N = (int)N;
+    p.H = (int)H;
+    p.eps = eps;
+    p.zcg = zcg ? 1 : 0;
+    p.residual = residual;
+    p.residual_out = residual_out;
+    p.workers = pr.workers;
+    p.Q = pr.Q;
+    p.rps_log2 = pr.rps_log2;
+    if ((st = launch_fwd_res(nk, bf16, pr.sh, kQMxRow, p, pr.l, false, stream)) != RN_OK) return st;
+    mx_x = residual_out;
+    mx_data = nullptr;
+    mx_row_scales = nullptr;
+  } else if (mode == RN_QUANT_MXFP8 && out->col_data == nullptr) {
     // rowwise blocks only: the row kernel in one pass (no 32-row tiles)
     FwdPlan pl;
     if ((st = plan_fwd(nk, (int)H, esz, (int)N, sm_margin, di, &pl)) != RN_OK) return st;
@@ -442,11 +475,11 @@ rn_status fwd_common(int nk, const void* x, rn_dtype dt, const float* gamma, con
     const bool box = plan_mx_box(nk, (int)H, esz, (int)N, sm_margin, di, &pl) == RN_OK;
     if (!box && (st = plan_mx(nk, (int)H, esz, (int)N, sm_margin, di, &pl)) != RN_OK) return st;
     MxParams p{};
-    p.x = x;
+    p.x = mx_x;
     p.gamma = gamma;
     p.beta = beta;
-    p.data = static_cast<uint8_t*>(out->data);
-    p.row_scales = out->row_scales;
+    p.data = mx_data;
+    p.row_scales = mx_row_scales;
     p.col_data = out->col_data;
     p.col_scales = out->col_scales;
     p.mu = mu;

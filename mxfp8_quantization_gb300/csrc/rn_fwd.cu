@@ -537,7 +537,9 @@ __global__ void __launch_bounds__(max_threads<NC>(), 1) rn_fwd_kernel(const FwdP
           const float w = __shfl_xor_sync(0xffffffffu, bm, o);
           asm("max.NaN.f32 %0, %0, %1;" : "+f"(bm) : "f"(w));
         }
-        if (k < nvalid_apply) {
+        // (no rowwise output: the residual add's first kernel when only the
+        // columnwise blocks are asked for)
+        if (k < nvalid_apply && p.out != nullptr) {
           const uint32_t code = e8m0_code(bm);
           store_chunk<PAIRS, QM>(orow + (size_t)k * ostep, 0, y, e8m0_inv_scale(code));
           if ((lane & (32 / VEC - 1)) == 0) srow[(size_t)k * (CSTEP * VEC / 32)] = (uint8_t)code;

@@ -39,9 +39,10 @@ def _workload(name, N, H):
     return w
 
 
-def _run(w, ln, mode, sm_margin=0):
+def _run(w, ln, mode, sm_margin=0, rowwise=True, colwise=True):
     x, r, g = to_dev(w.x, w.dtype), to_dev(w.residual, w.dtype), to_dev(w.gamma, "f32")
-    kw = dict(quant=mode, sm_margin=sm_margin, scale=w.scale if mode == "fp8_delayed" else None)
+    kw = dict(quant=mode, sm_margin=sm_margin, scale=w.scale if mode == "fp8_delayed" else None,
+              rowwise=rowwise, colwise=colwise)
     if ln:
         out, h, mu, rs = rn.layernorm_add_fwd(x, r, g, to_dev(w.beta, "f32"), w.eps, **kw)
         return out, h, mu.cpu().numpy(), rs.cpu().numpy()
@@ -88,10 +89,15 @@ def _check(w, ln, mode, got, ref):
     check_stats(mu, rs, hf, ref.get("mu"), ref["rsigma"])
     wt = term_magnitude(hf, ref.get("mu") if ln else None, ref["rsigma"], w.gamma,
                         w.beta if ln else None, False)
-    if mode == "mxfp8":   # rowwise blocks only with the residual add
-        assert out.col_data is None and out.col_scales is None
-        check_mx(out.data.cpu().numpy(), out.row_scales.cpu().numpy(), ref["y"].astype(np.float32),
-                 wt, "residual mx-row")
+    if mode == "mxfp8":
+        y32 = ref["y"].astype(np.float32)
+        if out.data is not None:
+            check_mx(out.data.cpu().numpy(), out.row_scales.cpu().numpy(), y32, wt, "residual mx-row")
+        if out.col_data is not None:
+            # the columnwise copy holds the blocks of y transposed: the
+            # rowwise blocks of y.T
+            check_mx(out.col_data.cpu().numpy(), out.col_scales.cpu().numpy(),
+                     np.ascontiguousarray(y32.T), np.ascontiguousarray(wt.T), "residual mx-col")
         return
     if mode == "none":
         if w.dtype == "bf16":
@@ -124,10 +130,46 @@ def test_residual_add_full_size_and_margin():
     assert np.array_equal(a[3], b[3]) and torch.equal(a[0].amax, b[0].amax)
 
 
-def test_residual_add_mxfp8_is_rowwise_only():
-    """With the residual add, MXFP8 gives the rowwise blocks (a columnwise
-    request is refused on the host: tests/test_cpu_abi.py)."""
-    w = _workload("rms_add", 64, 256)
-    out, h, rs = rn.rmsnorm_add_fwd(to_dev(w.x, "bf16"), to_dev(w.residual, "bf16"),
-                                    to_dev(w.gamma, "f32"), w.eps, quant="mxfp8")
-    assert out.col_data is None and out.data.shape == (64, 256) and out.row_scales.shape == (64, 8)
+MX_DIRECTIONS = [
+    # (workload, N, H, ln, rowwise, colwise): the box kernel (bf16 H % 64 == 0,
+    # fp32), the ring kernel (bf16 H % 64 == 32), each direction alone
+    ("rms_add", 96, 2048, True, False, True),
+    ("rms_add", 64, 2080, False, True, True),
+    ("rms_add", 128, 1024, True, True, False),
+    ("bwd_f32", 64, 1056, False, False, True),
+]
+
+
+@pytest.mark.parametrize("case", MX_DIRECTIONS,
+                         ids=lambda c: f"{c[0]}-{c[1]}x{c[2]}-{'ln' if c[3] else 'rms'}-r{int(c[4])}c{int(c[5])}")
+def test_residual_add_mxfp8_directions(case):
+    """MXFP8 after the residual add, each block direction alone and both: the
+    stored sum, the statistics and the requested blocks against the oracle;
+    the blocks not asked for are not allocated."""
+    name, N, H, ln, rowwise, colwise = case
+    w = _workload(name, N, H)
+    got = _run(w, ln, "mxfp8", rowwise=rowwise, colwise=colwise)
+    out = got[0]
+    assert (out.data is not None) == rowwise and (out.col_data is not None) == colwise
+    _check(w, ln, "mxfp8", got, _oracle(w, ln, "mxfp8"))
+
+
+def test_residual_add_mxfp8_full_size_and_margin():
+    """Both directions after the residual add at 65536 x 2048 (the MXFP8
+    workload's shape, the residual drawn as in the residual-add workload):
+    the result does not depend on sm_margin, and matches the plain forward of
+    the stored sum."""
+    w = _workload("rms_add", 65536, 2048)
+    x, r, g = to_dev(w.x, "bf16"), to_dev(w.residual, "bf16"), to_dev(w.gamma, "f32")
+    a, h, rs = rn.rmsnorm_add_fwd(x, r, g, w.eps, quant="mxfp8")
+    b, h2, rs2 = rn.rmsnorm_add_fwd(x, r, g, w.eps, quant="mxfp8", sm_margin=16)
+    assert torch.equal(h, h2) and torch.equal(rs, rs2)
+    assert torch.equal(a.data, b.data) and torch.equal(a.row_scales, b.row_scales)
+    assert torch.equal(a.col_data, b.col_data) and torch.equal(a.col_scales, b.col_scales)
+    # the rowwise blocks are the row kernel's, the columnwise ones (and the
+    # last rsigma written) the two-direction kernel's, each on the stored sum
+    row, _ = rn.rmsnorm_fwd(h, g, w.eps, quant="mxfp8", colwise=False)
+    col, rs3 = rn.rmsnorm_fwd(h, g, w.eps, quant="mxfp8", rowwise=False)
+    assert torch.equal(a.data, row.data) and torch.equal(a.row_scales, row.row_scales)
+    assert torch.equal(a.col_data, col.col_data) and torch.equal(a.col_scales, col.col_scales)
+    assert torch.equal(rs, rs3)
