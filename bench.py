@@ -82,6 +82,8 @@ def algorithmic_bytes(kind, N, H, esz, ln, extra=None):
         return 3 * E * esz + stats + H * 4 + vec
     if kind == "fwd_add_fp8":                # x, residual in; h and codes out
         return 3 * E * esz + E * 1 + vec + stats
+    if kind == "fwd_add_mxfp8":              # x, residual in; h, row + col codes and scales out
+        return 3 * E * esz + 2 * E + 2 * (E // 32) + vec + stats
     # scaled SwiGLU, E = N x H outputs from N x 2H inputs, row scales fp32
     if kind == "act_fwd_none":               # x in (2E), y out
         return 2 * E * esz + E * esz + 4 * N
@@ -715,6 +717,11 @@ def run_other_workloads(torch, rn, lib, rn_inputs, flush, peak, steps, warmup, o
                        flush)
         report("rms_add_8192x4096_fwd_fp8_delayed", "fwd_add_fp8", w.N, w.H, 2, False,
                statistics.mean(t["add"]), 2)
+        # MXFP8 in both directions after the add: the row kernel (h, rowwise
+        # blocks), then the two-direction kernel reading h back
+        t = time_calls(torch, lib, [("addmx", P.add_args("mxfp8"))], steps, warmup, flush)
+        report("rms_add_8192x4096_fwd_mxfp8", "fwd_add_mxfp8", w.N, w.H, 2, False,
+               statistics.mean(t["addmx"]), 2)
         del P, w
     if want("moe_act"):
         # scaled SwiGLU of a mixture-of-experts MLP: 65536 tokens x 2048

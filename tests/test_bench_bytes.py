@@ -42,3 +42,6 @@ def test_activation_and_residual_bytes():
     E = N * H
     # residual add + FP8: x, residual in, h out, codes out
     assert bench.algorithmic_bytes("fwd_add_fp8", N, H, 2, False) == 6 * E + E + 4 * H + 4 * N
+    # the same add with MXFP8 in both directions: two code bytes and two
+    # E8M0 bytes per 32 elements instead of one code byte
+    assert bench.algorithmic_bytes("fwd_add_mxfp8", N, H, 2, False) == 6 * E + 2 * E + 2 * (E // 32) + 4 * H + 4 * N
