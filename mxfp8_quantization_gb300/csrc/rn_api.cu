@@ -127,9 +127,9 @@ rn_status plan_roles(int nchunks, size_t per_slot, size_t fixed, const DeviceInf
 // Row-wise forward: rows are taken by groups of G warps, the fewest that
 // hold a row with <= 16 chunks of 16 bytes a lane (NC = 4 or 8 chunks for
 // short rows; see plan_fwd for the bf16 LayerNorm exception); every chunk
-// keeps its bounds test (the kernel's FULL variants,
-// without them, need more than the 128 registers a thread of a 512-thread
-// CTA has).  Threads a CTA follow from NC (512 for NC = 16, 768 for 8, 1024
+// keeps its bounds test (variants without them needed more than the 128
+// registers a thread of a 512-thread CTA has).  Threads a CTA follow from
+// NC (512 for NC = 16, 768 for 8, 1024
 // for 4: the registers of the row part); W = every warp but the producer, in whole
 // groups, at most 14 groups of G >= 2; one CTA per SM; a ring of Q slots of
 // 2^rps_log2 adjacent rows each, W / G <= (Q - 1) 2^rps_log2.
@@ -174,6 +174,10 @@ rn_status plan_fwd(int nk, int H, int esz, int N, int sm_margin, const DeviceInf
   int lg = 0;
   while (lg < 3 && (row_bytes << lg) < 8192 && (long long)(N >> (lg + 1)) >= 4 * sms) ++lg;
   const int rps = 1 << lg;
+  // one row a slot compiled as such: every shape but the two shortest-row
+  // ones (1 x 4 and 1 x 8 chunks a lane, which group at large N) has that
+  // instantiation
+  sh.one = lg == 0 && !(sh.g == 1 && sh.nc < 16);
   // fixed: gamma/beta, group exchange (14 groups x 4 x 8 floats), amax words
   // (32), slack; per slot: the rows, their (mu, rsigma), two mbarriers
   // (+ extra_bytes after the barriers: the NVFP4 factor table)

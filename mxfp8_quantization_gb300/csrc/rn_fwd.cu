@@ -65,12 +65,12 @@
 #define RN_FWD_RES_TU 0
 #endif
 
-// the (G, NC, FULL) row shapes compiled in
+// the (G, NC, ONE) row shapes compiled in
 #ifndef RN_FWD_SHAPES
 #define RN_FWD_SHAPES                                                              \
   RN_FWD_SHAPE(1, 4, false) RN_FWD_SHAPE(1, 8, false) RN_FWD_SHAPE(1, 16, false)    \
-  RN_FWD_SHAPE(2, 8, false) RN_FWD_SHAPE(2, 16, false) RN_FWD_SHAPE(4, 16, false)   \
-  RN_FWD_SHAPE(8, 16, false)
+  RN_FWD_SHAPE(1, 16, true) RN_FWD_SHAPE(2, 8, false) RN_FWD_SHAPE(2, 8, true)      \
+  RN_FWD_SHAPE(2, 16, true) RN_FWD_SHAPE(4, 16, true) RN_FWD_SHAPE(8, 16, true)
 #endif
 
 namespace rn {
@@ -170,12 +170,17 @@ __device__ __forceinline__ uint32_t pack_e2m1(const float2* q) {
 // The row groups of this CTA: b, b + g, b + 2g, ... (b = blockIdx.x,
 // g = gridDim.x), from the last one when reverse; group k holds rows
 // k rps .. k rps + rps - 1 (the last group of all may be short).
+template <bool ONE>
 struct RowSeq {
   int first, step, count;
   __device__ __forceinline__ explicit RowSeq(const FwdParams& p) {
     const int b = blockIdx.x, g = gridDim.x;
-    const int ng = (p.N + (1 << p.rps_log2) - 1) >> p.rps_log2;
-    count = b < ng ? (ng - b + g - 1) / g : 0;
+    if constexpr (ONE) {
+      count = b < p.N ? (p.N - b + g - 1) / g : 0;
+    } else {
+      const int ng = (p.N + (1 << p.rps_log2) - 1) >> p.rps_log2;
+      count = b < ng ? (ng - b + g - 1) / g : 0;
+    }
     first = p.reverse ? b + (count - 1) * g : b;
     step = p.reverse ? -g : g;
   }
@@ -202,9 +207,12 @@ __device__ __forceinline__ float group_sum(float v, float* red, int group, int w
   }
 }
 
-// FULL: every lane holds exactly NC chunks of every row (H = NC * 32 * G
-// chunks), so no chunk needs a bounds test
-template <typename TIn, int NK, int QM, int G, int NC, bool FULL, bool RES>
+// ONE: one row a slot, fixed at compile time.  Rows of 8 KB or more never
+// share a slot, and shorter ones only at large N; the general form (slot
+// size, row group and position arithmetic at run time) cost the 8192 x 4096
+// FP8 forwards ~1.7 us in generated code, so the shapes that meet one row a
+// slot are also compiled this way.
+template <typename TIn, int NK, int QM, int G, int NC, bool ONE, bool RES>
 __global__ void __launch_bounds__(max_threads<NC>(), 1) rn_fwd_kernel(const FwdParams p) {
   constexpr int VEC = 16 / (int)sizeof(TIn);
   using V = Vec<TIn, VEC>;
@@ -227,9 +235,9 @@ __global__ void __launch_bounds__(max_threads<NC>(), 1) rn_fwd_kernel(const FwdP
   const int H = p.H;
   const int nchunks = H / VEC;
   const uint32_t row_bytes = (uint32_t)H * sizeof(TIn);
-  const int lg = p.rps_log2;
+  const int lg = ONE ? 0 : p.rps_log2;
   const int rps = 1 << lg;                             // rows a slot holds
-  const uint32_t grp_bytes = (uint32_t)rps * row_bytes;
+  const uint32_t grp_bytes = ONE ? row_bytes : (uint32_t)rps * row_bytes;
   const uint32_t slot_bytes = RES ? 2 * grp_bytes : grp_bytes;  // x rows (then the residual rows)
   const uint32_t Q = (uint32_t)p.Q;
   const size_t gb_bytes = GB_SMEM ? (size_t)H * sizeof(float) * (LN ? 2 : 1) : 0;
@@ -238,7 +246,7 @@ __global__ void __launch_bounds__(max_threads<NC>(), 1) rn_fwd_kernel(const FwdP
   float4* bsm = gsm + (size_t)F4 * nchunks;       // same for beta (LayerNorm)
   unsigned char* ring = smem + gb_bytes;
   float2* rstat = reinterpret_cast<float2*>(ring + (size_t)Q * slot_bytes);  // [Q][rps] (mu, rsigma)
-  float* red = reinterpret_cast<float*>(rstat + (size_t)Q * rps);     // [kMaxGroups][4][8]
+  float* red = reinterpret_cast<float*>(ONE ? rstat + Q : rstat + (size_t)Q * rps);  // [kMaxGroups][4][8]
   uint32_t* red2 = reinterpret_cast<uint32_t*>(red + kMaxGroups * 4 * 8);  // [32]
   uint64_t* full = reinterpret_cast<uint64_t*>(red2 + 32);                  // row landed
   uint64_t* empty = full + Q;                                               // row read out
@@ -250,12 +258,12 @@ __global__ void __launch_bounds__(max_threads<NC>(), 1) rn_fwd_kernel(const FwdP
 
   for (uint32_t i = threadIdx.x; i < Q; i += blockDim.x) {
     mbar_init(smem_u32(&full[i]), META ? 2 : 1);
-    mbar_init(smem_u32(&empty[i]), G * rps);
+    mbar_init(smem_u32(&empty[i]), ONE ? G : G * rps);
     fence_barrier_init();
   }
   __syncthreads();
 
-  const RowSeq seq(p);
+  const RowSeq<ONE> seq(p);
 
   if (warp == W) {
     // ------------------------------------------------------------ producer
@@ -265,9 +273,17 @@ __global__ void __launch_bounds__(max_threads<NC>(), 1) rn_fwd_kernel(const FwdP
       const unsigned char* xb = static_cast<const unsigned char*>(p.x);
       RingPos pos{0u, 0u};
       for (int i = 0; i < seq.count; ++i) {
-        const int r0 = seq.group(i) << lg;
-        const int nr = min(rps, p.N - r0);  // rows of this group
-        const uint32_t bytes = (uint32_t)nr * row_bytes;
+        int r0, nr;
+        uint32_t bytes;
+        if constexpr (ONE) {
+          r0 = seq.group(i);
+          nr = 1;
+          bytes = row_bytes;
+        } else {
+          r0 = seq.group(i) << lg;
+          nr = min(rps, p.N - r0);  // rows of this group
+          bytes = (uint32_t)nr * row_bytes;
+        }
         const uint32_t s = pos.slot;
         // a start-up burst of whole rings from every SM lands all at once,
         // late; instead the first kStartRows slots go out alone and the rest
@@ -276,9 +292,14 @@ __global__ void __launch_bounds__(max_threads<NC>(), 1) rn_fwd_kernel(const FwdP
         if (i >= (int)Q) mbar_wait(smem_u32(&empty[s]), pos.phase ^ 1u, &g_err_fwd, kErrEmptyWait);
         const uint32_t bar = smem_u32(&full[s]);
         if constexpr (META) {
-          for (int j = 0; j < nr; ++j) {
-            if (LN) cp_async4(smem_u32(&rstat[s * rps + j].x), p.mu + r0 + j);
-            cp_async4(smem_u32(&rstat[s * rps + j].y), p.rsigma + r0 + j);
+          if constexpr (ONE) {
+            if (LN) cp_async4(smem_u32(&rstat[s].x), p.mu + r0);
+            cp_async4(smem_u32(&rstat[s].y), p.rsigma + r0);
+          } else {
+            for (int j = 0; j < nr; ++j) {
+              if (LN) cp_async4(smem_u32(&rstat[s * rps + j].x), p.mu + r0 + j);
+              cp_async4(smem_u32(&rstat[s * rps + j].y), p.rsigma + r0 + j);
+            }
           }
           cp_async_arrive(bar);
         }
@@ -321,7 +342,7 @@ __global__ void __launch_bounds__(max_threads<NC>(), 1) rn_fwd_kernel(const FwdP
   const int cbase = wg * 32 + lane;
   constexpr int CSTEP = 32 * G;
   const int nv = cbase < nchunks ? (nchunks - cbase + CSTEP - 1) / CSTEP : 0;
-  const int nvalid = FULL ? NC : (nv < NC ? nv : NC);
+  const int nvalid = nv < NC ? nv : NC;
   // the apply loop keeps a (then always true) test per chunk even for full
   // rows: with the chunks in one straight block the scheduler overlaps the
   // gamma / beta reads of many chunks and runs out of registers
@@ -363,18 +384,27 @@ __global__ void __launch_bounds__(max_threads<NC>(), 1) rn_fwd_kernel(const FwdP
   // position i of the CTA's rows: row i & (rps - 1) of its group i >> lg,
   // whose slot and phase `pos` tracks (groups advance by less than Q per
   // step: NGR <= (Q - 1) rps)
-  RingPos pos{0u, 0u};
-  int kg = group >> lg;
-  pos.advance((uint32_t)kg, Q);
+  // (one row a slot: position i is slot use i, and pos advances by NGR
+  // after each use)
+  RingPos pos{ONE ? (uint32_t)group : 0u, 0u};
+  int kgp = group >> lg;  // the previous position's row group
+  if constexpr (!ONE) pos.advance((uint32_t)kgp, Q);
   int par = 0;
-  for (int i = group; i < (seq.count << lg); i += NGR) {
-    pos.advance((uint32_t)((i >> lg) - kg), Q);
-    kg = i >> lg;
-    const int jr = i & (rps - 1);
-    const int r = (seq.group(kg) << lg) + jr;
-    // the short last group of all: its missing rows are skipped by every
-    // warp of the group (that slot is never used again)
-    if (r >= p.N) continue;
+  for (int i = group; i < (ONE ? seq.count : seq.count << lg); i += NGR) {
+    int kg, jr, r;
+    if constexpr (ONE) {
+      kg = i;
+      jr = 0;
+      r = seq.group(i);
+    } else {
+      pos.advance((uint32_t)((i >> lg) - kgp), Q);
+      kg = kgp = i >> lg;
+      jr = i & (rps - 1);
+      r = (seq.group(kg) << lg) + jr;
+      // the short last group of all: its missing rows are skipped by every
+      // warp of the group (that slot is never used again)
+      if (r >= p.N) continue;
+    }
     const uint32_t s = pos.slot;
     // before waiting for this use of the slot, wait for the previous use to
     // be released: that use has then landed, so the parity wait below cannot
@@ -398,6 +428,7 @@ __global__ void __launch_bounds__(max_threads<NC>(), 1) rn_fwd_kernel(const FwdP
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(smem_u32(&empty[s]));
+    if constexpr (ONE) pos.advance((uint32_t)NGR, Q);
     if constexpr (RES) {
       // the new residual stream: h in the input dtype
       unsigned char* hrow = static_cast<unsigned char*>(p.residual_out) + (size_t)r * row_bytes;
@@ -571,9 +602,10 @@ __global__ void rn_fwd_init_kernel(float* amax, const float* scale, float* scale
 }
 #endif
 
-template <typename TIn, int NK, int QM, int G, int NC, bool FULL>
+template <typename TIn, int NK, int QM, int G, int NC, bool ONE>
 rn_status launch_t(const FwdParams& p, const Launch& l, bool pdl, cudaStream_t s) {
-  auto k = rn_fwd_kernel<TIn, NK, QM, G, NC, FULL, RN_FWD_RES_TU != 0>;
+  auto k = rn_fwd_kernel<TIn, NK, QM, G, NC, ONE, RN_FWD_RES_TU != 0>;
+  if (ONE && p.rps_log2 != 0) return RN_ERR_UNSUPPORTED;
   // the shared-memory exchange buffers and named barriers exist for at most
   // kMaxGroups groups of G >= 2 warps and 31 worker warps
   const int workers = l.threads / 32 - 1;
@@ -599,12 +631,12 @@ rn_status launch_t(const FwdParams& p, const Launch& l, bool pdl, cudaStream_t s
   return cudaGetLastError() == cudaSuccess ? RN_OK : RN_ERR_CUDA;
 }
 
-// row shapes (G, NC, FULL); the planner picks one of these
+// row shapes (G, NC, ONE); the planner picks one of these
 template <typename TIn, int NK, int QM>
 rn_status launch_shape(const FwdShape& sh, const FwdParams& p, const Launch& l, bool pdl,
                        cudaStream_t s) {
-#define RN_FWD_SHAPE(G_, NC_, FULL_) \
-  if (sh.g == G_ && sh.nc == NC_ && sh.full == FULL_) return launch_t<TIn, NK, QM, G_, NC_, FULL_>(p, l, pdl, s);
+#define RN_FWD_SHAPE(G_, NC_, ONE_) \
+  if (sh.g == G_ && sh.nc == NC_ && sh.one == ONE_) return launch_t<TIn, NK, QM, G_, NC_, ONE_>(p, l, pdl, s);
   RN_FWD_SHAPES
 #undef RN_FWD_SHAPE
   return RN_ERR_UNSUPPORTED;

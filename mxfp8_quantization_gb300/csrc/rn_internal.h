@@ -151,11 +151,12 @@ rn_status persistent_grid(Kernel k, const Launch& l, int* grid) {
 }
 
 // launch functions (one per translation unit family)
-// row shape of the forward: G warps per row, NC 16-byte chunks per lane,
-// full = every lane holds exactly NC chunks (H * esz == 16 * 32 * G * NC)
+// row shape of the forward: G warps per row, NC 16-byte chunks per lane;
+// one: one row a slot, compiled as such (the planner sets it when it
+// groups no rows and the shape has that instantiation)
 struct FwdShape {
   int g, nc;
-  bool full;
+  bool one;
 };
 // pdl: launch as a programmatic dependent of the previous kernel
 rn_status launch_fwd(int nk, bool bf16, const FwdShape& sh, int qmode, const FwdParams& p,
