@@ -53,11 +53,12 @@
  *     RN_ERR_UNSUPPORTED (shape/alignment) or RN_ERR_INVALID (missing
  *     pointer, bad enum, negative size) before anything is launched.
  *   - Row widths (with 227 KB of shared memory per block, as on GB300):
- *     every mode but two-direction MXFP8 takes H up to 32768 bf16 / 16384
- *     fp32 columns.  MXFP8 with the columnwise copy: bf16 rows with
- *     H % 64 == 0 and every fp32 row take a kernel that holds no whole
- *     32-row tile, up to H = 41216 bf16 / 20608 fp32 (its per-tile
- *     statistics partials must fit beside 4 copy slots); bf16 rows with
+ *     every forward mode but two-direction MXFP8 takes H up to 32768 bf16 /
+ *     16384 fp32 columns; the backward H up to 16384 bf16 / 8192 fp32.
+ *     MXFP8 with the columnwise copy: bf16 rows with H % 64 == 0 and every
+ *     fp32 row take a kernel that holds no whole 32-row tile, up to
+ *     H = 41216 bf16 / 20608 fp32 (its per-tile statistics partials must
+ *     fit beside 4 copy slots); bf16 rows with
  *     H % 64 == 32 take a kernel that holds a 32-row tile plus look-ahead,
  *     up to H = 3104 (LayerNorm) / 3296 (RMSNorm).  Wider rows return
  *     RN_ERR_UNSUPPORTED.

@@ -81,7 +81,9 @@ size_t cta_smem_budget(const DeviceInfo& di, int per_sm) {
 // the compact shape; fewer than the ring's slots, which their pacing on slot
 // releases relies on), one producer.  Compact shape: NG = 1 (A <= 8) or 4
 // (A <= 4), two CTAs per SM when each still holds a ring of >= 6 slots.
-// Otherwise the wide shape: one CTA per SM, NG in {2, 4, 8}, A <= 16.
+// Otherwise the wide shape: one CTA per SM, NG 2 or 4 (4 when 2 would take
+// the CTA past 512 threads: the 512-thread build has 128 registers a
+// thread, the larger one 96), A <= 16, at most kBwdWideThreads threads.
 struct Roles {
   int ng, A, S, per_sm, Q;
 };
@@ -108,17 +110,32 @@ rn_status plan_roles(int nchunks, size_t per_slot, size_t fixed, const DeviceInf
       return RN_OK;
     }
   }
-  int ng = pick_ng(nchunks, 512, 8);
-  if (ng == 0) return RN_ERR_UNSUPPORTED;
-  if (ng < 2) ng = 2;
   const size_t budget = cta_smem_budget(di, 1);
   int Q = budget > fixed ? (int)((budget - fixed) / per_slot) : 0;
   if (Q > q_cap) Q = q_cap;
   if (Q < 2) return RN_ERR_UNSUPPORTED;
+  auto roles = [&](int ng, int* A, int* S) {
+    *A = round_up((nchunks + ng - 1) / ng, 32) / 32;
+    *S = *A / 2 > 2 ? *A / 2 : 2;
+    if (*S > Q - 1) *S = Q - 1;  // stats warps must be fewer than slots
+    const int cap = kBwdWideThreads / 32 - *A - 1;
+    if (*S > cap) *S = cap;
+  };
+  int ng = 0, A = 0, S = 0;
+  for (int g = 2; g <= 4 && ng == 0; g *= 2) {
+    if ((nchunks + g - 1) / g > 512) continue;
+    roles(g, &A, &S);
+    if (32 * (A + S + 1) <= kBwdWideThreads512) ng = g;
+  }
+  if (ng == 0) {
+    ng = (nchunks + 1) / 2 <= 512 ? 2 : 4;
+    if ((nchunks + ng - 1) / ng > 512) return RN_ERR_UNSUPPORTED;
+    roles(ng, &A, &S);
+  }
+  if (S < 1) return RN_ERR_UNSUPPORTED;
   r->ng = ng;
-  r->A = round_up((nchunks + ng - 1) / ng, 32) / 32;
-  r->S = r->A / 2 > 2 ? r->A / 2 : 2;
-  if (r->S > Q - 1) r->S = Q - 1;  // stats warps must be fewer than slots
+  r->A = A;
+  r->S = S;
   r->per_sm = 1;
   r->Q = Q;
   return RN_OK;

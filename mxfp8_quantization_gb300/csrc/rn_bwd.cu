@@ -14,8 +14,9 @@
 // saved mu / rsigma with 4-byte cp.async, all on the slot's "full" barrier;
 //   stats warps  take rows in turn and form the two row means mean(dy) and
 //                mean(dy * xhat) (g from a shared-memory copy laid out for
-//                conflict-free reads), published on the slot's "ready"
-//                barrier;
+//                conflict-free reads, which the stats and apply warps fill
+//                while the producer streams the first rows), published on
+//                the slot's "ready" barrier;
 //   apply warps  own fixed 16-byte column chunks: dx for every row in order,
 //                plus running per-column sums of dz * xhat and dz in
 //                registers; they release the slot ("empty").
@@ -38,16 +39,29 @@ __device__ unsigned g_err_bwd;
 
 // compact shape: at most 8 apply + 3 stats warps + the producer, two CTAs
 // per SM (24 warps an SM leave 80 registers a thread: a fourth stats warp
-// cut that to 72 and made the apply warps spill); wide shape: up to 16
-// apply + 8 stats warps + the producer, one CTA
+// cut that to 72 and made the apply warps spill); wide shape: one CTA per
+// SM, compiled twice: for at most 512 threads (128 registers a thread) and
+// for at most 576 (96).  (Compiled for 800 threads, i.e. 72 registers, the
+// bf16 LayerNorm kernel spilled: 3000 x 5120 took 33.2 us against 28.9 us
+// with the 512-thread build.)
 constexpr int kMaxThreads = 384;
-constexpr int kMaxThreadsWide = 800;
+constexpr int kMaxThreadsWide = kBwdWideThreads;
+constexpr int kMaxThreadsWide512 = kBwdWideThreads512;
 // compact shape with 4 chunks a thread: 4 apply + 3 stats warps + the
 // producer (256 threads, 128 registers: the 4 chunks' gamma and dgamma /
 // dbeta sums stay in registers)
 constexpr int kMaxThreadsNg4 = 256;
 // rows the producer issues before waiting for the first one to land
 constexpr uint32_t kStartRows = 2;
+
+// launch shapes of the stats-warp kernel
+enum BwdShapeKind : int { kCompact = 0, kWide512 = 1, kWide = 2 };
+
+template <int SK, int NG>
+constexpr int bwd_max_threads() {
+  return SK == kWide ? kMaxThreadsWide
+                     : (SK == kWide512 ? kMaxThreadsWide512 : (NG >= 4 ? kMaxThreadsNg4 : kMaxThreads));
+}
 
 __device__ __forceinline__ void named_sync(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
@@ -68,9 +82,8 @@ __device__ __forceinline__ void store_dx<float>(void* base, size_t elem, const f
   *reinterpret_cast<float4*>(static_cast<float*>(base) + elem) = make_float4(d[0].x, d[0].y, d[1].x, d[1].y);
 }
 
-template <typename TIn, int NG, bool LN, bool WIDE>
-__global__ void __launch_bounds__(WIDE ? kMaxThreadsWide : (NG >= 4 ? kMaxThreadsNg4 : kMaxThreads),
-                                  WIDE ? 1 : 2)
+template <typename TIn, int NG, bool LN, int SK>
+__global__ void __launch_bounds__(bwd_max_threads<SK, NG>(), SK == kCompact ? 2 : 1)
     rn_bwd_kernel(const BwdParams p) {
   constexpr int VEC = 16 / (int)sizeof(TIn);
   using V = Vec<TIn, VEC>;
@@ -105,15 +118,38 @@ __global__ void __launch_bounds__(WIDE ? kMaxThreadsWide : (NG >= 4 ? kMaxThread
     mbar_init(smem_u32(&empty[i]), A);
     fence_barrier_init();
   }
-  for (int j = threadIdx.x; j < H / 4; j += blockDim.x) {
-    float4 g4 = make_float4(p.gamma[4 * j], p.gamma[4 * j + 1], p.gamma[4 * j + 2], p.gamma[4 * j + 3]);
-    if (p.zcg) g4 = make_float4(1.0f + g4.x, 1.0f + g4.y, 1.0f + g4.z, 1.0f + g4.w);
-    const int c = j / (VEC / 4), part_j = j % (VEC / 4);
-    gsv[part_j * nchunks + c] = g4;
-  }
   __syncthreads();
-
   const int warp = threadIdx.x >> 5;
+  // g is staged by the stats and apply warps while the producer already
+  // streams the first rows; a thread issues the loads of up to 4 items
+  // before its first store (one trip to memory, not one per item).  Staged
+  // behind a CTA barrier ahead of the producer, g held the first row back by
+  // ~2 us.
+  if (warp < A + S) {
+    const int NT = (A + S) * 32, items = H / 4;
+    const bool al = (reinterpret_cast<uintptr_t>(p.gamma) & 15) == 0;
+    for (int j0 = threadIdx.x; j0 < items; j0 += 4 * NT) {
+      float4 g4[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int j = j0 + k * NT;
+        if (j < items)
+          g4[k] = al ? __ldg(reinterpret_cast<const float4*>(p.gamma) + j)
+                     : make_float4(p.gamma[4 * j], p.gamma[4 * j + 1], p.gamma[4 * j + 2],
+                                   p.gamma[4 * j + 3]);
+      }
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int j = j0 + k * NT;
+        if (j < items) {
+          float4 g = g4[k];
+          if (p.zcg) g = make_float4(1.0f + g.x, 1.0f + g.y, 1.0f + g.z, 1.0f + g.w);
+          gsv[(j % (VEC / 4)) * nchunks + j / (VEC / 4)] = g;
+        }
+      }
+    }
+    named_sync(1, NT);
+  }
   const int lane = threadIdx.x & 31;
   const int G = gridDim.x;
   const int R = p.chunk_rows;
@@ -579,9 +615,9 @@ __global__ void __launch_bounds__(1024) rn_colreduce_kernel(const ColReduceParam
   }
 }
 
-template <typename TIn, int NG, bool LN, bool WIDE>
+template <typename TIn, int NG, bool LN, int SK>
 rn_status launch_t(const BwdParams& p, const Launch& l, cudaStream_t s) {
-  auto k = rn_bwd_kernel<TIn, NG, LN, WIDE>;
+  auto k = rn_bwd_kernel<TIn, NG, LN, SK>;
   if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)l.smem) !=
       cudaSuccess)
     return RN_ERR_CUDA;
@@ -591,27 +627,34 @@ rn_status launch_t(const BwdParams& p, const Launch& l, cudaStream_t s) {
   return cudaGetLastError() == cudaSuccess ? RN_OK : RN_ERR_CUDA;
 }
 
-// compact shape for NG 1, 2 and 4; wide shape for NG 2, 4 and 8
+template <typename TIn, bool LN, int SK>
+rn_status launch_wide(int ng, const BwdParams& p, const Launch& l, cudaStream_t s) {
+  switch (ng) {
+    case 2: return launch_t<TIn, 2, LN, SK>(p, l, s);
+    case 4: return launch_t<TIn, 4, LN, SK>(p, l, s);
+    default: return RN_ERR_UNSUPPORTED;
+  }
+}
+
+// compact shape for NG 1, 2 and 4; wide shape: NG 2 and 4 in the 512-thread
+// build, NG 4 in the larger one (the planner takes NG 2 only within 512)
 template <typename TIn, bool LN>
 rn_status launch_ng(int ng, const BwdParams& p, const Launch& l, cudaStream_t s) {
   const bool wide = l.threads > kMaxThreads || l.per_sm == 1;
   if (!wide) {
     switch (ng) {
-      case 1: return launch_t<TIn, 1, LN, false>(p, l, s);
-      case 2: return launch_t<TIn, 2, LN, false>(p, l, s);
+      case 1: return launch_t<TIn, 1, LN, kCompact>(p, l, s);
+      case 2: return launch_t<TIn, 2, LN, kCompact>(p, l, s);
       case 4:
         if (l.threads > kMaxThreadsNg4) return RN_ERR_UNSUPPORTED;
-        return launch_t<TIn, 4, LN, false>(p, l, s);
+        return launch_t<TIn, 4, LN, kCompact>(p, l, s);
       default: return RN_ERR_UNSUPPORTED;
     }
   }
   if (l.threads > kMaxThreadsWide) return RN_ERR_UNSUPPORTED;
-  switch (ng) {
-    case 2: return launch_t<TIn, 2, LN, true>(p, l, s);
-    case 4: return launch_t<TIn, 4, LN, true>(p, l, s);
-    case 8: return launch_t<TIn, 8, LN, true>(p, l, s);
-    default: return RN_ERR_UNSUPPORTED;
-  }
+  if (l.threads <= kMaxThreadsWide512) return launch_wide<TIn, LN, kWide512>(ng, p, l, s);
+  if (ng != 4) return RN_ERR_UNSUPPORTED;
+  return launch_t<TIn, 4, LN, kWide>(p, l, s);
 }
 
 }  // namespace
@@ -643,10 +686,12 @@ rn_status launch_bwd_fused(bool ln, bool big, const BwdParams& p, const Launch& 
              : launch_fused_t<float, 4, false, false>(p, l, s);
 }
 
+// bf16 rows only: every fp32 row the library accepts (H <= 8192) takes the
+// fused kernel
 rn_status launch_bwd(bool ln, bool bf16, int ng, const BwdParams& p, const Launch& l,
                      cudaStream_t s) {
-  if (bf16) return ln ? launch_ng<uint16_t, true>(ng, p, l, s) : launch_ng<uint16_t, false>(ng, p, l, s);
-  return ln ? launch_ng<float, true>(ng, p, l, s) : launch_ng<float, false>(ng, p, l, s);
+  if (!bf16) return RN_ERR_UNSUPPORTED;
+  return ln ? launch_ng<uint16_t, true>(ng, p, l, s) : launch_ng<uint16_t, false>(ng, p, l, s);
 }
 
 // launched as a programmatic dependent of the backward kernel: its CTAs are

@@ -175,7 +175,13 @@ rn_status launch_mx(int nk, bool bf16, int ng, const MxParams& p, const Launch& 
 constexpr int kMxBoxThreads = 32 * 16;
 constexpr size_t kMxBoxBytes = 16384;
 rn_status launch_mx_box(int nk, bool bf16, const MxParams& p, const Launch& l, cudaStream_t s);
-// backward with stats warps (rows of any length)
+// backward with stats warps: bf16 rows (fp32 rows take the fused kernel);
+// the wide shape (one CTA per SM) is compiled for at most 512 threads (128
+// registers a thread) and for at most kBwdWideThreads (96 registers), the
+// most its planner asks for (16 apply warps, 1 stats warp and the producer
+// at H = 16384)
+constexpr int kBwdWideThreads512 = 512;
+constexpr int kBwdWideThreads = 576;
 rn_status launch_bwd(bool ln, bool bf16, int ng, const BwdParams& p, const Launch& l,
                      cudaStream_t s);
 // backward without stats or producer warps, fp32 rows of up to 16 warps x

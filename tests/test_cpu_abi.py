@@ -126,6 +126,18 @@ def test_backward_workspace_query_needs_no_device(lib):
     assert lib.rn_rmsnorm_bwd(None, None, 0, None, None, 64, 64, 0, 0, None, None, None, None, None) == 1
 
 
+def test_backward_width_limits_on_host(lib):
+    """The backward's widest rows (the header's conventions): bf16 H = 16384,
+    fp32 H = 8192; the next width is refused at the workspace query."""
+    n = ctypes.c_size_t(0)
+    for dt, ok, bad in ((0, 16384, 16392), (1, 8192, 8196)):
+        assert lib.rn_layernorm_bwd(None, None, dt, None, None, None, 64, ok, 0, 0, None, None,
+                                    None, None, ctypes.byref(n), None) == 0
+        assert n.value == 8 * 2 * ok * 4
+        assert lib.rn_rmsnorm_bwd(None, None, dt, None, None, 64, bad, 0, 0, None, None, None,
+                                  ctypes.byref(n), None) == 2
+
+
 def test_backward_rejects_small_workspace_on_host(lib):
     p = ctypes.c_void_p(0x10000)
     n = ctypes.c_size_t(16)

@@ -318,6 +318,14 @@ BWD_CASES = [
     ("bwd_bf16", 45, None, False),
     ("bwd_bf16", 1, 5120, True),
     ("bwd_f32", 3, 8, True),
+    # the wide stats-warp kernel in both of its builds: 512 threads (2 and 4
+    # chunks a thread) and 576 threads (4 chunks a thread; 14336 and 16384,
+    # the widest bf16 row)
+    ("bwd_bf16", 24, 8192, True),
+    ("bwd_bf16", 16, 10240, False),
+    ("bwd_bf16", 8, 14336, True),
+    ("bwd_bf16", 8, 16384, False),
+    ("bwd_f32", 5, 8192, True),
 ]
 
 
