@@ -1,10 +1,12 @@
 """GPU parity of the scaled activations (rn_scaled_act_fwd / _bwd) against
 the oracle (oracle/act.py), through the C ABI.
 
-Tolerances (the arithmetic is a few fp32 products, one fp32 exp and one
-2-ulp division per element, so the kernel's y32 lies within
-a few fp32 ulps of the oracle's y; w is the magnitude of the product of
-terms that forms a value, which also covers the bc + 1 of the clamped form):
+Tolerances (the arithmetic is a few fp32 products, one hardware exponential
+-- relative error at most 2 + 1.17 |z| ulp, under 2**-18 for the |z| <= 25
+these inputs stay within (x ~ N(0, 2), alpha * x for the clamped form) -- and
+one 2-ulp division per element, so the kernel's y32 lies within a few tens
+of fp32 ulps of the oracle's y; w is the magnitude of the product of terms
+that forms a value, which also covers the bc + 1 of the clamped form):
 * bf16 outputs within one bf16 ulp of the oracle's rounded value plus
   2**-18 * w; fp32 outputs within 2**-18 * w;
 * FP8 and MXFP8 codes as for the normalization (one-step misses only
