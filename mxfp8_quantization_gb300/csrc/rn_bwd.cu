@@ -25,7 +25,7 @@
 // chunk size depends on N only, and each partial is summed in row order, so
 // the partials do not depend on the grid.
 // Kernel 2 adds the partials of each column in a fixed order that depends
-// on the chunk count only.  Arithmetic is on element pairs (f32x2), with
+// on the chunk count and H only.  Arithmetic is on element pairs (f32x2), with
 // bf16 inputs entering through the mixed-precision forms.
 #include <cuda_runtime.h>
 
@@ -615,6 +615,60 @@ __global__ void __launch_bounds__(1024) rn_colreduce_kernel(const ColReduceParam
   }
 }
 
+// The same sums with 32-column blocks of 16 warps (lane = one column; warp
+// w sums chunks w, w+16, ... into the eight accumulators, the tree, then the
+// 16 warp sums in warp order), taken when the 64-column blocks would number
+// more than kRedOneWave (slices x accumulators; one block an SM of a GB300
+// holds): the smaller blocks then spread over every SM in one wave (3000 x
+// 5120 LayerNorm 27.0 against 28.8 us, 2000 x 12288 RMSNorm 41.2 against
+// 43.0 us), while up to that count the 64-column ones are 1-4 us faster
+// (8192 x 4096).  A column's order depends on the warp count and the chunk
+// count, so on H and N only.
+constexpr int kRedOneWave = 152;
+
+__device__ __forceinline__ float ld_hint_f1(const float* p, uint64_t pol) {
+  float v;
+  asm volatile("ld.global.L2::cache_hint.f32 %0, [%1], %2;" : "=f"(v) : "l"(p), "l"(pol));
+  return v;
+}
+
+__global__ void __launch_bounds__(16 * 32) rn_colreduce_narrow_kernel(const ColReduceParams p) {
+  constexpr int NW = 16;
+  __shared__ float red[NW][33];
+  pdl_wait();  // the partials come from the backward kernel
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int a = blockIdx.y;
+  const int col = blockIdx.x * 32 + lane;
+  float acc[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+  if (col < p.H) {
+    const float* base = p.part + (size_t)a * p.H + col;
+    const size_t stride = (size_t)p.nacc * p.H;
+    const uint64_t pol = l2_evict_first();  // the partials are read once
+    int c = warp;
+    for (; c + 7 * NW < p.n_chunks; c += 8 * NW) {
+      float v[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) v[i] = ld_hint_f1(base + (size_t)(c + NW * i) * stride, pol);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[i] += v[i];
+    }
+    // the rest: fewer than 8 chunks a warp
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      if (c + NW * i < p.n_chunks) acc[i] += ld_hint_f1(base + (size_t)(c + NW * i) * stride, pol);
+  }
+  red[warp][lane] = ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    const int j = blockIdx.x * 32 + threadIdx.x;
+    float r = 0.f;
+    for (int w = 0; w < NW; ++w) r += red[w][threadIdx.x];
+    if (j < p.H) (a == 0 ? p.dgamma : p.dbeta)[j] = r;
+  }
+}
+
 template <typename TIn, int NG, bool LN, int SK>
 rn_status launch_t(const BwdParams& p, const Launch& l, cudaStream_t s) {
   auto k = rn_bwd_kernel<TIn, NG, LN, SK>;
@@ -698,9 +752,11 @@ rn_status launch_bwd(bool ln, bool bf16, int ng, const BwdParams& p, const Launc
 // placed as the backward's CTAs retire and wait (griddepcontrol.wait) for
 // the partials
 rn_status launch_colreduce(const ColReduceParams& p, cudaStream_t s) {
+  const bool narrow = p.nacc * ((p.H + 63) / 64) > kRedOneWave;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)((p.H + 63) / 64), (unsigned)p.nacc);
-  cfg.blockDim = dim3(1024);
+  cfg.gridDim = narrow ? dim3((unsigned)((p.H + 31) / 32), (unsigned)p.nacc)
+                       : dim3((unsigned)((p.H + 63) / 64), (unsigned)p.nacc);
+  cfg.blockDim = dim3(narrow ? 16 * 32 : 32 * 32);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
@@ -708,7 +764,9 @@ rn_status launch_colreduce(const ColReduceParams& p, cudaStream_t s) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, rn_colreduce_kernel, p) != cudaSuccess) return RN_ERR_CUDA;
+  const cudaError_t e = narrow ? cudaLaunchKernelEx(&cfg, rn_colreduce_narrow_kernel, p)
+                               : cudaLaunchKernelEx(&cfg, rn_colreduce_kernel, p);
+  if (e != cudaSuccess) return RN_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? RN_OK : RN_ERR_CUDA;
 }
 
