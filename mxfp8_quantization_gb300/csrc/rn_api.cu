@@ -88,9 +88,17 @@ struct Roles {
   int ng, A, S, per_sm, Q;
 };
 
-rn_status plan_roles(int nchunks, size_t per_slot, size_t fixed, const DeviceInfo& di, int q_cap,
-                     Roles* r) {
-  if (nchunks <= 512) {
+rn_status plan_roles(int nchunks, bool ln, size_t per_slot, size_t fixed, const DeviceInfo& di,
+                     int q_cap, Roles* r) {
+  // LayerNorm rows of more than 480 chunks (bf16 H > 3840) take the wide
+  // shape, one CTA per SM with 8 apply and 4 stats warps at H = 4096: no SM
+  // is left with one CTA running its last chunk alone (8192 x 4096: 39.2
+  // against 41.2 us; 16384 x 4096: 70.7 against 73.7 us; 4096 x 4096: 26.8
+  // against 27.4 us; sm_margin 16: 41.7 against 45.2 us).  Narrower
+  // LayerNorm rows measured no better or worse that way (H = 2560: 53.4
+  // against 49.4 us, 3072 even, 3584: 40.5 against 39.1 us at 12288 /
+  // 8192 rows), and RMSNorm rows worse (8192 x 4096: 37.1 against 35.3 us).
+  if (nchunks <= 512 && !(ln && nchunks > 480)) {
     // rows of 257 .. 512 chunks: 4 chunks a thread and 4 apply warps (the
     // per-row waits and addressing spread over twice the elements: 42.7 ->
     // 41.2 us at 8192 x 4096 LayerNorm bf16 against 2 chunks and 8 warps)
@@ -689,7 +697,7 @@ rn_status bwd_common(bool ln, const void* dz, const void* x, rn_dtype dt, const 
     const size_t fixed = (size_t)H * sizeof(float) + 64;
     const size_t per_slot = 2 * row_bytes + sizeof(float2) + sizeof(float4) + 24;
     Roles ro;
-    if ((st = plan_roles(nch, per_slot, fixed, di, 64, &ro)) != RN_OK) return st;
+    if ((st = plan_roles(nch, ln, per_slot, fixed, di, 64, &ro)) != RN_OK) return st;
     p.apply_warps = ro.A;
     p.stats_warps = ro.S;
     p.Q = ro.Q;
