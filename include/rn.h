@@ -195,8 +195,8 @@ rn_status rn_rmsnorm_add_fwd(const void* x, const void* residual, rn_dtype dtype
  *   gamma: fp32 [H] (stored value; zero_centered_gamma as in the forward);
  *   dgamma, dbeta: fp32 [H], overwritten.
  * dgamma/dbeta are reduced in two deterministic stages: fixed row chunks
- * (their size depends on N only) write fp32 partial sums, each in row
- * order, into the workspace, then a second kernel adds the chunks of every
+ * (their size depends on N, H and the device's SM count, never on
+ * sm_margin) write fp32 partial sums, each in row order, into the workspace, then a second kernel adds the chunks of every
  * column in a fixed order that depends on the chunk count and H only.
  * Results are bitwise reproducible and independent of sm_margin.
  * Workspace protocol: with workspace == NULL the call only stores the

@@ -18,6 +18,7 @@ std::atomic<int> g_smem_sm[kMaxDevices];
 constexpr int kMaxConsumers = 512;
 constexpr int kBwdTileRows = 8;
 constexpr int kBwdTargetChunks = 1024;  // chunks per call, roughly
+constexpr int kBwdWideChunksPerCta = 3;  // wide shape: chunks a CTA at sm_margin 0
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
@@ -311,10 +312,11 @@ rn_status plan_mx_box(int nk, int H, int esz, int N, int sm_margin, const Device
   return RN_OK;
 }
 
-// backward chunking: a chunk is R = 8 * max(1, N / 8192) rows, a function
-// of N only (never of the grid or the device), so the dgamma/dbeta partials
-// and their sum are independent of sm_margin; a tile (T rows, T | 8) never
-// straddles two chunks
+// backward chunking: a chunk is R_N = 8 * max(1, N / 8192) rows, a function
+// of N only (the wide stats-warp shape takes longer chunks, a function of N
+// and the device's SM count, in bwd_common), never of the grid or
+// sm_margin, so the dgamma/dbeta partials and their sum are independent of
+// sm_margin; the workspace is sized for R_N chunks, the most any shape uses
 struct BwdShape {
   int chunk_rows, n_chunks;
 };
@@ -704,6 +706,22 @@ rn_status bwd_common(bool ln, const void* dz, const void* x, rn_dtype dt, const 
     l.threads = 32 * (ro.A + ro.S + 1);
     l.smem = (size_t)ro.Q * per_slot + fixed;
     l.per_sm = ro.per_sm;
+    if (ro.per_sm == 1) {
+      // one CTA per SM: chunks of R = max(R_N, ceil(N / (3 SMs))) rows, so
+      // that at sm_margin 0 no CTA gets more than 3 chunks and the CTAs hold
+      // near-equal rows, with fewer partials (8192 x 4096 LayerNorm: 456
+      // chunks of 18 rows, 35.9 against 39.2 us with 1024 of 8; sm_margin
+      // 16: 42.8 against 41.6 us; 2 a CTA: 34.9 / 45.1 us, 4: 37.0 / 42.9,
+      // 6: 38.8 / 41.3).  R depends on N and the device, never on
+      // sm_margin, and is never below R_N, so the workspace the query
+      // reports (for R_N) covers it.
+      const int64_t per = (int64_t)kBwdWideChunksPerCta * di.sms;
+      int64_t R = (N + per - 1) / per;
+      if (R < sh.chunk_rows) R = sh.chunk_rows;
+      p.chunk_rows = (int)R;
+      p.n_chunks = (int)((N + R - 1) / R);
+      l.work = p.n_chunks;
+    }
     if ((st = launch_bwd(ln, dt == RN_BF16, ro.ng, p, l, stream)) != RN_OK) return st;
   }
   ColReduceParams c{};
@@ -711,7 +729,7 @@ rn_status bwd_common(bool ln, const void* dz, const void* x, rn_dtype dt, const 
   c.dgamma = dgamma;
   c.dbeta = dbeta;
   c.H = (int)H;
-  c.n_chunks = sh.n_chunks;
+  c.n_chunks = p.n_chunks;
   c.nacc = ln ? 2 : 1;
   return launch_colreduce(c, stream);
 }

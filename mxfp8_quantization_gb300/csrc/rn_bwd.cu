@@ -22,8 +22,9 @@
 //                registers; they release the slot ("empty").
 // Rows are grouped in fixed chunks of chunk_rows rows; at the end of a chunk
 // its column sums are written to the workspace as one fp32 partial row.  The
-// chunk size depends on N only, and each partial is summed in row order, so
-// the partials do not depend on the grid.
+// chunk size depends on N (and, for the one-CTA-per-SM shape, on the
+// device's SM count), never on the grid or sm_margin, and each partial is
+// summed in row order, so the partials do not depend on the grid.
 // Kernel 2 adds the partials of each column in a fixed order that depends
 // on the chunk count and H only.  Arithmetic is on element pairs (f32x2), with
 // bf16 inputs entering through the mixed-precision forms.
