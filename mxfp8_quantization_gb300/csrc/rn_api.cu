@@ -18,7 +18,7 @@ std::atomic<int> g_smem_sm[kMaxDevices];
 constexpr int kMaxConsumers = 512;
 constexpr int kBwdTileRows = 8;
 constexpr int kBwdTargetChunks = 1024;  // chunks per call, roughly
-constexpr int kBwdWideChunksPerCta = 3;  // wide shape: chunks a CTA at sm_margin 0
+constexpr int kBwdWideChunksPerCta = 3;  // wide shape: at most chunks a CTA at sm_margin 0
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
@@ -707,17 +707,28 @@ rn_status bwd_common(bool ln, const void* dz, const void* x, rn_dtype dt, const 
     l.smem = (size_t)ro.Q * per_slot + fixed;
     l.per_sm = ro.per_sm;
     if (ro.per_sm == 1) {
-      // one CTA per SM: chunks of R = max(R_N, ceil(N / (3 SMs))) rows, so
-      // that at sm_margin 0 no CTA gets more than 3 chunks and the CTAs hold
-      // near-equal rows, with fewer partials (8192 x 4096 LayerNorm: 456
-      // chunks of 18 rows, 35.9 against 39.2 us with 1024 of 8; sm_margin
+      // one CTA per SM: chunks of R = max(R_N, ceil(N / (k SMs))) rows with
+      // k = 3 or 2 chunks a CTA at sm_margin 0, whichever leaves the
+      // busiest CTA fewer rows (3 on a tie), so that the CTAs hold
+      // near-equal rows, with fewer partials.  8192 x 4096 LayerNorm: 456
+      // chunks of 18 rows, 35.9 against 39.2 us with 1024 of 8 (sm_margin
       // 16: 42.8 against 41.6 us; 2 a CTA: 34.9 / 45.1 us, 4: 37.0 / 42.9,
-      // 6: 38.8 / 41.3).  R depends on N and the device, never on
-      // sm_margin, and is never below R_N, so the workspace the query
-      // reports (for R_N) covers it.
-      const int64_t per = (int64_t)kBwdWideChunksPerCta * di.sms;
-      int64_t R = (N + per - 1) / per;
-      if (R < sh.chunk_rows) R = sh.chunk_rows;
+      // 6: 38.8 / 41.3); 3000 x 5120: 300 chunks of 10 rows, LayerNorm 24.7
+      // against 27.1 us, RMSNorm 22.7 against 24.8 us (sm_margin 16: 28.7
+      // against 26.8, 26.4 against 24.0 us).  R depends on N and the
+      // device, never on sm_margin, and is never below R_N, so the
+      // workspace the query reports (for R_N) covers it.
+      int64_t R = 0, busiest = -1;
+      for (int k = kBwdWideChunksPerCta; k >= 2; --k) {
+        const int64_t per = (int64_t)k * di.sms;
+        int64_t r = (N + per - 1) / per;
+        if (r < sh.chunk_rows) r = sh.chunk_rows;
+        const int64_t rows = ((N + r - 1) / r + di.sms - 1) / di.sms * r;
+        if (busiest < 0 || rows < busiest) {
+          busiest = rows;
+          R = r;
+        }
+      }
       p.chunk_rows = (int)R;
       p.n_chunks = (int)((N + R - 1) / R);
       l.work = p.n_chunks;
