@@ -98,7 +98,9 @@ rn_status plan_roles(int nchunks, bool ln, size_t per_slot, size_t fixed, const 
   // against 27.4 us; sm_margin 16: 41.7 against 45.2 us).  Narrower
   // LayerNorm rows measured no better or worse that way (H = 2560: 53.4
   // against 49.4 us, 3072 even, 3584: 40.5 against 39.1 us at 12288 /
-  // 8192 rows), and RMSNorm rows worse (8192 x 4096: 37.1 against 35.3 us).
+  // 8192 rows), and RMSNorm rows worse (8192 x 4096: 37.1 against 35.3 us;
+  // with the wide shape's 2-3 chunks a CTA even, 35.1 against 35.4 us, but
+  // 41.5 against 37.3 us at sm_margin 16).
   if (nchunks <= 512 && !(ln && nchunks > 480)) {
     // rows of 257 .. 512 chunks: 4 chunks a thread and 4 apply warps (the
     // per-row waits and addressing spread over twice the elements: 42.7 ->
