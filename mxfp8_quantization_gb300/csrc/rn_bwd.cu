@@ -624,7 +624,7 @@ __global__ void __launch_bounds__(1024) rn_colreduce_kernel(const ColReduceParam
 // 5120 LayerNorm 27.0 against 28.8 us, 2000 x 12288 RMSNorm 41.2 against
 // 43.0 us), while up to that count the 64-column ones are 1-4 us faster
 // (8192 x 4096).  A column's order depends on the warp count and the chunk
-// count, so on H and N only.
+// count, so on the problem (and the device's SM count), never on sm_margin.
 constexpr int kRedOneWave = 152;
 
 __device__ __forceinline__ float ld_hint_f1(const float* p, uint64_t pol) {
