@@ -196,9 +196,11 @@ rn_status rn_rmsnorm_add_fwd(const void* x, const void* residual, rn_dtype dtype
  *   dgamma, dbeta: fp32 [H], overwritten.
  * dgamma/dbeta are reduced in two deterministic stages: fixed row chunks
  * (their size depends on N, H and the device's SM count, never on
- * sm_margin) write fp32 partial sums, each in row order, into the workspace, then a second kernel adds the chunks of every
- * column in a fixed order that depends on the chunk count and H only.
- * Results are bitwise reproducible and independent of sm_margin.
+ * sm_margin) write fp32 partial sums, each in row order, into the
+ * workspace, then a second kernel adds the chunks of every column in a
+ * fixed order that depends on the chunk count and H only.  Results are
+ * bitwise reproducible and independent of sm_margin.  The size the query
+ * reports depends on N, H and dtype only (it covers every chunking).
  * Workspace protocol: with workspace == NULL the call only stores the
  * required byte count in *workspace_bytes and returns RN_OK; otherwise
  * *workspace_bytes must hold the size of `workspace` (16-byte aligned,
